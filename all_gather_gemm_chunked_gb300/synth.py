@@ -1,0 +1,97 @@
+"""Seeded synthetic inputs for the streamed AllGather+GEMM workloads.
+
+This module only draws random numbers; it holds none of the method's
+arithmetic, and both the CUDA path and the CPU oracle consume what it makes.
+
+Distributions follow the workloads the pages describe:
+
+* fp16 path: A and B ~ N(0, 1) rounded to fp16 (the Pallas collective-matmul
+  page draws ``jax.random.normal`` operands; the Triton-distributed tutorial
+  draws ``torch.randn`` fp16 operands).
+* int8 path ("AllGather矩阵乘法反量化算子设计文档", 1.3 and 8.3): A, B uniform
+  int8 on [-127, 127] (symmetric quantisation), bias uniform int32 on
+  [-1000, 1000], per-channel scale uniform fp32 on [1e-5, 1e-4].
+
+Each shard is an independent array, so shards behave like separate ranks'
+buffers.  Seeds: ``0xA66E0000 + workload id``, then a fixed offset per tensor.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+SEED_BASE = 0xA66E0000
+OFF_B, OFF_BIAS, OFF_SCALE = 100, 200, 300
+
+
+@dataclass(frozen=True)
+class Workload:
+    """One AllGather+GEMM problem: S shards of R rows, K, N, dtype, chunking."""
+    wid: int
+    name: str
+    S: int
+    M: int
+    K: int
+    N: int
+    dtype: str           # "f16" or "i8"
+    chunk_rows: int      # 0 = chosen by the library (64..128 chunks per source)
+
+    @property
+    def R(self) -> int:
+        return self.M // self.S
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+
+# The five workloads: a small parity case, two compute-bound fp16 cases, a
+# compute-bound int8 dequant case and a memory-bound skinny int8 case.
+WORKLOADS = {
+    1: Workload(1, "f16 2x128 rows, K=256, N=128, chunk 16", 2, 256, 256, 128, "f16", 16),
+    2: Workload(2, "f16 2x2048 rows, K=4096, N=4096", 2, 4096, 4096, 4096, "f16", 0),
+    3: Workload(3, "f16 8x1024 rows, K=4096, N=4096", 8, 8192, 4096, 4096, "f16", 0),
+    4: Workload(4, "i8 dequant 4x4096 rows, K=27392, N=4096", 4, 16384, 27392, 4096, "i8", 0),
+    5: Workload(5, "i8 dequant skinny 2x32 rows, K=16384, N=7168", 2, 64, 16384, 7168, "i8", 0),
+}
+
+
+def _rng(seed: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(seed))
+
+
+def normal_f16(seed: int, shape) -> np.ndarray:
+    """N(0,1) samples rounded to float16 (numpy's round-to-nearest cast)."""
+    return _rng(seed).standard_normal(shape, dtype=np.float64).astype(np.float16)
+
+
+def uniform_i8(seed: int, shape, lo: int = -127, hi: int = 127) -> np.ndarray:
+    return _rng(seed).integers(lo, hi + 1, size=shape, dtype=np.int8)
+
+
+def uniform_i32(seed: int, shape, lo: int = -1000, hi: int = 1000) -> np.ndarray:
+    return _rng(seed).integers(lo, hi + 1, size=shape, dtype=np.int32)
+
+
+def uniform_f32(seed: int, shape, lo: float = 1e-5, hi: float = 1e-4) -> np.ndarray:
+    return _rng(seed).uniform(lo, hi, size=shape).astype(np.float32)
+
+
+def make_inputs(S: int, R: int, K: int, N: int, dtype: str, seed: int):
+    """Return dict(shards=[S arrays R x K], B=K x N, bias, scale) on the host."""
+    if dtype == "f16":
+        shards = [normal_f16(seed + s, (R, K)) for s in range(S)]
+        B = normal_f16(seed + OFF_B, (K, N))
+        return {"shards": shards, "B": B, "bias": None, "scale": None}
+    if dtype == "i8":
+        shards = [uniform_i8(seed + s, (R, K)) for s in range(S)]
+        B = uniform_i8(seed + OFF_B, (K, N))
+        bias = uniform_i32(seed + OFF_BIAS, (N,))
+        scale = uniform_f32(seed + OFF_SCALE, (N,))
+        return {"shards": shards, "B": B, "bias": bias, "scale": scale}
+    raise ValueError(f"unknown dtype {dtype!r}")
+
+
+def workload_inputs(w: Workload):
+    return make_inputs(w.S, w.R, w.K, w.N, w.dtype, SEED_BASE + w.wid)
