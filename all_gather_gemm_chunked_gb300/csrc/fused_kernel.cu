@@ -1,0 +1,506 @@
+// fused_kernel.cu -- the streamed AllGather+GEMM as ONE persistent,
+// cooperative, warp-specialised kernel for sm_103a.
+//
+// The method ("AllGather + GEMM 通算融合算子示例", sections 整体架构 and
+// 优化说明): a communication engine sends A chunk by chunk and bumps a
+// per-source counter after each chunk; the compute engine first multiplies the
+// local row group with no wait, then each remote row group after waiting on
+// its counter, with continuous K accumulation and double-buffered operand
+// staging.  On one GB300 the "ranks" are shards in this GPU's memory, and both
+// engines live in the same launch:
+//
+//   warp 0      TMA warp: waits (remote tiles only) on the ready counters of
+//               the chunks a tile reads, then streams A and B k-blocks into a
+//               4-stage shared-memory ring with cp.async.bulk.tensor.
+//   warp 1      MMA warp: one thread issues tcgen05.mma kind::f16 into a TMEM
+//               accumulator (two 256-column buffers, so the epilogue of tile i
+//               overlaps the MMAs of tile i+1).
+//   warps 2-3   copy warps ("comm blocks"): copy items of the remote shards'
+//               chunks into the staging workspace, in consumption order, and
+//               release the chunk's counter after each item.  Every CTA runs
+//               two, so the gather uses the whole GPU's load/store bandwidth.
+//   warps 4-7   epilogue: TMEM -> registers -> global (fp32 C, or for int8
+//               the exact int32 fold, bias, int32 C and fp16 D).
+//
+// Counter waits cross CTAs, so the grid is launched cooperatively: every CTA
+// is resident for the whole launch and no wait can depend on an unscheduled
+// CTA.  Every wait is bounded; on timeout the kernel records a status word,
+// stops issuing work, drains what it has in flight, frees TMEM and returns.
+//
+// int8: sm_103a has no tcgen05 kind::i8, so int8 x int8 is computed exactly on
+// the fp16 tensor path: int8 values are exact in fp16, products of two int8
+// values are exact in fp32, and K is cut into segments of 1024 so every fp32
+// partial sum is an integer below 2^24 (exact).  After each segment the
+// epilogue converts the fp32 accumulator to int32 and adds it to an int32
+// running sum kept in the other half of TMEM.
+
+#include <cuda_fp16.h>
+
+#include "fused_kernel.cuh"
+#include "sm103.cuh"
+
+namespace agg {
+
+__device__ __forceinline__ void set_status(uint32_t* status, uint32_t kind, uint32_t detail) {
+  if (atomicCAS(status, 0u, kind) == 0u) atomicExch(status + 1, detail);
+}
+
+// ------------------------------------------------------------------ copy warps
+__device__ __forceinline__ void warp_copy16(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                            int64_t n, int lane) {
+  constexpr int U = 8;
+  int64_t i = lane;
+  for (; i + (U - 1) * 32 < n; i += U * 32) {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) v[u] = ld_nc_v4(src + i + u * 32);
+#pragma unroll
+    for (int u = 0; u < U; ++u) dst[i + u * 32] = v[u];
+  }
+  for (; i < n; i += 32) dst[i] = ld_nc_v4(src + i);
+}
+
+__device__ __forceinline__ void widen16(const uint4 v, uint4& a, uint4& b) {
+  i8x4_to_f16x4(v.x, a.x, a.y);
+  i8x4_to_f16x4(v.y, a.z, a.w);
+  i8x4_to_f16x4(v.z, b.x, b.y);
+  i8x4_to_f16x4(v.w, b.z, b.w);
+}
+
+// n source vectors of 16 int8 -> 2n destination vectors of 8 fp16.
+__device__ __forceinline__ void warp_widen16(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                             int64_t n, int lane) {
+  constexpr int U = 4;
+  int64_t i = lane;
+  for (; i + (U - 1) * 32 < n; i += U * 32) {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) v[u] = ld_nc_v4(src + i + u * 32);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      uint4 a, b;
+      widen16(v[u], a, b);
+      dst[2 * (i + u * 32)] = a;
+      dst[2 * (i + u * 32) + 1] = b;
+    }
+  }
+  for (; i < n; i += 32) {
+    uint4 a, b;
+    widen16(ld_nc_v4(src + i), a, b);
+    dst[2 * i] = a;
+    dst[2 * i + 1] = b;
+  }
+}
+
+template <bool kI8>
+__device__ void copy_warp(const FusedParams& p, int64_t gw, int64_t n_warps, int lane) {
+  const Geometry& g = p.g;
+  for (int64_t i = gw; i < g.items; i += n_warps) {
+    int pos, piece;
+    int64_t q, v0, v1;
+    item_coords(g, i, pos, q, piece, v0, v1);
+    if (i == p.debug_skip_item) continue;  // failure injection: this chunk never completes
+    if (p.debug_delay_ns) __nanosleep(p.debug_delay_ns);
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.src[pos]) +
+                                                      q * g.c * g.K * g.src_esize);
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.staging) +
+                                          ((int64_t)(pos - 1) * g.R + q * g.c) * g.K * 2);
+    if (kI8)
+      warp_widen16(src + v0, dst + 2 * v0, v1 - v0, lane);
+    else
+      warp_copy16(src + v0, dst + v0, v1 - v0, lane);
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) red_release_gpu_add(p.counters + (int64_t)(pos - 1) * g.Q + q, 1u);
+  }
+}
+
+// ------------------------------------------------------------------ TMA warp
+// All 32 lanes poll the counters of the chunks that m-tile `mt` of position
+// `pos` reads; returns false (and raises the abort flag) on timeout.
+__device__ bool wait_chunks(const FusedParams& p, int pos, int64_t mt, int lane,
+                            volatile int* abort) {
+  const Geometry& g = p.g;
+  int64_t q0, q1;
+  tile_chunks(g, mt, q0, q1);
+  const uint32_t target = p.epoch * static_cast<uint32_t>(g.P);
+  const uint32_t* cnt = p.counters + (int64_t)(pos - 1) * g.Q;
+  bool ok = true;
+  for (int64_t q = q0 + lane; q <= q1 && ok; q += 32) {
+    if (ld_acquire_gpu(cnt + q) >= target) continue;
+    const uint64_t deadline = globaltimer_ns() + p.timeout_ns;
+    uint32_t spins = 0;
+    while (ld_acquire_gpu(cnt + q) < target) {
+      __nanosleep(64);
+      if (++spins == 16) {
+        spins = 0;
+        if (*abort || *reinterpret_cast<volatile uint32_t*>(p.status) != 0u ||
+            globaltimer_ns() > deadline) {
+          ok = false;
+          break;
+        }
+      }
+    }
+  }
+  ok = __all_sync(0xffffffffu, ok);
+  if (!ok && lane == 0) {
+    set_status(p.status, kStatusChunkTimeout,
+               (static_cast<uint32_t>(pos) << 24) | static_cast<uint32_t>(q0 & 0xFFFFFF));
+    *abort = 1;
+  }
+  __syncwarp();
+  return ok;
+}
+
+template <bool kI8>
+__device__ void tma_warp(const FusedParams& p, uint8_t* sA, uint8_t* sB, uint64_t* full,
+                         uint64_t* empty, int lane, volatile int* abort) {
+  const Geometry& g = p.g;
+  const bool wait = (p.flags & kFlagWait) != 0;
+  const uint32_t tx = static_cast<uint32_t>(kABytes + g.BN * kBlockK * 2);
+  const int nb = g.BN / 64;
+  int stage = 0;
+  uint32_t phase = 0, issued = 0, issued_phase = 0;  // bit s: stage s used / parity of last use
+  if (lane == 0) {
+    tma_prefetch_desc(&p.tm_a_local);
+    tma_prefetch_desc(&p.tm_a_stage);
+    tma_prefetch_desc(&p.tm_b);
+  }
+  bool ok = true;
+  for (int64_t t = blockIdx.x; t < g.tiles && ok; t += gridDim.x) {
+    int pos;
+    int64_t mt, nt;
+    tile_coords(g, t, pos, mt, nt);
+    if (pos > 0 && wait && !wait_chunks(p, pos, mt, lane, abort)) break;
+    if (lane == 0) {
+      if (pos > 0) {
+        fence_acq_rel_gpu();
+        fence_proxy_async_global();
+      }
+      const int32_t y = static_cast<int32_t>(mt * kBlockM);
+      for (int64_t kb = 0; kb < g.KB; ++kb) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u, p.pipe_timeout_ns, abort)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[stage], tx);
+        const int32_t x = static_cast<int32_t>(kb * kBlockK);
+        uint8_t* a_dst = sA + stage * kABytes;
+        if (pos == 0)
+          tma_load_2d(a_dst, &p.tm_a_local, &full[stage], x, y);
+        else
+          tma_load_3d(a_dst, &p.tm_a_stage, &full[stage], x, y, pos - 1);
+        uint8_t* b_dst = sB + stage * kBBytes;
+        for (int i = 0; i < nb; ++i)
+          tma_load_2d(b_dst + i * (64 * kBlockK * 2), &p.tm_b, &full[stage],
+                      static_cast<int32_t>(nt * g.BN + i * 64), x);
+        issued |= 1u << stage;
+        issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  }
+  if (lane == 0) {
+    if (!ok) {
+      set_status(p.status, kStatusPipelineTimeout, 0x100u);
+      *abort = 1;
+    }
+    // Drain: every load this warp issued must have landed before the CTA exits.
+    volatile int never = 0;
+    for (int s = 0; s < kStages; ++s)
+      if (issued & (1u << s)) mbar_wait(&full[s], (issued_phase >> s) & 1u, p.pipe_timeout_ns, &never);
+  }
+  __syncwarp();
+}
+
+// ------------------------------------------------------------------ MMA warp
+template <bool kI8>
+__device__ void mma_warp(const FusedParams& p, const uint8_t* sA, const uint8_t* sB,
+                         uint64_t* full, uint64_t* empty, uint64_t* tfull, uint64_t* tempty,
+                         uint32_t tmem, volatile int* abort) {
+  const Geometry& g = p.g;
+  const uint32_t idesc = idesc_f16_f32(kBlockM, g.BN, /*a_mn=*/false, /*b_mn=*/true);
+  const int64_t seg_len = kI8 ? kSegBlocks : g.KB;
+  const int64_t nseg = ceil_div(g.KB, seg_len);
+  const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+  int stage = 0;
+  uint32_t phase = 0, unit = 0;
+  bool ok = true;
+  for (int64_t t = blockIdx.x; t < g.tiles && ok; t += gridDim.x) {
+    for (int64_t seg = 0; seg < nseg && ok; ++seg) {
+      const uint32_t buf = kI8 ? 0u : (unit & 1u);
+      const uint32_t use = kI8 ? unit : (unit >> 1);
+      if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, p.pipe_timeout_ns, abort)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d = tmem + buf * 256u;
+      const int64_t kb0 = seg * seg_len;
+      const int64_t kb1 = kb0 + seg_len < g.KB ? kb0 + seg_len : g.KB;
+      for (int64_t kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(&full[stage], phase, p.pipe_timeout_ns, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t as = a0 + stage * kABytes, bs = b0 + stage * kBBytes;
+#pragma unroll
+        for (int k = 0; k < kBlockK / kUmmaK; ++k) {
+          // A: K-major, 128B swizzle: 8-row groups 1024 B apart; a 16-element
+          // K slice is 32 B further along the swizzled row.
+          const uint64_t ad = smem_desc_sw128(as + k * (kUmmaK * 2), 16, 1024);
+          // B: MN-major, 128B swizzle: 64-column groups 8 KB apart (LBO),
+          // 8-k-row groups 1024 B apart (SBO); a 16-row K slice is 2 KB on.
+          const uint64_t bd = smem_desc_sw128(bs + k * (kUmmaK * 128), 64 * kBlockK * 2, 1024);
+          mma_f16(d, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+        }
+        mma_commit(&empty[stage]);  // frees the smem stage once these MMAs have read it
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      mma_commit(&tfull[buf]);  // accumulator ready for the epilogue
+      ++unit;
+    }
+  }
+  if (!ok) {
+    set_status(p.status, kStatusPipelineTimeout, 0x200u);
+    *abort = 1;
+  }
+}
+
+// ------------------------------------------------------------------ epilogue
+__device__ __forceinline__ void st_v4(void* ptr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+template <bool kI8>
+__device__ void epilogue_warp(const FusedParams& p, int quad, int lane, uint64_t* tfull,
+                              uint64_t* tempty, uint32_t tmem, volatile int* abort) {
+  const Geometry& g = p.g;
+  const int64_t seg_len = kI8 ? kSegBlocks : g.KB;
+  const int64_t nseg = ceil_div(g.KB, seg_len);
+  const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+  uint32_t unit = 0;
+  for (int64_t t = blockIdx.x; t < g.tiles; t += gridDim.x) {
+    int pos;
+    int64_t mt, nt;
+    tile_coords(g, t, pos, mt, nt);
+    const int src = source_of(g, p.local, pos);
+    const int64_t r = mt * kBlockM + quad * 32 + lane;
+    const bool row_ok = r < g.R;
+    const int64_t grow = static_cast<int64_t>(src) * g.R + r;
+    for (int64_t seg = 0; seg < nseg; ++seg) {
+      const uint32_t buf = kI8 ? 0u : (unit & 1u);
+      const uint32_t use = kI8 ? unit : (unit >> 1);
+      if (!mbar_wait(&tfull[buf], use & 1u, p.pipe_timeout_ns, abort)) {
+        if (lane == 0) {
+          set_status(p.status, kStatusPipelineTimeout, 0x300u);
+          *abort = 1;
+        }
+        return;
+      }
+      tc_fence_after();
+      if (!kI8) {
+        for (int j = 0; j < g.BN / 32; ++j) {
+          uint32_t v[32];
+          tmem_ld32(lane_base + buf * 256u + j * 32, v);
+          tmem_ld_wait();
+          const int64_t n0 = nt * g.BN + j * 32;
+          if (row_ok) {
+            float* dst = p.C + grow * g.N + n0;
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              if (n0 + e < g.N) st_v4(dst + e, v[e], v[e + 1], v[e + 2], v[e + 3]);
+          }
+        }
+      } else {
+        const bool first = seg == 0, last = seg == nseg - 1;
+        for (int j = 0; j < g.BN / 32; ++j) {
+          uint32_t f[32], s[32];
+          tmem_ld32(lane_base + j * 32, f);
+          if (!first) tmem_ld32(lane_base + 256u + j * 32, s);
+          tmem_ld_wait();
+          // fp32 partial (an exact integer) -> int32, added to the running sum
+          uint32_t acc[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            acc[e] = (first ? 0u : s[e]) +
+                     static_cast<uint32_t>(__float2int_rn(__uint_as_float(f[e])));
+          if (!last) {
+            tmem_st32(lane_base + 256u + j * 32, acc);
+          } else if (row_ok) {
+            const int64_t n0 = nt * g.BN + j * 32;
+#pragma unroll
+            for (int e = 0; e < 32; e += 8) {
+              if (n0 + e >= g.N) continue;
+              const int4 b0 = __ldg(reinterpret_cast<const int4*>(p.bias + n0 + e));
+              const int4 b1 = __ldg(reinterpret_cast<const int4*>(p.bias + n0 + e + 4));
+              const float4 s0 = __ldg(reinterpret_cast<const float4*>(p.scale + n0 + e));
+              const float4 s1 = __ldg(reinterpret_cast<const float4*>(p.scale + n0 + e + 4));
+              const int32_t bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+              const float ss[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+              uint32_t c[8];
+              uint32_t h[4];
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const int32_t cv = static_cast<int32_t>(acc[e + u] + static_cast<uint32_t>(bb[u]));
+                c[u] = static_cast<uint32_t>(cv);
+                const float dv = __fmul_rn(__int2float_rn(cv), ss[u]);
+                const uint32_t hb = __half_as_ushort(__float2half_rn(dv));
+                if (u & 1)
+                  h[u >> 1] |= hb << 16;
+                else
+                  h[u >> 1] = hb;
+              }
+              int32_t* cdst = p.C_i32 + grow * g.N + n0 + e;
+              st_v4(cdst, c[0], c[1], c[2], c[3]);
+              st_v4(cdst + 4, c[4], c[5], c[6], c[7]);
+              st_v4(p.D_f16 + grow * g.N + n0 + e, h[0], h[1], h[2], h[3]);
+            }
+          }
+        }
+        if (!last) tmem_st_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
+      ++unit;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+template <bool kI8>
+__global__ void __launch_bounds__(kThreads, 1) ag_fused_kernel(const __grid_constant__ FusedParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kABytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kBBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* tfull = bars + 2 * kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool gemm = (p.flags & kFlagGemm) != 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);
+    }
+    mbar_init(drain, 1);
+    *tmem_slot = 0;
+    *abort = 0;
+    fence_mbar_init();
+  }
+  if (gemm && warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (gemm) tma_warp<kI8>(p, sA, sB, full, empty, lane, abort);
+  } else if (warp == 1) {
+    if (gemm && lane == 0) mma_warp<kI8>(p, sA, sB, full, empty, tfull, tempty, tmem, abort);
+  } else if (warp < 4) {
+    if (p.flags & kFlagCopy)
+      copy_warp<kI8>(p, static_cast<int64_t>(blockIdx.x) * 2 + (warp - 2),
+                     static_cast<int64_t>(gridDim.x) * 2, lane);
+  } else {
+    if (gemm) epilogue_warp<kI8>(p, warp - 4, lane, tfull, tempty, tmem, abort);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (gemm && warp == 1) {
+    if (lane == 0) {
+      // Every MMA this CTA issued must be complete before TMEM is released.
+      mma_commit(drain);
+      volatile int never = 0;
+      mbar_wait(drain, 0, p.pipe_timeout_ns, &never);
+    }
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------------ int8 widening
+// fp16 copies of B and of the local shard for the int8 path (exact).
+__global__ void __launch_bounds__(256) widen_kernel(const uint4* __restrict__ s0,
+                                                    uint4* __restrict__ d0, int64_t n0,
+                                                    const uint4* __restrict__ s1,
+                                                    uint4* __restrict__ d1, int64_t n1) {
+  const int64_t total = n0 + n1;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += stride) {
+    const bool first = i < n0;
+    const int64_t j = first ? i : i - n0;
+    const uint4 v = ld_nc_v4((first ? s0 : s1) + j);
+    uint4 a, b;
+    widen16(v, a, b);
+    uint4* d = (first ? d0 : d1) + 2 * j;
+    d[0] = a;
+    d[1] = b;
+  }
+}
+
+// ------------------------------------------------------------------ launchers
+cudaError_t fused_max_blocks_per_sm(int dtype, int* blocks) {
+  const void* fn = dtype == 1 ? reinterpret_cast<const void*>(&ag_fused_kernel<true>)
+                              : reinterpret_cast<const void*>(&ag_fused_kernel<false>);
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, fn, kThreads, kSmemBytes);
+}
+
+cudaError_t launch_fused(const FusedParams& p, int grid, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (p.g.dtype == 1) return cudaLaunchKernelEx(&cfg, ag_fused_kernel<true>, p);
+  return cudaLaunchKernelEx(&cfg, ag_fused_kernel<false>, p);
+}
+
+cudaError_t launch_widen(const int8_t* src0, uint16_t* dst0, int64_t n0, const int8_t* src1,
+                         uint16_t* dst1, int64_t n1, int grid, cudaStream_t stream) {
+  widen_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const uint4*>(src0),
+                                         reinterpret_cast<uint4*>(dst0), n0 / 16,
+                                         reinterpret_cast<const uint4*>(src1),
+                                         reinterpret_cast<uint4*>(dst1), n1 / 16);
+  return cudaGetLastError();
+}
+
+}  // namespace agg

@@ -1,0 +1,60 @@
+// fused_kernel.cuh -- parameters shared by the host plan and the fused
+// streamed AllGather+GEMM kernel.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "schedule.h"
+
+namespace agg {
+
+// Status word values (low byte = kind, upper bits = detail).
+enum : uint32_t {
+  kStatusOk = 0,
+  kStatusChunkTimeout = 1,     // a ready counter did not reach its target in time
+  kStatusPipelineTimeout = 2,  // an mbarrier of the TMA/MMA/epilogue pipeline ran out
+};
+
+enum : int {
+  kFlagCopy = 1,   // producer warps copy remote chunks and release counters
+  kFlagGemm = 2,   // TMA / MMA / epilogue warps compute C
+  kFlagWait = 4,   // the TMA warp waits on the ready counters of remote chunks
+};
+
+struct FusedParams {
+  CUtensorMap tm_a_local;   // fp16 [R][K] local shard (2D: K, R)
+  CUtensorMap tm_a_stage;   // fp16 [S-1][R][K] staging (3D: K, R, slot)
+  CUtensorMap tm_b;         // fp16 [K][N] (2D: N, K), loaded MN-major
+  Geometry g;
+  const void* src[kMaxShards];  // shard pointers by consumption position
+  void* staging;                // fp16 [(S-1)][R][K]
+  uint32_t* counters;           // [(S-1)][Q] ready counters, monotonic
+  uint32_t* status;             // [2]: status word, detail
+  float* C;                     // f16 path output, M x N fp32
+  int32_t* C_i32;               // i8 path outputs
+  uint16_t* D_f16;
+  const int32_t* bias;
+  const float* scale;
+  int local;                    // local rank
+  int flags;                    // kFlag*
+  uint32_t epoch;               // run number since the last reset (>= 1)
+  uint64_t timeout_ns;          // limit of a wait on a ready counter
+  uint64_t pipe_timeout_ns;     // limit of a wait on a pipeline mbarrier (longer)
+  int64_t debug_skip_item;      // -1 = none
+  uint32_t debug_delay_ns;
+};
+
+constexpr int kThreads = 256;                     // 8 warps
+constexpr int kABytes = kBlockM * kBlockK * 2;    // 16 KB
+constexpr int kBBytes = kMaxBlockN * kBlockK * 2; // 32 KB
+constexpr int kSmemBytes = kStages * (kABytes + kBBytes) + 1024 /*barriers*/ + 1024 /*align*/;
+
+// Launchers (fused_kernel.cu).
+cudaError_t launch_fused(const FusedParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_widen(const int8_t* src0, uint16_t* dst0, int64_t n0, const int8_t* src1,
+                         uint16_t* dst1, int64_t n1, int grid, cudaStream_t stream);
+cudaError_t fused_max_blocks_per_sm(int dtype, int* blocks);
+
+}  // namespace agg

@@ -1,0 +1,588 @@
+// plan.cu -- host side of libaggemm.so: argument validation, chunk sizing,
+// workspace ownership, TMA descriptors and the launch sequence of each run
+// mode.  Implements include/ag_gemm.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "ag_gemm.h"
+#include "fused_kernel.cuh"
+#include "schedule.h"
+
+using agg::Geometry;
+
+// ------------------------------------------------------------------ errors
+namespace {
+thread_local int g_last_error = AG_GEMM_OK;
+thread_local char g_last_msg[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  g_last_error = code;
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_msg, sizeof(g_last_msg), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(e == cudaErrorMemoryAllocation ? AG_GEMM_ERR_OOM : AG_GEMM_ERR_CUDA, "%s: %s",
+              what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ------------------------------------------------------------------ TMA descriptors
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// fp16 tensor, innermost dimension first; 128-byte swizzle, zero fill out of bounds.
+int encode_f16(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
+               const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(AG_GEMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  cuuint32_t estride[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, static_cast<cuuint32_t>(rank),
+                  const_cast<void*>(base), dims, strides_bytes, box, estride,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(AG_GEMM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return AG_GEMM_OK;
+}
+
+// A operand rows x K (K contiguous), box 64 x 128.
+int encode_a(CUtensorMap* map, const void* base, int64_t rows, int64_t K) {
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  cuuint32_t box[2] = {agg::kBlockK, agg::kBlockM};
+  return encode_f16(map, base, 2, dims, strides, box);
+}
+
+// Staging: slots x R x K, box 64 x 128 x 1 (rows past R of a slot read as zero).
+int encode_stage(CUtensorMap* map, const void* base, int64_t slots, int64_t R, int64_t K) {
+  cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)R, (cuuint64_t)slots};
+  cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)R * K * 2};
+  cuuint32_t box[3] = {agg::kBlockK, agg::kBlockM, 1};
+  return encode_f16(map, base, 3, dims, strides, box);
+}
+
+// B: K x N (N contiguous), box 64 (n) x 64 (k): one MN-major swizzle column group.
+int encode_b(CUtensorMap* map, const void* base, int64_t K, int64_t N) {
+  cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)K};
+  cuuint64_t strides[1] = {(cuuint64_t)N * 2};
+  cuuint32_t box[2] = {64, agg::kBlockK};
+  return encode_f16(map, base, 2, dims, strides, box);
+}
+
+int check_problem(int S, int64_t M, int64_t K, int64_t N, int dtype, int64_t chunk_rows) {
+  if (dtype != AG_GEMM_F16 && dtype != AG_GEMM_I8)
+    return fail(AG_GEMM_ERR_INVALID, "dtype must be AG_GEMM_F16 or AG_GEMM_I8 (got %d)", dtype);
+  if (S < 1 || S > agg::kMaxShards)
+    return fail(AG_GEMM_ERR_INVALID, "n_shards must be in [1, %d] (got %d)", agg::kMaxShards, S);
+  if (M <= 0 || K <= 0 || N <= 0)
+    return fail(AG_GEMM_ERR_INVALID, "M, K, N must be positive (got %lld, %lld, %lld)",
+                (long long)M, (long long)K, (long long)N);
+  if (M % S != 0)
+    return fail(AG_GEMM_ERR_INVALID, "M (%lld) must be a multiple of n_shards (%d)", (long long)M, S);
+  const int64_t R = M / S;
+  if (chunk_rows < 0 || (chunk_rows > 0 && R % chunk_rows != 0))
+    return fail(AG_GEMM_ERR_INVALID, "chunk_rows (%lld) must be 0 or divide the %lld rows of a shard",
+                (long long)chunk_rows, (long long)R);
+  if (dtype == AG_GEMM_F16 && (K % 8 != 0 || N % 8 != 0))
+    return fail(AG_GEMM_ERR_INVALID, "fp16 needs K %% 8 == 0 and N %% 8 == 0 (16-byte rows)");
+  if (dtype == AG_GEMM_I8 && (K % 16 != 0 || N % 16 != 0))
+    return fail(AG_GEMM_ERR_INVALID, "int8 needs K %% 16 == 0 and N %% 16 == 0 (16-byte rows)");
+  if (dtype == AG_GEMM_I8 && K > agg::kMaxKI8)
+    return fail(AG_GEMM_ERR_UNSUPPORTED, "int8 needs K <= %lld so that K*127^2 fits in int32",
+                (long long)agg::kMaxKI8);
+  // TMA coordinates are 32-bit.
+  if (K > (1LL << 31) || N > (1LL << 31) || R > (1LL << 31))
+    return fail(AG_GEMM_ERR_UNSUPPORTED, "dimension too large for 32-bit TMA coordinates");
+  return AG_GEMM_OK;
+}
+
+void to_public(const Geometry& g, ag_gemm_geometry* out) {
+  std::memset(out, 0, sizeof(*out));
+  out->n_shards = g.S;
+  out->dtype = g.dtype;
+  out->M = g.M;
+  out->K = g.K;
+  out->N = g.N;
+  out->R = g.R;
+  out->chunk_rows = g.c;
+  out->chunks_per_source = g.Q;
+  out->pieces_per_chunk = g.P;
+  out->block_m = agg::kBlockM;
+  out->block_n = g.BN;
+  out->block_k = agg::kBlockK;
+  out->group_m = agg::kGroupM;
+  out->kseg_blocks = g.dtype == AG_GEMM_I8 ? agg::kSegBlocks : 0;
+  out->m_tiles = g.MT;
+  out->n_tiles = g.NT;
+  out->tiles = g.tiles;
+  out->producer_items = g.items;
+  const int64_t slots = g.S > 1 ? g.S - 1 : 1;
+  out->staging_bytes = slots * g.R * g.K * 2;
+  int64_t ws = out->staging_bytes + slots * g.Q * 4 + 64;
+  if (g.dtype == AG_GEMM_I8) ws += (g.K * g.N + g.R * g.K) * 2;
+  out->workspace_bytes = ws;
+}
+
+bool from_public(const ag_gemm_geometry* in, Geometry& g) {
+  if (!in || check_problem(in->n_shards, in->M, in->K, in->N, in->dtype, in->chunk_rows) != AG_GEMM_OK)
+    return false;
+  agg::make_geometry(g, in->n_shards, in->M, in->K, in->N, in->dtype, in->chunk_rows);
+  return true;
+}
+
+// Restores the caller's current device on scope exit.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) { ok = false; return; }
+    if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+}  // namespace
+
+// ------------------------------------------------------------------ plan
+struct ag_gemm_plan {
+  Geometry g{};
+  int device = 0;
+  int sm_count = 0;
+  int grid = 0;
+  int mode = AG_GEMM_MODE_PIPELINED;
+  int local = 0;
+  uint64_t timeout_ns = 1000000000ull;
+  int debug_flags = 0;
+  int64_t debug_arg = 0;
+  void* staging = nullptr;
+  int64_t staging_bytes = 0;
+  uint32_t* counters = nullptr;
+  int64_t counter_count = 0;
+  uint32_t* status = nullptr;
+  uint16_t* b16 = nullptr;  // int8 path: fp16 copy of B
+  uint16_t* a16 = nullptr;  // int8 path: fp16 copy of the local shard
+  uint32_t epoch = 0;
+  cudaEvent_t done = nullptr;
+  cudaStream_t last_stream = nullptr;
+  bool has_run = false;
+  CUtensorMap tm_stage{};
+  CUtensorMap tm_a16{}, tm_b16{};
+  const void* cached_a = nullptr;
+  CUtensorMap tm_a_cached{};
+  const void* cached_b = nullptr;
+  CUtensorMap tm_b_cached{};
+};
+
+namespace {
+
+void free_plan(ag_gemm_plan* p) {
+  if (!p) return;
+  if (p->done) cudaEventSynchronize(p->done);
+  cudaFree(p->staging);
+  cudaFree(p->counters);
+  cudaFree(p->status);
+  cudaFree(p->b16);
+  cudaFree(p->a16);
+  if (p->done) cudaEventDestroy(p->done);
+  delete p;
+}
+
+int launch_fused(ag_gemm_plan* p, agg::FusedParams& fp, int flags, cudaStream_t stream) {
+  fp.flags = flags;
+  cudaError_t e = agg::launch_fused(fp, p->grid, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "fused kernel launch");
+  return AG_GEMM_OK;
+}
+
+// One run: the launch sequence of the plan's mode on `stream`.
+int run_impl(ag_gemm_plan* p, const void* const* shard_ptrs, const void* B, float* C,
+             int32_t* C_i32, void* D, const int32_t* bias, const float* scale, void* stream_v) {
+  const Geometry& g = p->g;
+  const bool int8 = g.dtype == AG_GEMM_I8;
+  if (!shard_ptrs) return fail(AG_GEMM_ERR_INVALID, "shard_ptrs is NULL");
+  for (int s = 0; s < g.S; ++s) {
+    if (!shard_ptrs[s]) return fail(AG_GEMM_ERR_INVALID, "shard_ptrs[%d] is NULL", s);
+    if (!aligned16(shard_ptrs[s])) return fail(AG_GEMM_ERR_INVALID, "shard_ptrs[%d] is not 16-byte aligned", s);
+  }
+  const void* outs[4] = {B, int8 ? static_cast<const void*>(C_i32) : static_cast<const void*>(C),
+                         int8 ? D : B, int8 ? static_cast<const void*>(bias) : B};
+  const char* names[4] = {"B", int8 ? "C_i32" : "C", "D_f16", "bias"};
+  for (int i = 0; i < 4; ++i) {
+    if (!outs[i]) return fail(AG_GEMM_ERR_INVALID, "%s is NULL", names[i]);
+    if (!aligned16(outs[i])) return fail(AG_GEMM_ERR_INVALID, "%s is not 16-byte aligned", names[i]);
+  }
+  if (int8 && (!scale || !aligned16(scale)))
+    return fail(AG_GEMM_ERR_INVALID, "scale is NULL or not 16-byte aligned");
+
+  DeviceGuard dg(p->device);
+  if (!dg.ok) return fail(AG_GEMM_ERR_CUDA, "cannot select the plan's device %d", p->device);
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  cudaError_t e;
+  // Runs on one plan share its staging and counters: order them.
+  if (p->has_run && p->last_stream != stream) {
+    e = cudaStreamWaitEvent(stream, p->done, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent");
+  }
+  // Counters are monotonic: after run e each holds e * P.  Restart before overflow.
+  if (static_cast<uint64_t>(p->epoch + 1) * static_cast<uint64_t>(g.P) >= (1ull << 31)) {
+    e = cudaMemsetAsync(p->counters, 0, sizeof(uint32_t) * p->counter_count, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "counter reset");
+    p->epoch = 0;
+  }
+
+  agg::FusedParams fp;
+  std::memset(&fp, 0, sizeof(fp));
+  fp.g = g;
+  for (int pos = 0; pos < g.S; ++pos) fp.src[pos] = shard_ptrs[agg::source_of(g, p->local, pos)];
+  const void* local_ptr = fp.src[0];
+  int rc;
+  if (int8) {
+    fp.tm_a_local = p->tm_a16;
+    fp.tm_b = p->tm_b16;
+  } else {
+    if (p->cached_a != local_ptr) {
+      p->cached_a = nullptr;
+      if ((rc = encode_a(&p->tm_a_cached, local_ptr, g.R, g.K)) != AG_GEMM_OK) return rc;
+      p->cached_a = local_ptr;
+    }
+    if (p->cached_b != B) {
+      p->cached_b = nullptr;
+      if ((rc = encode_b(&p->tm_b_cached, B, g.K, g.N)) != AG_GEMM_OK) return rc;
+      p->cached_b = B;
+    }
+    fp.tm_a_local = p->tm_a_cached;
+    fp.tm_b = p->tm_b_cached;
+  }
+  fp.tm_a_stage = p->tm_stage;
+  fp.staging = p->staging;
+  fp.counters = p->counters;
+  fp.status = p->status;
+  fp.C = C;
+  fp.C_i32 = C_i32;
+  fp.D_f16 = static_cast<uint16_t*>(D);
+  fp.bias = bias;
+  fp.scale = scale;
+  fp.local = p->local;
+  fp.epoch = p->epoch + 1;
+  fp.timeout_ns = p->timeout_ns;
+  // Pipeline stages only wait on each other; give them more room than the
+  // counter waits so that a missing chunk is reported as such.
+  fp.pipe_timeout_ns = p->timeout_ns * 4 > 2000000000ull ? p->timeout_ns * 4 : 2000000000ull;
+  fp.debug_skip_item = (p->debug_flags & AG_GEMM_DEBUG_SKIP_ITEM) ? p->debug_arg : -1;
+  fp.debug_delay_ns = (p->debug_flags & AG_GEMM_DEBUG_DELAY_NS)
+                          ? static_cast<uint32_t>(p->debug_arg > 1000000 ? 1000000 : p->debug_arg)
+                          : 0u;
+
+  const int mode = p->mode;
+  const bool runs_gemm = mode != AG_GEMM_MODE_COPY_ONLY;
+  const bool runs_copy = mode != AG_GEMM_MODE_COMPUTE_ONLY && g.S > 1;
+  if (runs_copy && (p->debug_flags & AG_GEMM_DEBUG_POISON_STAGING)) {
+    // fp16 0x7E7E is a NaN: a tile read before its chunk landed turns C into NaN.
+    e = cudaMemsetAsync(p->staging, 0x7E, static_cast<size_t>(p->staging_bytes), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "poison staging");
+  }
+  if (int8 && runs_gemm) {
+    e = agg::launch_widen(static_cast<const int8_t*>(B), p->b16, g.K * g.N,
+                          static_cast<const int8_t*>(local_ptr), p->a16, g.R * g.K,
+                          p->sm_count * 4, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "int8 widen launch");
+  }
+  using namespace agg;
+  switch (mode) {
+    case AG_GEMM_MODE_PIPELINED:
+      rc = launch_fused(p, fp, kFlagGemm | kFlagWait | (runs_copy ? kFlagCopy : 0), stream);
+      break;
+    case AG_GEMM_MODE_COMPUTE_ONLY:
+      rc = launch_fused(p, fp, kFlagGemm, stream);
+      break;
+    case AG_GEMM_MODE_SEQUENTIAL:
+      rc = runs_copy ? launch_fused(p, fp, kFlagCopy, stream) : AG_GEMM_OK;
+      if (rc == AG_GEMM_OK) rc = launch_fused(p, fp, kFlagGemm | kFlagWait, stream);
+      break;
+    case AG_GEMM_MODE_COPY_ONLY:
+      rc = runs_copy ? launch_fused(p, fp, kFlagCopy, stream) : AG_GEMM_OK;
+      break;
+    default:
+      rc = fail(AG_GEMM_ERR_STATE, "unknown mode %d", mode);
+  }
+  if (rc != AG_GEMM_OK) return rc;
+  // The counters advanced only if copies ran; compute-only runs leave them as they are.
+  if (runs_copy) p->epoch += 1;
+  e = cudaEventRecord(p->done, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  p->last_stream = stream;
+  p->has_run = true;
+  return AG_GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t ag_gemm_choose_chunk_rows(int64_t R) {
+  if (R < 1) return fail(AG_GEMM_ERR_INVALID, "R must be positive");
+  return agg::choose_chunk_rows(R);
+}
+
+int ag_gemm_validate(int n_shards, int64_t M, int64_t K, int64_t N, int dtype,
+                     int64_t chunk_rows) {
+  return check_problem(n_shards, M, K, N, dtype, chunk_rows);
+}
+
+int ag_gemm_geometry_of(int n_shards, int64_t M, int64_t K, int64_t N, int dtype,
+                        int64_t chunk_rows, ag_gemm_geometry* out) {
+  if (!out) return fail(AG_GEMM_ERR_INVALID, "out is NULL");
+  int rc = check_problem(n_shards, M, K, N, dtype, chunk_rows);
+  if (rc != AG_GEMM_OK) return rc;
+  Geometry g;
+  agg::make_geometry(g, n_shards, M, K, N, dtype, chunk_rows);
+  to_public(g, out);
+  return AG_GEMM_OK;
+}
+
+int ag_gemm_tile_at(const ag_gemm_geometry* geo, int local_rank, int64_t t, int64_t out[3]) {
+  Geometry g;
+  if (!out || !from_public(geo, g)) return fail(AG_GEMM_ERR_INVALID, "bad geometry");
+  if (local_rank < 0 || local_rank >= g.S || t < 0 || t >= g.tiles)
+    return fail(AG_GEMM_ERR_INVALID, "tile or local rank out of range");
+  int pos;
+  int64_t mt, nt;
+  agg::tile_coords(g, t, pos, mt, nt);
+  out[0] = agg::source_of(g, local_rank, pos);
+  out[1] = mt;
+  out[2] = nt;
+  return AG_GEMM_OK;
+}
+
+int ag_gemm_item_at(const ag_gemm_geometry* geo, int local_rank, int64_t i, int64_t out[4]) {
+  Geometry g;
+  if (!out || !from_public(geo, g)) return fail(AG_GEMM_ERR_INVALID, "bad geometry");
+  if (local_rank < 0 || local_rank >= g.S || i < 0 || i >= g.items)
+    return fail(AG_GEMM_ERR_INVALID, "item or local rank out of range");
+  int pos, piece;
+  int64_t q, v0, v1;
+  agg::item_coords(g, i, pos, q, piece, v0, v1);
+  const int64_t chunk0 = q * g.c * g.K * g.src_esize;
+  out[0] = agg::source_of(g, local_rank, pos);
+  out[1] = q;
+  out[2] = chunk0 + v0 * 16;
+  out[3] = chunk0 + v1 * 16;
+  return AG_GEMM_OK;
+}
+
+}  // extern "C"
+
+extern "C" {
+
+ag_gemm_plan* ag_gemm_plan_create(int n_shards, int64_t M, int64_t K, int64_t N, int dtype,
+                                  int64_t chunk_rows) {
+  if (check_problem(n_shards, M, K, N, dtype, chunk_rows) != AG_GEMM_OK) return nullptr;
+  ag_gemm_plan* p = new (std::nothrow) ag_gemm_plan();
+  if (!p) {
+    fail(AG_GEMM_ERR_OOM, "host allocation failed");
+    return nullptr;
+  }
+  agg::make_geometry(p->g, n_shards, M, K, N, dtype, chunk_rows);
+  const Geometry& g = p->g;
+  cudaError_t e;
+  int major = 0, minor = 0;
+  if ((e = cudaGetDevice(&p->device)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, p->device)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, p->device)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, p->device)) != cudaSuccess) {
+    cuda_fail(e, "device query");
+    delete p;
+    return nullptr;
+  }
+  if (major != 10 || minor != 3) {
+    fail(AG_GEMM_ERR_UNSUPPORTED, "needs an sm_103 (GB300) device, found sm_%d%d", major, minor);
+    delete p;
+    return nullptr;
+  }
+  int blocks = 0;
+  if ((e = agg::fused_max_blocks_per_sm(dtype, &blocks)) != cudaSuccess || blocks < 1) {
+    if (e == cudaSuccess) fail(AG_GEMM_ERR_UNSUPPORTED, "fused kernel does not fit on an SM");
+    else cuda_fail(e, "fused kernel occupancy");
+    delete p;
+    return nullptr;
+  }
+  p->grid = p->sm_count;  // one CTA per SM; all co-resident (cooperative launch)
+  const int64_t slots = g.S > 1 ? g.S - 1 : 1;
+  p->staging_bytes = slots * g.R * g.K * 2;
+  p->counter_count = slots * g.Q;
+  if ((e = cudaMalloc(&p->staging, p->staging_bytes)) != cudaSuccess ||
+      (e = cudaMalloc(&p->counters, sizeof(uint32_t) * p->counter_count)) != cudaSuccess ||
+      (e = cudaMalloc(&p->status, 2 * sizeof(uint32_t))) != cudaSuccess ||
+      (e = cudaMemset(p->counters, 0, sizeof(uint32_t) * p->counter_count)) != cudaSuccess ||
+      (e = cudaMemset(p->status, 0, 2 * sizeof(uint32_t))) != cudaSuccess ||
+      (e = cudaEventCreateWithFlags(&p->done, cudaEventDisableTiming)) != cudaSuccess) {
+    cuda_fail(e, "plan allocation");
+    free_plan(p);
+    return nullptr;
+  }
+  if (dtype == AG_GEMM_I8) {
+    if ((e = cudaMalloc(&p->b16, static_cast<size_t>(g.K * g.N * 2))) != cudaSuccess ||
+        (e = cudaMalloc(&p->a16, static_cast<size_t>(g.R * g.K * 2))) != cudaSuccess) {
+      cuda_fail(e, "plan allocation (int8 widening buffers)");
+      free_plan(p);
+      return nullptr;
+    }
+    if (encode_a(&p->tm_a16, p->a16, g.R, g.K) != AG_GEMM_OK ||
+        encode_b(&p->tm_b16, p->b16, g.K, g.N) != AG_GEMM_OK) {
+      free_plan(p);
+      return nullptr;
+    }
+  }
+  if (encode_stage(&p->tm_stage, p->staging, slots, g.R, g.K) != AG_GEMM_OK) {
+    free_plan(p);
+    return nullptr;
+  }
+  return p;
+}
+
+void ag_gemm_plan_destroy(ag_gemm_plan* plan) {
+  if (!plan) return;
+  DeviceGuard dg(plan->device);
+  free_plan(plan);
+}
+
+int ag_gemm_plan_geometry(const ag_gemm_plan* plan, ag_gemm_geometry* out) {
+  if (!plan || !out) return fail(AG_GEMM_ERR_INVALID, "plan or out is NULL");
+  to_public(plan->g, out);
+  return AG_GEMM_OK;
+}
+
+int64_t ag_gemm_plan_chunk_rows(const ag_gemm_plan* plan) {
+  if (!plan) return fail(AG_GEMM_ERR_INVALID, "plan is NULL");
+  return plan->g.c;
+}
+
+int ag_gemm_plan_grid(const ag_gemm_plan* plan) {
+  if (!plan) return fail(AG_GEMM_ERR_INVALID, "plan is NULL");
+  return plan->grid;
+}
+
+int ag_gemm_run(ag_gemm_plan* plan, const void* const* shard_ptrs, const void* B, float* C,
+                void* stream) {
+  if (!plan) return fail(AG_GEMM_ERR_INVALID, "plan is NULL");
+  if (plan->g.dtype != AG_GEMM_F16)
+    return fail(AG_GEMM_ERR_INVALID, "ag_gemm_run needs an fp16 plan (use ag_gemm_dequant_run)");
+  return run_impl(plan, shard_ptrs, B, C, nullptr, nullptr, nullptr, nullptr, stream);
+}
+
+int ag_gemm_dequant_run(ag_gemm_plan* plan, const void* const* shard_ptrs, const void* B,
+                        const int32_t* bias, const float* scale, int32_t* C_i32, void* D_f16,
+                        void* stream) {
+  if (!plan) return fail(AG_GEMM_ERR_INVALID, "plan is NULL");
+  if (plan->g.dtype != AG_GEMM_I8)
+    return fail(AG_GEMM_ERR_INVALID, "ag_gemm_dequant_run needs an int8 plan");
+  return run_impl(plan, shard_ptrs, B, nullptr, C_i32, D_f16, bias, scale, stream);
+}
+
+int64_t ag_gemm_plan_status_word(ag_gemm_plan* plan) {
+  if (!plan) return fail(AG_GEMM_ERR_INVALID, "plan is NULL");
+  DeviceGuard dg(plan->device);
+  cudaError_t e;
+  if (plan->has_run && (e = cudaEventSynchronize(plan->done)) != cudaSuccess)
+    return cuda_fail(e, "cudaEventSynchronize");
+  uint32_t w[2] = {0, 0};
+  if ((e = cudaMemcpy(w, plan->status, sizeof(w), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "status read");
+  return static_cast<int64_t>(w[0]) | (static_cast<int64_t>(w[1]) << 32);
+}
+
+int ag_gemm_plan_status(ag_gemm_plan* plan) {
+  int64_t w = ag_gemm_plan_status_word(plan);
+  if (w < 0) return static_cast<int>(w);
+  const uint32_t kind = static_cast<uint32_t>(w & 0xFF);
+  if (kind == agg::kStatusOk) return AG_GEMM_OK;
+  return fail(AG_GEMM_ERR_TIMEOUT, "device wait timed out (status 0x%llx)", (unsigned long long)w);
+}
+
+int ag_gemm_plan_reset(ag_gemm_plan* plan, void* stream_v) {
+  if (!plan) return fail(AG_GEMM_ERR_INVALID, "plan is NULL");
+  DeviceGuard dg(plan->device);
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  cudaError_t e;
+  if (plan->has_run && plan->last_stream != stream &&
+      (e = cudaStreamWaitEvent(stream, plan->done, 0)) != cudaSuccess)
+    return cuda_fail(e, "cudaStreamWaitEvent");
+  if ((e = cudaMemsetAsync(plan->counters, 0, sizeof(uint32_t) * plan->counter_count, stream)) != cudaSuccess ||
+      (e = cudaMemsetAsync(plan->status, 0, 2 * sizeof(uint32_t), stream)) != cudaSuccess ||
+      (e = cudaEventRecord(plan->done, stream)) != cudaSuccess)
+    return cuda_fail(e, "plan reset");
+  plan->epoch = 0;
+  plan->last_stream = stream;
+  plan->has_run = true;
+  return AG_GEMM_OK;
+}
+
+int ag_gemm_plan_set_mode(ag_gemm_plan* plan, int mode) {
+  if (!plan) return fail(AG_GEMM_ERR_INVALID, "plan is NULL");
+  if (mode < AG_GEMM_MODE_PIPELINED || mode > AG_GEMM_MODE_COPY_ONLY)
+    return fail(AG_GEMM_ERR_INVALID, "unknown mode %d", mode);
+  plan->mode = mode;
+  return AG_GEMM_OK;
+}
+
+int ag_gemm_plan_set_local_rank(ag_gemm_plan* plan, int local_rank) {
+  if (!plan) return fail(AG_GEMM_ERR_INVALID, "plan is NULL");
+  if (local_rank < 0 || local_rank >= plan->g.S)
+    return fail(AG_GEMM_ERR_INVALID, "local_rank %d out of [0, %d)", local_rank, plan->g.S);
+  plan->local = local_rank;
+  return AG_GEMM_OK;
+}
+
+int ag_gemm_plan_set_timeout_ns(ag_gemm_plan* plan, int64_t ns) {
+  if (!plan) return fail(AG_GEMM_ERR_INVALID, "plan is NULL");
+  if (ns <= 0) return fail(AG_GEMM_ERR_INVALID, "timeout must be positive");
+  plan->timeout_ns = static_cast<uint64_t>(ns);
+  return AG_GEMM_OK;
+}
+
+int ag_gemm_plan_set_debug(ag_gemm_plan* plan, int flags, int64_t arg) {
+  if (!plan) return fail(AG_GEMM_ERR_INVALID, "plan is NULL");
+  if (flags & ~(AG_GEMM_DEBUG_POISON_STAGING | AG_GEMM_DEBUG_SKIP_ITEM | AG_GEMM_DEBUG_DELAY_NS))
+    return fail(AG_GEMM_ERR_INVALID, "unknown debug flags 0x%x", flags);
+  if ((flags & AG_GEMM_DEBUG_SKIP_ITEM) && (flags & AG_GEMM_DEBUG_DELAY_NS))
+    return fail(AG_GEMM_ERR_INVALID, "SKIP_ITEM and DELAY_NS share `arg`; set one at a time");
+  if (arg < 0) return fail(AG_GEMM_ERR_INVALID, "arg must be >= 0");
+  plan->debug_flags = flags;
+  plan->debug_arg = arg;
+  return AG_GEMM_OK;
+}
+
+int ag_gemm_last_error(void) { return g_last_error; }
+
+const char* ag_gemm_last_error_message(void) { return g_last_msg; }
+
+}  // extern "C"

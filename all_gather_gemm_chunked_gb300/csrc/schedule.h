@@ -1,0 +1,120 @@
+// schedule.h -- problem geometry, persistent tile order and producer copy
+// items of the streamed AllGather+GEMM.  Used by the host plan code and by the
+// device kernels, so that both walk exactly the same schedule.
+#pragma once
+
+#include <stdint.h>
+
+#if defined(__CUDACC__)
+#define AGG_HD __host__ __device__ __forceinline__
+#else
+#define AGG_HD inline
+#endif
+
+namespace agg {
+
+constexpr int kMaxShards = 64;
+constexpr int kBlockM = 128;        // rows of a CTA tile (one TMEM lane per row)
+constexpr int kBlockK = 64;         // fp16 elements per k-block: one 128-byte swizzle row
+constexpr int kUmmaK = 16;          // K of one tcgen05.mma kind::f16
+constexpr int kStages = 4;          // TMA -> MMA shared-memory ring depth
+constexpr int kMaxBlockN = 256;
+constexpr int kGroupM = 8;          // m-tiles per swizzle group
+// int8 emulation: |a*b| <= 127^2 = 16129 and 16 k-blocks = 1024 terms keep every
+// fp32 partial sum an integer below 2^24, hence exact.
+constexpr int kSegBlocks = 16;
+constexpr int64_t kPieceBytes = 32 * 1024;  // target source bytes per copy item
+constexpr int64_t kMaxKI8 = 133000;
+
+struct Geometry {
+  int S;
+  int dtype;             // 0 = f16, 1 = i8
+  int64_t M, K, N, R;
+  int64_t c;             // chunk rows
+  int64_t Q;             // chunks per source
+  int P;                 // copy items (pieces) per chunk
+  int BN;                // block_n
+  int64_t MT, NT;        // m-tiles per source, n-tiles
+  int64_t tiles;
+  int64_t KB;            // k-blocks
+  int64_t items;         // producer copy items
+  int64_t src_esize;     // bytes per source element (2 for f16, 1 for i8)
+};
+
+AGG_HD int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ComputeOptimalChunkSize analogue: 64..128 chunks per source.
+AGG_HD int64_t choose_chunk_rows(int64_t R) {
+  if (R < 1) return -1;
+  if (R < 64) return 1;
+  for (int64_t q = 64; q <= 128; ++q)
+    if (R % q == 0) return R / q;
+  int64_t best = 1;
+  for (int64_t c = 1; c <= R / 64; ++c)
+    if (R % c == 0) best = c;
+  return best;
+}
+
+AGG_HD void make_geometry(Geometry& g, int S, int64_t M, int64_t K, int64_t N,
+                          int dtype, int64_t chunk_rows) {
+  g.S = S; g.dtype = dtype; g.M = M; g.K = K; g.N = N;
+  g.R = M / S;
+  g.c = chunk_rows > 0 ? chunk_rows : choose_chunk_rows(g.R);
+  g.Q = g.R / g.c;
+  g.src_esize = dtype == 1 ? 1 : 2;
+  int64_t chunk_bytes = g.c * K * g.src_esize;
+  int64_t p = ceil_div(chunk_bytes, kPieceBytes);
+  int64_t vecs = chunk_bytes / 16;
+  if (p > vecs) p = vecs;
+  if (p < 1) p = 1;
+  g.P = (int)p;
+  g.BN = N <= 128 ? 128 : 256;
+  g.MT = ceil_div(g.R, kBlockM);
+  g.NT = ceil_div(N, g.BN);
+  g.tiles = (int64_t)S * g.MT * g.NT;
+  g.KB = ceil_div(K, kBlockK);
+  g.items = (int64_t)(S - 1) * g.Q * g.P;
+}
+
+// Tile t -> (consumption position, m-tile, n-tile).  Position 0 is the local
+// shard; within a position, groups of kGroupM m-tiles are walked m-fastest.
+AGG_HD void tile_coords(const Geometry& g, int64_t t, int& pos, int64_t& mt,
+                        int64_t& nt) {
+  int64_t per = g.MT * g.NT;
+  pos = (int)(t / per);
+  int64_t u = t - (int64_t)pos * per;
+  int64_t group = (int64_t)kGroupM * g.NT;
+  int64_t first_m = (u / group) * kGroupM;
+  int64_t gm = g.MT - first_m < kGroupM ? g.MT - first_m : kGroupM;
+  int64_t w = u % group;
+  mt = first_m + w % gm;
+  nt = w / gm;
+}
+
+AGG_HD int source_of(const Geometry& g, int local, int pos) {
+  return (local + pos) % g.S;
+}
+
+// Copy item i -> (consumption position >= 1, chunk q, piece p) and the
+// 16-byte-vector range [v0, v1) of the source chunk it covers.
+AGG_HD void item_coords(const Geometry& g, int64_t i, int& pos, int64_t& q,
+                        int& piece, int64_t& v0, int64_t& v1) {
+  int64_t per_pos = g.Q * g.P;
+  pos = 1 + (int)(i / per_pos);
+  int64_t r = i - (int64_t)(pos - 1) * per_pos;
+  q = r / g.P;
+  piece = (int)(r - q * g.P);
+  int64_t vecs = g.c * g.K * g.src_esize / 16;
+  v0 = vecs * piece / g.P;
+  v1 = vecs * (piece + 1) / g.P;
+}
+
+// Chunks [q0, q1] of a source that an m-tile reads.
+AGG_HD void tile_chunks(const Geometry& g, int64_t mt, int64_t& q0, int64_t& q1) {
+  int64_t r0 = mt * kBlockM;
+  int64_t r1 = r0 + kBlockM < g.R ? r0 + kBlockM : g.R;
+  q0 = r0 / g.c;
+  q1 = (r1 - 1) / g.c;
+}
+
+}  // namespace agg

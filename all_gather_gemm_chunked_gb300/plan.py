@@ -1,0 +1,130 @@
+"""Torch-tensor front end of the C ABI: checks tensors and passes their device
+pointers and the current CUDA stream to libaggemm.so.  No arithmetic here."""
+from __future__ import annotations
+
+import torch
+
+from . import binding as B_
+
+_DTYPES = {"f16": B_.F16, "i8": B_.I8}
+
+
+def _stream_handle(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def _check(t: torch.Tensor, name: str, dtype, shape):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be on a CUDA device")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+class Plan:
+    """One AllGather+GEMM problem: owns the library plan (staging, counters)."""
+
+    def __init__(self, n_shards: int, M: int, K: int, N: int, dtype: str = "f16",
+                 chunk_rows: int = 0):
+        if dtype not in _DTYPES:
+            raise ValueError("dtype must be 'f16' or 'i8'")
+        self.n_shards, self.M, self.K, self.N, self.dtype = n_shards, M, K, N, dtype
+        self.R = M // n_shards if n_shards else 0
+        self.handle = B_.ag_gemm_plan_create(n_shards, M, K, N, _DTYPES[dtype], chunk_rows)
+
+    # -- lifecycle
+    def close(self):
+        if getattr(self, "handle", None):
+            B_.ag_gemm_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    # -- knobs
+    @property
+    def geometry(self) -> dict:
+        return B_.ag_gemm_plan_geometry(self.handle).as_dict()
+
+    @property
+    def chunk_rows(self) -> int:
+        return B_.ag_gemm_plan_chunk_rows(self.handle)
+
+    @property
+    def grid(self) -> int:
+        return B_.ag_gemm_plan_grid(self.handle)
+
+    def set_mode(self, mode: int):
+        B_.ag_gemm_plan_set_mode(self.handle, mode)
+
+    def set_local_rank(self, r: int):
+        B_.ag_gemm_plan_set_local_rank(self.handle, r)
+
+    def set_timeout_ns(self, ns: int):
+        B_.ag_gemm_plan_set_timeout_ns(self.handle, ns)
+
+    def set_debug(self, flags: int, arg: int = 0):
+        B_.ag_gemm_plan_set_debug(self.handle, flags, arg)
+
+    def status(self) -> int:
+        return B_.ag_gemm_plan_status(self.handle)
+
+    def status_word(self) -> int:
+        return B_.ag_gemm_plan_status_word(self.handle)
+
+    def reset(self, stream=None):
+        B_.ag_gemm_plan_reset(self.handle, _stream_handle(stream))
+
+    # -- runs
+    def run(self, shards, B, C=None, stream=None) -> torch.Tensor:
+        """C (M x N fp32) = AllGather(shards) x B for fp16 shards (R x K) and B (K x N)."""
+        if self.dtype != "f16":
+            raise ValueError("run() needs an f16 plan")
+        if len(shards) != self.n_shards:
+            raise ValueError(f"expected {self.n_shards} shards")
+        for i, s in enumerate(shards):
+            _check(s, f"shards[{i}]", torch.float16, (self.R, self.K))
+        _check(B, "B", torch.float16, (self.K, self.N))
+        if C is None:
+            C = torch.empty((self.M, self.N), dtype=torch.float32, device=B.device)
+        _check(C, "C", torch.float32, (self.M, self.N))
+        B_.ag_gemm_run(self.handle, [s.data_ptr() for s in shards], B.data_ptr(), C.data_ptr(),
+                       _stream_handle(stream))
+        return C
+
+    def dequant_run(self, shards, B, bias, scale, C_i32=None, D=None, stream=None):
+        """(C_i32, D) of the int8 AllGatherMatmulDequant for int8 shards and B."""
+        if self.dtype != "i8":
+            raise ValueError("dequant_run() needs an i8 plan")
+        if len(shards) != self.n_shards:
+            raise ValueError(f"expected {self.n_shards} shards")
+        for i, s in enumerate(shards):
+            _check(s, f"shards[{i}]", torch.int8, (self.R, self.K))
+        _check(B, "B", torch.int8, (self.K, self.N))
+        _check(bias, "bias", torch.int32, (self.N,))
+        _check(scale, "scale", torch.float32, (self.N,))
+        if C_i32 is None:
+            C_i32 = torch.empty((self.M, self.N), dtype=torch.int32, device=B.device)
+        if D is None:
+            D = torch.empty((self.M, self.N), dtype=torch.float16, device=B.device)
+        _check(C_i32, "C_i32", torch.int32, (self.M, self.N))
+        _check(D, "D", torch.float16, (self.M, self.N))
+        B_.ag_gemm_dequant_run(self.handle, [s.data_ptr() for s in shards], B.data_ptr(),
+                               bias.data_ptr(), scale.data_ptr(), C_i32.data_ptr(), D.data_ptr(),
+                               _stream_handle(stream))
+        return C_i32, D

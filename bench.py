@@ -1,0 +1,435 @@
+"""Benchmark of the streamed AllGather+GEMM on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 2] [--impl ours|reference]
+
+Metric: streamed gather+GEMM throughput 2*M*N*K / t in TFLOP/s (TOP/s for the
+int8 workloads), where t is the device time of one run (PIPELINED mode: chunk
+copies and GEMM concurrently, one cooperative launch for fp16) on inputs
+already resident in HBM.  L2 is flushed (512 MiB write) before every timed
+step, outside the timed events.  One JSON line is printed by rank 0.
+
+N > 1 (torchrun): every rank runs its own full replica of the workload on its
+own GPU (the shards are simulated ranks inside one GPU, so nothing is
+exchanged between GPUs); the step time is the max over ranks and `value` is
+the whole-job throughput N * flops / t_max ("scaling": "weak").
+
+--impl reference times the CPU oracle (plain single-threaded C loops) on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "streamed gather+GEMM TFLOPS/TOPS (2MNK/t), % of GB300 dense tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+KERNEL_SOURCES = ["all_gather_gemm_chunked_gb300/csrc/fused_kernel.cu",
+                  "all_gather_gemm_chunked_gb300/csrc/sm103.cuh",
+                  "all_gather_gemm_chunked_gb300/csrc/fused_kernel.cuh",
+                  "all_gather_gemm_chunked_gb300/csrc/schedule.h"]
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (also exercised on CPU with gloo by the tests)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), ws, int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def reduce_max(value: float, device=None) -> float:
+    """Max of a float over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.barrier()
+
+
+def whole_job_value(units_per_rank: float, n_ranks: int, t_max_s: float, scale=1e-12) -> float:
+    """Weak scaling: every rank does units_per_rank; the job takes the slowest rank's time."""
+    return units_per_rank * n_ranks / t_max_s * scale
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload_id: int):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary,
+    if it was taken on the current kernel sources (else None)."""
+    path = os.path.join(PROFILE_DIR, f"traffic_workload{workload_id}.txt")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"kernel_sources_sha256_16\s*=\s*(\w+)", text)
+    m_bytes = re.search(r"dram_bytes_per_launch\s*=\s*([0-9.eE+]+)", text)
+    if not (m_hash and m_bytes) or m_hash.group(1) != kernel_hash():
+        return None
+    return float(m_bytes.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = max(smax, float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        finally:
+            os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_model() -> str:
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part", "hardware")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline and --impl reference)
+# ---------------------------------------------------------------------------
+
+def time_oracle(w, x, budget_s: float, row_block: int = 2):
+    """Run the oracle on whole rows of C (all N columns) until `budget_s` passes."""
+    import oracle
+    oracle.build()
+    rows_done, t0 = 0, time.perf_counter()
+    cols = np.arange(w.N, dtype=np.int64)
+    while True:
+        rows = np.arange(rows_done, rows_done + row_block) % w.M
+        rr = np.repeat(rows, w.N)
+        cc = np.tile(cols, row_block)
+        if w.dtype == "f16":
+            oracle.ag_gemm_f16_at(x["shards"], x["B"], rr, cc)
+        else:
+            oracle.ag_gemm_dequant_at(x["shards"], x["B"], x["bias"], x["scale"], rr, cc)
+        rows_done += row_block
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    ops = 2.0 * rows_done * w.N * w.K
+    return ops / el * 1e-12, rows_done, el
+
+
+def run_reference(args, w, rank):
+    if rank != 0:
+        return 0
+    from all_gather_gemm_chunked_gb300 import synth
+    x = synth.workload_inputs(w)
+    per_step = []
+    rows_total = 0
+    # one untimed warm-up sample, then K bounded samples
+    for i in range(args.warmup + args.steps):
+        v, rows, el = time_oracle(w, x, budget_s=args.ref_step_seconds)
+        if i >= args.warmup:
+            per_step.append(el / rows)
+            rows_total += rows
+    s_per_row = float(np.mean(per_step))
+    value = 2.0 * w.N * w.K / s_per_row * 1e-12
+    unit = "TFLOP/s" if w.dtype == "f16" else "TOP/s"
+    full_ms = s_per_row * w.M * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": unit,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": full_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64" if w.dtype == "f16" else "int64",
+        "data": "synthetic", "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
+                         "sample": f"{rows_total} whole rows of C over {args.steps} steps "
+                                   f"(~{args.ref_step_seconds:.0f} s each); ms_per_step is "
+                                   f"the extrapolated full-workload time",
+                         "cpu": cpu_model()},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w):
+    return {"workload": w.name, "n_shards": w.S, "M": w.M, "K": w.K, "N": w.N,
+            "dtype": w.dtype, "chunk_rows": w.chunk_rows or "auto",
+            "l2": "flushed before each timed step (512 MiB write)"}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, w, rank, world, local_rank):
+    import torch
+
+    from all_gather_gemm_chunked_gb300 import binding as B_
+    from all_gather_gemm_chunked_gb300 import synth
+    from all_gather_gemm_chunked_gb300.plan import Plan
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    x = synth.workload_inputs(w)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    h_shards = [pin(s) for s in x["shards"]]
+    h_B = pin(x["B"])
+    shards = [t.to(dev) for t in h_shards]
+    Bd = h_B.to(dev)
+    int8 = w.dtype == "i8"
+    if int8:
+        h_bias, h_scale = pin(x["bias"]), pin(x["scale"])
+        bias, scale = h_bias.to(dev), h_scale.to(dev)
+        Ci = torch.empty((w.M, w.N), dtype=torch.int32, device=dev)
+        D = torch.empty((w.M, w.N), dtype=torch.float16, device=dev)
+        h_Ci = torch.empty((w.M, w.N), dtype=torch.int32).pin_memory()
+        h_D = torch.empty((w.M, w.N), dtype=torch.float16).pin_memory()
+    else:
+        C = torch.empty((w.M, w.N), dtype=torch.float32, device=dev)
+        h_C = torch.empty((w.M, w.N), dtype=torch.float32).pin_memory()
+    plan = Plan(w.S, w.M, w.K, w.N, w.dtype, w.chunk_rows)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        if int8:
+            plan.dequant_run(shards, Bd, bias, scale, Ci, D)
+        else:
+            plan.run(shards, Bd, C)
+
+    def timed(n, mode, fn=step):
+        plan.set_mode(mode)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        for a, b in evs:
+            flush.fill_(1.0)
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        return [a.elapsed_time(b) for a, b in evs]
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    if plan.status() != 0:
+        raise RuntimeError(f"warm-up run failed: status {plan.status_word():#x}")
+
+    clocks = ClockSampler(local_rank)
+    barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    times_ms = timed(args.steps, B_.MODE_PIPELINED)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    barrier()
+    status = plan.status()
+    if status != 0:
+        raise RuntimeError(f"timed runs failed: status {plan.status_word():#x}")
+    t_local = float(np.sum(times_ms)) / 1e3
+    t_max = reduce_max(t_local, dev)
+    ms_per_step = t_max / args.steps * 1e3
+    value = whole_job_value(w.flops * args.steps, world, t_max)
+
+    # the other run modes (context: overlap of copy and GEMM)
+    modes = {}
+    if not args.no_modes:
+        nm = max(3, min(args.steps, 10))
+        t_compute = float(np.median(timed(nm, B_.MODE_COMPUTE_ONLY)))
+        t_copy = float(np.median(timed(nm, B_.MODE_COPY_ONLY)))
+        t_seq = float(np.median(timed(nm, B_.MODE_SEQUENTIAL)))
+        t_pipe = float(np.median(times_ms))
+        overlap = (t_copy + t_compute - t_pipe) / max(min(t_copy, t_compute), 1e-9)
+        modes = {"pipelined_ms": t_pipe, "compute_only_ms": t_compute, "copy_only_ms": t_copy,
+                 "sequential_ms": t_seq, "overlap_efficiency": overlap,
+                 "speedup_vs_sequential": t_seq / t_pipe}
+        plan.set_mode(B_.MODE_PIPELINED)
+
+    # end to end through the C ABI with host buffers
+    def e2e_step():
+        for hs, ds in zip(h_shards, shards):
+            ds.copy_(hs, non_blocking=True)
+        Bd.copy_(h_B, non_blocking=True)
+        if int8:
+            bias.copy_(h_bias, non_blocking=True)
+            scale.copy_(h_scale, non_blocking=True)
+        step()
+        if int8:
+            h_Ci.copy_(Ci, non_blocking=True)
+            h_D.copy_(D, non_blocking=True)
+        else:
+            h_C.copy_(C, non_blocking=True)
+
+    ne = max(3, min(args.steps, 10))
+    e2e_ms = timed(ne, B_.MODE_PIPELINED, e2e_step)
+    e2e_t = reduce_max(float(np.sum(e2e_ms)) / 1e3, dev)
+    h2d = sum(t.numel() * t.element_size() for t in h_shards) + h_B.numel() * h_B.element_size()
+    if int8:
+        h2d += h_bias.numel() * 4 + h_scale.numel() * 4
+        d2h = h_Ci.numel() * 4 + h_D.numel() * 2
+    else:
+        d2h = h_C.numel() * 4
+    unit = "TOP/s" if int8 else "TFLOP/s"
+    e2e = {"value": whole_job_value(w.flops * ne, world, e2e_t), "unit": unit,
+           "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    peaks, peak_src = load_peaks()
+    # the fused kernel is a dense fp16 contraction: its peak is the measured dense
+    # bf16 figure (fp16 and bf16 share the same nominal dense rate)
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    traffic = profiled_traffic(w.wid)
+    # per-launch time of the dominant (fused) kernel: for fp16 one run is exactly
+    # one launch; for int8 a run also launches the widening kernel first
+    launches_per_run = 2 if int8 else 1
+    kernel_ms = float(np.mean(times_ms))
+    achieved = w.flops / (kernel_ms * 1e-3) * 1e-12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "peak_source": f"{peak_src} bf16 dense burst (fp16 dense = bf16 dense nominal)",
+                "kernel": "ag_fused_kernel" + ("<int8> + widen_kernel" if int8 else "<fp16>")}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v, rows, el = time_oracle(w, x, budget_s=args.cpu_seconds)
+        cpu = {"value": v, "unit": unit, "cores": 1, "kind": "oracle",
+               "sample": f"{rows} whole rows of C ({rows * w.N} outputs), {el:.1f} s",
+               "cpu": cpu_model()}
+
+    plan.close()
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "i8" if int8 else "f16", "data": "synthetic",
+        "config": workload_config(w),
+        "pct_of_peak": 100.0 * value / world / peak,
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
+        "gpu_launches": launches_per_run * args.steps, "modes": modes,
+        "grid": B_.ag_gemm_geometry_of(w.S, w.M, w.K, w.N, 1 if int8 else 0,
+                                        w.chunk_rows).as_dict(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=4.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-modes", action="store_true")
+    args = ap.parse_args(argv)
+
+    from all_gather_gemm_chunked_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, w, rank)
+        return run_ours(args, w, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            if dist.is_initialized():
+                dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

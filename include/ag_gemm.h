@@ -1,0 +1,237 @@
+/*
+ * ag_gemm.h -- C ABI of the GB300 (sm_103a) streamed AllGather+GEMM library
+ * (libaggemm.so).
+ *
+ * What it computes
+ *   C = AllGather(A) x B.  A (M x K) arrives as n_shards row shards of
+ *   R = M / n_shards rows each; shard s owns global rows [s*R, (s+1)*R).
+ *   B (K x N) is replicated.  Each shard is cut into chunks of chunk_rows rows
+ *   and the GEMM consumes a chunk as soon as it has landed, instead of after
+ *   the whole gather ("AllGather + GEMM 通算融合算子示例", sections 计算功能
+ *   and 流式流水线).  One GPU holds every shard ("simulated ranks"): the local
+ *   shard is read in place, every other shard is copied chunk by chunk into a
+ *   plan-owned staging workspace, and a per-chunk ready counter is released
+ *   after each copy.
+ *
+ *   fp16 path (ag_gemm_run): fp16 A and B, fp32 accumulation, fp32 C.
+ *   int8 path (ag_gemm_dequant_run), "AllGather矩阵乘法反量化算子设计文档"
+ *   sections 1.2 and 2.2:
+ *       C_i32[m][n] = sum_k A[m][k] * B[k][n] + bias[n]          (exact int32)
+ *       D[m][n]     = fp16_rn( fp32_rn( fp32_rn(C_i32[m][n]) * scale[n] ) )
+ *
+ * Conventions (every entry point)
+ *   - Matrices are dense and row-major: shard s is R x K, B is K x N, C, C_i32
+ *     and D are M x N.  Row m of C belongs to shard m / R.
+ *   - All matrix, vector and workspace pointers are DEVICE pointers of the
+ *     current CUDA device; shard_ptrs itself is a HOST array of n_shards
+ *     device pointers.  The caller owns every pointer it passes; the library
+ *     never frees them and keeps none of them after the call returns
+ *     (except as keys of a cache of TMA descriptors).
+ *   - Every device pointer must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Runs
+ *     are asynchronous: on return the work is enqueued on `stream`, and any
+ *     later work on `stream` observes C (and C_i32 / D) complete.  Runs on one
+ *     plan are serialised by the library: a run on a different stream first
+ *     waits for the plan's previous run.
+ *   - Errors are returned as negative ag_gemm_status codes (or NULL from
+ *     ag_gemm_plan_create); the thread-local ag_gemm_last_error() and
+ *     ag_gemm_last_error_message() describe the last failure.  Nothing aborts
+ *     and no C++ exception crosses this boundary.
+ */
+#ifndef AG_GEMM_H
+#define AG_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct ag_gemm_plan ag_gemm_plan;
+
+typedef enum {
+    AG_GEMM_F16 = 0, /* fp16 x fp16 -> fp32 */
+    AG_GEMM_I8 = 1   /* int8 x int8 -> int32 (+bias) -> fp16 dequant */
+} ag_gemm_dtype;
+
+typedef enum {
+    AG_GEMM_OK = 0,
+    AG_GEMM_ERR_INVALID = -1,     /* bad shape, pointer, alignment or argument */
+    AG_GEMM_ERR_UNSUPPORTED = -2, /* not an sm_103 device, or a size limit */
+    AG_GEMM_ERR_CUDA = -3,        /* a CUDA runtime/driver call failed */
+    AG_GEMM_ERR_OOM = -4,         /* device allocation failed */
+    AG_GEMM_ERR_TIMEOUT = -5,     /* a device-side wait ran out (see status) */
+    AG_GEMM_ERR_STATE = -6        /* the call does not fit the plan's state */
+} ag_gemm_status;
+
+/*
+ * Run modes (the three benchmark modes of "AllGather + GEMM 通算融合算子示例",
+ * section Benchmark 与输出说明, plus a copy-only mode):
+ *   PIPELINED    -- chunk copies and GEMM run concurrently; the GEMM waits on
+ *                   each remote chunk's ready counter (the method itself).
+ *   COMPUTE_ONLY -- GEMM only; every chunk is treated as ready and the staging
+ *                   workspace is read as it stands (it must hold the current
+ *                   shards from an earlier run for C to be right).
+ *   SEQUENTIAL   -- all chunk copies complete, then the GEMM runs.
+ *   COPY_ONLY    -- chunk copies only; C is not written.
+ */
+typedef enum {
+    AG_GEMM_MODE_PIPELINED = 0,
+    AG_GEMM_MODE_COMPUTE_ONLY = 1,
+    AG_GEMM_MODE_SEQUENTIAL = 2,
+    AG_GEMM_MODE_COPY_ONLY = 3
+} ag_gemm_mode;
+
+/* Debug knobs for race and failure testing (ag_gemm_plan_set_debug). */
+typedef enum {
+    AG_GEMM_DEBUG_NONE = 0,
+    AG_GEMM_DEBUG_POISON_STAGING = 1, /* fill staging with NaN / 0x7E before each run */
+    AG_GEMM_DEBUG_SKIP_ITEM = 2,      /* producer skips copy item `arg` (its chunk never becomes ready) */
+    AG_GEMM_DEBUG_DELAY_NS = 4        /* producer sleeps `arg` ns before each copy item */
+} ag_gemm_debug_flag;
+
+/* Sizes the library derives from a problem (no GPU needed to compute them). */
+typedef struct {
+    int32_t n_shards;
+    int32_t dtype;
+    int64_t M, K, N, R;
+    int64_t chunk_rows;        /* c: rows per chunk */
+    int64_t chunks_per_source; /* Q = R / c */
+    int32_t pieces_per_chunk;  /* P: copy items per chunk (counter target = epoch * P) */
+    int32_t block_m, block_n, block_k;
+    int32_t group_m;           /* m-tiles per swizzle group */
+    int32_t kseg_blocks;       /* int8 path: k-blocks accumulated in fp32 before an int32 fold */
+    int64_t m_tiles;           /* per source */
+    int64_t n_tiles;
+    int64_t tiles;             /* n_shards * m_tiles * n_tiles */
+    int64_t producer_items;    /* (n_shards - 1) * Q * P */
+    int64_t staging_bytes;     /* plan-owned staging workspace */
+    int64_t workspace_bytes;   /* everything the plan allocates on the device */
+} ag_gemm_geometry;
+
+/*
+ * Chunk size rule (ComputeOptimalChunkSize of "AllGather + GEMM 通算融合算子示例",
+ * section 优化说明: keep 64-128 chunks per source).  For R rows per source:
+ * Q = the smallest divisor of R in [64, 128], c = R / Q; if R has no such
+ * divisor, c = the largest divisor of R with R / c >= 64; if R < 64, c = 1.
+ * Returns c, or AG_GEMM_ERR_INVALID for R < 1.  Pure host function.
+ */
+int64_t ag_gemm_choose_chunk_rows(int64_t R);
+
+/*
+ * Check a problem without touching the GPU: n_shards in [1, 64], M, K, N > 0,
+ * M % n_shards == 0, chunk_rows == 0 (auto) or a divisor of R;
+ * fp16: K % 8 == 0 and N % 8 == 0; int8: K % 16 == 0, N % 16 == 0 and
+ * K <= 133000 (so that K * 127^2 plus a bias stays inside int32).
+ * Returns AG_GEMM_OK or the error code (and sets the last error).
+ */
+int ag_gemm_validate(int n_shards, int64_t M, int64_t K, int64_t N, int dtype,
+                     int64_t chunk_rows);
+
+/* Fill *out with the derived sizes of a valid problem.  Pure host function. */
+int ag_gemm_geometry_of(int n_shards, int64_t M, int64_t K, int64_t N,
+                        int dtype, int64_t chunk_rows, ag_gemm_geometry *out);
+
+/*
+ * Persistent tile schedule, as the kernel walks it.  Tile t in
+ * [0, geometry.tiles) maps to out[0] = source shard (global rank), out[1] =
+ * m-tile within that shard, out[2] = n-tile.  Tiles are ordered by
+ * consumption position p = 0..n_shards-1, where position p holds shard
+ * (local_rank + p) % n_shards: the local shard first with no wait, then the
+ * remote shards in ring order ("Collective matrix multiplication", section
+ * Ring All-Gather: at step i device d computes A_{(d+i) % D}).  Within a
+ * shard, tiles are swizzled in groups of group_m m-tiles.
+ */
+int ag_gemm_tile_at(const ag_gemm_geometry *g, int local_rank, int64_t t,
+                    int64_t out[3]);
+
+/*
+ * Producer copy item i in [0, geometry.producer_items): out[0] = source
+ * shard, out[1] = chunk index q within it, out[2] / out[3] = first / one-past-
+ * last byte of the shard covered by the item.  Items are numbered in
+ * consumption order (the send order equals the consumption order,
+ * "AllGather + GEMM 通算融合算子示例" section 优化说明) and handed to the
+ * producer warps round-robin.
+ */
+int ag_gemm_item_at(const ag_gemm_geometry *g, int local_rank, int64_t i,
+                    int64_t out[4]);
+
+/*
+ * Create a plan on the current CUDA device: validates the problem (as
+ * ag_gemm_validate), requires an sm_103 device, and allocates the staging
+ * workspace ((n_shards-1) x R x K fp16), the per-chunk ready counters and a
+ * status word (plus, for int8, fp16 copies of B and of the local shard).
+ * chunk_rows = 0 picks c with ag_gemm_choose_chunk_rows.
+ * Returns NULL on failure (see ag_gemm_last_error()).
+ */
+ag_gemm_plan *ag_gemm_plan_create(int n_shards, int64_t M, int64_t K,
+                                  int64_t N, int dtype, int64_t chunk_rows);
+
+/* Wait for the plan's last run, then free everything the plan owns. NULL is a no-op. */
+void ag_gemm_plan_destroy(ag_gemm_plan *plan);
+
+/* The derived sizes of a plan. */
+int ag_gemm_plan_geometry(const ag_gemm_plan *plan, ag_gemm_geometry *out);
+
+/* c actually used by the plan, or a negative status. */
+int64_t ag_gemm_plan_chunk_rows(const ag_gemm_plan *plan);
+
+/*
+ * fp16 AllGather+GEMM.  shard_ptrs: host array of n_shards device pointers,
+ * each to an R x K fp16 matrix; B: K x N fp16; C: M x N fp32 (written, every
+ * element).  Enqueues the work on `stream` (see the run modes).
+ */
+int ag_gemm_run(ag_gemm_plan *plan, const void *const *shard_ptrs,
+                const void *B, float *C, void *stream);
+
+/*
+ * int8 AllGatherMatmulDequant.  shard_ptrs: n_shards device pointers to
+ * R x K int8; B: K x N int8; bias: N int32; scale: N fp32; C_i32: M x N int32
+ * and D_f16: M x N fp16, both written.  If |A x B + bias| reaches 2^31 the
+ * int32 result wraps (two's complement) -- keep |bias| < 2^31 - K * 127^2.
+ */
+int ag_gemm_dequant_run(ag_gemm_plan *plan, const void *const *shard_ptrs,
+                        const void *B, const int32_t *bias, const float *scale,
+                        int32_t *C_i32, void *D_f16, void *stream);
+
+/*
+ * Wait for the plan's last run and read its device status word: AG_GEMM_OK,
+ * or AG_GEMM_ERR_TIMEOUT if a wait on a ready counter or a pipeline barrier
+ * ran out (C is then undefined).  A timed-out plan keeps failing until
+ * ag_gemm_plan_reset.
+ */
+int ag_gemm_plan_status(ag_gemm_plan *plan);
+
+/* Raw status word of the last run (0 = ok; low byte = kind; see the source). */
+int64_t ag_gemm_plan_status_word(ag_gemm_plan *plan);
+
+/* Zero the ready counters and the status word on `stream`; the epoch restarts. */
+int ag_gemm_plan_reset(ag_gemm_plan *plan, void *stream);
+
+/* Select an ag_gemm_mode for later runs (default PIPELINED). */
+int ag_gemm_plan_set_mode(ag_gemm_plan *plan, int mode);
+
+/*
+ * Which shard is local (default 0).  It only changes the consumption order
+ * (local first, then (local+1) % n, ...); C does not depend on it.
+ */
+int ag_gemm_plan_set_local_rank(ag_gemm_plan *plan, int local_rank);
+
+/* Limit of every device-side wait, in ns (default 1e9; must be > 0). */
+int ag_gemm_plan_set_timeout_ns(ag_gemm_plan *plan, int64_t ns);
+
+/* OR of ag_gemm_debug_flag values; `arg` is the item index or the delay. */
+int ag_gemm_plan_set_debug(ag_gemm_plan *plan, int flags, int64_t arg);
+
+/* Number of CTAs the plan launches (one per SM, all co-resident). */
+int ag_gemm_plan_grid(const ag_gemm_plan *plan);
+
+/* Thread-local code and text of the last error raised on this thread. */
+int ag_gemm_last_error(void);
+const char *ag_gemm_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* AG_GEMM_H */

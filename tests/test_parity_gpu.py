@@ -1,0 +1,320 @@
+"""GPU parity: the CUDA path against the CPU oracle, through the C ABI.
+
+fp16 path: relative Frobenius error <= 1e-4 and max abs error <= 1e-3 sqrt(K)
+against the fp64 oracle.  int8 path: C_i32 bit-exact; D within 1 fp16 ulp (the
+oracle follows the same fp32 dequant definition, so D is expected bit-exact).
+Small and ragged cases are compared element by element; the full-size
+workloads are compared at sampled points (every tile's corners plus random
+points) and through row/column checksums that hold at any size.  The streaming
+machinery is checked by invariants: every run mode, chunk size and local rank
+gives bit-identical C, poisoned staging never leaks, injected delays change
+nothing, and a chunk that never lands ends in a TIMEOUT status, not a hang.
+"""
+import numpy as np
+import pytest
+
+from gpu_util import check_f16, f16_ulp_distance, tile_samples
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+from all_gather_gemm_chunked_gb300 import binding as B_  # noqa: E402
+from all_gather_gemm_chunked_gb300 import synth  # noqa: E402
+from all_gather_gemm_chunked_gb300.plan import Plan  # noqa: E402
+
+DEV = torch.device("cuda:0")
+
+
+def _to_dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def run_f16(x, S, R, K, N, chunk_rows=0, mode=None, local=None, debug=None, plan=None):
+    own = plan is None
+    if own:
+        plan = Plan(S, S * R, K, N, "f16", chunk_rows)
+    try:
+        if mode is not None:
+            plan.set_mode(mode)
+        if local is not None:
+            plan.set_local_rank(local)
+        if debug is not None:
+            plan.set_debug(*debug)
+        shards = [_to_dev(s) for s in x["shards"]]
+        Bd = _to_dev(x["B"])
+        C = torch.full((S * R, N), float("nan"), dtype=torch.float32, device=DEV)
+        plan.run(shards, Bd, C)
+        torch.cuda.synchronize()
+        assert plan.status() == 0, f"status word {plan.status_word():#x}"
+        return C.cpu().numpy()
+    finally:
+        if own:
+            plan.close()
+
+
+def run_i8(x, S, R, K, N, chunk_rows=0, mode=None, local=None, plan=None):
+    own = plan is None
+    if own:
+        plan = Plan(S, S * R, K, N, "i8", chunk_rows)
+    try:
+        if mode is not None:
+            plan.set_mode(mode)
+        if local is not None:
+            plan.set_local_rank(local)
+        shards = [_to_dev(s) for s in x["shards"]]
+        Ci = torch.full((S * R, N), -7, dtype=torch.int32, device=DEV)
+        D = torch.full((S * R, N), float("nan"), dtype=torch.float16, device=DEV)
+        plan.dequant_run(shards, _to_dev(x["B"]), _to_dev(x["bias"]), _to_dev(x["scale"]), Ci, D)
+        torch.cuda.synchronize()
+        assert plan.status() == 0, f"status word {plan.status_word():#x}"
+        return Ci.cpu().numpy(), D.cpu().numpy()
+    finally:
+        if own:
+            plan.close()
+
+
+# ---------------------------------------------------------------------------
+# fp16, element by element
+# ---------------------------------------------------------------------------
+
+def test_f16_workload1_full(oracle):
+    w = synth.WORKLOADS[1]
+    x = synth.workload_inputs(w)
+    C = run_f16(x, w.S, w.R, w.K, w.N, w.chunk_rows)
+    check_f16(C, oracle.ag_gemm_f16(x["shards"], x["B"]), w.K, "workload 1")
+
+
+@pytest.mark.parametrize("S,R,K,N,c", [
+    (3, 200, 328, 392, 0),    # ragged M tiles, K tail (328 = 5*64 + 8), N tail
+    (2, 130, 72, 136, 0),     # N < 256 after the first tile
+    (1, 257, 136, 264, 0),    # single shard = plain GEMM
+    (4, 37, 64, 8, 1),        # N = 8, one-row chunks
+    (2, 300, 8, 520, 0),      # K = 8
+    (5, 256, 1024, 512, 64),  # several full tiles per shard
+])
+def test_f16_ragged_full(oracle, S, R, K, N, c):
+    x = synth.make_inputs(S, R, K, N, "f16", 1000 + S * 7 + K)
+    C = run_f16(x, S, R, K, N, c)
+    check_f16(C, oracle.ag_gemm_f16(x["shards"], x["B"]), K, f"S={S} R={R} K={K} N={N}")
+
+
+def test_f16_gather_placement(oracle):
+    """Shard s holds s+1 in column 0 and B = e_0 e_0^T: C rows of shard s equal s+1."""
+    S, R, K, N = 4, 160, 64, 256
+    shards = [np.zeros((R, K), np.float16) for _ in range(S)]
+    for s in range(S):
+        shards[s][:, 0] = s + 1
+    Bm = np.zeros((K, N), np.float16)
+    Bm[0, 0] = 1
+    for local in range(S):
+        C = run_f16({"shards": shards, "B": Bm}, S, R, K, N, 0, local=local)
+        want = np.zeros((S * R, N))
+        want[:, 0] = np.repeat(np.arange(1, S + 1), R)
+        assert np.array_equal(C, want)
+
+
+# ---------------------------------------------------------------------------
+# streaming machinery (invariants)
+# ---------------------------------------------------------------------------
+
+def test_f16_modes_bit_identical():
+    S, R, K, N = 3, 256, 512, 512
+    x = synth.make_inputs(S, R, K, N, "f16", 77)
+    with Plan(S, S * R, K, N, "f16") as plan:
+        pipelined = run_f16(x, S, R, K, N, plan=plan, mode=B_.MODE_PIPELINED)
+        compute = run_f16(x, S, R, K, N, plan=plan, mode=B_.MODE_COMPUTE_ONLY)
+        sequential = run_f16(x, S, R, K, N, plan=plan, mode=B_.MODE_SEQUENTIAL)
+        plan.set_mode(B_.MODE_COPY_ONLY)
+        plan.run([_to_dev(s) for s in x["shards"]], _to_dev(x["B"]))
+        torch.cuda.synchronize()
+        assert plan.status() == 0
+        compute2 = run_f16(x, S, R, K, N, plan=plan, mode=B_.MODE_COMPUTE_ONLY)
+    assert np.array_equal(pipelined, compute)
+    assert np.array_equal(pipelined, sequential)
+    assert np.array_equal(pipelined, compute2)
+
+
+def test_f16_invariant_to_chunk_rows_and_local_rank():
+    S, R, K, N = 4, 256, 256, 384
+    x = synth.make_inputs(S, R, K, N, "f16", 78)
+    ref = run_f16(x, S, R, K, N, 0)
+    for c in (256, 128, 64, 16, 1):
+        assert np.array_equal(run_f16(x, S, R, K, N, c), ref), f"chunk_rows={c}"
+    for local in range(S):
+        assert np.array_equal(run_f16(x, S, R, K, N, 0, local=local), ref), f"local={local}"
+
+
+def test_f16_poisoned_staging_and_delays():
+    S, R, K, N = 3, 384, 512, 512
+    x = synth.make_inputs(S, R, K, N, "f16", 79)
+    ref = run_f16(x, S, R, K, N, 0)
+    poisoned = run_f16(x, S, R, K, N, 0, debug=(B_.DEBUG_POISON_STAGING, 0))
+    assert np.array_equal(poisoned, ref)
+    delayed = run_f16(x, S, R, K, N, 0, debug=(B_.DEBUG_POISON_STAGING | B_.DEBUG_DELAY_NS, 20000))
+    assert np.array_equal(delayed, ref)
+
+
+def test_f16_repeated_runs_epochs():
+    """Counters are monotonic across runs (epoch * pieces): many runs stay right."""
+    S, R, K, N = 2, 256, 128, 256
+    x = synth.make_inputs(S, R, K, N, "f16", 80)
+    with Plan(S, S * R, K, N, "f16") as plan:
+        ref = run_f16(x, S, R, K, N, plan=plan)
+        shards = [_to_dev(s) for s in x["shards"]]
+        Bd = _to_dev(x["B"])
+        C = torch.empty((S * R, N), dtype=torch.float32, device=DEV)
+        for _ in range(50):
+            plan.run(shards, Bd, C)
+        torch.cuda.synchronize()
+        assert plan.status() == 0
+        assert np.array_equal(C.cpu().numpy(), ref)
+
+
+def test_f16_timeout_then_reset():
+    """A chunk whose copy is skipped never becomes ready: the consumer's bounded
+    wait ends with TIMEOUT (no hang, context stays usable); after a reset the
+    plan runs correctly again."""
+    S, R, K, N = 2, 256, 128, 256
+    x = synth.make_inputs(S, R, K, N, "f16", 81)
+    with Plan(S, S * R, K, N, "f16") as plan:
+        ref = run_f16(x, S, R, K, N, plan=plan)
+        plan.set_timeout_ns(20_000_000)
+        plan.set_debug(B_.DEBUG_SKIP_ITEM, 3)
+        shards = [_to_dev(s) for s in x["shards"]]
+        Bd = _to_dev(x["B"])
+        plan.run(shards, Bd)
+        torch.cuda.synchronize()
+        assert plan.status() == B_.ERR_TIMEOUT
+        assert plan.status_word() & 0xFF == 1
+        plan.set_debug(0, 0)
+        plan.reset()
+        again = run_f16(x, S, R, K, N, plan=plan)
+        assert np.array_equal(again, ref)
+
+
+def test_f16_abi_errors_on_gpu():
+    S, R, K, N = 2, 128, 64, 64
+    with Plan(S, S * R, K, N, "f16") as plan:
+        a = torch.zeros((R, K), dtype=torch.float16, device=DEV)
+        Bd = torch.zeros((K, N), dtype=torch.float16, device=DEV)
+        C = torch.zeros((S * R, N), dtype=torch.float32, device=DEV)
+        h = plan.handle
+        with pytest.raises(B_.AgGemmError) as e:
+            B_.ag_gemm_run(h, [a.data_ptr(), 0], Bd.data_ptr(), C.data_ptr(), 0)
+        assert e.value.code == B_.ERR_INVALID
+        with pytest.raises(B_.AgGemmError) as e:
+            B_.ag_gemm_run(h, [a.data_ptr(), a.data_ptr() + 2], Bd.data_ptr(), C.data_ptr(), 0)
+        assert e.value.code == B_.ERR_INVALID
+        with pytest.raises(B_.AgGemmError) as e:
+            B_.ag_gemm_dequant_run(h, [a.data_ptr()] * 2, Bd.data_ptr(), C.data_ptr(),
+                                   C.data_ptr(), C.data_ptr(), C.data_ptr(), 0)
+        assert e.value.code == B_.ERR_INVALID
+        with pytest.raises(B_.AgGemmError):
+            plan.set_local_rank(2)
+        with pytest.raises(B_.AgGemmError):
+            plan.set_mode(9)
+
+
+# ---------------------------------------------------------------------------
+# fp16 full-size workloads (the bench's launch configuration)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("wid", [2, 3])
+def test_f16_full_size_workload(oracle, wid):
+    w = synth.WORKLOADS[wid]
+    x = synth.workload_inputs(w)
+    C = run_f16(x, w.S, w.R, w.K, w.N, w.chunk_rows)
+    assert np.all(np.isfinite(C))
+    rng = np.random.default_rng(wid)
+    rows, cols = tile_samples(rng, w.M, w.N, w.R)
+    ref = oracle.ag_gemm_f16_at(x["shards"], x["B"], rows, cols)
+    check_f16(C[rows, cols], ref, w.K, f"workload {wid} samples")
+    A = np.concatenate(x["shards"]).astype(np.float64)
+    Bf = x["B"].astype(np.float64)
+    row_ref = A @ Bf.sum(axis=1)
+    col_ref = A.sum(axis=0) @ Bf
+    Cd = C.astype(np.float64)
+    assert np.abs(Cd.sum(axis=1) - row_ref).max() <= 1e-3 * np.sqrt(w.K * w.N)
+    assert np.abs(Cd.sum(axis=0) - col_ref).max() <= 1e-3 * np.sqrt(w.K * w.M)
+
+
+# ---------------------------------------------------------------------------
+# int8 dequant
+# ---------------------------------------------------------------------------
+
+def _check_i8(Ci, D, Cref, Dref, what=""):
+    assert np.array_equal(Ci, Cref), f"{what}: C_i32 differs in {np.count_nonzero(Ci != Cref)} places"
+    ulp = f16_ulp_distance(D, Dref)
+    assert ulp.max() <= 1, f"{what}: D off by {ulp.max()} ulp"
+
+
+@pytest.mark.parametrize("S,R,K,N,c", [
+    (2, 200, 1056, 208, 0),    # two K segments (1024 + 32), ragged tiles
+    (3, 64, 2064, 96, 0),
+    (1, 130, 16, 16, 0),
+    (4, 33, 3072, 272, 3),
+])
+def test_i8_ragged_full(oracle, S, R, K, N, c):
+    x = synth.make_inputs(S, R, K, N, "i8", 2000 + S * 11 + K)
+    Ci, D = run_i8(x, S, R, K, N, c)
+    Cref, Dref = oracle.ag_gemm_dequant(x["shards"], x["B"], x["bias"], x["scale"])
+    _check_i8(Ci, D, Cref, Dref, f"S={S} R={R} K={K} N={N}")
+
+
+def test_i8_worst_case_magnitudes_exact(oracle):
+    """All entries +-127 and K = 27392: every fp32 segment partial reaches
+    1024 * 127^2 and the int32 sum reaches 27392 * 127^2 - the exactness limit
+    of the fp16-emulated int8 MMA is exercised."""
+    S, R, K, N = 2, 64, 27392, 256
+    rng = np.random.default_rng(5)
+    shards = [np.full((R, K), 127, np.int8) for _ in range(S)]
+    shards[1][::2] = -127
+    Bm = np.full((K, N), 127, np.int8)
+    Bm[:, 1::3] = -127
+    signs = rng.choice(np.array([-127, 127], np.int8), size=(K, 8))
+    Bm[:, -8:] = signs
+    x = {"shards": shards, "B": Bm, "bias": rng.integers(-1000, 1001, N, dtype=np.int32),
+         "scale": rng.uniform(1e-5, 1e-4, N).astype(np.float32)}
+    Ci, D = run_i8(x, S, R, K, N)
+    Cref, Dref = oracle.ag_gemm_dequant(x["shards"], x["B"], x["bias"], x["scale"])
+    _check_i8(Ci, D, Cref, Dref, "worst case")
+
+
+def test_i8_modes_and_local_rank_bit_identical():
+    S, R, K, N = 3, 128, 1024, 256
+    x = synth.make_inputs(S, R, K, N, "i8", 90)
+    ref = run_i8(x, S, R, K, N)
+    with Plan(S, S * R, K, N, "i8") as plan:
+        for mode in (B_.MODE_SEQUENTIAL, B_.MODE_PIPELINED, B_.MODE_COMPUTE_ONLY):
+            got = run_i8(x, S, R, K, N, plan=plan, mode=mode)
+            assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])
+    for local in range(S):
+        got = run_i8(x, S, R, K, N, local=local)
+        assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])
+
+
+@pytest.mark.parametrize("wid", [4, 5])
+def test_i8_full_size_workload(oracle, wid):
+    w = synth.WORKLOADS[wid]
+    x = synth.workload_inputs(w)
+    Ci, D = run_i8(x, w.S, w.R, w.K, w.N, w.chunk_rows)
+    rng = np.random.default_rng(wid)
+    rows, cols = tile_samples(rng, w.M, w.N, w.R, per_tile=2)
+    Cs, Ds = oracle.ag_gemm_dequant_at(x["shards"], x["B"], x["bias"], x["scale"], rows, cols)
+    _check_i8(Ci[rows, cols], D[rows, cols], Cs, Ds, f"workload {wid} samples")
+    # exact checksums over every element
+    bsum = x["B"].astype(np.int64).sum(axis=1).astype(np.float64)
+    row_ref = np.concatenate([s.astype(np.float64) @ bsum for s in x["shards"]])
+    row_ref = row_ref.astype(np.int64) + int(x["bias"].astype(np.int64).sum())
+    assert np.array_equal(Ci.astype(np.int64).sum(axis=1), row_ref)
+    asum = sum(s.astype(np.int64).sum(axis=0) for s in x["shards"]).astype(np.float64)
+    col_ref = (asum @ x["B"].astype(np.float64)).astype(np.int64) + w.M * x["bias"].astype(np.int64)
+    assert np.array_equal(Ci.astype(np.int64).sum(axis=0), col_ref)
+    # every D element is the fp32 dequant of its (checked) C_i32
+    with np.errstate(over="ignore"):
+        want = (Ci.astype(np.float32) * x["scale"][None, :]).astype(np.float16)
+    assert f16_ulp_distance(D, want).max() <= 1
