@@ -1,31 +1,39 @@
 // fused_kernel.cu -- the streamed AllGather+GEMM as ONE persistent,
-// cooperative, warp-specialised kernel for sm_103a.
+// warp-specialised kernel of CTA pairs for sm_103a.
 //
 // The method ("AllGather + GEMM 通算融合算子示例", sections 整体架构 and
 // 优化说明): a communication engine sends A chunk by chunk and bumps a
 // per-source counter after each chunk; the compute engine first multiplies the
 // local row group with no wait, then each remote row group after waiting on
-// its counter, with continuous K accumulation and double-buffered operand
+// its counter, with continuous K accumulation and multi-buffered operand
 // staging.  On one GB300 the "ranks" are shards in this GPU's memory, and both
-// engines live in the same launch:
+// engines live in the same launch.
 //
-//   warp 0      TMA warp: waits (remote tiles only) on the ready counters of
-//               the chunks a tile reads, then streams A and B k-blocks into a
-//               4-stage shared-memory ring with cp.async.bulk.tensor.
-//   warp 1      MMA warp: one thread issues tcgen05.mma kind::f16 into a TMEM
-//               accumulator (two 256-column buffers, so the epilogue of tile i
-//               overlaps the MMAs of tile i+1).
-//   warps 2-3   copy warps ("comm blocks"): copy items of the remote shards'
-//               chunks into the staging workspace, in consumption order, and
-//               release the chunk's counter after each item.  Every CTA runs
-//               two, so the gather uses the whole GPU's load/store bandwidth.
+// Tiles are 256 x BN (BN = 256, or 128 for narrow N) and belong to a cluster
+// of two CTAs on neighbouring SMs that run one tcgen05 MMA with cta_group::2:
+// each CTA stages its own 128 rows of A and its own BN/2 columns of B, the
+// even CTA issues the MMA, and each CTA's TMEM receives its 128 rows of the
+// 256 x BN accumulator.  Per SM that is 32 KB of operands per 64-deep k-block
+// instead of 48 KB for a single-SM 128 x 256 tile, and six stages fit.
+//
+//   warp 0      TMA warp (both CTAs): for remote tiles all 32 lanes poll the
+//               ready counters of the chunks this CTA's 128 rows read, then
+//               lane 0 streams A and B k-blocks into a 6-stage ring; the bytes
+//               of both CTAs are counted on the even CTA's "full" barrier.
+//   warp 1      MMA warp (even CTA): one thread issues tcgen05.mma; commits
+//               free both CTAs' ring stages and signal both epilogues.
+//               Owns the pair's TMEM allocation (512 columns per CTA).
+//   warps 2-3   copy warps ("comm blocks"): take copy items in consumption
+//               order from a grid-wide counter, copy (or, for int8, widen) them
+//               into the staging workspace and release the chunk's counter.
 //   warps 4-7   epilogue: TMEM -> registers -> global (fp32 C, or for int8
 //               the exact int32 fold, bias, int32 C and fp16 D).
 //
-// Counter waits cross CTAs, so the grid is launched cooperatively: every CTA
-// is resident for the whole launch and no wait can depend on an unscheduled
-// CTA.  Every wait is bounded; on timeout the kernel records a status word,
-// stops issuing work, drains what it has in flight, frees TMEM and returns.
+// No CTA ever waits for a copy item that only a specific other CTA could
+// perform: items are taken dynamically, so any resident CTA's copy warps make
+// progress and the waits need no co-residency guarantee.  Every wait is
+// bounded; on timeout the kernel records a status word, stops issuing work,
+// drains what it has in flight, frees TMEM and returns.
 //
 // int8: sm_103a has no tcgen05 kind::i8, so int8 x int8 is computed exactly on
 // the fp16 tensor path: int8 values are exact in fp16, products of two int8
@@ -93,9 +101,14 @@ __device__ __forceinline__ void warp_widen16(const uint4* __restrict__ src, uint
 }
 
 template <bool kI8>
-__device__ void copy_warp(const FusedParams& p, int64_t gw, int64_t n_warps, int lane) {
+__device__ void copy_warp(const FusedParams& p, int lane) {
   const Geometry& g = p.g;
-  for (int64_t i = gw; i < g.items; i += n_warps) {
+  for (;;) {
+    unsigned long long ticket = 0;
+    if (lane == 0) ticket = atomicAdd(p.item_counter, 1ull);
+    ticket = __shfl_sync(0xffffffffu, ticket, 0);
+    const int64_t i = static_cast<int64_t>(ticket - p.item_base);
+    if (i >= g.items) break;  // exactly one failing ticket per copy warp and run
     int pos, piece;
     int64_t q, v0, v1;
     item_coords(g, i, pos, q, piece, v0, v1);
@@ -116,13 +129,13 @@ __device__ void copy_warp(const FusedParams& p, int64_t gw, int64_t n_warps, int
 }
 
 // ------------------------------------------------------------------ TMA warp
-// All 32 lanes poll the counters of the chunks that m-tile `mt` of position
-// `pos` reads; returns false (and raises the abort flag) on timeout.
-__device__ bool wait_chunks(const FusedParams& p, int pos, int64_t mt, int lane,
+// All 32 lanes poll the counters of the chunks that the 128 rows starting at
+// row0 of position `pos` read; false (and the abort flag raised) on timeout.
+__device__ bool wait_chunks(const FusedParams& p, int pos, int64_t row0, int lane,
                             volatile int* abort) {
   const Geometry& g = p.g;
   int64_t q0, q1;
-  tile_chunks(g, mt, q0, q1);
+  if (!rows_chunks(g, row0, q0, q1)) return true;  // rows past the shard: nothing to wait for
   const uint32_t target = p.epoch * static_cast<uint32_t>(g.P);
   const uint32_t* cnt = p.counters + (int64_t)(pos - 1) * g.Q;
   bool ok = true;
@@ -153,12 +166,15 @@ __device__ bool wait_chunks(const FusedParams& p, int pos, int64_t mt, int lane,
 }
 
 template <bool kI8>
-__device__ void tma_warp(const FusedParams& p, uint8_t* sA, uint8_t* sB, uint64_t* full,
-                         uint64_t* empty, int lane, volatile int* abort) {
+__device__ void tma_warp(const FusedParams& p, uint32_t rank, uint8_t* sA, uint8_t* sB,
+                         uint64_t* full, uint64_t* empty, int lane, volatile int* abort) {
   const Geometry& g = p.g;
+  const volatile uint32_t* gstatus = p.status;
   const bool wait = (p.flags & kFlagWait) != 0;
-  const uint32_t tx = static_cast<uint32_t>(kABytes + g.BN * kBlockK * 2);
-  const int nb = g.BN / 64;
+  const int half = g.BN / 2;                                   // B columns this CTA stages
+  const uint32_t pair_tx = static_cast<uint32_t>(2 * (kABytes + half * kBlockK * 2));
+  const uint32_t full0 = mapa_shared(smem_u32(full), 0);       // the even CTA's barriers
+  const int64_t n_clusters = gridDim.x / 2, cluster = blockIdx.x / 2;
   int stage = 0;
   uint32_t phase = 0, issued = 0, issued_phase = 0;  // bit s: stage s used / parity of last use
   if (lane == 0) {
@@ -167,33 +183,35 @@ __device__ void tma_warp(const FusedParams& p, uint8_t* sA, uint8_t* sB, uint64_
     tma_prefetch_desc(&p.tm_b);
   }
   bool ok = true;
-  for (int64_t t = blockIdx.x; t < g.tiles && ok; t += gridDim.x) {
+  for (int64_t t = cluster; t < g.tiles && ok; t += n_clusters) {
     int pos;
     int64_t mt, nt;
     tile_coords(g, t, pos, mt, nt);
-    if (pos > 0 && wait && !wait_chunks(p, pos, mt, lane, abort)) break;
+    const int64_t row0 = mt * kPairM + rank * kBlockM;
+    if (pos > 0 && wait && !wait_chunks(p, pos, row0, lane, abort)) break;
     if (lane == 0) {
       if (pos > 0) {
         fence_acq_rel_gpu();
         fence_proxy_async_global();
       }
-      const int32_t y = static_cast<int32_t>(mt * kBlockM);
+      const int32_t y = static_cast<int32_t>(row0);
+      const int32_t xb = static_cast<int32_t>(nt * g.BN + rank * half);
       for (int64_t kb = 0; kb < g.KB; ++kb) {
-        if (!mbar_wait(&empty[stage], phase ^ 1u, p.pipe_timeout_ns, abort)) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u, p.pipe_timeout_ns, abort, gstatus)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&full[stage], tx);
+        const uint32_t bar = full0 + stage * 8;
+        if (rank == 0) mbar_arrive_expect_tx(&full[stage], pair_tx);
         const int32_t x = static_cast<int32_t>(kb * kBlockK);
         uint8_t* a_dst = sA + stage * kABytes;
         if (pos == 0)
-          tma_load_2d(a_dst, &p.tm_a_local, &full[stage], x, y);
+          tma_load_2d_pair(a_dst, &p.tm_a_local, bar, x, y);
         else
-          tma_load_3d(a_dst, &p.tm_a_stage, &full[stage], x, y, pos - 1);
+          tma_load_3d_pair(a_dst, &p.tm_a_stage, bar, x, y, pos - 1);
         uint8_t* b_dst = sB + stage * kBBytes;
-        for (int i = 0; i < nb; ++i)
-          tma_load_2d(b_dst + i * (64 * kBlockK * 2), &p.tm_b, &full[stage],
-                      static_cast<int32_t>(nt * g.BN + i * 64), x);
+        for (int i = 0; i < half / 64; ++i)
+          tma_load_2d_pair(b_dst + i * (64 * kBlockK * 2), &p.tm_b, bar, xb + i * 64, x);
         issued |= 1u << stage;
         issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
         if (++stage == kStages) {
@@ -206,35 +224,41 @@ __device__ void tma_warp(const FusedParams& p, uint8_t* sA, uint8_t* sB, uint64_
   }
   if (lane == 0) {
     if (!ok) {
-      set_status(p.status, kStatusPipelineTimeout, 0x100u);
+      set_status(p.status, kStatusPipelineTimeout, 0x100u | rank);
       *abort = 1;
     }
-    // Drain: every load this warp issued must have landed before the CTA exits.
-    volatile int never = 0;
-    for (int s = 0; s < kStages; ++s)
-      if (issued & (1u << s)) mbar_wait(&full[s], (issued_phase >> s) & 1u, p.pipe_timeout_ns, &never);
+    if (rank == 0) {
+      // Drain: every load counted on this CTA's barriers must have landed
+      // (the peer's bytes are counted here too) before the pair exits.
+      volatile int never = 0;
+      const uint64_t limit = ok ? p.pipe_timeout_ns : 20000000ull;
+      for (int s = 0; s < kStages; ++s)
+        if (issued & (1u << s)) mbar_wait(&full[s], (issued_phase >> s) & 1u, limit, &never);
+    }
   }
   __syncwarp();
 }
 
-// ------------------------------------------------------------------ MMA warp
+// ------------------------------------------------------------------ MMA warp (even CTA)
 template <bool kI8>
 __device__ void mma_warp(const FusedParams& p, const uint8_t* sA, const uint8_t* sB,
                          uint64_t* full, uint64_t* empty, uint64_t* tfull, uint64_t* tempty,
                          uint32_t tmem, volatile int* abort) {
   const Geometry& g = p.g;
-  const uint32_t idesc = idesc_f16_f32(kBlockM, g.BN, /*a_mn=*/false, /*b_mn=*/true);
+  const volatile uint32_t* gstatus = p.status;
+  const uint32_t idesc = idesc_f16_f32(kPairM, g.BN, /*a_mn=*/false, /*b_mn=*/true);
   const int64_t seg_len = kI8 ? kSegBlocks : g.KB;
   const int64_t nseg = ceil_div(g.KB, seg_len);
   const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+  const int64_t n_clusters = gridDim.x / 2, cluster = blockIdx.x / 2;
   int stage = 0;
   uint32_t phase = 0, unit = 0;
   bool ok = true;
-  for (int64_t t = blockIdx.x; t < g.tiles && ok; t += gridDim.x) {
+  for (int64_t t = cluster; t < g.tiles && ok; t += n_clusters) {
     for (int64_t seg = 0; seg < nseg && ok; ++seg) {
       const uint32_t buf = kI8 ? 0u : (unit & 1u);
       const uint32_t use = kI8 ? unit : (unit >> 1);
-      if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, p.pipe_timeout_ns, abort)) {
+      if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, p.pipe_timeout_ns, abort, gstatus)) {
         ok = false;
         break;
       }
@@ -243,7 +267,7 @@ __device__ void mma_warp(const FusedParams& p, const uint8_t* sA, const uint8_t*
       const int64_t kb0 = seg * seg_len;
       const int64_t kb1 = kb0 + seg_len < g.KB ? kb0 + seg_len : g.KB;
       for (int64_t kb = kb0; kb < kb1; ++kb) {
-        if (!mbar_wait(&full[stage], phase, p.pipe_timeout_ns, abort)) {
+        if (!mbar_wait(&full[stage], phase, p.pipe_timeout_ns, abort, gstatus)) {
           ok = false;
           break;
         }
@@ -252,21 +276,23 @@ __device__ void mma_warp(const FusedParams& p, const uint8_t* sA, const uint8_t*
 #pragma unroll
         for (int k = 0; k < kBlockK / kUmmaK; ++k) {
           // A: K-major, 128B swizzle: 8-row groups 1024 B apart; a 16-element
-          // K slice is 32 B further along the swizzled row.
+          // K slice is 32 B further along the swizzled row.  Rows 0..127 come
+          // from this CTA, rows 128..255 from the peer (same offset).
           const uint64_t ad = smem_desc_sw128(as + k * (kUmmaK * 2), 16, 1024);
           // B: MN-major, 128B swizzle: 64-column groups 8 KB apart (LBO),
           // 8-k-row groups 1024 B apart (SBO); a 16-row K slice is 2 KB on.
+          // Columns 0..BN/2-1 come from this CTA, the rest from the peer.
           const uint64_t bd = smem_desc_sw128(bs + k * (kUmmaK * 128), 64 * kBlockK * 2, 1024);
-          mma_f16(d, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+          mma_f16_pair(d, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
         }
-        mma_commit(&empty[stage]);  // frees the smem stage once these MMAs have read it
+        mma_commit_pair_both(&empty[stage]);  // frees this stage in both CTAs
         if (++stage == kStages) {
           stage = 0;
           phase ^= 1u;
         }
       }
       if (!ok) break;
-      mma_commit(&tfull[buf]);  // accumulator ready for the epilogue
+      mma_commit_pair_both(&tfull[buf]);  // accumulator ready for both epilogues
       ++unit;
     }
   }
@@ -284,27 +310,31 @@ __device__ __forceinline__ void st_v4(void* ptr, uint32_t a, uint32_t b, uint32_
 }
 
 template <bool kI8>
-__device__ void epilogue_warp(const FusedParams& p, int quad, int lane, uint64_t* tfull,
-                              uint64_t* tempty, uint32_t tmem, volatile int* abort) {
+__device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int lane,
+                              uint64_t* tfull, uint64_t* tempty, uint32_t tmem,
+                              volatile int* abort) {
   const Geometry& g = p.g;
+  const volatile uint32_t* gstatus = p.status;
   const int64_t seg_len = kI8 ? kSegBlocks : g.KB;
   const int64_t nseg = ceil_div(g.KB, seg_len);
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+  const uint32_t tempty0 = mapa_shared(smem_u32(tempty), 0);  // the even CTA's barriers
+  const int64_t n_clusters = gridDim.x / 2, cluster = blockIdx.x / 2;
   uint32_t unit = 0;
-  for (int64_t t = blockIdx.x; t < g.tiles; t += gridDim.x) {
+  for (int64_t t = cluster; t < g.tiles; t += n_clusters) {
     int pos;
     int64_t mt, nt;
     tile_coords(g, t, pos, mt, nt);
     const int src = source_of(g, p.local, pos);
-    const int64_t r = mt * kBlockM + quad * 32 + lane;
+    const int64_t r = mt * kPairM + rank * kBlockM + quad * 32 + lane;
     const bool row_ok = r < g.R;
     const int64_t grow = static_cast<int64_t>(src) * g.R + r;
     for (int64_t seg = 0; seg < nseg; ++seg) {
       const uint32_t buf = kI8 ? 0u : (unit & 1u);
       const uint32_t use = kI8 ? unit : (unit >> 1);
-      if (!mbar_wait(&tfull[buf], use & 1u, p.pipe_timeout_ns, abort)) {
+      if (!mbar_wait(&tfull[buf], use & 1u, p.pipe_timeout_ns, abort, gstatus)) {
         if (lane == 0) {
-          set_status(p.status, kStatusPipelineTimeout, 0x300u);
+          set_status(p.status, kStatusPipelineTimeout, 0x300u | rank);
           *abort = 1;
         }
         return;
@@ -373,7 +403,13 @@ __device__ void epilogue_warp(const FusedParams& p, int quad, int lane, uint64_t
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[buf]);
+      if (lane == 0) {
+        // the even CTA's MMA waits for all 8 epilogue warps of the pair
+        if (rank == 0)
+          mbar_arrive(&tempty[buf]);
+        else
+          mbar_arrive_cluster(tempty0 + buf * 8);
+      }
       ++unit;
     }
   }
@@ -381,7 +417,8 @@ __device__ void epilogue_warp(const FusedParams& p, int quad, int lane, uint64_t
 
 // ------------------------------------------------------------------ kernel
 template <bool kI8>
-__global__ void __launch_bounds__(kThreads, 1) ag_fused_kernel(const __grid_constant__ FusedParams p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    ag_fused_kernel(const __grid_constant__ FusedParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -397,6 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) ag_fused_kernel(const __grid_cons
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
   const bool gemm = (p.flags & kFlagGemm) != 0;
 
   if (threadIdx.x == 0) {
@@ -406,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1) ag_fused_kernel(const __grid_cons
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 4);
+      mbar_init(&tempty[b], 8);  // 4 epilogue warps in each CTA of the pair
     }
     mbar_init(drain, 1);
     *tmem_slot = 0;
@@ -414,38 +452,45 @@ __global__ void __launch_bounds__(kThreads, 1) ag_fused_kernel(const __grid_cons
     fence_mbar_init();
   }
   if (gemm && warp == 1) {
-    tmem_alloc(tmem_slot, 512);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_slot, 512);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // barriers initialised and TMEM allocated in both CTAs
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    if (gemm) tma_warp<kI8>(p, sA, sB, full, empty, lane, abort);
+    if (gemm) tma_warp<kI8>(p, rank, sA, sB, full, empty, lane, abort);
   } else if (warp == 1) {
-    if (gemm && lane == 0) mma_warp<kI8>(p, sA, sB, full, empty, tfull, tempty, tmem, abort);
-  } else if (warp < 4) {
-    if (p.flags & kFlagCopy)
-      copy_warp<kI8>(p, static_cast<int64_t>(blockIdx.x) * 2 + (warp - 2),
-                     static_cast<int64_t>(gridDim.x) * 2, lane);
+    if (gemm && rank == 0 && lane == 0)
+      mma_warp<kI8>(p, sA, sB, full, empty, tfull, tempty, tmem, abort);
+  } else if (warp < 2 + kCopyWarpsPerCta) {
+    if (p.flags & kFlagCopy) copy_warp<kI8>(p, lane);
   } else {
-    if (gemm) epilogue_warp<kI8>(p, warp - 4, lane, tfull, tempty, tmem, abort);
+    if (gemm) epilogue_warp<kI8>(p, rank, warp - 4, lane, tfull, tempty, tmem, abort);
   }
 
   tc_fence_before();
   __syncthreads();
+  if (gemm && rank == 0 && warp == 1 && lane == 0) {
+    // Every MMA of the pair must be complete before either CTA releases TMEM
+    // or shared memory.
+    mma_commit_pair_local(drain);
+    volatile int never = 0;
+    mbar_wait(drain, 0, p.pipe_timeout_ns, &never);
+  }
+  if (*abort || *reinterpret_cast<volatile uint32_t*>(p.status) != 0u) {
+    // After a timeout the peer may still have TMA loads landing in this CTA's
+    // shared memory that no barrier of ours counts; give them time to land.
+    if (threadIdx.x == 0) __nanosleep(100000);
+  }
+  __syncthreads();
+  tc_fence_before();
+  cluster_sync();
   if (gemm && warp == 1) {
-    if (lane == 0) {
-      // Every MMA this CTA issued must be complete before TMEM is released.
-      mma_commit(drain);
-      volatile int never = 0;
-      mbar_wait(drain, 0, p.pipe_timeout_ns, &never);
-    }
-    __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc_pair(tmem, 512);
   }
 }
 
@@ -471,12 +516,20 @@ __global__ void __launch_bounds__(256) widen_kernel(const uint4* __restrict__ s0
 }
 
 // ------------------------------------------------------------------ launchers
-cudaError_t fused_max_blocks_per_sm(int dtype, int* blocks) {
-  const void* fn = dtype == 1 ? reinterpret_cast<const void*>(&ag_fused_kernel<true>)
-                              : reinterpret_cast<const void*>(&ag_fused_kernel<false>);
+static const void* fused_fn(int dtype) {
+  return dtype == 1 ? reinterpret_cast<const void*>(&ag_fused_kernel<true>)
+                    : reinterpret_cast<const void*>(&ag_fused_kernel<false>);
+}
+
+cudaError_t fused_max_clusters(int dtype, int grid, int* clusters) {
+  const void* fn = fused_fn(dtype);
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, fn, kThreads, kSmemBytes);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  return cudaOccupancyMaxActiveClusters(clusters, fn, &cfg);
 }
 
 cudaError_t launch_fused(const FusedParams& p, int grid, cudaStream_t stream) {
@@ -485,11 +538,6 @@ cudaError_t launch_fused(const FusedParams& p, int grid, cudaStream_t stream) {
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   if (p.g.dtype == 1) return cudaLaunchKernelEx(&cfg, ag_fused_kernel<true>, p);
   return cudaLaunchKernelEx(&cfg, ag_fused_kernel<false>, p);
 }

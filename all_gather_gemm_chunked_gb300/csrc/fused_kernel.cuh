@@ -31,6 +31,8 @@ struct FusedParams {
   const void* src[kMaxShards];  // shard pointers by consumption position
   void* staging;                // fp16 [(S-1)][R][K]
   uint32_t* counters;           // [(S-1)][Q] ready counters, monotonic
+  unsigned long long* item_counter;  // copy items handed out so far (monotonic)
+  unsigned long long item_base;      // item_counter value at the start of this run
   uint32_t* status;             // [2]: status word, detail
   float* C;                     // f16 path output, M x N fp32
   int32_t* C_i32;               // i8 path outputs
@@ -46,15 +48,17 @@ struct FusedParams {
   uint32_t debug_delay_ns;
 };
 
-constexpr int kThreads = 256;                     // 8 warps
-constexpr int kABytes = kBlockM * kBlockK * 2;    // 16 KB
-constexpr int kBBytes = kMaxBlockN * kBlockK * 2; // 32 KB
+constexpr int kThreads = 256;                         // 8 warps
+constexpr int kABytes = kBlockM * kBlockK * 2;        // 16 KB: this CTA's 128 rows of A
+constexpr int kBBytes = kMaxBlockN / 2 * kBlockK * 2; // 16 KB: this CTA's half of B's columns
 constexpr int kSmemBytes = kStages * (kABytes + kBBytes) + 1024 /*barriers*/ + 1024 /*align*/;
+constexpr int kCopyWarpsPerCta = 2;
 
 // Launchers (fused_kernel.cu).
 cudaError_t launch_fused(const FusedParams& p, int grid, cudaStream_t stream);
+cudaError_t fused_max_clusters(int dtype, int grid, int* clusters);
 cudaError_t launch_widen(const int8_t* src0, uint16_t* dst0, int64_t n0, const int8_t* src1,
                          uint16_t* dst1, int64_t n1, int grid, cudaStream_t stream);
-cudaError_t fused_max_blocks_per_sm(int dtype, int* blocks);
+
 
 }  // namespace agg

@@ -187,6 +187,8 @@ struct ag_gemm_plan {
   int64_t staging_bytes = 0;
   uint32_t* counters = nullptr;
   int64_t counter_count = 0;
+  unsigned long long* item_counter = nullptr;  // copy items handed out (monotonic)
+  unsigned long long item_base = 0;
   uint32_t* status = nullptr;
   uint16_t* b16 = nullptr;  // int8 path: fp16 copy of B
   uint16_t* a16 = nullptr;  // int8 path: fp16 copy of the local shard
@@ -209,6 +211,7 @@ void free_plan(ag_gemm_plan* p) {
   if (p->done) cudaEventSynchronize(p->done);
   cudaFree(p->staging);
   cudaFree(p->counters);
+  cudaFree(p->item_counter);
   cudaFree(p->status);
   cudaFree(p->b16);
   cudaFree(p->a16);
@@ -218,8 +221,13 @@ void free_plan(ag_gemm_plan* p) {
 
 int launch_fused(ag_gemm_plan* p, agg::FusedParams& fp, int flags, cudaStream_t stream) {
   fp.flags = flags;
+  fp.item_base = p->item_base;
   cudaError_t e = agg::launch_fused(fp, p->grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "fused kernel launch");
+  // Each copy warp draws every item's ticket plus one failing ticket.
+  if (flags & agg::kFlagCopy)
+    p->item_base += static_cast<unsigned long long>(p->g.items) +
+                    static_cast<unsigned long long>(p->grid) * agg::kCopyWarpsPerCta;
   return AG_GEMM_OK;
 }
 
@@ -285,6 +293,7 @@ int run_impl(ag_gemm_plan* p, const void* const* shard_ptrs, const void* B, floa
   fp.tm_a_stage = p->tm_stage;
   fp.staging = p->staging;
   fp.counters = p->counters;
+  fp.item_counter = p->item_counter;
   fp.status = p->status;
   fp.C = C;
   fp.C_i32 = C_i32;
@@ -428,19 +437,23 @@ ag_gemm_plan* ag_gemm_plan_create(int n_shards, int64_t M, int64_t K, int64_t N,
     delete p;
     return nullptr;
   }
-  int blocks = 0;
-  if ((e = agg::fused_max_blocks_per_sm(dtype, &blocks)) != cudaSuccess || blocks < 1) {
-    if (e == cudaSuccess) fail(AG_GEMM_ERR_UNSUPPORTED, "fused kernel does not fit on an SM");
+  // One CTA per SM, in clusters of two (a CTA pair shares each MMA tile).
+  int clusters = 0;
+  const int want = (p->sm_count / 2) * 2;
+  if ((e = agg::fused_max_clusters(dtype, want, &clusters)) != cudaSuccess || clusters < 1) {
+    if (e == cudaSuccess) fail(AG_GEMM_ERR_UNSUPPORTED, "fused kernel clusters do not fit");
     else cuda_fail(e, "fused kernel occupancy");
     delete p;
     return nullptr;
   }
-  p->grid = p->sm_count;  // one CTA per SM; all co-resident (cooperative launch)
+  p->grid = clusters * 2 < want ? clusters * 2 : want;
   const int64_t slots = g.S > 1 ? g.S - 1 : 1;
   p->staging_bytes = slots * g.R * g.K * 2;
   p->counter_count = slots * g.Q;
   if ((e = cudaMalloc(&p->staging, p->staging_bytes)) != cudaSuccess ||
       (e = cudaMalloc(&p->counters, sizeof(uint32_t) * p->counter_count)) != cudaSuccess ||
+      (e = cudaMalloc(&p->item_counter, sizeof(unsigned long long))) != cudaSuccess ||
+      (e = cudaMemset(p->item_counter, 0, sizeof(unsigned long long))) != cudaSuccess ||
       (e = cudaMalloc(&p->status, 2 * sizeof(uint32_t))) != cudaSuccess ||
       (e = cudaMemset(p->counters, 0, sizeof(uint32_t) * p->counter_count)) != cudaSuccess ||
       (e = cudaMemset(p->status, 0, 2 * sizeof(uint32_t))) != cudaSuccess ||
@@ -537,10 +550,12 @@ int ag_gemm_plan_reset(ag_gemm_plan* plan, void* stream_v) {
       (e = cudaStreamWaitEvent(stream, plan->done, 0)) != cudaSuccess)
     return cuda_fail(e, "cudaStreamWaitEvent");
   if ((e = cudaMemsetAsync(plan->counters, 0, sizeof(uint32_t) * plan->counter_count, stream)) != cudaSuccess ||
+      (e = cudaMemsetAsync(plan->item_counter, 0, sizeof(unsigned long long), stream)) != cudaSuccess ||
       (e = cudaMemsetAsync(plan->status, 0, 2 * sizeof(uint32_t), stream)) != cudaSuccess ||
       (e = cudaEventRecord(plan->done, stream)) != cudaSuccess)
     return cuda_fail(e, "plan reset");
   plan->epoch = 0;
+  plan->item_base = 0;
   plan->last_stream = stream;
   plan->has_run = true;
   return AG_GEMM_OK;

@@ -14,10 +14,11 @@
 namespace agg {
 
 constexpr int kMaxShards = 64;
-constexpr int kBlockM = 128;        // rows of a CTA tile (one TMEM lane per row)
+constexpr int kBlockM = 128;        // rows per CTA (one TMEM lane per row)
+constexpr int kPairM = 256;         // rows of a CTA-pair tile (tcgen05 cta_group::2, M = 256)
 constexpr int kBlockK = 64;         // fp16 elements per k-block: one 128-byte swizzle row
 constexpr int kUmmaK = 16;          // K of one tcgen05.mma kind::f16
-constexpr int kStages = 4;          // TMA -> MMA shared-memory ring depth
+constexpr int kStages = 6;          // TMA -> MMA shared-memory ring depth
 constexpr int kMaxBlockN = 256;
 constexpr int kGroupM = 8;          // m-tiles per swizzle group
 // int8 emulation: |a*b| <= 127^2 = 16129 and 16 k-blocks = 1024 terms keep every
@@ -33,8 +34,8 @@ struct Geometry {
   int64_t c;             // chunk rows
   int64_t Q;             // chunks per source
   int P;                 // copy items (pieces) per chunk
-  int BN;                // block_n
-  int64_t MT, NT;        // m-tiles per source, n-tiles
+  int BN;                // block_n of a pair tile (each CTA loads BN / 2 columns of B)
+  int64_t MT, NT;        // pair m-tiles (256 rows) per source, n-tiles
   int64_t tiles;
   int64_t KB;            // k-blocks
   int64_t items;         // producer copy items
@@ -69,7 +70,7 @@ AGG_HD void make_geometry(Geometry& g, int S, int64_t M, int64_t K, int64_t N,
   if (p < 1) p = 1;
   g.P = (int)p;
   g.BN = N <= 128 ? 128 : 256;
-  g.MT = ceil_div(g.R, kBlockM);
+  g.MT = ceil_div(g.R, kPairM);
   g.NT = ceil_div(N, g.BN);
   g.tiles = (int64_t)S * g.MT * g.NT;
   g.KB = ceil_div(K, kBlockK);
@@ -109,12 +110,14 @@ AGG_HD void item_coords(const Geometry& g, int64_t i, int& pos, int64_t& q,
   v1 = vecs * (piece + 1) / g.P;
 }
 
-// Chunks [q0, q1] of a source that an m-tile reads.
-AGG_HD void tile_chunks(const Geometry& g, int64_t mt, int64_t& q0, int64_t& q1) {
-  int64_t r0 = mt * kBlockM;
-  int64_t r1 = r0 + kBlockM < g.R ? r0 + kBlockM : g.R;
-  q0 = r0 / g.c;
+// Chunks [q0, q1] of a source that the 128 rows starting at row0 touch;
+// false if the rows lie past the end of the shard.
+AGG_HD bool rows_chunks(const Geometry& g, int64_t row0, int64_t& q0, int64_t& q1) {
+  if (row0 >= g.R) return false;
+  int64_t r1 = row0 + kBlockM < g.R ? row0 + kBlockM : g.R;
+  q0 = row0 / g.c;
   q1 = (r1 - 1) / g.c;
+  return true;
 }
 
 }  // namespace agg
