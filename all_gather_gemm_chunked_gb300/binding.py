@@ -80,6 +80,7 @@ def _load():
         "ag_gemm_plan_set_timeout_ns": (i32, [vp, i64]),
         "ag_gemm_plan_set_debug": (i32, [vp, i32, i64]),
         "ag_gemm_plan_grid": (i32, [vp]),
+        "ag_gemm_run_noalloc": (i32, [i32, i64, i64, i64, i64, ctypes.POINTER(vp), vp, vp, vp, vp]),
         "ag_gemm_last_error": (i32, []),
         "ag_gemm_last_error_message": (ctypes.c_char_p, []),
     }
@@ -210,6 +211,14 @@ def ag_gemm_plan_set_debug(plan: int, flags: int, arg: int = 0) -> int:
 
 def ag_gemm_plan_grid(plan: int) -> int:
     return _check(_lib.ag_gemm_plan_grid(plan))
+
+
+def ag_gemm_run_noalloc(n_shards, M, K, N, chunk_rows, shard_ptrs, B: int, C: int,
+                        status_out: int = 0, stream: int = 0) -> int:
+    """fp16 run that allocates nothing: scratch comes from the library's fixed array."""
+    p, _keep = _ptrs(shard_ptrs)
+    return _check(_lib.ag_gemm_run_noalloc(n_shards, M, K, N, chunk_rows, p, B, C,
+                                           status_out or None, stream))
 
 
 def ag_gemm_last_error() -> int:

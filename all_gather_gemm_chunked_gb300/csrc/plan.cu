@@ -601,3 +601,132 @@ int ag_gemm_last_error(void) { return g_last_error; }
 const char* ag_gemm_last_error_message(void) { return g_last_msg; }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ no-allocation entry point
+// The fp16 run above needs a plan, and a plan allocates its staging workspace,
+// ready counters and status word with cudaMalloc.  This entry point runs the
+// same fused kernel with all of that scratch taken from a fixed array that is
+// part of the library's device image, so a call allocates nothing.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 64ull << 20;  // 64 MiB, held on every device that loads the library
+constexpr size_t kNoAllocCtrlBytes = 512;              // status (8 B) + item counter (8 B), padded
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct NoAllocDevice {
+  bool ready = false;
+  unsigned char* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+  int grid = 0;
+};
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
+std::mutex g_noalloc_mu;
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Once per device, with that device current: find the array's device address
+// (the host-side symbol is only a stand-in) and prepare the kernel.
+int noalloc_setup(int dev, NoAllocDevice** out) {
+  if (dev < 0 || dev >= kNoAllocMaxDevices)
+    return fail(AG_GEMM_ERR_UNSUPPORTED, "device ordinal %d beyond %d", dev, kNoAllocMaxDevices);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  NoAllocDevice& d = g_noalloc_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0, sms = 0;
+    cudaError_t e;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "device query");
+    if (major != 10 || minor != 3)
+      return fail(AG_GEMM_ERR_UNSUPPORTED, "needs an sm_103 (GB300) device, found sm_%d%d", major, minor);
+    void* ptr = nullptr;
+    if ((e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch)) != cudaSuccess)
+      return cuda_fail(e, "cudaGetSymbolAddress of the no-allocation scratch array");
+    int clusters = 0;
+    const int want = (sms / 2) * 2;
+    if ((e = agg::fused_max_clusters(AG_GEMM_F16, want, &clusters)) != cudaSuccess)
+      return cuda_fail(e, "fused kernel occupancy");
+    if (clusters < 1) return fail(AG_GEMM_ERR_UNSUPPORTED, "fused kernel clusters do not fit");
+    d.scratch = static_cast<unsigned char*>(ptr);
+    d.grid = clusters * 2 < want ? clusters * 2 : want;
+    d.ready = true;
+  }
+  *out = &d;
+  return AG_GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" int ag_gemm_run_noalloc(int n_shards, int64_t M, int64_t K, int64_t N,
+                                   int64_t chunk_rows, const void* const* shard_ptrs,
+                                   const void* B, float* C, uint32_t* status_out,
+                                   void* stream_v) {
+  int rc = check_problem(n_shards, M, K, N, AG_GEMM_F16, chunk_rows);
+  if (rc != AG_GEMM_OK) return rc;
+  Geometry g;
+  agg::make_geometry(g, n_shards, M, K, N, AG_GEMM_F16, chunk_rows);
+  const int64_t slots = g.S > 1 ? g.S - 1 : 1;
+  const size_t counter_bytes = round256(sizeof(uint32_t) * static_cast<size_t>(slots * g.Q));
+  const size_t staging_bytes = static_cast<size_t>(slots * g.R * g.K * 2);
+  const size_t need = kNoAllocCtrlBytes + counter_bytes + staging_bytes;
+  if (need > kNoAllocScratchBytes)
+    return fail(AG_GEMM_ERR_UNSUPPORTED,
+                "ag_gemm_run_noalloc: this problem needs %zu bytes of scratch, more than the "
+                "library's fixed %zu-byte array (use a plan instead)",
+                need, kNoAllocScratchBytes);
+  if (!shard_ptrs) return fail(AG_GEMM_ERR_INVALID, "shard_ptrs is NULL");
+  for (int s = 0; s < g.S; ++s)
+    if (!shard_ptrs[s] || !aligned16(shard_ptrs[s]))
+      return fail(AG_GEMM_ERR_INVALID, "shard_ptrs[%d] is NULL or not 16-byte aligned", s);
+  if (!B || !aligned16(B)) return fail(AG_GEMM_ERR_INVALID, "B is NULL or not 16-byte aligned");
+  if (!C || !aligned16(C)) return fail(AG_GEMM_ERR_INVALID, "C is NULL or not 16-byte aligned");
+  if (status_out && (reinterpret_cast<uintptr_t>(status_out) & 7u))
+    return fail(AG_GEMM_ERR_INVALID, "status_out is not 8-byte aligned");
+
+  int dev = 0;
+  cudaError_t e;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  NoAllocDevice* d = nullptr;
+  if ((rc = noalloc_setup(dev, &d)) != AG_GEMM_OK) return rc;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+
+  unsigned char* ctrl = d->scratch;
+  uint32_t* status = reinterpret_cast<uint32_t*>(ctrl);
+  unsigned long long* item_counter = reinterpret_cast<unsigned long long*>(ctrl + 256);
+  uint32_t* counters = reinterpret_cast<uint32_t*>(ctrl + kNoAllocCtrlBytes);
+  unsigned char* staging = ctrl + kNoAllocCtrlBytes + counter_bytes;
+
+  agg::FusedParams fp;
+  std::memset(&fp, 0, sizeof(fp));
+  fp.g = g;
+  for (int pos = 0; pos < g.S; ++pos) fp.src[pos] = shard_ptrs[agg::source_of(g, 0, pos)];
+  if ((rc = encode_a(&fp.tm_a_local, fp.src[0], g.R, g.K)) != AG_GEMM_OK ||
+      (rc = encode_b(&fp.tm_b, B, g.K, g.N)) != AG_GEMM_OK ||
+      (rc = encode_stage(&fp.tm_a_stage, staging, slots, g.R, g.K)) != AG_GEMM_OK)
+    return rc;
+  fp.staging = staging;
+  fp.counters = counters;
+  fp.item_counter = item_counter;
+  fp.item_base = 0;
+  fp.status = status;
+  fp.C = C;
+  fp.local = 0;
+  fp.epoch = 1;
+  fp.timeout_ns = 1000000000ull;
+  fp.pipe_timeout_ns = 4000000000ull;
+  fp.debug_skip_item = -1;
+  fp.flags = agg::kFlagGemm | agg::kFlagWait | (g.S > 1 ? agg::kFlagCopy : 0);
+  // Every call shares the array and finds the previous call's values in it:
+  // the status word, the item counter and the ready counters must start at zero.
+  if ((e = cudaMemsetAsync(ctrl, 0, kNoAllocCtrlBytes + counter_bytes, stream)) != cudaSuccess)
+    return cuda_fail(e, "clearing the no-allocation scratch");
+  if ((e = agg::launch_fused(fp, d->grid, stream)) != cudaSuccess)
+    return cuda_fail(e, "fused kernel launch");
+  if (status_out &&
+      (e = cudaMemcpyAsync(status_out, status, 2 * sizeof(uint32_t), cudaMemcpyDeviceToDevice,
+                           stream)) != cudaSuccess)
+    return cuda_fail(e, "status copy");
+  return AG_GEMM_OK;
+}

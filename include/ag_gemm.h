@@ -226,6 +226,40 @@ int ag_gemm_plan_set_debug(ag_gemm_plan *plan, int flags, int64_t arg);
 /* Number of CTAs the plan launches (one per SM, all co-resident). */
 int ag_gemm_plan_grid(const ag_gemm_plan *plan);
 
+/*
+ * fp16 AllGather+GEMM that allocates nothing (the pages have no counterpart
+ * of this entry point).  It is for callers that are not allowed to call
+ * cudaMalloc: for example a host application whose own allocator has already
+ * reserved the device's memory, or a latency-critical path on which
+ * cudaMalloc/cudaFree (which may synchronise the device and can take
+ * unbounded time) are not acceptable.  It runs the same PIPELINED fused kernel
+ * as ag_gemm_run with local rank 0, but the staging workspace, ready counters
+ * and status word live in a fixed 64 MiB array inside the library's device
+ * image, which every GPU that loads the library holds until the process
+ * exits.  Arguments are as for ag_gemm_plan_create + ag_gemm_run
+ * (chunk_rows = 0 picks the chunk size); the caller still provides the
+ * shards, B and C.  status_out (device pointer, 2 x uint32, 8-byte aligned,
+ * may be NULL) receives the status word of the run (0 = ok, low byte 1 or 2 =
+ * a device wait timed out).
+ *
+ * Limits and behaviour:
+ *  - the problem must need at most 64 MiB of scratch: 512 B + the counters
+ *    ((n_shards-1) * chunks per source * 4 B, rounded to 256 B) + the staging
+ *    workspace ((n_shards-1) * R * K * 2 B); larger problems are rejected with
+ *    AG_GEMM_ERR_UNSUPPORTED and a message giving the size needed;
+ *  - the first call on a device (with that device current) looks up the
+ *    array's device address and prepares the kernel; make that first call
+ *    before any stream capture;
+ *  - every call clears the counters and status in the array on `stream`
+ *    before its kernel; calls share the one array, so calls whose work
+ *    overlaps on the GPU (different streams without ordering between them)
+ *    race and give wrong results.
+ */
+int ag_gemm_run_noalloc(int n_shards, int64_t M, int64_t K, int64_t N,
+                        int64_t chunk_rows, const void *const *shard_ptrs,
+                        const void *B, float *C, uint32_t *status_out,
+                        void *stream);
+
 /* Thread-local code and text of the last error raised on this thread. */
 int ag_gemm_last_error(void);
 const char *ag_gemm_last_error_message(void);
