@@ -311,7 +311,7 @@ __device__ __forceinline__ void st_v4(void* ptr, uint32_t a, uint32_t b, uint32_
 
 template <bool kI8>
 __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int lane,
-                              uint64_t* tfull, uint64_t* tempty, uint32_t tmem,
+                              uint64_t* tfull, uint64_t* tempty, uint32_t tmem, uint8_t* sEpi,
                               volatile int* abort) {
   const Geometry& g = p.g;
   const volatile uint32_t* gstatus = p.status;
@@ -320,6 +320,8 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
   const uint32_t tempty0 = mapa_shared(smem_u32(tempty), 0);  // the even CTA's barriers
   const int64_t n_clusters = gridDim.x / 2, cluster = blockIdx.x / 2;
+  uint8_t* my_boxes = sEpi + quad * (2 * kEpiBoxBytes);  // this warp's two staging boxes
+  uint32_t boxes = 0;
   uint32_t unit = 0;
   for (int64_t t = cluster; t < g.tiles; t += n_clusters) {
     int pos;
@@ -336,22 +338,40 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
         if (lane == 0) {
           set_status(p.status, kStatusPipelineTimeout, 0x300u | rank);
           *abort = 1;
+          bulk_wait_group_all();
         }
         return;
       }
       tc_fence_after();
       if (!kI8) {
+        // 32 rows (one per lane) x 32 columns at a time: registers -> swizzled
+        // shared box -> one TMA store of 32 full 128-byte row segments.  Rows
+        // past the shard and columns past N are clipped by the descriptor.
+        const int64_t r0 = mt * kPairM + rank * kBlockM + quad * 32;
         for (int j = 0; j < g.BN / 32; ++j) {
           uint32_t v[32];
           tmem_ld32(lane_base + buf * 256u + j * 32, v);
           tmem_ld_wait();
           const int64_t n0 = nt * g.BN + j * 32;
-          if (row_ok) {
-            float* dst = p.C + grow * g.N + n0;
+          if (r0 >= g.R || n0 >= g.N) continue;  // warp-uniform: nothing of this box exists
+          uint8_t* box = my_boxes + (boxes & 1u) * kEpiBoxBytes;
+          if (lane == 0) bulk_wait_group_read<1>();  // the store that last read this box is done
+          __syncwarp();
+          uint8_t* row = box + lane * 128;
 #pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              if (n0 + e < g.N) st_v4(dst + e, v[e], v[e + 1], v[e + 2], v[e + 3]);
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t off = static_cast<uint32_t>((c ^ (lane & 7)) * 16);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(row + off)),
+                         "r"(v[4 * c]), "r"(v[4 * c + 1]), "r"(v[4 * c + 2]), "r"(v[4 * c + 3])
+                         : "memory");
           }
+          fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&p.tm_c, box, static_cast<int32_t>(n0), static_cast<int32_t>(r0), src);
+            bulk_commit_group();
+          }
+          ++boxes;
         }
       } else {
         const bool first = seg == 0, last = seg == nseg - 1;
@@ -413,6 +433,8 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
       ++unit;
     }
   }
+  if (lane == 0) bulk_wait_group_all();  // every C store performed before the CTA exits
+  __syncwarp();
 }
 
 // ------------------------------------------------------------------ kernel
@@ -424,7 +446,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kABytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kBBytes);
+  uint8_t* sEpi = sB + kStages * kBBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + kEpiBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
   uint64_t* tfull = bars + 2 * kStages;
@@ -468,7 +491,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp < 2 + kCopyWarpsPerCta) {
     if (p.flags & kFlagCopy) copy_warp<kI8>(p, lane);
   } else {
-    if (gemm) epilogue_warp<kI8>(p, rank, warp - 4, lane, tfull, tempty, tmem, abort);
+    if (gemm) epilogue_warp<kI8>(p, rank, warp - 4, lane, tfull, tempty, tmem, sEpi, abort);
   }
 
   tc_fence_before();

@@ -27,6 +27,7 @@ struct FusedParams {
   CUtensorMap tm_a_local;   // fp16 [R][K] local shard (2D: K, R)
   CUtensorMap tm_a_stage;   // fp16 [S-1][R][K] staging (3D: K, R, slot)
   CUtensorMap tm_b;         // fp16 [K][N] (2D: N, K), loaded MN-major
+  CUtensorMap tm_c;         // fp16 path: fp32 C as [S][R][N] (3D: N, R, S), stored in 32x32 boxes
   Geometry g;
   const void* src[kMaxShards];  // shard pointers by consumption position
   void* staging;                // fp16 [(S-1)][R][K]
@@ -51,7 +52,12 @@ struct FusedParams {
 constexpr int kThreads = 256;                         // 8 warps
 constexpr int kABytes = kBlockM * kBlockK * 2;        // 16 KB: this CTA's 128 rows of A
 constexpr int kBBytes = kMaxBlockN / 2 * kBlockK * 2; // 16 KB: this CTA's half of B's columns
-constexpr int kSmemBytes = kStages * (kABytes + kBBytes) + 1024 /*barriers*/ + 1024 /*align*/;
+// fp16 epilogue: each of the 4 epilogue warps stages 32 rows x 32 fp32 columns
+// (4 KB, 128-byte swizzled) in two buffers and writes them with TMA stores.
+constexpr int kEpiBoxBytes = 32 * 32 * 4;
+constexpr int kEpiBytes = 4 * 2 * kEpiBoxBytes;  // 32 KB
+constexpr int kSmemBytes =
+    kStages * (kABytes + kBBytes) + kEpiBytes + 1024 /*barriers*/ + 1024 /*align*/;
 constexpr int kCopyWarpsPerCta = 2;
 
 // Launchers (fused_kernel.cu).

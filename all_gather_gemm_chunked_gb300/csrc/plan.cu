@@ -57,18 +57,32 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// fp16 tensor, innermost dimension first; 128-byte swizzle, zero fill out of bounds.
-int encode_f16(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
-               const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+// Tensor, innermost dimension first; 128-byte swizzle, zero fill out of bounds.
+int encode_tiled(CUtensorMap* map, CUtensorMapDataType type, const void* base, int rank,
+                 const cuuint64_t* dims, const cuuint64_t* strides_bytes, const cuuint32_t* box) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return fail(AG_GEMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
   cuuint32_t estride[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, static_cast<cuuint32_t>(rank),
+  CUresult r = fn(map, type, static_cast<cuuint32_t>(rank),
                   const_cast<void*>(base), dims, strides_bytes, box, estride,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(AG_GEMM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   return AG_GEMM_OK;
+}
+
+int encode_f16(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
+               const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, base, rank, dims, strides_bytes, box);
+}
+
+// fp32 C viewed as [S][R][N] so that a box never crosses into the next shard's
+// rows: box 32 columns x 32 rows (128-byte rows, swizzled like the staging box).
+int encode_c(CUtensorMap* map, const void* base, int64_t S, int64_t R, int64_t N) {
+  cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)R, (cuuint64_t)S};
+  cuuint64_t strides[2] = {(cuuint64_t)N * 4, (cuuint64_t)R * N * 4};
+  cuuint32_t box[3] = {32, 32, 1};
+  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, 3, dims, strides, box);
 }
 
 // A operand rows x K (K contiguous), box 64 x 128.
@@ -202,6 +216,8 @@ struct ag_gemm_plan {
   CUtensorMap tm_a_cached{};
   const void* cached_b = nullptr;
   CUtensorMap tm_b_cached{};
+  const void* cached_c = nullptr;
+  CUtensorMap tm_c_cached{};
 };
 
 namespace {
@@ -287,8 +303,14 @@ int run_impl(ag_gemm_plan* p, const void* const* shard_ptrs, const void* B, floa
       if ((rc = encode_b(&p->tm_b_cached, B, g.K, g.N)) != AG_GEMM_OK) return rc;
       p->cached_b = B;
     }
+    if (p->cached_c != C) {
+      p->cached_c = nullptr;
+      if ((rc = encode_c(&p->tm_c_cached, C, g.S, g.R, g.N)) != AG_GEMM_OK) return rc;
+      p->cached_c = C;
+    }
     fp.tm_a_local = p->tm_a_cached;
     fp.tm_b = p->tm_b_cached;
+    fp.tm_c = p->tm_c_cached;
   }
   fp.tm_a_stage = p->tm_stage;
   fp.staging = p->staging;
@@ -704,7 +726,8 @@ extern "C" int ag_gemm_run_noalloc(int n_shards, int64_t M, int64_t K, int64_t N
   for (int pos = 0; pos < g.S; ++pos) fp.src[pos] = shard_ptrs[agg::source_of(g, 0, pos)];
   if ((rc = encode_a(&fp.tm_a_local, fp.src[0], g.R, g.K)) != AG_GEMM_OK ||
       (rc = encode_b(&fp.tm_b, B, g.K, g.N)) != AG_GEMM_OK ||
-      (rc = encode_stage(&fp.tm_a_stage, staging, slots, g.R, g.K)) != AG_GEMM_OK)
+      (rc = encode_stage(&fp.tm_a_stage, staging, slots, g.R, g.K)) != AG_GEMM_OK ||
+      (rc = encode_c(&fp.tm_c, C, g.S, g.R, g.N)) != AG_GEMM_OK)
     return rc;
   fp.staging = staging;
   fp.counters = counters;

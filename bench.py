@@ -236,10 +236,11 @@ def run_reference(args, w, rank):
     return 0
 
 
-def workload_config(w):
+def workload_config(w, flush=True):
     return {"workload": w.name, "n_shards": w.S, "M": w.M, "K": w.K, "N": w.N,
             "dtype": w.dtype, "chunk_rows": w.chunk_rows or "auto",
-            "l2": "flushed before each timed step (512 MiB write)"}
+            "l2": ("flushed before each timed step (512 MiB write)" if flush
+                   else "NOT flushed (analysis run; inputs may be L2-resident)")}
 
 
 # ---------------------------------------------------------------------------
@@ -287,7 +288,8 @@ def run_ours(args, w, rank, world, local_rank):
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(n)]
         for a, b in evs:
-            flush.fill_(1.0)
+            if not args.no_flush:
+                flush.fill_(1.0)
             a.record(stream)
             fn()
             b.record(stream)
@@ -388,7 +390,7 @@ def run_ours(args, w, rank, world, local_rank):
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "i8" if int8 else "f16", "data": "synthetic",
-        "config": workload_config(w),
+        "config": workload_config(w, not args.no_flush),
         "pct_of_peak": 100.0 * value / world / peak,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
         "gpu_launches": launches_per_run * args.steps, "modes": modes,
@@ -410,6 +412,8 @@ def main(argv=None):
     ap.add_argument("--ref-step-seconds", type=float, default=4.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-modes", action="store_true")
+    ap.add_argument("--no-flush", action="store_true",
+                    help="analysis only: keep inputs L2-resident between timed steps")
     args = ap.parse_args(argv)
 
     from all_gather_gemm_chunked_gb300 import synth
