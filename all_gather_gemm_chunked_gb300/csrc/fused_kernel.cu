@@ -26,8 +26,9 @@
 //   warps 2-3   copy warps ("comm blocks"): take copy items in consumption
 //               order from a grid-wide counter, copy (or, for int8, widen) them
 //               into the staging workspace and release the chunk's counter.
-//   warps 4-7   epilogue: TMEM -> registers -> global (fp32 C, or for int8
-//               the exact int32 fold, bias, int32 C and fp16 D).
+//   warps 4-11  epilogue: TMEM -> registers -> global (fp32 C, or for int8
+//               the exact int32 fold, bias, int32 C and fp16 D); warp w reads
+//               TMEM lane quadrant w % 4 and half of the tile's columns.
 //
 // No CTA ever waits for a copy item that only a specific other CTA could
 // perform: items are taken dynamically, so any resident CTA's copy warps make
@@ -310,7 +311,7 @@ __device__ __forceinline__ void st_v4(void* ptr, uint32_t a, uint32_t b, uint32_
 }
 
 template <bool kI8>
-__device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int lane,
+__device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int half, int lane,
                               uint64_t* tfull, uint64_t* tempty, uint32_t tmem, uint8_t* sEpi,
                               volatile int* abort) {
   const Geometry& g = p.g;
@@ -320,8 +321,9 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
   const uint32_t tempty0 = mapa_shared(smem_u32(tempty), 0);  // the even CTA's barriers
   const int64_t n_clusters = gridDim.x / 2, cluster = blockIdx.x / 2;
-  uint8_t* my_boxes = sEpi + quad * (2 * kEpiBoxBytes);  // this warp's two staging boxes
-  uint32_t boxes = 0;
+  const int nchunks = g.BN / 64;                      // 32-column chunks in this warp's half
+  const int chunk0 = half * nchunks;
+  uint8_t* box = sEpi + (half * 4 + quad) * kEpiBoxBytes;  // this warp's staging box
   uint32_t unit = 0;
   for (int64_t t = cluster; t < g.tiles; t += n_clusters) {
     int pos;
@@ -343,19 +345,33 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
         return;
       }
       tc_fence_after();
+      // Called once this warp has read its last accumulator column of the
+      // unit: the pair leader's MMA may then overwrite the buffer while this
+      // warp finishes converting and storing.
+      auto release = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (rank == 0)
+            mbar_arrive(&tempty[buf]);
+          else
+            mbar_arrive_cluster(tempty0 + buf * 8);
+        }
+      };
       if (!kI8) {
         // 32 rows (one per lane) x 32 columns at a time: registers -> swizzled
         // shared box -> one TMA store of 32 full 128-byte row segments.  Rows
         // past the shard and columns past N are clipped by the descriptor.
         const int64_t r0 = mt * kPairM + rank * kBlockM + quad * 32;
-        for (int j = 0; j < g.BN / 32; ++j) {
+        for (int jj = 0; jj < nchunks; ++jj) {
+          const int j = chunk0 + jj;
           uint32_t v[32];
           tmem_ld32(lane_base + buf * 256u + j * 32, v);
           tmem_ld_wait();
+          if (jj == nchunks - 1) release();
           const int64_t n0 = nt * g.BN + j * 32;
           if (r0 >= g.R || n0 >= g.N) continue;  // warp-uniform: nothing of this box exists
-          uint8_t* box = my_boxes + (boxes & 1u) * kEpiBoxBytes;
-          if (lane == 0) bulk_wait_group_read<1>();  // the store that last read this box is done
+          if (lane == 0) bulk_wait_group_read<0>();  // the previous store has read the box
           __syncwarp();
           uint8_t* row = box + lane * 128;
 #pragma unroll
@@ -371,15 +387,16 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
             tma_store_3d(&p.tm_c, box, static_cast<int32_t>(n0), static_cast<int32_t>(r0), src);
             bulk_commit_group();
           }
-          ++boxes;
         }
       } else {
         const bool first = seg == 0, last = seg == nseg - 1;
-        for (int j = 0; j < g.BN / 32; ++j) {
+        for (int jj = 0; jj < nchunks; ++jj) {
+          const int j = chunk0 + jj;
           uint32_t f[32], s[32];
           tmem_ld32(lane_base + j * 32, f);
           if (!first) tmem_ld32(lane_base + 256u + j * 32, s);
           tmem_ld_wait();
+          if (jj == nchunks - 1) release();
           // fp32 partial (an exact integer) -> int32, added to the running sum
           uint32_t acc[32];
 #pragma unroll
@@ -419,16 +436,8 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
             }
           }
         }
+        // the int32 sums must be in TMEM before this warp's next fold reads them
         if (!last) tmem_st_wait();
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        // the even CTA's MMA waits for all 8 epilogue warps of the pair
-        if (rank == 0)
-          mbar_arrive(&tempty[buf]);
-        else
-          mbar_arrive_cluster(tempty0 + buf * 8);
       }
       ++unit;
     }
@@ -467,7 +476,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 8);  // 4 epilogue warps in each CTA of the pair
+      mbar_init(&tempty[b], 2 * kEpiWarps);  // the epilogue warps of both CTAs of the pair
     }
     mbar_init(drain, 1);
     *tmem_slot = 0;
@@ -491,7 +500,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp < 2 + kCopyWarpsPerCta) {
     if (p.flags & kFlagCopy) copy_warp<kI8>(p, lane);
   } else {
-    if (gemm) epilogue_warp<kI8>(p, rank, warp - 4, lane, tfull, tempty, tmem, sEpi, abort);
+    if (gemm)
+      epilogue_warp<kI8>(p, rank, warp & 3, (warp - 4) >> 2, lane, tfull, tempty, tmem, sEpi,
+                         abort);
   }
 
   tc_fence_before();

@@ -49,20 +49,57 @@ struct FusedParams {
   uint32_t debug_delay_ns;
 };
 
-constexpr int kThreads = 256;                         // 8 warps
+constexpr int kThreads = 384;                         // 12 warps
+constexpr int kEpiWarps = 8;                          // 4 lane quadrants x 2 column halves
 constexpr int kABytes = kBlockM * kBlockK * 2;        // 16 KB: this CTA's 128 rows of A
 constexpr int kBBytes = kMaxBlockN / 2 * kBlockK * 2; // 16 KB: this CTA's half of B's columns
-// fp16 epilogue: each of the 4 epilogue warps stages 32 rows x 32 fp32 columns
-// (4 KB, 128-byte swizzled) in two buffers and writes them with TMA stores.
+// fp16 epilogue: each of the 8 epilogue warps stages 32 rows x 32 fp32 columns
+// (4 KB, 128-byte swizzled) in its own buffer and writes it with a TMA store.
 constexpr int kEpiBoxBytes = 32 * 32 * 4;
-constexpr int kEpiBytes = 4 * 2 * kEpiBoxBytes;  // 32 KB
+constexpr int kEpiBytes = kEpiWarps * kEpiBoxBytes;  // 32 KB
 constexpr int kSmemBytes =
     kStages * (kABytes + kBBytes) + kEpiBytes + 1024 /*barriers*/ + 1024 /*align*/;
 constexpr int kCopyWarpsPerCta = 2;
 
-// Launchers (fused_kernel.cu).
+// ---------------------------------------------------------------- skinny int8 path
+constexpr int kSkMaxRows = 128;   // the gathered A lives in TMEM: one lane per row
+
+struct SkinnyParams {
+  CUtensorMap tm_b8;        // int8 B (2D: N, K), box 128 x 64, 128-byte swizzle
+  CUtensorMap tm_a8_local;  // int8 local shard (2D: K, R), box 64 x R, 64-byte swizzle
+  CUtensorMap tm_a8_stage;  // int8 staging (3D: K, R, slot), box 64 x R x 1, 64-byte swizzle
+  Geometry g;
+  const void* src[kMaxShards];  // shard pointers by consumption position
+  int8_t* staging;              // int8 [S-1][R][K]
+  uint32_t* counters;           // [(S-1)][Q] ready counters, monotonic
+  unsigned long long* item_counter;
+  unsigned long long item_base;
+  int32_t* acc;                 // [M][N] int32 partial sums, zero between runs
+  uint32_t* tile_cnt;           // [n_tiles] finished units, monotonic
+  uint32_t* status;
+  const int32_t* bias;
+  const float* scale;
+  int32_t* C_i32;
+  uint16_t* D_f16;
+  int local;
+  int flags;
+  uint32_t epoch;               // ready-counter epoch (as the fused kernel)
+  uint32_t tile_epoch;          // GEMM launches since the last reset (>= 1)
+  uint64_t timeout_ns;
+  uint64_t pipe_timeout_ns;
+  int64_t debug_skip_item;
+  uint32_t debug_delay_ns;
+  int64_t n_tiles;              // ceil(N / 128)
+  int64_t k_segs;               // ceil(KB / 16): units per n-tile
+  int64_t units;                // n_tiles * k_segs
+};
+constexpr int kSkCopyWarpsPerCta = 1;
+
+// Launchers (fused_kernel.cu, skinny_kernel.cu).
 cudaError_t launch_fused(const FusedParams& p, int grid, cudaStream_t stream);
 cudaError_t fused_max_clusters(int dtype, int grid, int* clusters);
+cudaError_t skinny_prepare();
+cudaError_t launch_skinny(const SkinnyParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_widen(const int8_t* src0, uint16_t* dst0, int64_t n0, const int8_t* src1,
                          uint16_t* dst1, int64_t n1, int grid, cudaStream_t stream);
 
