@@ -211,8 +211,13 @@ __device__ void tma_warp(const FusedParams& p, uint32_t rank, uint8_t* sA, uint8
         else
           tma_load_3d_pair(a_dst, &p.tm_a_stage, bar, x, y, pos - 1);
         uint8_t* b_dst = sB + stage * kBBytes;
-        for (int i = 0; i < half / 64; ++i)
-          tma_load_2d_pair(b_dst + i * (64 * kBlockK * 2), &p.tm_b, bar, xb + i * 64, x);
+        // One TMA instruction per operand and k-block where possible: the TMA
+        // unit's per-instruction cost, not bandwidth, limits the ring on GB300.
+        if (p.b3d)
+          tma_load_3d_pair(b_dst, &p.tm_b, bar, 0, x, xb / 64);
+        else
+          for (int i = 0; i < half / 64; ++i)
+            tma_load_2d_pair(b_dst + i * (64 * kBlockK * 2), &p.tm_b, bar, xb + i * 64, x);
         issued |= 1u << stage;
         issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
         if (++stage == kStages) {

@@ -26,7 +26,7 @@ enum : int {
 struct FusedParams {
   CUtensorMap tm_a_local;   // fp16 [R][K] local shard (2D: K, R)
   CUtensorMap tm_a_stage;   // fp16 [S-1][R][K] staging (3D: K, R, slot)
-  CUtensorMap tm_b;         // fp16 [K][N] (2D: N, K), loaded MN-major
+  CUtensorMap tm_b;         // fp16 [K][N], loaded MN-major: 3D (64, K, N/64) when b3d, else 2D (N, K)
   CUtensorMap tm_c;         // fp16 path: fp32 C as [S][R][N] (3D: N, R, S), stored in 32x32 boxes
   Geometry g;
   const void* src[kMaxShards];  // shard pointers by consumption position
@@ -42,6 +42,7 @@ struct FusedParams {
   const float* scale;
   int local;                    // local rank
   int flags;                    // kFlag*
+  int b3d;                      // B half of a CTA in one 3D box (N % 64 == 0) instead of 64-wide 2D boxes
   uint32_t epoch;               // run number since the last reset (>= 1)
   uint64_t timeout_ns;          // limit of a wait on a ready counter
   uint64_t pipe_timeout_ns;     // limit of a wait on a pipeline mbarrier (longer)

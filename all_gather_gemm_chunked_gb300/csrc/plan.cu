@@ -59,13 +59,14 @@ EncodeTiledFn encode_fn() {
 
 // Tensor, innermost dimension first; 128-byte swizzle, zero fill out of bounds.
 int encode_tiled(CUtensorMap* map, CUtensorMapDataType type, const void* base, int rank,
-                 const cuuint64_t* dims, const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+                 const cuuint64_t* dims, const cuuint64_t* strides_bytes, const cuuint32_t* box,
+                 CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return fail(AG_GEMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
   cuuint32_t estride[3] = {1, 1, 1};
   CUresult r = fn(map, type, static_cast<cuuint32_t>(rank),
                   const_cast<void*>(base), dims, strides_bytes, box, estride,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(AG_GEMM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   return AG_GEMM_OK;
@@ -74,6 +75,30 @@ int encode_tiled(CUtensorMap* map, CUtensorMapDataType type, const void* base, i
 int encode_f16(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
                const cuuint64_t* strides_bytes, const cuuint32_t* box) {
   return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, base, rank, dims, strides_bytes, box);
+}
+
+// int8 descriptors of the skinny path: B (N, K) in 128 x 64 boxes with 128-byte
+// swizzle; a shard (K, R) and the int8 staging (K, R, slot) in 64 x R boxes
+// with 64-byte swizzle.
+int encode_b8(CUtensorMap* map, const void* base, int64_t K, int64_t N) {
+  cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)K};
+  cuuint64_t strides[1] = {(cuuint64_t)N};
+  cuuint32_t box[2] = {128, agg::kBlockK};
+  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, 2, dims, strides, box);
+}
+int encode_a8(CUtensorMap* map, const void* base, int64_t R, int64_t K) {
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)R};
+  cuuint64_t strides[1] = {(cuuint64_t)K};
+  cuuint32_t box[2] = {agg::kBlockK, (cuuint32_t)R};
+  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, 2, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_64B);
+}
+int encode_stage8(CUtensorMap* map, const void* base, int64_t slots, int64_t R, int64_t K) {
+  cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)R, (cuuint64_t)slots};
+  cuuint64_t strides[2] = {(cuuint64_t)K, (cuuint64_t)R * K};
+  cuuint32_t box[3] = {agg::kBlockK, (cuuint32_t)R, 1};
+  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, 3, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 // fp32 C viewed as [S][R][N] so that a box never crosses into the next shard's
@@ -101,8 +126,18 @@ int encode_stage(CUtensorMap* map, const void* base, int64_t slots, int64_t R, i
   return encode_f16(map, base, 3, dims, strides, box);
 }
 
-// B: K x N (N contiguous), box 64 (n) x 64 (k): one MN-major swizzle column group.
-int encode_b(CUtensorMap* map, const void* base, int64_t K, int64_t N) {
+// B: K x N (N contiguous), loaded MN-major in 64-column swizzle groups.  When
+// N % 64 == 0 it is described as 3D (64 columns, K, N / 64 groups) so that one
+// box brings a CTA's whole half of the tile (BN / 128 groups); otherwise as 2D
+// (N, K) with one 64 x 64 box per group.
+bool b_is_3d(int64_t N) { return N % 64 == 0; }
+int encode_b(CUtensorMap* map, const void* base, int64_t K, int64_t N, int BN) {
+  if (b_is_3d(N)) {
+    cuuint64_t dims[3] = {64, (cuuint64_t)K, (cuuint64_t)N / 64};
+    cuuint64_t strides[2] = {(cuuint64_t)N * 2, 128};
+    cuuint32_t box[3] = {64, agg::kBlockK, (cuuint32_t)(BN / 128)};
+    return encode_f16(map, base, 3, dims, strides, box);
+  }
   cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)K};
   cuuint64_t strides[1] = {(cuuint64_t)N * 2};
   cuuint32_t box[2] = {64, agg::kBlockK};
@@ -218,6 +253,18 @@ struct ag_gemm_plan {
   CUtensorMap tm_b_cached{};
   const void* cached_c = nullptr;
   CUtensorMap tm_c_cached{};
+  // int8 with at most 128 gathered rows: the skinny kernel
+  bool skinny = false;
+  int sk_grid = 0;
+  int32_t* acc = nullptr;        // [M][N] int32 partial sums (zero between runs)
+  uint32_t* tile_cnt = nullptr;  // [n-tiles of 128] finished units (monotonic)
+  int64_t sk_tiles = 0, sk_segs = 0;
+  uint32_t tile_epoch = 0;
+  CUtensorMap tm_stage8{};
+  const void* cached_a8 = nullptr;
+  CUtensorMap tm_a8_cached{};
+  const void* cached_b8 = nullptr;
+  CUtensorMap tm_b8_cached{};
 };
 
 namespace {
@@ -231,8 +278,31 @@ void free_plan(ag_gemm_plan* p) {
   cudaFree(p->status);
   cudaFree(p->b16);
   cudaFree(p->a16);
+  cudaFree(p->acc);
+  cudaFree(p->tile_cnt);
   if (p->done) cudaEventDestroy(p->done);
   delete p;
+}
+
+int launch_skinny(ag_gemm_plan* p, agg::SkinnyParams& sp, int flags, cudaStream_t stream) {
+  sp.flags = flags;
+  sp.item_base = p->item_base;
+  if (flags & agg::kFlagGemm) {
+    // each GEMM launch adds k_segs to every n-tile counter
+    if (static_cast<uint64_t>(p->tile_epoch + 1) * static_cast<uint64_t>(p->sk_segs) >= (1ull << 31)) {
+      cudaError_t e = cudaMemsetAsync(p->tile_cnt, 0, sizeof(uint32_t) * p->sk_tiles, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "tile counter reset");
+      p->tile_epoch = 0;
+    }
+    p->tile_epoch += 1;
+  }
+  sp.tile_epoch = p->tile_epoch;
+  cudaError_t e = agg::launch_skinny(sp, p->sk_grid, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "skinny kernel launch");
+  if (flags & agg::kFlagCopy)
+    p->item_base += static_cast<unsigned long long>(p->g.items) +
+                    static_cast<unsigned long long>(p->sk_grid) * agg::kSkCopyWarpsPerCta;
+  return AG_GEMM_OK;
 }
 
 int launch_fused(ag_gemm_plan* p, agg::FusedParams& fp, int flags, cudaStream_t stream) {
@@ -300,7 +370,7 @@ int run_impl(ag_gemm_plan* p, const void* const* shard_ptrs, const void* B, floa
     }
     if (p->cached_b != B) {
       p->cached_b = nullptr;
-      if ((rc = encode_b(&p->tm_b_cached, B, g.K, g.N)) != AG_GEMM_OK) return rc;
+      if ((rc = encode_b(&p->tm_b_cached, B, g.K, g.N, g.BN)) != AG_GEMM_OK) return rc;
       p->cached_b = B;
     }
     if (p->cached_c != C) {
@@ -323,6 +393,7 @@ int run_impl(ag_gemm_plan* p, const void* const* shard_ptrs, const void* B, floa
   fp.bias = bias;
   fp.scale = scale;
   fp.local = p->local;
+  fp.b3d = b_is_3d(g.N) ? 1 : 0;
   fp.epoch = p->epoch + 1;
   fp.timeout_ns = p->timeout_ns;
   // Pipeline stages only wait on each other; give them more room than the
@@ -340,6 +411,69 @@ int run_impl(ag_gemm_plan* p, const void* const* shard_ptrs, const void* B, floa
     // fp16 0x7E7E is a NaN: a tile read before its chunk landed turns C into NaN.
     e = cudaMemsetAsync(p->staging, 0x7E, static_cast<size_t>(p->staging_bytes), stream);
     if (e != cudaSuccess) return cuda_fail(e, "poison staging");
+  }
+  if (p->skinny) {
+    agg::SkinnyParams sp;
+    std::memset(&sp, 0, sizeof(sp));
+    sp.g = g;
+    for (int pos = 0; pos < g.S; ++pos) sp.src[pos] = fp.src[pos];
+    if (p->cached_b8 != B) {
+      p->cached_b8 = nullptr;
+      if ((rc = encode_b8(&p->tm_b8_cached, B, g.K, g.N)) != AG_GEMM_OK) return rc;
+      p->cached_b8 = B;
+    }
+    if (p->cached_a8 != local_ptr) {
+      p->cached_a8 = nullptr;
+      if ((rc = encode_a8(&p->tm_a8_cached, local_ptr, g.R, g.K)) != AG_GEMM_OK) return rc;
+      p->cached_a8 = local_ptr;
+    }
+    sp.tm_b8 = p->tm_b8_cached;
+    sp.tm_a8_local = p->tm_a8_cached;
+    sp.tm_a8_stage = p->tm_stage8;
+    sp.staging = static_cast<int8_t*>(p->staging);
+    sp.counters = p->counters;
+    sp.item_counter = p->item_counter;
+    sp.acc = p->acc;
+    sp.tile_cnt = p->tile_cnt;
+    sp.status = p->status;
+    sp.bias = bias;
+    sp.scale = scale;
+    sp.C_i32 = C_i32;
+    sp.D_f16 = static_cast<uint16_t*>(D);
+    sp.local = p->local;
+    sp.epoch = fp.epoch;
+    sp.timeout_ns = fp.timeout_ns;
+    sp.pipe_timeout_ns = fp.pipe_timeout_ns;
+    sp.debug_skip_item = fp.debug_skip_item;
+    sp.debug_delay_ns = fp.debug_delay_ns;
+    sp.n_tiles = p->sk_tiles;
+    sp.k_segs = p->sk_segs;
+    sp.units = p->sk_tiles * p->sk_segs;
+    using namespace agg;
+    switch (mode) {
+      case AG_GEMM_MODE_PIPELINED:
+        rc = launch_skinny(p, sp, kFlagGemm | kFlagWait | (runs_copy ? kFlagCopy : 0), stream);
+        break;
+      case AG_GEMM_MODE_COMPUTE_ONLY:
+        rc = launch_skinny(p, sp, kFlagGemm, stream);
+        break;
+      case AG_GEMM_MODE_SEQUENTIAL:
+        rc = runs_copy ? launch_skinny(p, sp, kFlagCopy, stream) : AG_GEMM_OK;
+        if (rc == AG_GEMM_OK) rc = launch_skinny(p, sp, kFlagGemm | kFlagWait, stream);
+        break;
+      case AG_GEMM_MODE_COPY_ONLY:
+        rc = runs_copy ? launch_skinny(p, sp, kFlagCopy, stream) : AG_GEMM_OK;
+        break;
+      default:
+        rc = fail(AG_GEMM_ERR_STATE, "unknown mode %d", mode);
+    }
+    if (rc != AG_GEMM_OK) return rc;
+    if (runs_copy) p->epoch += 1;
+    e = cudaEventRecord(p->done, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    p->last_stream = stream;
+    p->has_run = true;
+    return AG_GEMM_OK;
   }
   if (int8 && runs_gemm) {
     e = agg::launch_widen(static_cast<const int8_t*>(B), p->b16, g.K * g.N,
@@ -484,7 +618,25 @@ ag_gemm_plan* ag_gemm_plan_create(int n_shards, int64_t M, int64_t K, int64_t N,
     free_plan(p);
     return nullptr;
   }
-  if (dtype == AG_GEMM_I8) {
+  p->skinny = dtype == AG_GEMM_I8 && g.M <= agg::kSkMaxRows && g.R % 8 == 0;
+  if (p->skinny) {
+    p->sk_tiles = (g.N + 127) / 128;
+    p->sk_segs = (g.KB + agg::kSegBlocks - 1) / agg::kSegBlocks;
+    p->sk_grid = p->sm_count;
+    if ((e = agg::skinny_prepare()) != cudaSuccess ||
+        (e = cudaMalloc(&p->acc, static_cast<size_t>(g.M * g.N * 4))) != cudaSuccess ||
+        (e = cudaMalloc(&p->tile_cnt, sizeof(uint32_t) * p->sk_tiles)) != cudaSuccess ||
+        (e = cudaMemset(p->acc, 0, static_cast<size_t>(g.M * g.N * 4))) != cudaSuccess ||
+        (e = cudaMemset(p->tile_cnt, 0, sizeof(uint32_t) * p->sk_tiles)) != cudaSuccess) {
+      cuda_fail(e, "plan allocation (skinny int8 path)");
+      free_plan(p);
+      return nullptr;
+    }
+    if (encode_stage8(&p->tm_stage8, p->staging, slots, g.R, g.K) != AG_GEMM_OK) {
+      free_plan(p);
+      return nullptr;
+    }
+  } else if (dtype == AG_GEMM_I8) {
     if ((e = cudaMalloc(&p->b16, static_cast<size_t>(g.K * g.N * 2))) != cudaSuccess ||
         (e = cudaMalloc(&p->a16, static_cast<size_t>(g.R * g.K * 2))) != cudaSuccess) {
       cuda_fail(e, "plan allocation (int8 widening buffers)");
@@ -492,7 +644,7 @@ ag_gemm_plan* ag_gemm_plan_create(int n_shards, int64_t M, int64_t K, int64_t N,
       return nullptr;
     }
     if (encode_a(&p->tm_a16, p->a16, g.R, g.K) != AG_GEMM_OK ||
-        encode_b(&p->tm_b16, p->b16, g.K, g.N) != AG_GEMM_OK) {
+        encode_b(&p->tm_b16, p->b16, g.K, g.N, g.BN) != AG_GEMM_OK) {
       free_plan(p);
       return nullptr;
     }
@@ -573,11 +725,15 @@ int ag_gemm_plan_reset(ag_gemm_plan* plan, void* stream_v) {
     return cuda_fail(e, "cudaStreamWaitEvent");
   if ((e = cudaMemsetAsync(plan->counters, 0, sizeof(uint32_t) * plan->counter_count, stream)) != cudaSuccess ||
       (e = cudaMemsetAsync(plan->item_counter, 0, sizeof(unsigned long long), stream)) != cudaSuccess ||
+      (plan->skinny &&
+       ((e = cudaMemsetAsync(plan->tile_cnt, 0, sizeof(uint32_t) * plan->sk_tiles, stream)) != cudaSuccess ||
+        (e = cudaMemsetAsync(plan->acc, 0, static_cast<size_t>(plan->g.M * plan->g.N * 4), stream)) != cudaSuccess)) ||
       (e = cudaMemsetAsync(plan->status, 0, 2 * sizeof(uint32_t), stream)) != cudaSuccess ||
       (e = cudaEventRecord(plan->done, stream)) != cudaSuccess)
     return cuda_fail(e, "plan reset");
   plan->epoch = 0;
   plan->item_base = 0;
+  plan->tile_epoch = 0;
   plan->last_stream = stream;
   plan->has_run = true;
   return AG_GEMM_OK;
@@ -725,7 +881,7 @@ extern "C" int ag_gemm_run_noalloc(int n_shards, int64_t M, int64_t K, int64_t N
   fp.g = g;
   for (int pos = 0; pos < g.S; ++pos) fp.src[pos] = shard_ptrs[agg::source_of(g, 0, pos)];
   if ((rc = encode_a(&fp.tm_a_local, fp.src[0], g.R, g.K)) != AG_GEMM_OK ||
-      (rc = encode_b(&fp.tm_b, B, g.K, g.N)) != AG_GEMM_OK ||
+      (rc = encode_b(&fp.tm_b, B, g.K, g.N, g.BN)) != AG_GEMM_OK ||
       (rc = encode_stage(&fp.tm_a_stage, staging, slots, g.R, g.K)) != AG_GEMM_OK ||
       (rc = encode_c(&fp.tm_c, C, g.S, g.R, g.N)) != AG_GEMM_OK)
     return rc;
@@ -736,6 +892,7 @@ extern "C" int ag_gemm_run_noalloc(int n_shards, int64_t M, int64_t K, int64_t N
   fp.status = status;
   fp.C = C;
   fp.local = 0;
+  fp.b3d = b_is_3d(g.N) ? 1 : 0;
   fp.epoch = 1;
   fp.timeout_ns = 1000000000ull;
   fp.pipe_timeout_ns = 4000000000ull;

@@ -130,7 +130,7 @@ class ClockSampler:
             os.close(fd)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -301,6 +301,11 @@ def run_ours(args, w, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     if plan.status() != 0:
         raise RuntimeError(f"warm-up run failed: status {plan.status_word():#x}")
+    if args.steps is None:
+        # size the timed region so that the clock sampler sees it for ~2 s
+        est = float(np.median(timed(5, B_.MODE_PIPELINED))) * 1e-3 + 1e-4  # + flush
+        args.steps = int(min(20000, max(20, np.ceil(2.0 / est))))
+        args.steps = int(reduce_max(args.steps, dev))
 
     clocks = ClockSampler(local_rank)
     barrier()
@@ -404,7 +409,8 @@ def run_ours(args, w, rank, world, local_rank):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: enough for ~2 s of timed GPU work, >= 20)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
@@ -426,6 +432,8 @@ def main(argv=None):
         dist.init_process_group(backend=backend)
     try:
         if args.impl == "reference":
+            if args.steps is None:
+                args.steps = 10
             return run_reference(args, w, rank)
         return run_ours(args, w, rank, world, local_rank)
     finally:

@@ -318,3 +318,65 @@ def test_i8_full_size_workload(oracle, wid):
     with np.errstate(over="ignore"):
         want = (Ci.astype(np.float32) * x["scale"][None, :]).astype(np.float16)
     assert f16_ulp_distance(D, want).max() <= 1
+
+
+# ---------------------------------------------------------------------------
+# int8 with few gathered rows (the B-streaming skinny kernel: M <= 128, R % 8 == 0)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("S,R,K,N,c", [
+    (2, 32, 1056, 208, 0),     # two K segments + a K tail, a ragged 128-column n-tile
+    (4, 8, 64, 16, 0),         # one k-block, one tiny n-tile
+    (2, 64, 2048, 384, 16),    # 128 rows (every TMEM lane)
+    (1, 40, 512, 128, 0),      # a single shard
+    (3, 16, 4096, 256, 2),
+])
+def test_i8_skinny_full(oracle, S, R, K, N, c):
+    x = synth.make_inputs(S, R, K, N, "i8", 3000 + S * 13 + K)
+    Ci, D = run_i8(x, S, R, K, N, c)
+    Cref, Dref = oracle.ag_gemm_dequant(x["shards"], x["B"], x["bias"], x["scale"])
+    _check_i8(Ci, D, Cref, Dref, f"skinny S={S} R={R} K={K} N={N}")
+
+
+def test_i8_skinny_worst_case_magnitudes_exact(oracle):
+    S, R, K, N = 2, 32, 16384, 256
+    rng = np.random.default_rng(6)
+    shards = [np.full((R, K), 127, np.int8), np.full((R, K), -127, np.int8)]
+    Bm = np.full((K, N), 127, np.int8)
+    Bm[:, ::5] = -127
+    x = {"shards": shards, "B": Bm, "bias": rng.integers(-1000, 1001, N, dtype=np.int32),
+         "scale": rng.uniform(1e-5, 1e-4, N).astype(np.float32)}
+    Ci, D = run_i8(x, S, R, K, N)
+    Cref, Dref = oracle.ag_gemm_dequant(x["shards"], x["B"], x["bias"], x["scale"])
+    _check_i8(Ci, D, Cref, Dref, "skinny worst case")
+
+
+def test_i8_skinny_modes_local_rank_and_repeats():
+    S, R, K, N = 2, 32, 2048, 640
+    x = synth.make_inputs(S, R, K, N, "i8", 91)
+    ref = run_i8(x, S, R, K, N)
+    with Plan(S, S * R, K, N, "i8") as plan:
+        for mode in (B_.MODE_SEQUENTIAL, B_.MODE_PIPELINED, B_.MODE_COMPUTE_ONLY,
+                     B_.MODE_PIPELINED, B_.MODE_PIPELINED):
+            got = run_i8(x, S, R, K, N, plan=plan, mode=mode)
+            assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])
+    for local in range(S):
+        got = run_i8(x, S, R, K, N, local=local)
+        assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])
+
+
+def test_i8_skinny_timeout_then_reset():
+    S, R, K, N = 2, 32, 1024, 256
+    x = synth.make_inputs(S, R, K, N, "i8", 92)
+    ref = run_i8(x, S, R, K, N)
+    with Plan(S, S * R, K, N, "i8") as plan:
+        plan.set_timeout_ns(20_000_000)
+        plan.set_debug(B_.DEBUG_SKIP_ITEM, 5)
+        shards = [_to_dev(s) for s in x["shards"]]
+        plan.dequant_run(shards, _to_dev(x["B"]), _to_dev(x["bias"]), _to_dev(x["scale"]))
+        torch.cuda.synchronize()
+        assert plan.status() == B_.ERR_TIMEOUT
+        plan.set_debug(0, 0)
+        plan.reset()
+        got = run_i8(x, S, R, K, N, plan=plan)
+        assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])
