@@ -76,7 +76,6 @@ struct SkinnyParams {
   unsigned long long* item_counter;
   unsigned long long item_base;
   int32_t* acc;                 // [M][N] int32 partial sums, zero between runs
-  uint32_t* tile_cnt;           // [n_tiles] finished units, monotonic
   uint32_t* status;
   const int32_t* bias;
   const float* scale;
@@ -85,14 +84,11 @@ struct SkinnyParams {
   int local;
   int flags;
   uint32_t epoch;               // ready-counter epoch (as the fused kernel)
-  uint32_t tile_epoch;          // GEMM launches since the last reset (>= 1)
   uint64_t timeout_ns;
   uint64_t pipe_timeout_ns;
   int64_t debug_skip_item;
   uint32_t debug_delay_ns;
   int64_t n_tiles;              // ceil(N / 128)
-  int64_t k_segs;               // ceil(KB / 16): units per n-tile
-  int64_t units;                // n_tiles * k_segs
 };
 constexpr int kSkCopyWarpsPerCta = 1;
 

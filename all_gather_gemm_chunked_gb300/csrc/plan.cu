@@ -257,9 +257,7 @@ struct ag_gemm_plan {
   bool skinny = false;
   int sk_grid = 0;
   int32_t* acc = nullptr;        // [M][N] int32 partial sums (zero between runs)
-  uint32_t* tile_cnt = nullptr;  // [n-tiles of 128] finished units (monotonic)
-  int64_t sk_tiles = 0, sk_segs = 0;
-  uint32_t tile_epoch = 0;
+  int64_t sk_tiles = 0;          // 128-column n-tiles
   CUtensorMap tm_stage8{};
   const void* cached_a8 = nullptr;
   CUtensorMap tm_a8_cached{};
@@ -279,7 +277,6 @@ void free_plan(ag_gemm_plan* p) {
   cudaFree(p->b16);
   cudaFree(p->a16);
   cudaFree(p->acc);
-  cudaFree(p->tile_cnt);
   if (p->done) cudaEventDestroy(p->done);
   delete p;
 }
@@ -287,16 +284,6 @@ void free_plan(ag_gemm_plan* p) {
 int launch_skinny(ag_gemm_plan* p, agg::SkinnyParams& sp, int flags, cudaStream_t stream) {
   sp.flags = flags;
   sp.item_base = p->item_base;
-  if (flags & agg::kFlagGemm) {
-    // each GEMM launch adds k_segs to every n-tile counter
-    if (static_cast<uint64_t>(p->tile_epoch + 1) * static_cast<uint64_t>(p->sk_segs) >= (1ull << 31)) {
-      cudaError_t e = cudaMemsetAsync(p->tile_cnt, 0, sizeof(uint32_t) * p->sk_tiles, stream);
-      if (e != cudaSuccess) return cuda_fail(e, "tile counter reset");
-      p->tile_epoch = 0;
-    }
-    p->tile_epoch += 1;
-  }
-  sp.tile_epoch = p->tile_epoch;
   cudaError_t e = agg::launch_skinny(sp, p->sk_grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "skinny kernel launch");
   if (flags & agg::kFlagCopy)
@@ -434,7 +421,6 @@ int run_impl(ag_gemm_plan* p, const void* const* shard_ptrs, const void* B, floa
     sp.counters = p->counters;
     sp.item_counter = p->item_counter;
     sp.acc = p->acc;
-    sp.tile_cnt = p->tile_cnt;
     sp.status = p->status;
     sp.bias = bias;
     sp.scale = scale;
@@ -447,8 +433,6 @@ int run_impl(ag_gemm_plan* p, const void* const* shard_ptrs, const void* B, floa
     sp.debug_skip_item = fp.debug_skip_item;
     sp.debug_delay_ns = fp.debug_delay_ns;
     sp.n_tiles = p->sk_tiles;
-    sp.k_segs = p->sk_segs;
-    sp.units = p->sk_tiles * p->sk_segs;
     using namespace agg;
     switch (mode) {
       case AG_GEMM_MODE_PIPELINED:
@@ -621,13 +605,10 @@ ag_gemm_plan* ag_gemm_plan_create(int n_shards, int64_t M, int64_t K, int64_t N,
   p->skinny = dtype == AG_GEMM_I8 && g.M <= agg::kSkMaxRows && g.R % 8 == 0;
   if (p->skinny) {
     p->sk_tiles = (g.N + 127) / 128;
-    p->sk_segs = (g.KB + agg::kSegBlocks - 1) / agg::kSegBlocks;
     p->sk_grid = p->sm_count;
     if ((e = agg::skinny_prepare()) != cudaSuccess ||
         (e = cudaMalloc(&p->acc, static_cast<size_t>(g.M * g.N * 4))) != cudaSuccess ||
-        (e = cudaMalloc(&p->tile_cnt, sizeof(uint32_t) * p->sk_tiles)) != cudaSuccess ||
-        (e = cudaMemset(p->acc, 0, static_cast<size_t>(g.M * g.N * 4))) != cudaSuccess ||
-        (e = cudaMemset(p->tile_cnt, 0, sizeof(uint32_t) * p->sk_tiles)) != cudaSuccess) {
+        (e = cudaMemset(p->acc, 0, static_cast<size_t>(g.M * g.N * 4))) != cudaSuccess) {
       cuda_fail(e, "plan allocation (skinny int8 path)");
       free_plan(p);
       return nullptr;
@@ -726,14 +707,12 @@ int ag_gemm_plan_reset(ag_gemm_plan* plan, void* stream_v) {
   if ((e = cudaMemsetAsync(plan->counters, 0, sizeof(uint32_t) * plan->counter_count, stream)) != cudaSuccess ||
       (e = cudaMemsetAsync(plan->item_counter, 0, sizeof(unsigned long long), stream)) != cudaSuccess ||
       (plan->skinny &&
-       ((e = cudaMemsetAsync(plan->tile_cnt, 0, sizeof(uint32_t) * plan->sk_tiles, stream)) != cudaSuccess ||
-        (e = cudaMemsetAsync(plan->acc, 0, static_cast<size_t>(plan->g.M * plan->g.N * 4), stream)) != cudaSuccess)) ||
+       (e = cudaMemsetAsync(plan->acc, 0, static_cast<size_t>(plan->g.M * plan->g.N * 4), stream)) != cudaSuccess) ||
       (e = cudaMemsetAsync(plan->status, 0, 2 * sizeof(uint32_t), stream)) != cudaSuccess ||
       (e = cudaEventRecord(plan->done, stream)) != cudaSuccess)
     return cuda_fail(e, "plan reset");
   plan->epoch = 0;
   plan->item_base = 0;
-  plan->tile_epoch = 0;
   plan->last_stream = stream;
   plan->has_run = true;
   return AG_GEMM_OK;

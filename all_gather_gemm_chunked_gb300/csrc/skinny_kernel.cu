@@ -6,32 +6,34 @@
 // shared by all rows, so the kernel streams B exactly once as int8, widens it
 // in shared memory and runs the tensor core on it with the (tiny) A held in
 // tensor memory.  sm_103a has no tcgen05 kind::i8, so the product is computed
-// exactly on kind::f16: every int8 is an exact fp16, and a unit never spans
-// more than 16 k-blocks (1024 k), which keeps every fp32 partial an integer
-// below 2^24.
+// exactly on kind::f16: every int8 is an exact fp16, and an fp32 accumulation
+// never spans more than 16 k-blocks (1024 k), which keeps every fp32 partial an
+// integer below 2^24; segments are folded into an int32 sum in TMEM.
 //
-// Work unit = (128-column n-tile, segment of <= 16 k-blocks); CTA b takes
-// units b, b + grid, ...  A unit's exact int32 partial is added with
-// coalesced red.add.s32 to an L2-resident int32 accumulator (integer addition
-// is exact in any order); the last unit of an n-tile to finish (a monotonic
-// per-n-tile counter reaching epoch * segments) adds the bias, writes C_i32
-// and the fp16 dequant D, and zeroes the accumulator for the next run.
+// Work: the (128-column n-tile, k-block) units, n-tile major, are cut into one
+// contiguous range per CTA (stream-K), so a CTA holds at most a few pieces of
+// n-tiles.  At the end of a piece its exact int32 sums (all rows x 128 columns)
+// are added with coalesced red.add.s32 into an L2-resident int32 accumulator
+// (integer addition is exact in any order).  A small stream-ordered kernel
+// (ag_skinny_finish_kernel) then adds the bias, writes C_i32 and the fp16
+// dequant D, and zeroes the accumulator for the next run.
 //
-// Roles (16 warps):
-//   warp 6      TMA warp: waits once for every remote chunk (the rows of the
-//               other shards, copied by the copy warps), then streams int8
-//               k-blocks of B (64 x 128) and of A (all rows x 64) into a raw
-//               shared-memory ring.
-//   warps 0-3   B widening: raw int8 B -> fp16 in the MN-major 128-byte
-//               swizzled layout the MMA reads.
-//   warps 8-11  A widening: raw int8 A rows -> fp16 -> tcgen05.st into TMEM
-//               (one row per TMEM lane; the MMA's A operand comes from TMEM).
-//   warp 4      MMA: one thread issues tcgen05.mma (M = 128, N = 128, K = 16).
-//   warp 5      copy warp: copies remote chunks into the int8 staging
-//               workspace and releases their ready counters.
-//   warps 12-15 epilogue: fp32 accumulator -> int32 -> transpose through
-//               shared memory -> red.add.s32; the n-tile's last unit finishes
-//               the dequant.
+// Roles (20 warps):
+//   warp 6        TMA warp: streams int8 k-blocks of B (64 x 128) and of A (all
+//                 rows x 64) into a raw ring; the B loads of the first stages go
+//                 out before it waits once for every remote chunk (the rows of
+//                 the other shards, copied by the copy warp).
+//   warps 0-3     B widening: raw int8 B -> fp16 in the MN-major 128-byte
+//                 swizzled layout the MMA reads.
+//   warps 8-11,   A widening: raw int8 rows -> fp16 -> tcgen05.st into TMEM (one
+//   16-19         row per lane; the MMA's A operand comes from TMEM); warp w
+//                 serves lane quadrant w % 4, the two warps of a quadrant take
+//                 alternate k-blocks.
+//   warp 4        MMA: one thread issues tcgen05.mma (M = 128, N = 128, K = 16).
+//   warp 5        copy warp: copies remote chunks into the int8 staging
+//                 workspace and releases their ready counters.
+//   warps 12-15   epilogue: fold fp32 segments into the int32 sums in TMEM;
+//                 flush each finished piece through shared memory with red.add.
 
 #include <cuda_fp16.h>
 
@@ -42,18 +44,21 @@ namespace agg {
 
 namespace {
 
-constexpr int kSkThreads = 512;
+constexpr int kSkWarps = 20;
+constexpr int kSkThreads = kSkWarps * 32;
 constexpr int kSkN = 128;              // n-tile
-constexpr int kSkRaw = 8;              // raw int8 ring stages
-constexpr int kSkFp = 4;               // fp16 B stages = A TMEM stages
+constexpr int kSkRaw = 6;              // raw int8 ring stages
+constexpr int kSkFp = 6;               // fp16 B stages
+constexpr int kSkA = 4;                // A stages in TMEM (32 columns each)
 constexpr int kSkRawB = kSkN * kBlockK;              // 8 KB int8
 constexpr int kSkRawA = kSkMaxRows * kBlockK;        // 8 KB int8 (<= 128 rows)
 constexpr int kSkRawStage = kSkRawB + kSkRawA;
 constexpr int kSkFpStage = kSkN * kBlockK * 2;       // 16 KB fp16
 constexpr int kSkTrans = 4 * 32 * 33 * 4;            // epilogue transposes
 constexpr int kSkSmem = kSkRaw * kSkRawStage + kSkFp * kSkFpStage + kSkTrans + 1024 + 1024;
-constexpr uint32_t kSkAcol = 0;        // TMEM columns [0, 128): A stages (32 each)
-constexpr uint32_t kSkDcol = 128;      // TMEM columns [128, 384): two 128-column accumulators
+constexpr uint32_t kSkAcol = 0;        // TMEM columns [0, 128): A stages
+constexpr uint32_t kSkDcol = 128;      // [128, 384): two fp32 accumulators
+constexpr uint32_t kSkScol = 384;      // [384, 512): int32 running sums
 
 __device__ __forceinline__ void sk_set_status(uint32_t* status, uint32_t kind, uint32_t detail) {
   if (atomicCAS(status, 0u, kind) == 0u) atomicExch(status + 1, detail);
@@ -66,12 +71,11 @@ __device__ __forceinline__ void widen16x(const uint4 v, uint4& a, uint4& b) {
   i8x4_to_f16x4(v.w, b.z, b.w);
 }
 
-__device__ __forceinline__ void unit_coords(const SkinnyParams& p, int64_t u, int64_t& nt,
-                                            int64_t& kb0, int64_t& kb1) {
-  nt = u % p.n_tiles;
-  const int64_t seg = u / p.n_tiles;
-  kb0 = seg * kSegBlocks;
-  kb1 = kb0 + kSegBlocks < p.g.KB ? kb0 + kSegBlocks : p.g.KB;
+// This CTA's unit range [u0, u1) of the n-major (n-tile, k-block) space.
+__device__ __forceinline__ void cta_range(const SkinnyParams& p, int64_t& u0, int64_t& u1) {
+  const int64_t U = p.n_tiles * p.g.KB;
+  u0 = U * blockIdx.x / gridDim.x;
+  u1 = U * (blockIdx.x + 1) / gridDim.x;
 }
 
 // ------------------------------------------------------------------ copy warp
@@ -138,56 +142,84 @@ __device__ bool sk_wait_all_chunks(const SkinnyParams& p, int lane, volatile int
   return ok;
 }
 
+__device__ __forceinline__ void sk_issue_a(const SkinnyParams& p, uint8_t* st, uint64_t* bar,
+                                           int32_t x) {
+  const Geometry& g = p.g;
+  // rows in global order: shard s fills rows [s*R, (s+1)*R)
+  for (int s = 0; s < g.S; ++s) {
+    uint8_t* a_dst = st + kSkRawB + s * g.R * kBlockK;
+    const int pos = (s - p.local + g.S) % g.S;
+    if (pos == 0)
+      tma_load_2d(a_dst, &p.tm_a8_local, bar, x, 0);
+    else
+      tma_load_3d(a_dst, &p.tm_a8_stage, bar, x, 0, pos - 1);
+  }
+}
+
 __device__ void sk_tma_warp(const SkinnyParams& p, uint8_t* sRaw, uint64_t* raw_full,
                             uint64_t* raw_empty, int lane, volatile int* abort) {
   const Geometry& g = p.g;
   const volatile uint32_t* gstatus = p.status;
   const uint32_t tx = static_cast<uint32_t>(kSkRawB + g.M * kBlockK);
-  if ((p.flags & kFlagWait) && g.S > 1 && !sk_wait_all_chunks(p, lane, abort)) return;
-  if (lane != 0) return;
-  fence_acq_rel_gpu();
-  fence_proxy_async_global();
-  tma_prefetch_desc(&p.tm_b8);
-  int stage = 0;
-  uint32_t phase = 0, issued = 0, issued_phase = 0;
-  bool ok = true;
-  for (int64_t u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-    int64_t nt, kb0, kb1;
-    unit_coords(p, u, nt, kb0, kb1);
-    for (int64_t kb = kb0; kb < kb1; ++kb) {
+  int64_t u0, u1;
+  cta_range(p, u0, u1);
+  const int64_t n = u1 - u0;
+  const bool wait = (p.flags & kFlagWait) && g.S > 1;
+  const int64_t head = n < kSkRaw ? n : kSkRaw;
+  if (lane == 0) {
+    tma_prefetch_desc(&p.tm_b8);
+    // B of the first stages before the remote rows are known to be ready
+    for (int64_t i = 0; i < head; ++i) {
+      const int64_t u = u0 + i, nt = u / g.KB, kb = u % g.KB;
+      mbar_arrive_expect_tx(&raw_full[i], tx);
+      tma_load_2d(sRaw + i * kSkRawStage, &p.tm_b8, &raw_full[i], static_cast<int32_t>(nt * kSkN),
+                  static_cast<int32_t>(kb * kBlockK));
+    }
+  }
+  __syncwarp();
+  bool ok = !wait || sk_wait_all_chunks(p, lane, abort);
+  uint32_t issued = 0, issued_phase = 0;
+  if (lane == 0) {
+    if (ok) {
+      fence_acq_rel_gpu();
+      fence_proxy_async_global();
+    }
+    for (int64_t i = 0; i < head; ++i) {
+      issued |= 1u << i;
+      if (ok)
+        sk_issue_a(p, sRaw + i * kSkRawStage, &raw_full[i],
+                   static_cast<int32_t>(((u0 + i) % g.KB) * kBlockK));
+    }
+    for (int64_t i = head; i < n && ok; ++i) {
+      const int stage = static_cast<int>(i % kSkRaw);
+      const uint32_t phase = static_cast<uint32_t>((i / kSkRaw) & 1);
       if (!mbar_wait(&raw_empty[stage], phase ^ 1u, p.pipe_timeout_ns, abort, gstatus)) {
         ok = false;
         break;
       }
-      mbar_arrive_expect_tx(&raw_full[stage], tx);
+      const int64_t u = u0 + i, nt = u / g.KB, kb = u % g.KB;
       uint8_t* st = sRaw + stage * kSkRawStage;
-      const int32_t x = static_cast<int32_t>(kb * kBlockK);
-      tma_load_2d(st, &p.tm_b8, &raw_full[stage], static_cast<int32_t>(nt * kSkN), x);
-      // A rows in global order: shard s fills rows [s*R, (s+1)*R)
-      for (int s = 0; s < g.S; ++s) {
-        uint8_t* a_dst = st + kSkRawB + s * g.R * kBlockK;
-        const int pos = (s - p.local + g.S) % g.S;
-        if (pos == 0)
-          tma_load_2d(a_dst, &p.tm_a8_local, &raw_full[stage], x, 0);
-        else
-          tma_load_3d(a_dst, &p.tm_a8_stage, &raw_full[stage], x, 0, pos - 1);
-      }
+      mbar_arrive_expect_tx(&raw_full[stage], tx);
+      tma_load_2d(st, &p.tm_b8, &raw_full[stage], static_cast<int32_t>(nt * kSkN),
+                  static_cast<int32_t>(kb * kBlockK));
+      sk_issue_a(p, st, &raw_full[stage], static_cast<int32_t>(kb * kBlockK));
       issued |= 1u << stage;
       issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-      if (++stage == kSkRaw) {
-        stage = 0;
-        phase ^= 1u;
-      }
+    }
+    if (!ok) {
+      sk_set_status(p.status, kStatusPipelineTimeout, 0x1100u);
+      *abort = 1;
+      // Drain: loads already issued must land before the CTA exits.  Stages
+      // whose A half was never issued cannot complete; their B halves land
+      // well within the sleep below.
+      volatile int never = 0;
+      for (int s = 0; s < kSkRaw; ++s)
+        if (issued & (1u << s))
+          mbar_wait(&raw_full[s], (issued_phase >> s) & 1u, 20000000ull, &never);
+      __nanosleep(100000);
     }
   }
-  if (!ok) {
-    sk_set_status(p.status, kStatusPipelineTimeout, 0x1100u);
-    *abort = 1;
-  }
-  volatile int never = 0;
-  const uint64_t limit = ok ? p.pipe_timeout_ns : 20000000ull;
-  for (int s = 0; s < kSkRaw; ++s)
-    if (issued & (1u << s)) mbar_wait(&raw_full[s], (issued_phase >> s) & 1u, limit, &never);
+  __syncwarp();
 }
 
 // ------------------------------------------------------------------ B widening (warps 0-3)
@@ -198,163 +230,152 @@ __device__ void sk_bwiden(const SkinnyParams& p, const uint8_t* sRaw, uint8_t* s
                           uint64_t* fp_empty, int t, volatile int* abort) {
   const volatile uint32_t* gstatus = p.status;
   const int krow = t >> 1, grp = t & 1, lane = t & 31;
-  int rs = 0, fs = 0;
-  uint32_t rphase = 0, fphase = 0;
-  for (int64_t u = blockIdx.x; u < p.units; u += gridDim.x) {
-    int64_t nt, kb0, kb1;
-    unit_coords(p, u, nt, kb0, kb1);
-    for (int64_t kb = kb0; kb < kb1; ++kb) {
-      if (!mbar_wait(&raw_full[rs], rphase, p.pipe_timeout_ns, abort, gstatus) ||
-          !mbar_wait(&fp_empty[fs], fphase ^ 1u, p.pipe_timeout_ns, abort, gstatus)) {
-        if (lane == 0) {
-          sk_set_status(p.status, kStatusPipelineTimeout, 0x1200u);
-          *abort = 1;
-        }
-        return;
-      }
-      // raw B arrives 128-byte swizzled: 16-byte chunk j of k-row r sits at j ^ (r % 8)
-      const uint8_t* src = sRaw + rs * kSkRawStage + krow * kSkN;
-      uint4 v[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        v[i] = *reinterpret_cast<const uint4*>(src + (((grp * 4 + i) ^ (krow & 7)) * 16));
-      uint8_t* dst = sFp + fs * kSkFpStage + grp * (64 * kBlockK * 2) + krow * 128;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint4 a, b;
-        widen16x(v[i], a, b);
-        const int c0 = 2 * i, c1 = 2 * i + 1;  // 16-byte chunks of 8 fp16 within the row
-        *reinterpret_cast<uint4*>(dst + ((c0 ^ (krow & 7)) * 16)) = a;
-        *reinterpret_cast<uint4*>(dst + ((c1 ^ (krow & 7)) * 16)) = b;
-      }
-      fence_proxy_async_shared();
-      __syncwarp();
+  int64_t u0, u1;
+  cta_range(p, u0, u1);
+  for (int64_t i = 0; i < u1 - u0; ++i) {
+    const int rs = static_cast<int>(i % kSkRaw), fs = static_cast<int>(i % kSkFp);
+    const uint32_t rph = static_cast<uint32_t>((i / kSkRaw) & 1);
+    const uint32_t fph = static_cast<uint32_t>((i / kSkFp) & 1);
+    if (!mbar_wait(&raw_full[rs], rph, p.pipe_timeout_ns, abort, gstatus) ||
+        !mbar_wait(&fp_empty[fs], fph ^ 1u, p.pipe_timeout_ns, abort, gstatus)) {
       if (lane == 0) {
-        mbar_arrive(&fp_full[fs]);
-        mbar_arrive(&raw_empty[rs]);
+        sk_set_status(p.status, kStatusPipelineTimeout, 0x1200u);
+        *abort = 1;
       }
-      if (++rs == kSkRaw) {
-        rs = 0;
-        rphase ^= 1u;
-      }
-      if (++fs == kSkFp) {
-        fs = 0;
-        fphase ^= 1u;
-      }
+      return;
+    }
+    // raw B arrives 128-byte swizzled: 16-byte chunk j of k-row r sits at j ^ (r % 8)
+    const uint8_t* src = sRaw + rs * kSkRawStage + krow * kSkN;
+    uint4 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      v[k] = *reinterpret_cast<const uint4*>(src + (((grp * 4 + k) ^ (krow & 7)) * 16));
+    uint8_t* dst = sFp + fs * kSkFpStage + grp * (64 * kBlockK * 2) + krow * 128;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint4 a, b;
+      widen16x(v[k], a, b);
+      const int c0 = 2 * k, c1 = 2 * k + 1;  // 16-byte chunks of 8 fp16 within the row
+      *reinterpret_cast<uint4*>(dst + ((c0 ^ (krow & 7)) * 16)) = a;
+      *reinterpret_cast<uint4*>(dst + ((c1 ^ (krow & 7)) * 16)) = b;
+    }
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(&fp_full[fs]);
+      mbar_arrive(&raw_empty[rs]);
     }
   }
 }
 
-// ------------------------------------------------------------------ A widening (warps 8-11)
-// Lane l of warp w holds row m = 32 * (w % 4) + l: 64 int8 of the k-block ->
-// 64 fp16 = 32 TMEM columns (k = 2c in the low half of column c).
+// ------------------------------------------------------------------ A widening
+// Lane l of a warp of quadrant q holds row m = 32 q + l: 64 int8 of the k-block
+// -> 64 fp16 = 32 TMEM columns (k = 2c in the low half of column c).  The two
+// warps of a quadrant take the k-blocks of parity `par` of this CTA's sequence.
 __device__ void sk_awiden(const SkinnyParams& p, const uint8_t* sRaw, uint64_t* raw_full,
-                          uint64_t* raw_empty, uint64_t* a_full, uint64_t* fp_empty,
-                          uint32_t tmem, int quad, int lane, volatile int* abort) {
+                          uint64_t* raw_empty, uint64_t* a_full, uint64_t* a_empty,
+                          uint32_t tmem, int quad, int par, int lane, volatile int* abort) {
   const volatile uint32_t* gstatus = p.status;
   const int m = quad * 32 + lane;
-  const bool has_rows = quad * 32 < p.g.M;  // warp-uniform
+  if (quad * 32 >= p.g.M) return;  // no rows in this quadrant (warp-uniform)
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-  int rs = 0, fs = 0;
-  uint32_t rphase = 0, fphase = 0;
-  for (int64_t u = blockIdx.x; u < p.units; u += gridDim.x) {
-    int64_t nt, kb0, kb1;
-    unit_coords(p, u, nt, kb0, kb1);
-    for (int64_t kb = kb0; kb < kb1; ++kb) {
-      if (!mbar_wait(&raw_full[rs], rphase, p.pipe_timeout_ns, abort, gstatus) ||
-          !mbar_wait(&fp_empty[fs], fphase ^ 1u, p.pipe_timeout_ns, abort, gstatus)) {
-        if (lane == 0) {
-          sk_set_status(p.status, kStatusPipelineTimeout, 0x1300u);
-          *abort = 1;
-        }
-        return;
-      }
-      if (has_rows) {
-        uint32_t r[32];
-        if (m < p.g.M) {
-          // raw A arrives 64-byte swizzled: chunk j of row m sits at j ^ ((m / 2) % 4)
-          const uint8_t* src = sRaw + rs * kSkRawStage + kSkRawB + m * kBlockK;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint4 a, b;
-            widen16x(*reinterpret_cast<const uint4*>(src + ((i ^ ((m >> 1) & 3)) * 16)), a, b);
-            r[8 * i + 0] = a.x; r[8 * i + 1] = a.y; r[8 * i + 2] = a.z; r[8 * i + 3] = a.w;
-            r[8 * i + 4] = b.x; r[8 * i + 5] = b.y; r[8 * i + 6] = b.z; r[8 * i + 7] = b.w;
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = 0u;
-        }
-        tmem_st32(lane_base + kSkAcol + fs * 32, r);
-        tmem_st_wait();
-      }
-      tc_fence_before();
-      __syncwarp();
+  int64_t u0, u1;
+  cta_range(p, u0, u1);
+  for (int64_t i = par; i < u1 - u0; i += 2) {
+    const int rs = static_cast<int>(i % kSkRaw), as = static_cast<int>(i % kSkA);
+    const uint32_t rph = static_cast<uint32_t>((i / kSkRaw) & 1);
+    const uint32_t aph = static_cast<uint32_t>((i / kSkA) & 1);
+    if (!mbar_wait(&raw_full[rs], rph, p.pipe_timeout_ns, abort, gstatus) ||
+        !mbar_wait(&a_empty[as], aph ^ 1u, p.pipe_timeout_ns, abort, gstatus)) {
       if (lane == 0) {
-        mbar_arrive(&a_full[fs]);
-        mbar_arrive(&raw_empty[rs]);
+        sk_set_status(p.status, kStatusPipelineTimeout, 0x1300u);
+        *abort = 1;
       }
-      if (++rs == kSkRaw) {
-        rs = 0;
-        rphase ^= 1u;
+      return;
+    }
+    uint32_t r[32];
+    if (m < p.g.M) {
+      // raw A arrives 64-byte swizzled: chunk j of row m sits at j ^ ((m / 2) % 4)
+      const uint8_t* src = sRaw + rs * kSkRawStage + kSkRawB + m * kBlockK;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint4 a, b;
+        widen16x(*reinterpret_cast<const uint4*>(src + ((k ^ ((m >> 1) & 3)) * 16)), a, b);
+        r[8 * k + 0] = a.x; r[8 * k + 1] = a.y; r[8 * k + 2] = a.z; r[8 * k + 3] = a.w;
+        r[8 * k + 4] = b.x; r[8 * k + 5] = b.y; r[8 * k + 6] = b.z; r[8 * k + 7] = b.w;
       }
-      if (++fs == kSkFp) {
-        fs = 0;
-        fphase ^= 1u;
-      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) r[k] = 0u;
+    }
+    tmem_st32(lane_base + kSkAcol + as * 32, r);
+    tmem_st_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(&a_full[as]);
+      mbar_arrive(&raw_empty[rs]);
     }
   }
 }
 
 // ------------------------------------------------------------------ MMA warp
+// Pieces: maximal runs of this CTA's units inside one n-tile; segments: at most
+// kSegBlocks k-blocks of a piece, each accumulated into one fp32 buffer.
 __device__ void sk_mma(const SkinnyParams& p, const uint8_t* sFp, uint64_t* fp_full,
-                       uint64_t* a_full, uint64_t* fp_empty, uint64_t* dfull, uint64_t* dempty,
-                       uint32_t tmem, volatile int* abort) {
+                       uint64_t* fp_empty, uint64_t* a_full, uint64_t* a_empty, uint64_t* dfull,
+                       uint64_t* dempty, uint32_t tmem, volatile int* abort) {
+  const Geometry& g = p.g;
   const volatile uint32_t* gstatus = p.status;
   // D fp32, A fp16 from TMEM (K-major), B fp16 MN-major, M = 128, N = 128
   const uint32_t idesc = idesc_f16_f32(128, kSkN, /*a_mn=*/false, /*b_mn=*/true);
   const uint32_t b0 = smem_u32(sFp);
-  int fs = 0;
-  uint32_t fphase = 0, unit = 0;
+  int64_t u0, u1;
+  cta_range(p, u0, u1);
+  int64_t i = 0;     // k-block sequence index of this CTA
+  uint32_t seg = 0;  // segment sequence index (accumulator buffer = seg & 1)
   bool ok = true;
-  for (int64_t u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-    int64_t nt, kb0, kb1;
-    unit_coords(p, u, nt, kb0, kb1);
-    const uint32_t buf = unit & 1u, use = unit >> 1;
-    if (!mbar_wait(&dempty[buf], (use & 1u) ^ 1u, p.pipe_timeout_ns, abort, gstatus)) {
-      ok = false;
-      break;
-    }
-    tc_fence_after();
-    const uint32_t d = tmem + kSkDcol + buf * kSkN;
-    for (int64_t kb = kb0; kb < kb1; ++kb) {
-      if (!mbar_wait(&fp_full[fs], fphase, p.pipe_timeout_ns, abort, gstatus) ||
-          !mbar_wait(&a_full[fs], fphase, p.pipe_timeout_ns, abort, gstatus)) {
+  for (int64_t u = u0; u < u1 && ok;) {
+    const int64_t nt = u / g.KB;
+    const int64_t piece_end = (nt + 1) * g.KB < u1 ? (nt + 1) * g.KB : u1;
+    for (int64_t s0 = u; s0 < piece_end && ok; s0 += kSegBlocks, ++seg) {
+      const int64_t s1 = s0 + kSegBlocks < piece_end ? s0 + kSegBlocks : piece_end;
+      const uint32_t buf = seg & 1u, use = seg >> 1;
+      if (!mbar_wait(&dempty[buf], (use & 1u) ^ 1u, p.pipe_timeout_ns, abort, gstatus)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t bs = b0 + fs * kSkFpStage;
+      const uint32_t d = tmem + kSkDcol + buf * kSkN;
+      for (int64_t uu = s0; uu < s1; ++uu, ++i) {
+        const int fs = static_cast<int>(i % kSkFp), as = static_cast<int>(i % kSkA);
+        const uint32_t fph = static_cast<uint32_t>((i / kSkFp) & 1);
+        const uint32_t aph = static_cast<uint32_t>((i / kSkA) & 1);
+        if (!mbar_wait(&fp_full[fs], fph, p.pipe_timeout_ns, abort, gstatus) ||
+            !mbar_wait(&a_full[as], aph, p.pipe_timeout_ns, abort, gstatus)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t bs = b0 + fs * kSkFpStage;
 #pragma unroll
-      for (int k = 0; k < kBlockK / kUmmaK; ++k) {
-        const uint32_t a_tmem = tmem + kSkAcol + fs * 32 + k * 8;
-        const uint64_t bd = smem_desc_sw128(bs + k * (kUmmaK * 128), 64 * kBlockK * 2, 1024);
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "setp.ne.b32 p, %4, 0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
-            "r"(a_tmem), "l"(bd), "r"(idesc), "r"((kb > kb0 || k > 0) ? 1u : 0u)
-            : "memory");
+        for (int k = 0; k < kBlockK / kUmmaK; ++k) {
+          const uint32_t a_tmem = tmem + kSkAcol + as * 32 + k * 8;
+          const uint64_t bd = smem_desc_sw128(bs + k * (kUmmaK * 128), 64 * kBlockK * 2, 1024);
+          asm volatile(
+              "{\n\t.reg .pred p;\n\t"
+              "setp.ne.b32 p, %4, 0;\n\t"
+              "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+              "r"(a_tmem), "l"(bd), "r"(idesc), "r"((uu > s0 || k > 0) ? 1u : 0u)
+              : "memory");
+        }
+        mma_commit(&fp_empty[fs]);
+        mma_commit(&a_empty[as]);
       }
-      mma_commit(&fp_empty[fs]);
-      if (++fs == kSkFp) {
-        fs = 0;
-        fphase ^= 1u;
-      }
+      if (!ok) break;
+      mma_commit(&dfull[buf]);
     }
-    if (!ok) break;
-    mma_commit(&dfull[buf]);
-    ++unit;
+    u = piece_end;
   }
   if (!ok) {
     sk_set_status(p.status, kStatusPipelineTimeout, 0x1400u);
@@ -364,103 +385,84 @@ __device__ void sk_mma(const SkinnyParams& p, const uint8_t* sFp, uint64_t* fp_f
 
 // ------------------------------------------------------------------ epilogue (warps 12-15)
 __device__ void sk_epilogue(const SkinnyParams& p, uint64_t* dfull, uint64_t* dempty,
-                            uint32_t tmem, float* sTrans, volatile uint32_t* sLast, int quad,
-                            int lane, volatile int* abort) {
+                            uint32_t tmem, float* sTrans, int quad, int lane,
+                            volatile int* abort) {
   const Geometry& g = p.g;
   const volatile uint32_t* gstatus = p.status;
   const int row0 = quad * 32;
   const bool has_rows = row0 < g.M;  // warp-uniform
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(row0) << 16);
-  float* tr = sTrans + quad * (32 * 33);
-  const uint32_t target = p.tile_epoch * static_cast<uint32_t>(p.k_segs);
-  uint32_t unit = 0;
-  for (int64_t u = blockIdx.x; u < p.units; u += gridDim.x) {
-    int64_t nt, kb0, kb1;
-    unit_coords(p, u, nt, kb0, kb1);
-    const uint32_t buf = unit & 1u, use = unit >> 1;
-    const bool mine = mbar_wait(&dfull[buf], use & 1u, p.pipe_timeout_ns, abort, gstatus);
-    // all four epilogue warps take the same decision (they meet at named barriers)
-    uint32_t all_ok;
-    asm volatile(
-        "{\n\t.reg .pred q, r;\n\tsetp.ne.u32 q, %1, 0;\n\t"
-        "bar.red.and.pred r, 1, 128, q;\n\tselp.u32 %0, 1, 0, r;\n\t}"
-        : "=r"(all_ok)
-        : "r"(mine ? 1u : 0u)
-        : "memory");
-    if (!all_ok) {
-      if (lane == 0) {
-        sk_set_status(p.status, kStatusPipelineTimeout, 0x1500u);
-        *abort = 1;
-      }
-      return;
-    }
-    tc_fence_after();
-    if (has_rows) {
-      for (int j = 0; j < kSkN / 32; ++j) {
-        uint32_t v[32];
-        tmem_ld32(lane_base + kSkDcol + buf * kSkN + j * 32, v);
-        tmem_ld_wait();
-        // row (row0 + lane), columns 32j..32j+31 -> transpose so that a warp
-        // instruction adds 32 consecutive columns of one row
-#pragma unroll
-        for (int e = 0; e < 32; ++e) tr[lane * 33 + e] = __uint_as_float(v[e]);
-        __syncwarp();
-        const int64_t n = nt * kSkN + j * 32 + lane;
-        if (n < g.N) {
-          for (int rr = 0; rr < 32 && row0 + rr < g.M; ++rr) {
-            const int32_t val = __float2int_rn(tr[rr * 33 + lane]);
-            if (val != 0) atomicAdd(p.acc + (int64_t)(row0 + rr) * g.N + n, val);
-          }
+  int32_t* tr = reinterpret_cast<int32_t*>(sTrans) + quad * (32 * 33);
+  int64_t u0, u1;
+  cta_range(p, u0, u1);
+  uint32_t seg = 0;
+  for (int64_t u = u0; u < u1;) {
+    const int64_t nt = u / g.KB;
+    const int64_t piece_end = (nt + 1) * g.KB < u1 ? (nt + 1) * g.KB : u1;
+    for (int64_t s0 = u; s0 < piece_end; s0 += kSegBlocks, ++seg) {
+      const bool first = s0 == u, last = s0 + kSegBlocks >= piece_end;
+      const uint32_t buf = seg & 1u, use = seg >> 1;
+      const bool mine = mbar_wait(&dfull[buf], use & 1u, p.pipe_timeout_ns, abort, gstatus);
+      // the four epilogue warps decide together
+      uint32_t all_ok;
+      asm volatile(
+          "{\n\t.reg .pred q, r;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+          "bar.red.and.pred r, 1, 128, q;\n\tselp.u32 %0, 1, 0, r;\n\t}"
+          : "=r"(all_ok)
+          : "r"(mine ? 1u : 0u)
+          : "memory");
+      if (!all_ok) {
+        if (lane == 0) {
+          sk_set_status(p.status, kStatusPipelineTimeout, 0x1500u);
+          *abort = 1;
         }
-        __syncwarp();
+        return;
       }
-    }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&dempty[buf]);
-    ++unit;
-    // the n-tile's last unit finishes the dequant
-    __threadfence();
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    if (quad == 0 && lane == 0) {
-      const uint32_t old = atomicAdd(p.tile_cnt + nt, 1u);
-      *sLast = (old + 1u == target) ? 1u : 0u;
-    }
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    if (*sLast && has_rows) {
-      __threadfence();
-      const int m = row0 + lane;
-      if (m < g.M) {
-        const int64_t n0 = nt * kSkN;
-        for (int64_t n = n0; n < n0 + kSkN && n < g.N; n += 8) {
-          int32_t* ap = p.acc + (int64_t)m * g.N + n;
-          const int4 a0 = __ldcg(reinterpret_cast<const int4*>(ap));
-          const int4 a1 = __ldcg(reinterpret_cast<const int4*>(ap + 4));
-          const int4 b0 = __ldg(reinterpret_cast<const int4*>(p.bias + n));
-          const int4 b1 = __ldg(reinterpret_cast<const int4*>(p.bias + n + 4));
-          const float4 s0 = __ldg(reinterpret_cast<const float4*>(p.scale + n));
-          const float4 s1 = __ldg(reinterpret_cast<const float4*>(p.scale + n + 4));
-          const int32_t av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-          const int32_t bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-          const float ss[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-          int32_t c[8];
-          uint32_t h[4];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            c[e] = static_cast<int32_t>(static_cast<uint32_t>(av[e]) + static_cast<uint32_t>(bb[e]));
-            const uint32_t hb = __half_as_ushort(__float2half_rn(__fmul_rn(__int2float_rn(c[e]), ss[e])));
-            if (e & 1) h[e >> 1] |= hb << 16; else h[e >> 1] = hb;
+      tc_fence_after();
+      if (has_rows) {
+        for (int j = 0; j < kSkN / 32; ++j) {
+          uint32_t f[32], s[32];
+          tmem_ld32(lane_base + kSkDcol + buf * kSkN + j * 32, f);
+          if (!first) tmem_ld32(lane_base + kSkScol + j * 32, s);
+          tmem_ld_wait();
+          if (j == kSkN / 32 - 1) {
+            // the fp32 buffer has been read: the MMA may reuse it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&dempty[buf]);
           }
-          *reinterpret_cast<int4*>(p.C_i32 + (int64_t)m * g.N + n) = make_int4(c[0], c[1], c[2], c[3]);
-          *reinterpret_cast<int4*>(p.C_i32 + (int64_t)m * g.N + n + 4) = make_int4(c[4], c[5], c[6], c[7]);
-          *reinterpret_cast<uint4*>(p.D_f16 + (int64_t)m * g.N + n) = make_uint4(h[0], h[1], h[2], h[3]);
-          // the accumulator starts every run at zero
-          *reinterpret_cast<int4*>(ap) = make_int4(0, 0, 0, 0);
-          *reinterpret_cast<int4*>(ap + 4) = make_int4(0, 0, 0, 0);
+          uint32_t acc[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            acc[e] = (first ? 0u : s[e]) +
+                     static_cast<uint32_t>(__float2int_rn(__uint_as_float(f[e])));
+          if (!last) {
+            tmem_st32(lane_base + kSkScol + j * 32, acc);
+            continue;
+          }
+          // flush: transpose so that a warp instruction adds 32 consecutive
+          // columns of one row
+#pragma unroll
+          for (int e = 0; e < 32; ++e) tr[lane * 33 + e] = static_cast<int32_t>(acc[e]);
+          __syncwarp();
+          const int64_t n = nt * kSkN + j * 32 + lane;
+          if (n < g.N) {
+            int32_t* col = p.acc + n;
+            for (int rr = 0; rr < 32 && row0 + rr < g.M; ++rr) {
+              const int32_t val = tr[rr * 33 + lane];
+              if (val != 0) atomicAdd(col + (int64_t)(row0 + rr) * g.N, val);
+            }
+          }
+          __syncwarp();
         }
+        if (!last) tmem_st_wait();
+      } else {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&dempty[buf]);
       }
     }
-    asm volatile("bar.sync 1, 128;" ::: "memory");
+    u = piece_end;
   }
 }
 
@@ -475,26 +477,30 @@ __global__ void __launch_bounds__(kSkThreads, 1) ag_skinny_kernel(const __grid_c
   uint64_t* raw_full = bars;
   uint64_t* raw_empty = raw_full + kSkRaw;
   uint64_t* fp_full = raw_empty + kSkRaw;
-  uint64_t* a_full = fp_full + kSkFp;
-  uint64_t* fp_empty = a_full + kSkFp;
-  uint64_t* dfull = fp_empty + kSkFp;
+  uint64_t* fp_empty = fp_full + kSkFp;
+  uint64_t* a_full = fp_empty + kSkFp;
+  uint64_t* a_empty = a_full + kSkA;
+  uint64_t* dfull = a_empty + kSkA;
   uint64_t* dempty = dfull + 2;
   uint64_t* drain = dempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-  volatile uint32_t* sLast = tmem_slot + 1;
-  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool gemm = (p.flags & kFlagGemm) != 0;
+  const int a_quads = static_cast<int>((p.g.M + 31) / 32);  // lane quadrants holding rows
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSkRaw; ++s) {
       mbar_init(&raw_full[s], 1);
-      mbar_init(&raw_empty[s], 8);  // 4 B-widening warps + 4 A-widening warps
+      mbar_init(&raw_empty[s], 4 + a_quads);  // B-widening warps + one A warp per quadrant
     }
     for (int s = 0; s < kSkFp; ++s) {
       mbar_init(&fp_full[s], 4);
-      mbar_init(&a_full[s], 4);
       mbar_init(&fp_empty[s], 1);
+    }
+    for (int s = 0; s < kSkA; ++s) {
+      mbar_init(&a_full[s], a_quads);
+      mbar_init(&a_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&dfull[b], 1);
@@ -502,7 +508,6 @@ __global__ void __launch_bounds__(kSkThreads, 1) ag_skinny_kernel(const __grid_c
     }
     mbar_init(drain, 1);
     *tmem_slot = 0;
-    *sLast = 0;
     *abort = 0;
     fence_mbar_init();
   }
@@ -518,15 +523,18 @@ __global__ void __launch_bounds__(kSkThreads, 1) ag_skinny_kernel(const __grid_c
   if (warp < 4) {
     if (gemm) sk_bwiden(p, sRaw, sFp, raw_full, raw_empty, fp_full, fp_empty, threadIdx.x, abort);
   } else if (warp == 4) {
-    if (gemm && lane == 0) sk_mma(p, sFp, fp_full, a_full, fp_empty, dfull, dempty, tmem, abort);
+    if (gemm && lane == 0)
+      sk_mma(p, sFp, fp_full, fp_empty, a_full, a_empty, dfull, dempty, tmem, abort);
   } else if (warp == 5) {
     if (p.flags & kFlagCopy) sk_copy_warp(p, lane);
   } else if (warp == 6) {
     if (gemm) sk_tma_warp(p, sRaw, raw_full, raw_empty, lane, abort);
-  } else if (warp >= 8 && warp < 12) {
-    if (gemm) sk_awiden(p, sRaw, raw_full, raw_empty, a_full, fp_empty, tmem, warp & 3, lane, abort);
-  } else if (warp >= 12) {
-    if (gemm) sk_epilogue(p, dfull, dempty, tmem, sTrans, sLast, warp & 3, lane, abort);
+  } else if ((warp >= 8 && warp < 12) || warp >= 16) {
+    if (gemm)
+      sk_awiden(p, sRaw, raw_full, raw_empty, a_full, a_empty, tmem, warp & 3, warp >= 16 ? 1 : 0,
+                lane, abort);
+  } else if (warp >= 12 && warp < 16) {
+    if (gemm) sk_epilogue(p, dfull, dempty, tmem, sTrans, warp & 3, lane, abort);
   }
 
   tc_fence_before();
@@ -543,6 +551,47 @@ __global__ void __launch_bounds__(kSkThreads, 1) ag_skinny_kernel(const __grid_c
   }
 }
 
+// C_i32 = acc + bias, D = fp16(fp32(C_i32) * scale), acc = 0: one thread per 8
+// consecutive outputs (N % 16 == 0, so a row holds a whole number of them).
+__global__ void __launch_bounds__(256) ag_skinny_finish_kernel(int32_t* __restrict__ acc,
+                                                               const int32_t* __restrict__ bias,
+                                                               const float* __restrict__ scale,
+                                                               int32_t* __restrict__ C_i32,
+                                                               uint16_t* __restrict__ D,
+                                                               int64_t M, int64_t N) {
+  const int64_t groups = M * N / 8;
+  for (int64_t gi = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; gi < groups;
+       gi += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t off = gi * 8, n = off % N;
+    int4* ap = reinterpret_cast<int4*>(acc + off);
+    const int4 a0 = __ldcg(ap), a1 = __ldcg(ap + 1);
+    const int4 b0 = __ldg(reinterpret_cast<const int4*>(bias + n));
+    const int4 b1 = __ldg(reinterpret_cast<const int4*>(bias + n + 4));
+    const float4 s0 = __ldg(reinterpret_cast<const float4*>(scale + n));
+    const float4 s1 = __ldg(reinterpret_cast<const float4*>(scale + n + 4));
+    const int32_t av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    const int32_t bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+    const float ss[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+    int32_t c[8];
+    uint32_t h[4];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      c[e] = static_cast<int32_t>(static_cast<uint32_t>(av[e]) + static_cast<uint32_t>(bb[e]));
+      const uint32_t hb =
+          __half_as_ushort(__float2half_rn(__fmul_rn(__int2float_rn(c[e]), ss[e])));
+      if (e & 1)
+        h[e >> 1] |= hb << 16;
+      else
+        h[e >> 1] = hb;
+    }
+    *reinterpret_cast<int4*>(C_i32 + off) = make_int4(c[0], c[1], c[2], c[3]);
+    *reinterpret_cast<int4*>(C_i32 + off + 4) = make_int4(c[4], c[5], c[6], c[7]);
+    *reinterpret_cast<uint4*>(D + off) = make_uint4(h[0], h[1], h[2], h[3]);
+    ap[0] = make_int4(0, 0, 0, 0);  // the accumulator starts every run at zero
+    ap[1] = make_int4(0, 0, 0, 0);
+  }
+}
+
 }  // namespace
 
 cudaError_t skinny_prepare() {
@@ -552,6 +601,10 @@ cudaError_t skinny_prepare() {
 
 cudaError_t launch_skinny(const SkinnyParams& p, int grid, cudaStream_t stream) {
   ag_skinny_kernel<<<grid, kSkThreads, kSkSmem, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || !(p.flags & kFlagGemm)) return e;
+  ag_skinny_finish_kernel<<<grid * 2, 256, 0, stream>>>(p.acc, p.bias, p.scale, p.C_i32, p.D_f16,
+                                                        p.g.M, p.g.N);
   return cudaGetLastError();
 }
 
