@@ -66,9 +66,7 @@ constexpr int kCopyWarpsPerCta = 2;
 constexpr int kSkMaxRows = 128;   // the gathered A lives in TMEM: one lane per row
 
 struct SkinnyParams {
-  CUtensorMap tm_b8;        // int8 B (2D: N, K), box 128 x 64, 128-byte swizzle
-  CUtensorMap tm_a8_local;  // int8 local shard (2D: K, R), box 64 x R, 64-byte swizzle
-  CUtensorMap tm_a8_stage;  // int8 staging (3D: K, R, slot), box 64 x R x 1, 64-byte swizzle
+  CUtensorMap tm_b8;        // int8 B (2D: N, K), box 128 x 256, 128-byte swizzle
   Geometry g;
   const void* src[kMaxShards];  // shard pointers by consumption position
   int8_t* staging;              // int8 [S-1][R][K]

@@ -77,28 +77,13 @@ int encode_f16(CUtensorMap* map, const void* base, int rank, const cuuint64_t* d
   return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, base, rank, dims, strides_bytes, box);
 }
 
-// int8 descriptors of the skinny path: B (N, K) in 128 x 64 boxes with 128-byte
-// swizzle; a shard (K, R) and the int8 staging (K, R, slot) in 64 x R boxes
-// with 64-byte swizzle.
+// int8 B (N, K) of the skinny path in 128 x 256 boxes (four k-blocks, 32 KB) with
+// 128-byte swizzle; rows past K read as zero.
 int encode_b8(CUtensorMap* map, const void* base, int64_t K, int64_t N) {
   cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)K};
   cuuint64_t strides[1] = {(cuuint64_t)N};
-  cuuint32_t box[2] = {128, agg::kBlockK};
+  cuuint32_t box[2] = {128, 4 * agg::kBlockK};
   return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, 2, dims, strides, box);
-}
-int encode_a8(CUtensorMap* map, const void* base, int64_t R, int64_t K) {
-  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)R};
-  cuuint64_t strides[1] = {(cuuint64_t)K};
-  cuuint32_t box[2] = {agg::kBlockK, (cuuint32_t)R};
-  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, 2, dims, strides, box,
-                      CU_TENSOR_MAP_SWIZZLE_64B);
-}
-int encode_stage8(CUtensorMap* map, const void* base, int64_t slots, int64_t R, int64_t K) {
-  cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)R, (cuuint64_t)slots};
-  cuuint64_t strides[2] = {(cuuint64_t)K, (cuuint64_t)R * K};
-  cuuint32_t box[3] = {agg::kBlockK, (cuuint32_t)R, 1};
-  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, 3, dims, strides, box,
-                      CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 // fp32 C viewed as [S][R][N] so that a box never crosses into the next shard's
@@ -258,9 +243,6 @@ struct ag_gemm_plan {
   int sk_grid = 0;
   int32_t* acc = nullptr;        // [M][N] int32 partial sums (zero between runs)
   int64_t sk_tiles = 0;          // 128-column n-tiles
-  CUtensorMap tm_stage8{};
-  const void* cached_a8 = nullptr;
-  CUtensorMap tm_a8_cached{};
   const void* cached_b8 = nullptr;
   CUtensorMap tm_b8_cached{};
 };
@@ -409,14 +391,7 @@ int run_impl(ag_gemm_plan* p, const void* const* shard_ptrs, const void* B, floa
       if ((rc = encode_b8(&p->tm_b8_cached, B, g.K, g.N)) != AG_GEMM_OK) return rc;
       p->cached_b8 = B;
     }
-    if (p->cached_a8 != local_ptr) {
-      p->cached_a8 = nullptr;
-      if ((rc = encode_a8(&p->tm_a8_cached, local_ptr, g.R, g.K)) != AG_GEMM_OK) return rc;
-      p->cached_a8 = local_ptr;
-    }
     sp.tm_b8 = p->tm_b8_cached;
-    sp.tm_a8_local = p->tm_a8_cached;
-    sp.tm_a8_stage = p->tm_stage8;
     sp.staging = static_cast<int8_t*>(p->staging);
     sp.counters = p->counters;
     sp.item_counter = p->item_counter;
@@ -602,7 +577,7 @@ ag_gemm_plan* ag_gemm_plan_create(int n_shards, int64_t M, int64_t K, int64_t N,
     free_plan(p);
     return nullptr;
   }
-  p->skinny = dtype == AG_GEMM_I8 && g.M <= agg::kSkMaxRows && g.R % 8 == 0;
+  p->skinny = dtype == AG_GEMM_I8 && g.M <= agg::kSkMaxRows;
   if (p->skinny) {
     p->sk_tiles = (g.N + 127) / 128;
     p->sk_grid = p->sm_count;
@@ -610,10 +585,6 @@ ag_gemm_plan* ag_gemm_plan_create(int n_shards, int64_t M, int64_t K, int64_t N,
         (e = cudaMalloc(&p->acc, static_cast<size_t>(g.M * g.N * 4))) != cudaSuccess ||
         (e = cudaMemset(p->acc, 0, static_cast<size_t>(g.M * g.N * 4))) != cudaSuccess) {
       cuda_fail(e, "plan allocation (skinny int8 path)");
-      free_plan(p);
-      return nullptr;
-    }
-    if (encode_stage8(&p->tm_stage8, p->staging, slots, g.R, g.K) != AG_GEMM_OK) {
       free_plan(p);
       return nullptr;
     }

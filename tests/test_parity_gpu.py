@@ -321,7 +321,7 @@ def test_i8_full_size_workload(oracle, wid):
 
 
 # ---------------------------------------------------------------------------
-# int8 with few gathered rows (the B-streaming skinny kernel: M <= 128, R % 8 == 0)
+# int8 with few gathered rows (the B-streaming skinny kernel: M <= 128)
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("S,R,K,N,c", [
@@ -330,6 +330,9 @@ def test_i8_full_size_workload(oracle, wid):
     (2, 64, 2048, 384, 16),    # 128 rows (every TMEM lane)
     (1, 40, 512, 128, 0),      # a single shard
     (3, 16, 4096, 256, 2),
+    (3, 13, 1040, 144, 0),     # rows of a shard not a multiple of 8, 3 lane quadrants
+    (2, 20, 112, 48, 0),       # K below one 256-row B box, two k-blocks
+    (1, 128, 320, 128, 0),     # 128 rows of one shard, a 1-k-block last unit
 ])
 def test_i8_skinny_full(oracle, S, R, K, N, c):
     x = synth.make_inputs(S, R, K, N, "i8", 3000 + S * 13 + K)
