@@ -63,17 +63,19 @@ constexpr int kSmemBytes =
 constexpr int kCopyWarpsPerCta = 2;
 
 // ---------------------------------------------------------------- skinny int8 path
-constexpr int kSkMaxRows = 128;   // the gathered A lives in TMEM: one lane per row
+constexpr int kSkMaxRows = 128;   // the gathered rows are the MMA's N operand (N <= 128 here)
 
 struct SkinnyParams {
   CUtensorMap tm_b8;        // int8 B (2D: N, K), box 128 x 256, 128-byte swizzle
+  CUtensorMap tm_a8_local;  // int8 local shard (2D: K, R), box 256 x R, unswizzled
+  CUtensorMap tm_a8_stage;  // int8 staging (3D: K, R, S - 1), box 256 x R x (S - 1)
   Geometry g;
   const void* src[kMaxShards];  // shard pointers by consumption position
   int8_t* staging;              // int8 [S-1][R][K]
   uint32_t* counters;           // [(S-1)][Q] ready counters, monotonic
   unsigned long long* item_counter;
   unsigned long long item_base;
-  int32_t* acc;                 // [M][N] int32 partial sums, zero between runs
+  int32_t* ws;                  // [n_tiles][cmax][M][128] int32 piece sums
   uint32_t* status;
   const int32_t* bias;
   const float* scale;
@@ -87,8 +89,11 @@ struct SkinnyParams {
   int64_t debug_skip_item;
   uint32_t debug_delay_ns;
   int64_t n_tiles;              // ceil(N / 128)
+  int64_t kq;                   // 4-k-block units per n-tile: ceil(KB / 4)
+  int64_t cmax;                 // workspace slots per n-tile
 };
-constexpr int kSkCopyWarpsPerCta = 1;
+constexpr int kSkCopyWarpsPerCta = 2;
+constexpr int kSkCopyParts = 8;   // tickets (and counter releases) per copy item
 
 // Launchers (fused_kernel.cu, skinny_kernel.cu).
 cudaError_t launch_fused(const FusedParams& p, int grid, cudaStream_t stream);

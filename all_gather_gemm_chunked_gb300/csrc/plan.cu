@@ -85,6 +85,22 @@ int encode_b8(CUtensorMap* map, const void* base, int64_t K, int64_t N) {
   cuuint32_t box[2] = {128, 4 * agg::kBlockK};
   return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, 2, dims, strides, box);
 }
+// int8 gathered rows of the skinny path, 256 k at a time, unswizzled: a shard
+// (K, R) in 256 x R boxes, the staging (K, R, S - 1) in 256 x R x (S - 1) boxes.
+int encode_a8(CUtensorMap* map, const void* base, int64_t R, int64_t K) {
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)R};
+  cuuint64_t strides[1] = {(cuuint64_t)K};
+  cuuint32_t box[2] = {4 * agg::kBlockK, (cuuint32_t)R};
+  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, 2, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+int encode_stage8(CUtensorMap* map, const void* base, int64_t slots, int64_t R, int64_t K) {
+  cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)R, (cuuint64_t)slots};
+  cuuint64_t strides[2] = {(cuuint64_t)K, (cuuint64_t)R * K};
+  cuuint32_t box[3] = {4 * agg::kBlockK, (cuuint32_t)R, (cuuint32_t)slots};
+  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, 3, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_NONE);
+}
 
 // fp32 C viewed as [S][R][N] so that a box never crosses into the next shard's
 // rows: box 32 columns x 32 rows (128-byte rows, swizzled like the staging box).
@@ -241,10 +257,15 @@ struct ag_gemm_plan {
   // int8 with at most 128 gathered rows: the skinny kernel
   bool skinny = false;
   int sk_grid = 0;
-  int32_t* acc = nullptr;        // [M][N] int32 partial sums (zero between runs)
+  int32_t* sk_ws = nullptr;      // piece sums, [n-tiles][sk_cmax][M][128] int32
   int64_t sk_tiles = 0;          // 128-column n-tiles
+  int64_t sk_kq = 0;             // 4-k-block units per n-tile
+  int64_t sk_cmax = 0;           // CTAs sharing an n-tile, at most
   const void* cached_b8 = nullptr;
   CUtensorMap tm_b8_cached{};
+  const void* cached_a8 = nullptr;
+  CUtensorMap tm_a8_cached{};
+  CUtensorMap tm_stage8{};
 };
 
 namespace {
@@ -258,7 +279,7 @@ void free_plan(ag_gemm_plan* p) {
   cudaFree(p->status);
   cudaFree(p->b16);
   cudaFree(p->a16);
-  cudaFree(p->acc);
+  cudaFree(p->sk_ws);
   if (p->done) cudaEventDestroy(p->done);
   delete p;
 }
@@ -269,7 +290,7 @@ int launch_skinny(ag_gemm_plan* p, agg::SkinnyParams& sp, int flags, cudaStream_
   cudaError_t e = agg::launch_skinny(sp, p->sk_grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "skinny kernel launch");
   if (flags & agg::kFlagCopy)
-    p->item_base += static_cast<unsigned long long>(p->g.items) +
+    p->item_base += static_cast<unsigned long long>(p->g.items) * agg::kSkCopyParts +
                     static_cast<unsigned long long>(p->sk_grid) * agg::kSkCopyWarpsPerCta;
   return AG_GEMM_OK;
 }
@@ -315,8 +336,10 @@ int run_impl(ag_gemm_plan* p, const void* const* shard_ptrs, const void* B, floa
     e = cudaStreamWaitEvent(stream, p->done, 0);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent");
   }
-  // Counters are monotonic: after run e each holds e * P.  Restart before overflow.
-  if (static_cast<uint64_t>(p->epoch + 1) * static_cast<uint64_t>(g.P) >= (1ull << 31)) {
+  // Counters are monotonic: after run e each holds e * P (times the copy parts per
+  // item on the skinny path).  Restart before overflow.
+  const uint64_t releases = static_cast<uint64_t>(g.P) * (p->skinny ? agg::kSkCopyParts : 1);
+  if (static_cast<uint64_t>(p->epoch + 1) * releases >= (1ull << 31)) {
     e = cudaMemsetAsync(p->counters, 0, sizeof(uint32_t) * p->counter_count, stream);
     if (e != cudaSuccess) return cuda_fail(e, "counter reset");
     p->epoch = 0;
@@ -391,11 +414,18 @@ int run_impl(ag_gemm_plan* p, const void* const* shard_ptrs, const void* B, floa
       if ((rc = encode_b8(&p->tm_b8_cached, B, g.K, g.N)) != AG_GEMM_OK) return rc;
       p->cached_b8 = B;
     }
+    if (p->cached_a8 != local_ptr) {
+      p->cached_a8 = nullptr;
+      if ((rc = encode_a8(&p->tm_a8_cached, local_ptr, g.R, g.K)) != AG_GEMM_OK) return rc;
+      p->cached_a8 = local_ptr;
+    }
     sp.tm_b8 = p->tm_b8_cached;
+    sp.tm_a8_local = p->tm_a8_cached;
+    sp.tm_a8_stage = p->tm_stage8;
     sp.staging = static_cast<int8_t*>(p->staging);
     sp.counters = p->counters;
     sp.item_counter = p->item_counter;
-    sp.acc = p->acc;
+    sp.ws = p->sk_ws;
     sp.status = p->status;
     sp.bias = bias;
     sp.scale = scale;
@@ -408,6 +438,8 @@ int run_impl(ag_gemm_plan* p, const void* const* shard_ptrs, const void* B, floa
     sp.debug_skip_item = fp.debug_skip_item;
     sp.debug_delay_ns = fp.debug_delay_ns;
     sp.n_tiles = p->sk_tiles;
+    sp.kq = p->sk_kq;
+    sp.cmax = p->sk_cmax;
     using namespace agg;
     switch (mode) {
       case AG_GEMM_MODE_PIPELINED:
@@ -581,10 +613,16 @@ ag_gemm_plan* ag_gemm_plan_create(int n_shards, int64_t M, int64_t K, int64_t N,
   if (p->skinny) {
     p->sk_tiles = (g.N + 127) / 128;
     p->sk_grid = p->sm_count;
+    p->sk_kq = (g.KB + 3) / 4;
+    p->sk_cmax = agg::skinny_max_sharers(p->sk_tiles, p->sk_kq, p->sk_grid);
     if ((e = agg::skinny_prepare()) != cudaSuccess ||
-        (e = cudaMalloc(&p->acc, static_cast<size_t>(g.M * g.N * 4))) != cudaSuccess ||
-        (e = cudaMemset(p->acc, 0, static_cast<size_t>(g.M * g.N * 4))) != cudaSuccess) {
+        (e = cudaMalloc(&p->sk_ws, static_cast<size_t>(p->sk_tiles * p->sk_cmax * g.M * 128 * 4))) !=
+            cudaSuccess) {
       cuda_fail(e, "plan allocation (skinny int8 path)");
+      free_plan(p);
+      return nullptr;
+    }
+    if (g.S > 1 && encode_stage8(&p->tm_stage8, p->staging, g.S - 1, g.R, g.K) != AG_GEMM_OK) {
       free_plan(p);
       return nullptr;
     }
@@ -677,8 +715,6 @@ int ag_gemm_plan_reset(ag_gemm_plan* plan, void* stream_v) {
     return cuda_fail(e, "cudaStreamWaitEvent");
   if ((e = cudaMemsetAsync(plan->counters, 0, sizeof(uint32_t) * plan->counter_count, stream)) != cudaSuccess ||
       (e = cudaMemsetAsync(plan->item_counter, 0, sizeof(unsigned long long), stream)) != cudaSuccess ||
-      (plan->skinny &&
-       (e = cudaMemsetAsync(plan->acc, 0, static_cast<size_t>(plan->g.M * plan->g.N * 4), stream)) != cudaSuccess) ||
       (e = cudaMemsetAsync(plan->status, 0, 2 * sizeof(uint32_t), stream)) != cudaSuccess ||
       (e = cudaEventRecord(plan->done, stream)) != cudaSuccess)
     return cuda_fail(e, "plan reset");

@@ -120,4 +120,25 @@ AGG_HD bool rows_chunks(const Geometry& g, int64_t row0, int64_t& q0, int64_t& q
   return true;
 }
 
+// Skinny int8 path: the U (n-tile, 4-k-block) units are cut into G contiguous
+// per-CTA ranges; CTA b takes [U b / G, U (b + 1) / G).
+AGG_HD void skinny_cta_range(int64_t U, int64_t b, int64_t G, int64_t& lo, int64_t& hi) {
+  lo = U * b / G;
+  hi = U * (b + 1) / G;
+}
+// The CTA whose range holds unit x (the largest b with U b / G <= x).
+AGG_HD int64_t skinny_owner(int64_t x, int64_t U, int64_t G) {
+  return ((x + 1) * G + U - 1) / U - 1;
+}
+// Most CTAs that share one n-tile of KQ units: the workspace slots per n-tile.
+inline int64_t skinny_max_sharers(int64_t n_tiles, int64_t KQ, int64_t G) {
+  const int64_t U = n_tiles * KQ;
+  int64_t most = 1;
+  for (int64_t nt = 0; nt < n_tiles; ++nt) {
+    const int64_t c = skinny_owner((nt + 1) * KQ - 1, U, G) - skinny_owner(nt * KQ, U, G) + 1;
+    if (c > most) most = c;
+  }
+  return most;
+}
+
 }  // namespace agg

@@ -46,24 +46,42 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete
+// sleeps until it completes or about `hint_ns` pass, instead of coming back at
+// once and spinning on the issue slots the working warps of its SM need.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait until the phase with parity `parity` of `bar` has completed.  Gives up
 // (returns false) after `timeout_ns`, or as soon as *abort (this CTA) or
-// *gstatus (any CTA of the grid, may be null) becomes non-zero.
+// *gstatus (any CTA of the grid, may be null) becomes non-zero.  Each try
+// sleeps up to kWaitSliceNs; the shared-memory abort flag and the timer are
+// checked between tries, and the grid status word (a global load) only once
+// the wait has lasted kSlowWaitNs.
+constexpr uint32_t kWaitSliceNs = 20000;
+constexpr uint64_t kSlowWaitNs = 20000;
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns,
                                           volatile int* abort,
                                           const volatile uint32_t* gstatus = nullptr) {
   if (mbar_try_wait(bar, parity)) return true;
-  uint64_t deadline = globaltimer_ns() + timeout_ns;
-  uint32_t spins = 0;
-  while (!mbar_try_wait(bar, parity)) {
-    if (++spins == 32) {
-      spins = 0;
-      if (*abort) return false;
-      if (gstatus && *gstatus) return false;
-      if (globaltimer_ns() > deadline) return false;
-    }
+  const uint64_t start = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, kWaitSliceNs)) return true;
+    if (*abort) return false;
+    const uint64_t waited = globaltimer_ns() - start;
+    if (waited > timeout_ns) return false;
+    if (waited > kSlowWaitNs && gstatus && *gstatus) return false;
   }
-  return true;
 }
 
 // ---------------------------------------------------------------- clusters
@@ -152,6 +170,10 @@ __device__ __forceinline__ void bulk_wait_group_all() {
 }
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA) reads of them.
+// Bulk prefetch of [src, src + bytes) into L2 (16-byte aligned, bytes % 16 == 0).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void fence_proxy_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
