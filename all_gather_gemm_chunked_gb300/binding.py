@@ -20,6 +20,7 @@ from . import build as _build
 F16, I8 = 0, 1
 MODE_PIPELINED, MODE_COMPUTE_ONLY, MODE_SEQUENTIAL, MODE_COPY_ONLY = 0, 1, 2, 3
 DEBUG_POISON_STAGING, DEBUG_SKIP_ITEM, DEBUG_DELAY_NS = 1, 2, 4
+PATH_FUSED_F16, PATH_FUSED_I8, PATH_SKINNY_I8 = 0, 1, 2
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_OOM, ERR_TIMEOUT, ERR_STATE = 0, -1, -2, -3, -4, -5, -6
 ERROR_NAMES = {ERR_INVALID: "INVALID", ERR_UNSUPPORTED: "UNSUPPORTED", ERR_CUDA: "CUDA",
                ERR_OOM: "OOM", ERR_TIMEOUT: "TIMEOUT", ERR_STATE: "STATE"}
@@ -80,6 +81,7 @@ def _load():
         "ag_gemm_plan_set_timeout_ns": (i32, [vp, i64]),
         "ag_gemm_plan_set_debug": (i32, [vp, i32, i64]),
         "ag_gemm_plan_grid": (i32, [vp]),
+        "ag_gemm_plan_path": (i32, [vp]),
         "ag_gemm_run_noalloc": (i32, [i32, i64, i64, i64, i64, ctypes.POINTER(vp), vp, vp, vp, vp]),
         "ag_gemm_last_error": (i32, []),
         "ag_gemm_last_error_message": (ctypes.c_char_p, []),
@@ -211,6 +213,10 @@ def ag_gemm_plan_set_debug(plan: int, flags: int, arg: int = 0) -> int:
 
 def ag_gemm_plan_grid(plan: int) -> int:
     return _check(_lib.ag_gemm_plan_grid(plan))
+
+
+def ag_gemm_plan_path(plan: int) -> int:
+    return _check(_lib.ag_gemm_plan_path(plan))
 
 
 def ag_gemm_run_noalloc(n_shards, M, K, N, chunk_rows, shard_ptrs, B: int, C: int,

@@ -665,7 +665,13 @@ int64_t ag_gemm_plan_chunk_rows(const ag_gemm_plan* plan) {
 
 int ag_gemm_plan_grid(const ag_gemm_plan* plan) {
   if (!plan) return fail(AG_GEMM_ERR_INVALID, "plan is NULL");
-  return plan->grid;
+  return plan->skinny ? plan->sk_grid : plan->grid;
+}
+
+int ag_gemm_plan_path(const ag_gemm_plan* plan) {
+  if (!plan) return fail(AG_GEMM_ERR_INVALID, "plan is NULL");
+  if (plan->skinny) return AG_GEMM_PATH_SKINNY_I8;
+  return plan->g.dtype == AG_GEMM_I8 ? AG_GEMM_PATH_FUSED_I8 : AG_GEMM_PATH_FUSED_F16;
 }
 
 int ag_gemm_run(ag_gemm_plan* plan, const void* const* shard_ptrs, const void* B, float* C,

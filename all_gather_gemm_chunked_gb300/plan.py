@@ -69,6 +69,11 @@ class Plan:
     def grid(self) -> int:
         return B_.ag_gemm_plan_grid(self.handle)
 
+    @property
+    def path(self) -> int:
+        """binding.PATH_FUSED_F16, PATH_FUSED_I8 or PATH_SKINNY_I8."""
+        return B_.ag_gemm_plan_path(self.handle)
+
     def set_mode(self, mode: int):
         B_.ag_gemm_plan_set_mode(self.handle, mode)
 

@@ -5,8 +5,11 @@
 Metric: streamed gather+GEMM throughput 2*M*N*K / t in TFLOP/s (TOP/s for the
 int8 workloads), where t is the device time of one run (PIPELINED mode: chunk
 copies and GEMM concurrently, one cooperative launch for fp16) on inputs
-already resident in HBM.  L2 is flushed (512 MiB write) before every timed
-step, outside the timed events.  One JSON line is printed by rank 0.
+already resident in HBM.  L2 is flushed before every timed step, outside the
+timed events: a 512 MiB buffer is written, then a second 512 MiB buffer is
+read, so that the written lines are back in HBM and L2 holds no data of the
+run and no dirty lines whose write-back would land in the timed step.  One
+JSON line is printed by rank 0.
 
 N > 1 (torchrun): every rank runs its own full replica of the workload on its
 own GPU (the shards are simulated ranks inside one GPU, so nothing is
@@ -37,10 +40,15 @@ if ROOT not in sys.path:
 METRIC = "streamed gather+GEMM TFLOPS/TOPS (2MNK/t), % of GB300 dense tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 PROFILE_DIR = os.path.join(ROOT, "profiles")
-KERNEL_SOURCES = ["all_gather_gemm_chunked_gb300/csrc/fused_kernel.cu",
-                  "all_gather_gemm_chunked_gb300/csrc/sm103.cuh",
-                  "all_gather_gemm_chunked_gb300/csrc/fused_kernel.cuh",
-                  "all_gather_gemm_chunked_gb300/csrc/schedule.h"]
+_COMMON_SOURCES = ["all_gather_gemm_chunked_gb300/csrc/sm103.cuh",
+                   "all_gather_gemm_chunked_gb300/csrc/fused_kernel.cuh",
+                   "all_gather_gemm_chunked_gb300/csrc/schedule.h"]
+# sources of the dominant kernel of each plan path (fused fp16, fused int8, skinny int8)
+KERNEL_SOURCES = {
+    0: ["all_gather_gemm_chunked_gb300/csrc/fused_kernel.cu"] + _COMMON_SOURCES,
+    1: ["all_gather_gemm_chunked_gb300/csrc/fused_kernel.cu"] + _COMMON_SOURCES,
+    2: ["all_gather_gemm_chunked_gb300/csrc/skinny_kernel.cu"] + _COMMON_SOURCES,
+}
 
 
 # ---------------------------------------------------------------------------
@@ -89,15 +97,15 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_hash() -> str:
+def kernel_hash(path_id: int = 0) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[path_id]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload_id: int):
+def profiled_traffic(workload_id: int, path_id: int):
     """DRAM bytes per launch of the dominant kernel from the committed ncu summary,
     if it was taken on the current kernel sources (else None)."""
     path = os.path.join(PROFILE_DIR, f"traffic_workload{workload_id}.txt")
@@ -107,7 +115,7 @@ def profiled_traffic(workload_id: int):
         return None
     m_hash = re.search(r"kernel_sources_sha256_16\s*=\s*(\w+)", text)
     m_bytes = re.search(r"dram_bytes_per_launch\s*=\s*([0-9.eE+]+)", text)
-    if not (m_hash and m_bytes) or m_hash.group(1) != kernel_hash():
+    if not (m_hash and m_bytes) or m_hash.group(1) != kernel_hash(path_id):
         return None
     return float(m_bytes.group(1))
 
@@ -239,7 +247,7 @@ def run_reference(args, w, rank):
 def workload_config(w, flush=True):
     return {"workload": w.name, "n_shards": w.S, "M": w.M, "K": w.K, "N": w.N,
             "dtype": w.dtype, "chunk_rows": w.chunk_rows or "auto",
-            "l2": ("flushed before each timed step (512 MiB write)" if flush
+            "l2": ("flushed before each timed step (512 MiB written, then 512 MiB read)" if flush
                    else "NOT flushed (analysis run; inputs may be L2-resident)")}
 
 
@@ -276,6 +284,8 @@ def run_ours(args, w, rank, world, local_rank):
     plan = Plan(w.S, w.M, w.K, w.N, w.dtype, w.chunk_rows)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    flush_rd = torch.ones(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    flush_sink = torch.empty((), dtype=torch.float32, device=dev)
 
     def step():
         if int8:
@@ -290,6 +300,7 @@ def run_ours(args, w, rank, world, local_rank):
         for a, b in evs:
             if not args.no_flush:
                 flush.fill_(1.0)
+                torch.sum(flush_rd, dim=0, out=flush_sink)
             a.record(stream)
             fn()
             b.record(stream)
@@ -366,19 +377,36 @@ def run_ours(args, w, rank, world, local_rank):
            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
     peaks, peak_src = load_peaks()
-    # the fused kernel is a dense fp16 contraction: its peak is the measured dense
-    # bf16 figure (fp16 and bf16 share the same nominal dense rate)
-    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    traffic = profiled_traffic(w.wid)
-    # per-launch time of the dominant (fused) kernel: for fp16 one run is exactly
-    # one launch; for int8 a run also launches the widening kernel first
-    launches_per_run = 2 if int8 else 1
+    path_id = plan.path
+    tensor_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    # kernels launched by one PIPELINED run: the fused kernel (fp16); the widening
+    # kernel and the fused kernel (int8); the skinny and the finish kernel (skinny)
+    launches_per_run = 1 if path_id == B_.PATH_FUSED_F16 else 2
+    traffic = profiled_traffic(w.wid, path_id)
+    # device time of one run (events around each run): the dominant kernel plus,
+    # for int8, the small kernel that runs with it
     kernel_ms = float(np.mean(times_ms))
-    achieved = w.flops / (kernel_ms * 1e-3) * 1e-12
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": traffic,
-                "peak_source": f"{peak_src} bf16 dense burst (fp16 dense = bf16 dense nominal)",
-                "kernel": "ag_fused_kernel" + ("<int8> + widen_kernel" if int8 else "<fp16>")}
+    if path_id == B_.PATH_SKINNY_I8:
+        # bound by HBM: algorithmic bytes of one run = B once, the gathered rows
+        # once, the remote shards copied (read + write), bias, scale, C_i32, D
+        algo = (w.K * w.N + w.M * w.K + 2 * (w.S - 1) * w.R * w.K + 8 * w.N
+                + 6 * w.M * w.N)
+        peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        achieved = algo / (kernel_ms * 1e-3) * 1e-9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                    "frac": achieved / peak, "traffic": traffic, "algorithmic_bytes": algo,
+                    "peak_source": f"{peak_src} HBM copy bandwidth",
+                    "kernel": "ag_skinny_kernel + ag_skinny_finish_kernel (one run)"}
+    else:
+        # a dense fp16 contraction: its peak is the measured dense bf16 figure
+        # (fp16 and bf16 share the same nominal dense rate)
+        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        achieved = w.flops / (kernel_ms * 1e-3) * 1e-12
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "traffic": traffic,
+                    "peak_source": f"{peak_src} bf16 dense burst (fp16 dense = bf16 dense nominal)",
+                    "kernel": "ag_fused_kernel" + ("<int8> + widen_kernel (one run)" if int8
+                                                   else "<fp16>")}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -396,7 +424,7 @@ def run_ours(args, w, rank, world, local_rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "i8" if int8 else "f16", "data": "synthetic",
         "config": workload_config(w, not args.no_flush),
-        "pct_of_peak": 100.0 * value / world / peak,
+        "pct_of_peak": 100.0 * value / world / tensor_peak,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
         "gpu_launches": launches_per_run * args.steps, "modes": modes,
         "grid": B_.ag_gemm_geometry_of(w.S, w.M, w.K, w.N, 1 if int8 else 0,

@@ -90,6 +90,15 @@ typedef enum {
     AG_GEMM_DEBUG_DELAY_NS = 4        /* producer sleeps `arg` ns before each copy item */
 } ag_gemm_debug_flag;
 
+/* Which kernels a plan runs (ag_gemm_plan_path). */
+typedef enum {
+    AG_GEMM_PATH_FUSED_F16 = 0,  /* fp16: the fused copy + tcgen05 GEMM kernel (CTA pairs) */
+    AG_GEMM_PATH_FUSED_I8 = 1,   /* int8, M > 128: B and the local shard widened to fp16,
+                                    then the fused kernel with the exact int8 epilogue */
+    AG_GEMM_PATH_SKINNY_I8 = 2   /* int8, M <= 128: the B-streaming skinny kernel and its
+                                    finish kernel (bias, dequant) */
+} ag_gemm_path;
+
 /* Sizes the library derives from a problem (no GPU needed to compute them). */
 typedef struct {
     int32_t n_shards;
@@ -223,8 +232,12 @@ int ag_gemm_plan_set_timeout_ns(ag_gemm_plan *plan, int64_t ns);
 /* OR of ag_gemm_debug_flag values; `arg` is the item index or the delay. */
 int ag_gemm_plan_set_debug(ag_gemm_plan *plan, int flags, int64_t arg);
 
-/* Number of CTAs the plan launches (one per SM, all co-resident). */
+/* Number of CTAs the plan's main kernel launches (one per SM). */
 int ag_gemm_plan_grid(const ag_gemm_plan *plan);
+
+/* The ag_gemm_path the plan runs (fixed at creation by dtype and M); a
+ * negative ag_gemm_status if plan is NULL. */
+int ag_gemm_plan_path(const ag_gemm_plan *plan);
 
 /*
  * fp16 AllGather+GEMM that allocates nothing (the pages have no counterpart

@@ -156,6 +156,8 @@ def test_null_plan_is_rejected(B):
     assert lib.ag_gemm_run(None, None, None, None, None) == B.ERR_INVALID
     assert lib.ag_gemm_plan_set_mode(None, 0) == B.ERR_INVALID
     assert lib.ag_gemm_plan_status(None) == B.ERR_INVALID
+    assert lib.ag_gemm_plan_path(None) == B.ERR_INVALID
+    assert lib.ag_gemm_plan_grid(None) == B.ERR_INVALID
     lib.ag_gemm_plan_destroy(None)  # no-op
 
 

@@ -341,6 +341,17 @@ def test_i8_skinny_full(oracle, S, R, K, N, c):
     _check_i8(Ci, D, Cref, Dref, f"skinny S={S} R={R} K={K} N={N}")
 
 
+def test_plan_path_and_grid():
+    """The plan picks its kernels by dtype and M; the skinny path runs one CTA per SM."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    with Plan(2, 64, 1024, 256, "i8") as p:
+        assert p.path == B_.PATH_SKINNY_I8 and p.grid == sms
+    with Plan(2, 512, 256, 256, "i8") as p:
+        assert p.path == B_.PATH_FUSED_I8
+    with Plan(2, 256, 256, 128, "f16") as p:
+        assert p.path == B_.PATH_FUSED_F16 and p.grid % 2 == 0 and 0 < p.grid <= sms
+
+
 def test_i8_skinny_worst_case_magnitudes_exact(oracle):
     S, R, K, N = 2, 32, 16384, 256
     rng = np.random.default_rng(6)
