@@ -69,6 +69,10 @@ def _load():
         lib.oracle_f16_to_f64.restype = ctypes.c_double
         lib.oracle_f64_to_f16_rn.argtypes = [ctypes.c_double]
         lib.oracle_f64_to_f16_rn.restype = ctypes.c_uint16
+        lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+        lib.oracle_bf16_to_f64.restype = ctypes.c_double
+        lib.oracle_f64_to_bf16_rn.argtypes = [ctypes.c_double]
+        lib.oracle_f64_to_bf16_rn.restype = ctypes.c_uint16
         lib.oracle_f64_to_f32_rn.argtypes = [ctypes.c_double]
         lib.oracle_f64_to_f32_rn.restype = ctypes.c_float
         lib.oracle_allgather.argtypes = [ctypes.c_int, i64, i64, ctypes.c_size_t,
@@ -77,6 +81,10 @@ def _load():
                                            u16p, dp]
         lib.oracle_ag_gemm_f16_at.argtypes = [ctypes.c_int, i64, i64, i64, vpp,
                                               u16p, i64, i64p, i64p, dp]
+        lib.oracle_ag_gemm_bf16.argtypes = [ctypes.c_int, i64, i64, i64, vpp,
+                                            u16p, dp]
+        lib.oracle_ag_gemm_bf16_at.argtypes = [ctypes.c_int, i64, i64, i64, vpp,
+                                               u16p, i64, i64p, i64p, dp]
         lib.oracle_ag_gemm_dequant.argtypes = [ctypes.c_int, i64, i64, i64, vpp,
                                                i8p, i32p, fp, i32p, u16p]
         lib.oracle_ag_gemm_dequant_at.argtypes = [ctypes.c_int, i64, i64, i64,
@@ -86,12 +94,16 @@ def _load():
         lib.oracle_f64_to_f16_rn_array.argtypes = [i64, dp, u16p]
         lib.oracle_f16_to_f64_array.argtypes = [i64, u16p, dp]
         lib.oracle_f64_to_f32_rn_array.argtypes = [i64, dp, fp]
+        lib.oracle_f64_to_bf16_rn_array.argtypes = [i64, dp, u16p]
+        lib.oracle_bf16_to_f64_array.argtypes = [i64, u16p, dp]
         for name in ("oracle_allgather", "oracle_ag_gemm_f16",
                      "oracle_ag_gemm_f16_at", "oracle_ag_gemm_dequant",
-                     "oracle_ag_gemm_dequant_at", "oracle_dequant"):
+                     "oracle_ag_gemm_dequant_at", "oracle_dequant",
+                     "oracle_ag_gemm_bf16", "oracle_ag_gemm_bf16_at"):
             getattr(lib, name).restype = ctypes.c_int
         for name in ("oracle_f64_to_f16_rn_array", "oracle_f16_to_f64_array",
-                     "oracle_f64_to_f32_rn_array"):
+                     "oracle_f64_to_f32_rn_array", "oracle_f64_to_bf16_rn_array",
+                     "oracle_bf16_to_f64_array"):
             getattr(lib, name).restype = None
         _lib = lib
         return lib
@@ -138,6 +150,25 @@ def f16_bits_to_f64(h) -> np.ndarray:
     out = np.empty(h.shape, dtype=np.float64)
     lib.oracle_f16_to_f64_array(h.size, _ptr(h, ctypes.c_uint16),
                                 _ptr(out, ctypes.c_double))
+    return out
+
+
+def f64_to_bf16_bits(x) -> np.ndarray:
+    """bfloat16 round-to-nearest-even of float64 values -> uint16 bit patterns."""
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(x.shape, dtype=np.uint16)
+    lib.oracle_f64_to_bf16_rn_array(x.size, _ptr(x, ctypes.c_double),
+                                    _ptr(out, ctypes.c_uint16))
+    return out
+
+
+def bf16_bits_to_f64(h) -> np.ndarray:
+    lib = _load()
+    h = np.ascontiguousarray(h, dtype=np.uint16)
+    out = np.empty(h.shape, dtype=np.float64)
+    lib.oracle_bf16_to_f64_array(h.size, _ptr(h, ctypes.c_uint16),
+                                 _ptr(out, ctypes.c_double))
     return out
 
 
@@ -251,3 +282,39 @@ def dequant(c, scale) -> np.ndarray:
                               _ptr(scale, ctypes.c_float),
                               _ptr(out, ctypes.c_uint16)), "dequant")
     return out.view(np.float16)
+
+
+# -- bf16 AllGather + GEMM ------------------------------------------------------
+# numpy has no bfloat16: shards and B are uint16 arrays of bfloat16 bit patterns.
+
+def ag_gemm_bf16(shards, B) -> np.ndarray:
+    """fp64 C = AllGather(shards) x B for bfloat16 bit patterns (uint16 arrays)."""
+    lib = _load()
+    arrs, ptrs, R, K = _shard_array(shards, np.uint16)
+    Bh = np.ascontiguousarray(B, dtype=np.uint16)
+    if Bh.shape[0] != K:
+        raise OracleError("B must be K x N")
+    N = Bh.shape[1]
+    C = np.empty((len(arrs) * R, N), dtype=np.float64)
+    _check(lib.oracle_ag_gemm_bf16(len(arrs), R, K, N, ptrs,
+                                   _ptr(Bh, ctypes.c_uint16),
+                                   _ptr(C, ctypes.c_double)), "ag_gemm_bf16")
+    return C
+
+
+def ag_gemm_bf16_at(shards, B, rows, cols) -> np.ndarray:
+    """fp64 C[rows[i], cols[i]] of AllGather(shards) x B, bfloat16 bit patterns."""
+    lib = _load()
+    arrs, ptrs, R, K = _shard_array(shards, np.uint16)
+    Bh = np.ascontiguousarray(B, dtype=np.uint16)
+    N = Bh.shape[1]
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    cols = np.ascontiguousarray(cols, dtype=np.int64)
+    out = np.empty(rows.shape, dtype=np.float64)
+    _check(lib.oracle_ag_gemm_bf16_at(len(arrs), R, K, N, ptrs,
+                                      _ptr(Bh, ctypes.c_uint16), rows.size,
+                                      _ptr(rows, ctypes.c_int64),
+                                      _ptr(cols, ctypes.c_int64),
+                                      _ptr(out, ctypes.c_double)),
+           "ag_gemm_bf16_at")
+    return out

@@ -21,10 +21,13 @@
  *  [TRI]  "全聚合-通用矩阵乘法（Allgather Gemm）" (Triton-distributed),
  *         torch_allgather_gemm golden: all_gather the shards, concatenate
  *         them along dim 0 in rank order, then matmul.
+ *  [MGPU] "Collective matrix multiplication" (Pallas:MGPU), 使用 Pallas 实现:
+ *         the same gathered GEMM with bfloat16 operands (the page's default
+ *         dtype); the bf16 variant below is the [PTO] GEMM with bf16 inputs.
  *
- * Precision: the fp16 GEMM is evaluated in fp64 (every fp16 value and every
- * product of two fp16 values is exact in fp64; the k-ordered sum rounds in
- * fp64).  The int8 GEMM is exact in int64.  The dequant step follows [CAT]
+ * Precision: the fp16 and bf16 GEMMs are evaluated in fp64 (every fp16 or
+ * bf16 value and every product of two of them is exact in fp64; the k-ordered
+ * sum rounds in fp64).  The int8 GEMM is exact in int64.  The dequant step follows [CAT]
  * 2.2 literally: the int32 result is rounded to fp32, multiplied by the fp32
  * scale in fp32 (correctly rounded), and the fp32 value is rounded to fp16.
  * All roundings are round-to-nearest-even and are written out below from the
@@ -34,7 +37,10 @@
  * Pins (tests/test_oracle_pins.py): IEEE encode/decode against numpy's
  * conversions and hand-picked boundary values; GEMM against one-hot and
  * permutation B, rank-1 closed forms, exact big-integer brute force on tiny
- * shapes and torch float64 on CPU; int8 path against Python integers and the
+ * shapes and torch float64 on CPU; bf16 encode/decode against float32 bit
+ * patterns and boundary values, the bf16 GEMM against one-hot B, rank-1 and
+ * dyadic closed forms and torch's bfloat16 -> float64 matmul; int8 path
+ * against Python integers and the
  * all-127 closed form; dequant against the all-ones debug mode of [CAT] 8.6.
  */
 #include <math.h>
@@ -63,6 +69,22 @@ double oracle_f16_to_f64(uint16_t h)
         v = frac ? NAN : INFINITY;
     else
         v = ldexp((double)(frac + 1024), efield - 25); /* 1.frac * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* bfloat16: 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits. */
+double oracle_bf16_to_f64(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int efield = (h >> 7) & 0xff;
+    int frac = h & 0x7f;
+    double v;
+    if (efield == 0)
+        v = ldexp((double)frac, -133); /* subnormal: frac * 2^-133 */
+    else if (efield == 255)
+        v = frac ? NAN : INFINITY;
+    else
+        v = ldexp((double)(frac + 128), efield - 134); /* 1.frac * 2^(e-127) */
     return sign ? -v : v;
 }
 
@@ -111,6 +133,27 @@ uint16_t oracle_f64_to_f16_rn(double x)
     int e = e2 - 1;          /* v in [2^e, 2^(e+1)), -14 <= e <= 15 */
     uint16_t frac = (uint16_t)(v / ldexp(1.0, e - 10) - 1024.0);
     return (uint16_t)(sign | ((uint16_t)(e + 15) << 10) | frac);
+}
+
+/* bfloat16 round-to-nearest-even from a double; overflow -> +-inf. */
+uint16_t oracle_f64_to_bf16_rn(double x)
+{
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    double a = fabs(x);
+    if (isnan(x))
+        return (uint16_t)(sign | 0x7fc0);
+    double v = round_rne(a, 8, -126);
+    if (v >= ldexp(1.0, 128)) /* beyond the largest finite (2 - 2^-7) * 2^127 */
+        return (uint16_t)(sign | 0x7f80);
+    if (v == 0.0)
+        return sign;
+    if (v < ldexp(1.0, -126)) /* subnormal: fraction = v / 2^-133 */
+        return (uint16_t)(sign | (uint16_t)(v / ldexp(1.0, -133)));
+    int e2;
+    frexp(v, &e2);
+    int e = e2 - 1;           /* v in [2^e, 2^(e+1)), -126 <= e <= 127 */
+    uint16_t frac = (uint16_t)(v / ldexp(1.0, e - 7) - 128.0);
+    return (uint16_t)(sign | ((uint16_t)(e + 127) << 7) | frac);
 }
 
 /* binary32 round-to-nearest-even from a double; overflow -> +-inf. */
@@ -208,6 +251,56 @@ int oracle_ag_gemm_f16_at(int S, int64_t R, int64_t K, int64_t N,
         double acc = 0.0;
         for (int64_t k = 0; k < K; ++k)
             acc += oracle_f16_to_f64(a[k]) * oracle_f16_to_f64(B[k * N + n]);
+        out[i] = acc;
+    }
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* bf16 AllGather + GEMM  ([PTO] 计算功能 with [MGPU]'s bfloat16 operands)    */
+/* ------------------------------------------------------------------------ */
+
+/* As oracle_ag_gemm_f16, the elements being bfloat16 bit patterns. */
+int oracle_ag_gemm_bf16(int S, int64_t R, int64_t K, int64_t N,
+                        const uint16_t *const *shards, const uint16_t *B,
+                        double *C)
+{
+    if (S < 1 || R < 0 || K < 0 || N < 0 || !shards || !B || !C)
+        return ORACLE_ERR_ARGS;
+    int64_t M = (int64_t)S * R;
+    for (int64_t m = 0; m < M; ++m) {
+        const uint16_t *a = gathered_row((const void *const *)shards, R, K,
+                                         m, sizeof(uint16_t));
+        double *c = C + m * N;
+        for (int64_t n = 0; n < N; ++n)
+            c[n] = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double av = oracle_bf16_to_f64(a[k]);
+            const uint16_t *b = B + k * N;
+            for (int64_t n = 0; n < N; ++n)
+                c[n] += av * oracle_bf16_to_f64(b[n]);
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* The same definition evaluated only at the points (rows[i], cols[i]). */
+int oracle_ag_gemm_bf16_at(int S, int64_t R, int64_t K, int64_t N,
+                           const uint16_t *const *shards, const uint16_t *B,
+                           int64_t npts, const int64_t *rows,
+                           const int64_t *cols, double *out)
+{
+    if (S < 1 || !shards || !B || !rows || !cols || !out)
+        return ORACLE_ERR_ARGS;
+    for (int64_t i = 0; i < npts; ++i) {
+        int64_t m = rows[i], n = cols[i];
+        if (m < 0 || m >= (int64_t)S * R || n < 0 || n >= N)
+            return ORACLE_ERR_ARGS;
+        const uint16_t *a = gathered_row((const void *const *)shards, R, K,
+                                         m, sizeof(uint16_t));
+        double acc = 0.0;
+        for (int64_t k = 0; k < K; ++k)
+            acc += oracle_bf16_to_f64(a[k]) * oracle_bf16_to_f64(B[k * N + n]);
         out[i] = acc;
     }
     return ORACLE_OK;
@@ -333,4 +426,16 @@ void oracle_f64_to_f32_rn_array(int64_t count, const double *x, float *f)
 {
     for (int64_t i = 0; i < count; ++i)
         f[i] = oracle_f64_to_f32_rn(x[i]);
+}
+
+void oracle_f64_to_bf16_rn_array(int64_t count, const double *x, uint16_t *h)
+{
+    for (int64_t i = 0; i < count; ++i)
+        h[i] = oracle_f64_to_bf16_rn(x[i]);
+}
+
+void oracle_bf16_to_f64_array(int64_t count, const uint16_t *h, double *x)
+{
+    for (int64_t i = 0; i < count; ++i)
+        x[i] = oracle_bf16_to_f64(h[i]);
 }

@@ -422,3 +422,179 @@ def test_oracle_dequant_vs_numpy(oracle):
     with np.errstate(over="ignore"):
         want = (c.astype(np.float32) * s).astype(np.float16)
     assert np.array_equal(oracle.dequant(c, s).view(np.uint16), want.view(np.uint16))
+
+
+# ---------------------------------------------------------------------------
+# bfloat16 (the Pallas:MGPU page's default operand type)
+# ---------------------------------------------------------------------------
+# numpy has no bfloat16; values are uint16 bit patterns.  A bfloat16 is the
+# upper half of a binary32, so numpy's float32 decoding of (bits << 16) and an
+# integer round-half-even on float32 bit patterns are independent references.
+
+def _bf16_ref_decode(bits):
+    with np.errstate(invalid="ignore"):
+        return (np.asarray(bits).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _bf16_ref_round_f32(x32):
+    """Round-to-nearest-even of float32 values to bfloat16, on the bit patterns."""
+    u = x32.view(np.uint32).astype(np.uint64)
+    r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return r.astype(np.uint16)
+
+
+def test_bf16_decode_all_bit_patterns(oracle):
+    bits = np.arange(65536, dtype=np.uint16)
+    got = oracle.bf16_bits_to_f64(bits)
+    ref = _bf16_ref_decode(bits)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.signbit(got[0x8000]) and not np.signbit(got[0])
+
+
+def test_bf16_encode_random_float32_vs_bit_rounding(oracle):
+    rng = np.random.default_rng(30)
+    x = np.concatenate([
+        rng.standard_normal(300_000) * 10.0 ** rng.integers(-40, 39, 300_000),
+        rng.uniform(-1e-38, 1e-38, 100_000),
+        rng.integers(-2 ** 24, 2 ** 24, 100_000).astype(np.float64),
+    ])
+    with np.errstate(over="ignore"):
+        x32 = x.astype(np.float32)
+    x32 = x32[np.isfinite(x32)]
+    got = oracle.f64_to_bf16_bits(x32.astype(np.float64))
+    assert np.array_equal(got, _bf16_ref_round_f32(x32))
+
+
+@pytest.mark.parametrize("x,bits", [
+    (1.0, 0x3F80), (-2.0, 0xC000), (1 + 2 ** -8, 0x3F80),      # tie -> even (1.0)
+    (1 + 3 * 2 ** -8, 0x3F82),                                  # tie -> even (1 + 2^-6)
+    (1 + 2 ** -8 + 2 ** -30, 0x3F81),                           # just above the tie
+    ((2 - 2 ** -7) * 2.0 ** 127, 0x7F7F),                       # largest finite
+    ((2 - 2 ** -8) * 2.0 ** 127, 0x7F80),                       # tie above it -> inf
+    (2.0 ** -133, 0x0001), (2.0 ** -134, 0x0000),               # smallest subnormal, its half
+    (1.5 * 2.0 ** -133, 0x0002), (2.0 ** -126, 0x0080),         # subnormal tie, smallest normal
+    (-0.0, 0x8000), (float("inf"), 0x7F80), (-float("inf"), 0xFF80),
+])
+def test_bf16_encode_boundaries(oracle, x, bits):
+    assert int(oracle.f64_to_bf16_bits(np.array([x]))[0]) == bits
+
+
+def _bf16_bits(rng, shape, scale=1.0):
+    return _bf16_ref_round_f32((rng.standard_normal(shape) * scale).astype(np.float32))
+
+
+def _bf16_of(values):
+    """Bit patterns of float values that bfloat16 represents exactly."""
+    x32 = np.asarray(values, np.float32)
+    bits = (x32.view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal(_bf16_ref_decode(bits), x32.astype(np.float64))
+    return bits
+
+
+def bpin_one_hot_permutation(impl):
+    """B[k][n] = [k == pi(n)]  =>  C[:, n] = A[:, pi(n)] exactly."""
+    rng = np.random.default_rng(31)
+    S, R, K, N = 3, 5, 11, 7
+    shards = [_bf16_bits(rng, (R, K)) for _ in range(S)]
+    pi = rng.permutation(K)[:N]
+    B = np.zeros((K, N), np.float32)
+    B[pi, np.arange(N)] = 1
+    A = _bf16_ref_decode(np.concatenate(shards))
+    return np.array_equal(impl(shards, _bf16_of(B)), A[:, pi])
+
+
+def bpin_rank_one(impl):
+    """A[m][k] = a_m, B[k][n] = b_n (small integers)  =>  C = K a_m b_n."""
+    S, R, K, N = 2, 3, 37, 5
+    a = np.arange(1, S * R + 1) - 3.0
+    b = np.array([2.0, -1.0, 3.0, 0.5, -4.0])
+    shards = [_bf16_of(np.repeat(a[s * R:(s + 1) * R, None], K, 1)) for s in range(S)]
+    B = _bf16_of(np.repeat(b[None, :], K, 0))
+    return np.array_equal(impl(shards, B), K * np.outer(a, b))
+
+
+def bpin_gather_order(impl):
+    """Shard s carries s + 1 in column 0, B = e_0 e_0^T: row block s of C is s + 1."""
+    S, R, K, N = 4, 3, 4, 2
+    vals = [np.zeros((R, K)) for _ in range(S)]
+    for s in range(S):
+        vals[s][:, 0] = s + 1
+    B = np.zeros((K, N))
+    B[0, 0] = 1
+    want = np.zeros((S * R, N))
+    want[:, 0] = np.repeat(np.arange(1, S + 1), R)
+    return np.array_equal(impl([_bf16_of(v) for v in vals], _bf16_of(B)), want)
+
+
+def bpin_brute_force_exact(impl):
+    """Dyadic inputs with small exponents: every partial sum is exact in fp64."""
+    rng = np.random.default_rng(32)
+    S, R, K, N = 3, 2, 16, 5
+    vals = [rng.integers(-8, 9, (R, K)) / 4.0 for _ in range(S)]
+    Bv = rng.integers(-8, 9, (K, N)) / 8.0
+    A = np.concatenate(vals)
+    want = np.array([[float(sum(Fraction(A[m, k]) * Fraction(Bv[k, n]) for k in range(K)))
+                      for n in range(N)] for m in range(S * R)])
+    return np.array_equal(impl([_bf16_of(v) for v in vals], _bf16_of(Bv)), want)
+
+
+def bpin_torch_f64(impl):
+    """Mid-size random case against torch's bfloat16 -> float64 matmul on the CPU."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(33)
+    S, R, K, N = 3, 37, 129, 65
+    shards = [_bf16_bits(rng, (R, K)) for _ in range(S)]
+    B = _bf16_bits(rng, (K, N))
+    to_t = lambda b: torch.from_numpy(b.view(np.int16).copy()).view(torch.bfloat16).double()  # noqa: E731
+    ref = (to_t(np.concatenate(shards)) @ to_t(B)).numpy()
+    C = impl(shards, B)
+    return C.shape == ref.shape and np.allclose(C, ref, rtol=1e-12, atol=1e-12)
+
+
+BF16_PINS = [bpin_one_hot_permutation, bpin_rank_one, bpin_gather_order,
+             bpin_brute_force_exact, bpin_torch_f64]
+
+
+@pytest.mark.parametrize("pin", BF16_PINS, ids=lambda p: p.__name__)
+def test_oracle_bf16_pins(oracle, pin):
+    assert pin(oracle.ag_gemm_bf16)
+
+
+def _bmut_decoded_as_f16(shards, B):
+    A = np.concatenate(shards).view(np.float16).astype(np.float64)
+    return A @ B.view(np.float16).astype(np.float64)
+
+
+def _bmut_transposed_b(shards, B):
+    A = _bf16_ref_decode(np.concatenate(shards))
+    Bd = _bf16_ref_decode(B)
+    return A @ (Bd.T if Bd.shape[0] == Bd.shape[1] else Bd[::-1])
+
+
+def _bmut_reversed_shards(shards, B):
+    return _bf16_ref_decode(np.concatenate(shards[::-1])) @ _bf16_ref_decode(B)
+
+
+def _bmut_truncated_mantissa(shards, B):
+    # a decode that drops the lowest fraction bit
+    A = _bf16_ref_decode(np.concatenate(shards) & 0xFFFE)
+    return A @ _bf16_ref_decode(B & 0xFFFE)
+
+
+@pytest.mark.parametrize("mutant", [_bmut_decoded_as_f16, _bmut_transposed_b,
+                                    _bmut_reversed_shards, _bmut_truncated_mantissa],
+                         ids=lambda f: f.__name__)
+def test_bf16_pins_catch_mutant(mutant):
+    assert not all(pin(mutant) for pin in BF16_PINS)
+
+
+def test_oracle_bf16_at_matches_full(oracle):
+    rng = np.random.default_rng(34)
+    shards = [_bf16_bits(rng, (6, 40)) for _ in range(3)]
+    B = _bf16_bits(rng, (40, 9))
+    C = oracle.ag_gemm_bf16(shards, B)
+    rows = rng.integers(0, 18, 50)
+    cols = rng.integers(0, 9, 50)
+    assert np.array_equal(oracle.ag_gemm_bf16_at(shards, B, rows, cols), C[rows, cols])
