@@ -17,7 +17,7 @@ import re
 
 from . import build as _build
 
-F16, I8 = 0, 1
+F16, I8, BF16 = 0, 1, 2
 MODE_PIPELINED, MODE_COMPUTE_ONLY, MODE_SEQUENTIAL, MODE_COPY_ONLY = 0, 1, 2, 3
 DEBUG_POISON_STAGING, DEBUG_SKIP_ITEM, DEBUG_DELAY_NS = 1, 2, 4
 PATH_FUSED_F16, PATH_FUSED_I8, PATH_SKINNY_I8 = 0, 1, 2

@@ -252,7 +252,8 @@ __device__ void mma_warp(const FusedParams& p, const uint8_t* sA, const uint8_t*
                          uint32_t tmem, volatile int* abort) {
   const Geometry& g = p.g;
   const volatile uint32_t* gstatus = p.status;
-  const uint32_t idesc = idesc_f16_f32(kPairM, g.BN, /*a_mn=*/false, /*b_mn=*/true);
+  const uint32_t idesc = idesc_f16_f32(kPairM, g.BN, /*a_mn=*/false, /*b_mn=*/true) |
+                         (p.bf16 ? kIdescAbBf16 : 0u);
   const int64_t seg_len = kI8 ? kSegBlocks : g.KB;
   const int64_t nseg = ceil_div(g.KB, seg_len);
   const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);

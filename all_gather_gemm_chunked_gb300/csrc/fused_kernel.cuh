@@ -43,6 +43,7 @@ struct FusedParams {
   int local;                    // local rank
   int flags;                    // kFlag*
   int b3d;                      // B half of a CTA in one 3D box (N % 64 == 0) instead of 64-wide 2D boxes
+  int bf16;                     // fp16-path operands are bfloat16 (same layout, kind::f16 bf16 format)
   uint32_t epoch;               // run number since the last reset (>= 1)
   uint64_t timeout_ns;          // limit of a wait on a ready counter
   uint64_t pipe_timeout_ns;     // limit of a wait on a pipeline mbarrier (longer)

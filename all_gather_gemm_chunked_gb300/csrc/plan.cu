@@ -72,6 +72,8 @@ int encode_tiled(CUtensorMap* map, CUtensorMapDataType type, const void* base, i
   return AG_GEMM_OK;
 }
 
+// 2-byte operands.  bf16 plans use the same descriptors: TMA copies bytes, the
+// element type only fixes the element size, and the zero fill is +0 in both.
 int encode_f16(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
                const cuuint64_t* strides_bytes, const cuuint32_t* box) {
   return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, base, rank, dims, strides_bytes, box);
@@ -146,8 +148,9 @@ int encode_b(CUtensorMap* map, const void* base, int64_t K, int64_t N, int BN) {
 }
 
 int check_problem(int S, int64_t M, int64_t K, int64_t N, int dtype, int64_t chunk_rows) {
-  if (dtype != AG_GEMM_F16 && dtype != AG_GEMM_I8)
-    return fail(AG_GEMM_ERR_INVALID, "dtype must be AG_GEMM_F16 or AG_GEMM_I8 (got %d)", dtype);
+  if (dtype != AG_GEMM_F16 && dtype != AG_GEMM_I8 && dtype != AG_GEMM_BF16)
+    return fail(AG_GEMM_ERR_INVALID,
+                "dtype must be AG_GEMM_F16, AG_GEMM_I8 or AG_GEMM_BF16 (got %d)", dtype);
   if (S < 1 || S > agg::kMaxShards)
     return fail(AG_GEMM_ERR_INVALID, "n_shards must be in [1, %d] (got %d)", agg::kMaxShards, S);
   if (M <= 0 || K <= 0 || N <= 0)
@@ -159,8 +162,8 @@ int check_problem(int S, int64_t M, int64_t K, int64_t N, int dtype, int64_t chu
   if (chunk_rows < 0 || (chunk_rows > 0 && R % chunk_rows != 0))
     return fail(AG_GEMM_ERR_INVALID, "chunk_rows (%lld) must be 0 or divide the %lld rows of a shard",
                 (long long)chunk_rows, (long long)R);
-  if (dtype == AG_GEMM_F16 && (K % 8 != 0 || N % 8 != 0))
-    return fail(AG_GEMM_ERR_INVALID, "fp16 needs K %% 8 == 0 and N %% 8 == 0 (16-byte rows)");
+  if (dtype != AG_GEMM_I8 && (K % 8 != 0 || N % 8 != 0))
+    return fail(AG_GEMM_ERR_INVALID, "fp16 and bf16 need K %% 8 == 0 and N %% 8 == 0 (16-byte rows)");
   if (dtype == AG_GEMM_I8 && (K % 16 != 0 || N % 16 != 0))
     return fail(AG_GEMM_ERR_INVALID, "int8 needs K %% 16 == 0 and N %% 16 == 0 (16-byte rows)");
   if (dtype == AG_GEMM_I8 && K > agg::kMaxKI8)
@@ -386,6 +389,7 @@ int run_impl(ag_gemm_plan* p, const void* const* shard_ptrs, const void* B, floa
   fp.scale = scale;
   fp.local = p->local;
   fp.b3d = b_is_3d(g.N) ? 1 : 0;
+  fp.bf16 = g.dtype == AG_GEMM_BF16 ? 1 : 0;
   fp.epoch = p->epoch + 1;
   fp.timeout_ns = p->timeout_ns;
   // Pipeline stages only wait on each other; give them more room than the
@@ -677,8 +681,9 @@ int ag_gemm_plan_path(const ag_gemm_plan* plan) {
 int ag_gemm_run(ag_gemm_plan* plan, const void* const* shard_ptrs, const void* B, float* C,
                 void* stream) {
   if (!plan) return fail(AG_GEMM_ERR_INVALID, "plan is NULL");
-  if (plan->g.dtype != AG_GEMM_F16)
-    return fail(AG_GEMM_ERR_INVALID, "ag_gemm_run needs an fp16 plan (use ag_gemm_dequant_run)");
+  if (plan->g.dtype == AG_GEMM_I8)
+    return fail(AG_GEMM_ERR_INVALID,
+                "ag_gemm_run needs an fp16 or bf16 plan (use ag_gemm_dequant_run)");
   return run_impl(plan, shard_ptrs, B, C, nullptr, nullptr, nullptr, nullptr, stream);
 }
 

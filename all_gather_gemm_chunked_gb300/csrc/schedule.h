@@ -29,7 +29,7 @@ constexpr int64_t kMaxKI8 = 133000;
 
 struct Geometry {
   int S;
-  int dtype;             // 0 = f16, 1 = i8
+  int dtype;             // 0 = f16, 1 = i8, 2 = bf16
   int64_t M, K, N, R;
   int64_t c;             // chunk rows
   int64_t Q;             // chunks per source

@@ -283,6 +283,8 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 // Instruction descriptor of tcgen05.mma kind::f16: fp16 A and B, fp32 D.
 // D format in bits [4,6) (1 = f32), A/B format [7,10)/[10,13) (0 = f16),
 // A/B major bits 15/16 (1 = MN-major), N >> 3 in [17,23), M >> 4 in [24,29).
+// The same descriptor with bfloat16 A and B (format 1 in both fields).
+constexpr uint32_t kIdescAbBf16 = (1u << 7) | (1u << 10);
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n, bool a_mn, bool b_mn) {
   return (1u << 4) | (a_mn ? (1u << 15) : 0u) | (b_mn ? (1u << 16) : 0u) |
          (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);

@@ -6,7 +6,8 @@ import torch
 
 from . import binding as B_
 
-_DTYPES = {"f16": B_.F16, "i8": B_.I8}
+_DTYPES = {"f16": B_.F16, "i8": B_.I8, "bf16": B_.BF16}
+_TORCH_2B = {"f16": torch.float16, "bf16": torch.bfloat16}
 
 
 def _stream_handle(stream) -> int:
@@ -33,7 +34,7 @@ class Plan:
     def __init__(self, n_shards: int, M: int, K: int, N: int, dtype: str = "f16",
                  chunk_rows: int = 0):
         if dtype not in _DTYPES:
-            raise ValueError("dtype must be 'f16' or 'i8'")
+            raise ValueError("dtype must be 'f16', 'bf16' or 'i8'")
         self.n_shards, self.M, self.K, self.N, self.dtype = n_shards, M, K, N, dtype
         self.R = M // n_shards if n_shards else 0
         self.handle = B_.ag_gemm_plan_create(n_shards, M, K, N, _DTYPES[dtype], chunk_rows)
@@ -97,14 +98,16 @@ class Plan:
 
     # -- runs
     def run(self, shards, B, C=None, stream=None) -> torch.Tensor:
-        """C (M x N fp32) = AllGather(shards) x B for fp16 shards (R x K) and B (K x N)."""
-        if self.dtype != "f16":
-            raise ValueError("run() needs an f16 plan")
+        """C (M x N fp32) = AllGather(shards) x B for fp16 (bf16 plans: bfloat16)
+        shards (R x K) and B (K x N)."""
+        if self.dtype not in _TORCH_2B:
+            raise ValueError("run() needs an f16 or bf16 plan")
         if len(shards) != self.n_shards:
             raise ValueError(f"expected {self.n_shards} shards")
+        tdt = _TORCH_2B[self.dtype]
         for i, s in enumerate(shards):
-            _check(s, f"shards[{i}]", torch.float16, (self.R, self.K))
-        _check(B, "B", torch.float16, (self.K, self.N))
+            _check(s, f"shards[{i}]", tdt, (self.R, self.K))
+        _check(B, "B", tdt, (self.K, self.N))
         if C is None:
             C = torch.empty((self.M, self.N), dtype=torch.float32, device=B.device)
         _check(C, "C", torch.float32, (self.M, self.N))

@@ -8,6 +8,9 @@ Distributions follow the workloads the pages describe:
 * fp16 path: A and B ~ N(0, 1) rounded to fp16 (the Pallas collective-matmul
   page draws ``jax.random.normal`` operands; the Triton-distributed tutorial
   draws ``torch.randn`` fp16 operands).
+* bf16 path: the same N(0, 1) operands rounded to bfloat16 (the Pallas
+  collective-matmul page's default dtype), as uint16 bit patterns (numpy has
+  no bfloat16 type).
 * int8 path ("AllGather矩阵乘法反量化算子设计文档", 1.3 and 8.3): A, B uniform
   int8 on [-127, 127] (symmetric quantisation), bias uniform int32 on
   [-1000, 1000], per-channel scale uniform fp32 on [1e-5, 1e-4].
@@ -34,7 +37,7 @@ class Workload:
     M: int
     K: int
     N: int
-    dtype: str           # "f16" or "i8"
+    dtype: str           # "f16", "bf16" or "i8"
     chunk_rows: int      # 0 = chosen by the library (64..128 chunks per source)
 
     @property
@@ -47,13 +50,15 @@ class Workload:
 
 
 # The five workloads: a small parity case, two compute-bound fp16 cases, a
-# compute-bound int8 dequant case and a memory-bound skinny int8 case.
+# compute-bound int8 dequant case and a memory-bound skinny int8 case; 6 is the
+# 4096^3 fp16 case with bfloat16 operands.
 WORKLOADS = {
     1: Workload(1, "f16 2x128 rows, K=256, N=128, chunk 16", 2, 256, 256, 128, "f16", 16),
     2: Workload(2, "f16 2x2048 rows, K=4096, N=4096", 2, 4096, 4096, 4096, "f16", 0),
     3: Workload(3, "f16 8x1024 rows, K=4096, N=4096", 8, 8192, 4096, 4096, "f16", 0),
     4: Workload(4, "i8 dequant 4x4096 rows, K=27392, N=4096", 4, 16384, 27392, 4096, "i8", 0),
     5: Workload(5, "i8 dequant skinny 2x32 rows, K=16384, N=7168", 2, 64, 16384, 7168, "i8", 0),
+    6: Workload(6, "bf16 2x2048 rows, K=4096, N=4096", 2, 4096, 4096, 4096, "bf16", 0),
 }
 
 
@@ -64,6 +69,14 @@ def _rng(seed: int) -> np.random.Generator:
 def normal_f16(seed: int, shape) -> np.ndarray:
     """N(0,1) samples rounded to float16 (numpy's round-to-nearest cast)."""
     return _rng(seed).standard_normal(shape, dtype=np.float64).astype(np.float16)
+
+
+def normal_bf16_bits(seed: int, shape) -> np.ndarray:
+    """N(0,1) samples rounded to bfloat16 (nearest, ties to even), as bit patterns:
+    cast to float32, then round the upper 16 bits of the float32 pattern."""
+    x = _rng(seed).standard_normal(shape, dtype=np.float64).astype(np.float32)
+    u = x.view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
 
 
 def uniform_i8(seed: int, shape, lo: int = -127, hi: int = 127) -> np.ndarray:
@@ -83,6 +96,10 @@ def make_inputs(S: int, R: int, K: int, N: int, dtype: str, seed: int):
     if dtype == "f16":
         shards = [normal_f16(seed + s, (R, K)) for s in range(S)]
         B = normal_f16(seed + OFF_B, (K, N))
+        return {"shards": shards, "B": B, "bias": None, "scale": None}
+    if dtype == "bf16":
+        shards = [normal_bf16_bits(seed + s, (R, K)) for s in range(S)]
+        B = normal_bf16_bits(seed + OFF_B, (K, N))
         return {"shards": shards, "B": B, "bias": None, "scale": None}
     if dtype == "i8":
         shards = [uniform_i8(seed + s, (R, K)) for s in range(S)]

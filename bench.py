@@ -200,6 +200,8 @@ def time_oracle(w, x, budget_s: float, row_block: int = 2):
         cc = np.tile(cols, row_block)
         if w.dtype == "f16":
             oracle.ag_gemm_f16_at(x["shards"], x["B"], rr, cc)
+        elif w.dtype == "bf16":
+            oracle.ag_gemm_bf16_at(x["shards"], x["B"], rr, cc)
         else:
             oracle.ag_gemm_dequant_at(x["shards"], x["B"], x["bias"], x["scale"], rr, cc)
         rows_done += row_block
@@ -225,13 +227,13 @@ def run_reference(args, w, rank):
             rows_total += rows
     s_per_row = float(np.mean(per_step))
     value = 2.0 * w.N * w.K / s_per_row * 1e-12
-    unit = "TFLOP/s" if w.dtype == "f16" else "TOP/s"
+    unit = "TOP/s" if w.dtype == "i8" else "TFLOP/s"
     full_ms = s_per_row * w.M * 1e3
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": unit,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": full_ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64" if w.dtype == "f16" else "int64",
+        "vs_baseline": None, "dtype": "int64" if w.dtype == "i8" else "f64",
         "data": "synthetic", "config": workload_config(w),
         "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
                          "sample": f"{rows_total} whole rows of C over {args.steps} steps "
@@ -268,6 +270,9 @@ def run_ours(args, w, rank, world, local_rank):
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
     h_shards = [pin(s) for s in x["shards"]]
     h_B = pin(x["B"])
+    if w.dtype == "bf16":  # bit patterns (numpy has no bfloat16) -> bfloat16 tensors
+        h_shards = [t.view(torch.int16).view(torch.bfloat16) for t in h_shards]
+        h_B = h_B.view(torch.int16).view(torch.bfloat16)
     shards = [t.to(dev) for t in h_shards]
     Bd = h_B.to(dev)
     int8 = w.dtype == "i8"
@@ -422,7 +427,7 @@ def run_ours(args, w, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "i8" if int8 else "f16", "data": "synthetic",
+        "dtype": w.dtype, "data": "synthetic",
         "config": workload_config(w, not args.no_flush),
         "pct_of_peak": 100.0 * value / world / tensor_peak,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
@@ -440,7 +445,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=None,
                     help="timed steps (default: enough for ~2 s of timed GPU work, >= 20)")
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6])
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-step-seconds", type=float, default=4.0)

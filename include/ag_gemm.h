@@ -50,8 +50,10 @@ extern "C" {
 typedef struct ag_gemm_plan ag_gemm_plan;
 
 typedef enum {
-    AG_GEMM_F16 = 0, /* fp16 x fp16 -> fp32 */
-    AG_GEMM_I8 = 1   /* int8 x int8 -> int32 (+bias) -> fp16 dequant */
+    AG_GEMM_F16 = 0,  /* fp16 x fp16 -> fp32 */
+    AG_GEMM_I8 = 1,   /* int8 x int8 -> int32 (+bias) -> fp16 dequant */
+    AG_GEMM_BF16 = 2  /* bf16 x bf16 -> fp32 (the operand type of "Collective matrix
+                         multiplication", section 使用 Pallas 实现; the fp16 path otherwise) */
 } ag_gemm_dtype;
 
 typedef enum {
@@ -92,7 +94,7 @@ typedef enum {
 
 /* Which kernels a plan runs (ag_gemm_plan_path). */
 typedef enum {
-    AG_GEMM_PATH_FUSED_F16 = 0,  /* fp16: the fused copy + tcgen05 GEMM kernel (CTA pairs) */
+    AG_GEMM_PATH_FUSED_F16 = 0,  /* fp16 / bf16: the fused copy + tcgen05 GEMM kernel (CTA pairs) */
     AG_GEMM_PATH_FUSED_I8 = 1,   /* int8, M > 128: B and the local shard widened to fp16,
                                     then the fused kernel with the exact int8 epilogue */
     AG_GEMM_PATH_SKINNY_I8 = 2   /* int8, M <= 128: the B-streaming skinny kernel and its
@@ -130,7 +132,7 @@ int64_t ag_gemm_choose_chunk_rows(int64_t R);
 /*
  * Check a problem without touching the GPU: n_shards in [1, 64], M, K, N > 0,
  * M % n_shards == 0, chunk_rows == 0 (auto) or a divisor of R;
- * fp16: K % 8 == 0 and N % 8 == 0; int8: K % 16 == 0, N % 16 == 0 and
+ * fp16 and bf16: K % 8 == 0 and N % 8 == 0; int8: K % 16 == 0, N % 16 == 0 and
  * K <= 133000 (so that K * 127^2 plus a bias stays inside int32).
  * Returns AG_GEMM_OK or the error code (and sets the last error).
  */
@@ -168,7 +170,7 @@ int ag_gemm_item_at(const ag_gemm_geometry *g, int local_rank, int64_t i,
 /*
  * Create a plan on the current CUDA device: validates the problem (as
  * ag_gemm_validate), requires an sm_103 device, and allocates the staging
- * workspace ((n_shards-1) x R x K fp16), the per-chunk ready counters and a
+ * workspace ((n_shards-1) x R x K 2-byte elements), the per-chunk ready counters and a
  * status word (plus, for int8, fp16 copies of B and of the local shard).
  * chunk_rows = 0 picks c with ag_gemm_choose_chunk_rows.
  * Returns NULL on failure (see ag_gemm_last_error()).
@@ -186,9 +188,10 @@ int ag_gemm_plan_geometry(const ag_gemm_plan *plan, ag_gemm_geometry *out);
 int64_t ag_gemm_plan_chunk_rows(const ag_gemm_plan *plan);
 
 /*
- * fp16 AllGather+GEMM.  shard_ptrs: host array of n_shards device pointers,
- * each to an R x K fp16 matrix; B: K x N fp16; C: M x N fp32 (written, every
- * element).  Enqueues the work on `stream` (see the run modes).
+ * fp16 (or bf16, for an AG_GEMM_BF16 plan) AllGather+GEMM.  shard_ptrs: host
+ * array of n_shards device pointers, each to an R x K fp16 (bf16) matrix;
+ * B: K x N fp16 (bf16); C: M x N fp32 (written, every element), accumulated in
+ * fp32.  Enqueues the work on `stream` (see the run modes).
  */
 int ag_gemm_run(ag_gemm_plan *plan, const void *const *shard_ptrs,
                 const void *B, float *C, void *stream);

@@ -50,6 +50,7 @@ def test_chunk_rule_keeps_64_to_128_chunks_when_possible(B):
 
 @pytest.mark.parametrize("args,code", [
     ((2, 256, 256, 128, 7, 0), -1),         # dtype
+    ((2, 256, 12, 128, 2, 0), -1),          # bf16: K % 8
     ((0, 256, 256, 128, 0, 0), -1),         # n_shards
     ((65, 65 * 4, 256, 128, 0, 0), -1),
     ((3, 256, 256, 128, 0, 0), -1),         # M % S
@@ -70,22 +71,24 @@ def test_validate_rejects(B, args, code):
     assert B.ag_gemm_last_error_message()
 
 
+_DT = {"f16": 0, "i8": 1, "bf16": 2}
+
+
 def test_validate_accepts_workloads(B):
     from all_gather_gemm_chunked_gb300.synth import WORKLOADS
     for w in WORKLOADS.values():
-        assert B.ag_gemm_validate(w.S, w.M, w.K, w.N, 0 if w.dtype == "f16" else 1,
-                                  w.chunk_rows) == 0
+        assert B.ag_gemm_validate(w.S, w.M, w.K, w.N, _DT[w.dtype], w.chunk_rows) == 0
 
 
 def test_geometry_of_workloads(B):
     from all_gather_gemm_chunked_gb300.synth import WORKLOADS
-    want = {1: (16, 8), 2: (32, 64), 3: (16, 64), 4: (64, 64), 5: (1, 32)}
+    want = {1: (16, 8), 2: (32, 64), 3: (16, 64), 4: (64, 64), 5: (1, 32), 6: (32, 64)}
     for wid, w in WORKLOADS.items():
-        g = B.ag_gemm_geometry_of(w.S, w.M, w.K, w.N, 0 if w.dtype == "f16" else 1, w.chunk_rows)
+        g = B.ag_gemm_geometry_of(w.S, w.M, w.K, w.N, _DT[w.dtype], w.chunk_rows)
         assert (g.chunk_rows, g.chunks_per_source) == want[wid]
         assert g.tiles == w.S * g.m_tiles * g.n_tiles
         assert g.producer_items == (w.S - 1) * g.chunks_per_source * g.pieces_per_chunk
-        esz = 2 if w.dtype == "f16" else 1
+        esz = 1 if w.dtype == "i8" else 2
         assert g.chunk_rows * w.K * esz // g.pieces_per_chunk <= 32 * 1024 + 16
 
 

@@ -243,6 +243,82 @@ def test_f16_full_size_workload(oracle, wid):
 
 
 # ---------------------------------------------------------------------------
+# bf16 operands (same kernel, kind::f16 with the bf16 operand format)
+# ---------------------------------------------------------------------------
+
+def _bf16_to_dev(bits):
+    t = torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint16).view(np.int16))
+    return t.view(torch.bfloat16).to(DEV)
+
+
+def run_bf16(x, S, R, K, N, chunk_rows=0, mode=None, local=None, plan=None):
+    own = plan is None
+    if own:
+        plan = Plan(S, S * R, K, N, "bf16", chunk_rows)
+    try:
+        if mode is not None:
+            plan.set_mode(mode)
+        if local is not None:
+            plan.set_local_rank(local)
+        shards = [_bf16_to_dev(s) for s in x["shards"]]
+        C = torch.full((S * R, N), float("nan"), dtype=torch.float32, device=DEV)
+        plan.run(shards, _bf16_to_dev(x["B"]), C)
+        torch.cuda.synchronize()
+        assert plan.status() == 0, f"status word {plan.status_word():#x}"
+        return C.cpu().numpy()
+    finally:
+        if own:
+            plan.close()
+
+
+@pytest.mark.parametrize("S,R,K,N,c", [
+    (3, 200, 328, 392, 0),    # ragged M tiles, K tail, N tail
+    (2, 130, 72, 136, 0),
+    (1, 257, 136, 264, 0),
+    (4, 37, 64, 8, 1),
+    (5, 256, 1024, 512, 64),
+])
+def test_bf16_ragged_full(oracle, S, R, K, N, c):
+    x = synth.make_inputs(S, R, K, N, "bf16", 1500 + S * 7 + K)
+    C = run_bf16(x, S, R, K, N, c)
+    check_f16(C, oracle.ag_gemm_bf16(x["shards"], x["B"]), K, f"bf16 S={S} R={R} K={K} N={N}")
+
+
+def test_bf16_full_size_workload(oracle):
+    """The 4096^3 case with bfloat16 operands: sampled points against the oracle,
+    every element against an fp64 BLAS product of the oracle-decoded operands."""
+    w = synth.WORKLOADS[6]
+    x = synth.workload_inputs(w)
+    C = run_bf16(x, w.S, w.R, w.K, w.N, w.chunk_rows)
+    rng = np.random.default_rng(6)
+    rows, cols = tile_samples(rng, w.M, w.N, w.R)
+    check_f16(C[rows, cols], oracle.ag_gemm_bf16_at(x["shards"], x["B"], rows, cols), w.K,
+              "bf16 workload samples")
+    A = oracle.bf16_bits_to_f64(np.concatenate(x["shards"]))
+    check_f16(C, A @ oracle.bf16_bits_to_f64(x["B"]), w.K, "bf16 workload full")
+
+
+def test_bf16_modes_chunks_and_local_rank_bit_identical():
+    S, R, K, N = 3, 256, 512, 384
+    x = synth.make_inputs(S, R, K, N, "bf16", 79)
+    ref = run_bf16(x, S, R, K, N)
+    with Plan(S, S * R, K, N, "bf16") as plan:
+        for mode in (B_.MODE_SEQUENTIAL, B_.MODE_COMPUTE_ONLY, B_.MODE_PIPELINED):
+            assert np.array_equal(run_bf16(x, S, R, K, N, plan=plan, mode=mode), ref)
+    for c in (128, 16, 1):
+        assert np.array_equal(run_bf16(x, S, R, K, N, c), ref), f"chunk_rows={c}"
+    for local in range(S):
+        assert np.array_equal(run_bf16(x, S, R, K, N, local=local), ref), f"local={local}"
+
+
+def test_bf16_plan_checks_operand_dtype():
+    with Plan(2, 256, 64, 128, "bf16") as plan:
+        f16 = [torch.zeros((128, 64), dtype=torch.float16, device=DEV) for _ in range(2)]
+        with pytest.raises(TypeError):
+            plan.run(f16, torch.zeros((64, 128), dtype=torch.float16, device=DEV))
+
+
+# ---------------------------------------------------------------------------
 # int8 dequant
 # ---------------------------------------------------------------------------
 
