@@ -72,6 +72,7 @@ def _load():
         "ag_gemm_plan_geometry": (i32, [vp, geo_p]),
         "ag_gemm_plan_chunk_rows": (i64, [vp]),
         "ag_gemm_run": (i32, [vp, ctypes.POINTER(vp), vp, vp, vp]),
+        "ag_gemm_run_ld": (i32, [vp, ctypes.POINTER(vp), vp, i64, vp, i64, vp]),
         "ag_gemm_dequant_run": (i32, [vp, ctypes.POINTER(vp), vp, vp, vp, vp, vp, vp]),
         "ag_gemm_plan_status": (i32, [vp]),
         "ag_gemm_plan_status_word": (i64, [vp]),
@@ -174,6 +175,12 @@ def ag_gemm_plan_chunk_rows(plan: int) -> int:
 def ag_gemm_run(plan: int, shard_ptrs, B: int, C: int, stream: int = 0) -> int:
     p, _keep = _ptrs(shard_ptrs)
     return _check(_lib.ag_gemm_run(plan, p, B, C, stream))
+
+
+def ag_gemm_run_ld(plan: int, shard_ptrs, B: int, ldb: int, C: int, ldc: int,
+                   stream: int = 0) -> int:
+    p, _keep = _ptrs(shard_ptrs)
+    return _check(_lib.ag_gemm_run_ld(plan, p, B, ldb, C, ldc, stream))
 
 
 def ag_gemm_dequant_run(plan: int, shard_ptrs, B: int, bias: int, scale: int, C_i32: int,

@@ -106,9 +106,11 @@ int encode_stage8(CUtensorMap* map, const void* base, int64_t slots, int64_t R, 
 
 // fp32 C viewed as [S][R][N] so that a box never crosses into the next shard's
 // rows: box 32 columns x 32 rows (128-byte rows, swizzled like the staging box).
-int encode_c(CUtensorMap* map, const void* base, int64_t S, int64_t R, int64_t N) {
+// Row m of C starts ldc floats after row m - 1 (ldc = N, or the row pitch of a
+// wider matrix whose column block C is).
+int encode_c(CUtensorMap* map, const void* base, int64_t S, int64_t R, int64_t N, int64_t ldc) {
   cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)R, (cuuint64_t)S};
-  cuuint64_t strides[2] = {(cuuint64_t)N * 4, (cuuint64_t)R * N * 4};
+  cuuint64_t strides[2] = {(cuuint64_t)ldc * 4, (cuuint64_t)R * ldc * 4};
   cuuint32_t box[3] = {32, 32, 1};
   return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, 3, dims, strides, box);
 }
@@ -134,15 +136,17 @@ int encode_stage(CUtensorMap* map, const void* base, int64_t slots, int64_t R, i
 // box brings a CTA's whole half of the tile (BN / 128 groups); otherwise as 2D
 // (N, K) with one 64 x 64 box per group.
 bool b_is_3d(int64_t N) { return N % 64 == 0; }
-int encode_b(CUtensorMap* map, const void* base, int64_t K, int64_t N, int BN) {
+// Row k of B starts ldb elements after row k - 1 (ldb = N, or the row pitch of a
+// wider matrix whose column block B is).
+int encode_b(CUtensorMap* map, const void* base, int64_t K, int64_t N, int64_t ldb, int BN) {
   if (b_is_3d(N)) {
     cuuint64_t dims[3] = {64, (cuuint64_t)K, (cuuint64_t)N / 64};
-    cuuint64_t strides[2] = {(cuuint64_t)N * 2, 128};
+    cuuint64_t strides[2] = {(cuuint64_t)ldb * 2, 128};
     cuuint32_t box[3] = {64, agg::kBlockK, (cuuint32_t)(BN / 128)};
     return encode_f16(map, base, 3, dims, strides, box);
   }
   cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)K};
-  cuuint64_t strides[1] = {(cuuint64_t)N * 2};
+  cuuint64_t strides[1] = {(cuuint64_t)ldb * 2};
   cuuint32_t box[2] = {64, agg::kBlockK};
   return encode_f16(map, base, 2, dims, strides, box);
 }
@@ -256,6 +260,7 @@ struct ag_gemm_plan {
   const void* cached_b = nullptr;
   CUtensorMap tm_b_cached{};
   const void* cached_c = nullptr;
+  int64_t cached_ldb = 0, cached_ldc = 0;  // row pitches the cached B / C maps were made for
   CUtensorMap tm_c_cached{};
   // int8 with at most 128 gathered rows: the skinny kernel
   bool skinny = false;
@@ -311,10 +316,17 @@ int launch_fused(ag_gemm_plan* p, agg::FusedParams& fp, int flags, cudaStream_t 
 }
 
 // One run: the launch sequence of the plan's mode on `stream`.
-int run_impl(ag_gemm_plan* p, const void* const* shard_ptrs, const void* B, float* C,
-             int32_t* C_i32, void* D, const int32_t* bias, const float* scale, void* stream_v) {
+int run_impl(ag_gemm_plan* p, const void* const* shard_ptrs, const void* B, int64_t ldb, float* C,
+             int64_t ldc, int32_t* C_i32, void* D, const int32_t* bias, const float* scale,
+             void* stream_v) {
   const Geometry& g = p->g;
   const bool int8 = g.dtype == AG_GEMM_I8;
+  if (ldb < g.N || ldc < g.N)
+    return fail(AG_GEMM_ERR_INVALID, "ldb (%lld) and ldc (%lld) must be at least N (%lld)",
+                (long long)ldb, (long long)ldc, (long long)g.N);
+  if (ldb % 8 != 0 || ldc % 4 != 0)
+    return fail(AG_GEMM_ERR_INVALID,
+                "row pitches must be multiples of 16 bytes: ldb %% 8 == 0, ldc %% 4 == 0");
   if (!shard_ptrs) return fail(AG_GEMM_ERR_INVALID, "shard_ptrs is NULL");
   for (int s = 0; s < g.S; ++s) {
     if (!shard_ptrs[s]) return fail(AG_GEMM_ERR_INVALID, "shard_ptrs[%d] is NULL", s);
@@ -363,15 +375,17 @@ int run_impl(ag_gemm_plan* p, const void* const* shard_ptrs, const void* B, floa
       if ((rc = encode_a(&p->tm_a_cached, local_ptr, g.R, g.K)) != AG_GEMM_OK) return rc;
       p->cached_a = local_ptr;
     }
-    if (p->cached_b != B) {
+    if (p->cached_b != B || p->cached_ldb != ldb) {
       p->cached_b = nullptr;
-      if ((rc = encode_b(&p->tm_b_cached, B, g.K, g.N, g.BN)) != AG_GEMM_OK) return rc;
+      if ((rc = encode_b(&p->tm_b_cached, B, g.K, g.N, ldb, g.BN)) != AG_GEMM_OK) return rc;
       p->cached_b = B;
+      p->cached_ldb = ldb;
     }
-    if (p->cached_c != C) {
+    if (p->cached_c != C || p->cached_ldc != ldc) {
       p->cached_c = nullptr;
-      if ((rc = encode_c(&p->tm_c_cached, C, g.S, g.R, g.N)) != AG_GEMM_OK) return rc;
+      if ((rc = encode_c(&p->tm_c_cached, C, g.S, g.R, g.N, ldc)) != AG_GEMM_OK) return rc;
       p->cached_c = C;
+      p->cached_ldc = ldc;
     }
     fp.tm_a_local = p->tm_a_cached;
     fp.tm_b = p->tm_b_cached;
@@ -638,7 +652,7 @@ ag_gemm_plan* ag_gemm_plan_create(int n_shards, int64_t M, int64_t K, int64_t N,
       return nullptr;
     }
     if (encode_a(&p->tm_a16, p->a16, g.R, g.K) != AG_GEMM_OK ||
-        encode_b(&p->tm_b16, p->b16, g.K, g.N, g.BN) != AG_GEMM_OK) {
+        encode_b(&p->tm_b16, p->b16, g.K, g.N, g.N, g.BN) != AG_GEMM_OK) {
       free_plan(p);
       return nullptr;
     }
@@ -684,7 +698,16 @@ int ag_gemm_run(ag_gemm_plan* plan, const void* const* shard_ptrs, const void* B
   if (plan->g.dtype == AG_GEMM_I8)
     return fail(AG_GEMM_ERR_INVALID,
                 "ag_gemm_run needs an fp16 or bf16 plan (use ag_gemm_dequant_run)");
-  return run_impl(plan, shard_ptrs, B, C, nullptr, nullptr, nullptr, nullptr, stream);
+  return run_impl(plan, shard_ptrs, B, plan->g.N, C, plan->g.N, nullptr, nullptr, nullptr,
+                  nullptr, stream);
+}
+
+int ag_gemm_run_ld(ag_gemm_plan* plan, const void* const* shard_ptrs, const void* B, int64_t ldb,
+                   float* C, int64_t ldc, void* stream) {
+  if (!plan) return fail(AG_GEMM_ERR_INVALID, "plan is NULL");
+  if (plan->g.dtype == AG_GEMM_I8)
+    return fail(AG_GEMM_ERR_INVALID, "ag_gemm_run_ld needs an fp16 or bf16 plan");
+  return run_impl(plan, shard_ptrs, B, ldb, C, ldc, nullptr, nullptr, nullptr, nullptr, stream);
 }
 
 int ag_gemm_dequant_run(ag_gemm_plan* plan, const void* const* shard_ptrs, const void* B,
@@ -693,7 +716,8 @@ int ag_gemm_dequant_run(ag_gemm_plan* plan, const void* const* shard_ptrs, const
   if (!plan) return fail(AG_GEMM_ERR_INVALID, "plan is NULL");
   if (plan->g.dtype != AG_GEMM_I8)
     return fail(AG_GEMM_ERR_INVALID, "ag_gemm_dequant_run needs an int8 plan");
-  return run_impl(plan, shard_ptrs, B, nullptr, C_i32, D_f16, bias, scale, stream);
+  return run_impl(plan, shard_ptrs, B, plan->g.N, nullptr, plan->g.N, C_i32, D_f16, bias, scale,
+                  stream);
 }
 
 int64_t ag_gemm_plan_status_word(ag_gemm_plan* plan) {
@@ -878,9 +902,9 @@ extern "C" int ag_gemm_run_noalloc(int n_shards, int64_t M, int64_t K, int64_t N
   fp.g = g;
   for (int pos = 0; pos < g.S; ++pos) fp.src[pos] = shard_ptrs[agg::source_of(g, 0, pos)];
   if ((rc = encode_a(&fp.tm_a_local, fp.src[0], g.R, g.K)) != AG_GEMM_OK ||
-      (rc = encode_b(&fp.tm_b, B, g.K, g.N, g.BN)) != AG_GEMM_OK ||
+      (rc = encode_b(&fp.tm_b, B, g.K, g.N, g.N, g.BN)) != AG_GEMM_OK ||
       (rc = encode_stage(&fp.tm_a_stage, staging, slots, g.R, g.K)) != AG_GEMM_OK ||
-      (rc = encode_c(&fp.tm_c, C, g.S, g.R, g.N)) != AG_GEMM_OK)
+      (rc = encode_c(&fp.tm_c, C, g.S, g.R, g.N, g.N)) != AG_GEMM_OK)
     return rc;
   fp.staging = staging;
   fp.counters = counters;

@@ -15,7 +15,10 @@ def _stream_handle(stream) -> int:
     return int(s.cuda_stream)
 
 
-def _check(t: torch.Tensor, name: str, dtype, shape):
+def _check(t: torch.Tensor, name: str, dtype, shape, pitched: bool = False) -> int:
+    """Validate a device matrix; returns its row pitch in elements.  With
+    `pitched`, a column block of a wider row-major matrix (unit column stride)
+    is accepted as well as a contiguous matrix."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.device.type != "cuda":
@@ -24,8 +27,12 @@ def _check(t: torch.Tensor, name: str, dtype, shape):
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
-    if not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous")
+    if t.is_contiguous():
+        return int(shape[-1]) if len(shape) > 1 else 1
+    if pitched and t.dim() == 2 and t.stride(1) == 1 and t.stride(0) >= t.shape[1]:
+        return int(t.stride(0))
+    raise ValueError(f"{name} must be contiguous" +
+                     (" or a column block of a row-major matrix" if pitched else ""))
 
 
 class Plan:
@@ -99,7 +106,9 @@ class Plan:
     # -- runs
     def run(self, shards, B, C=None, stream=None) -> torch.Tensor:
         """C (M x N fp32) = AllGather(shards) x B for fp16 (bf16 plans: bfloat16)
-        shards (R x K) and B (K x N)."""
+        shards (R x K) and B (K x N).  B and C may be column blocks of wider
+        row-major matrices (the N-sharded layout: rank d passes B[:, block d]
+        and C[:, block d]); they then go through ag_gemm_run_ld."""
         if self.dtype not in _TORCH_2B:
             raise ValueError("run() needs an f16 or bf16 plan")
         if len(shards) != self.n_shards:
@@ -107,12 +116,16 @@ class Plan:
         tdt = _TORCH_2B[self.dtype]
         for i, s in enumerate(shards):
             _check(s, f"shards[{i}]", tdt, (self.R, self.K))
-        _check(B, "B", tdt, (self.K, self.N))
+        ldb = _check(B, "B", tdt, (self.K, self.N), pitched=True)
         if C is None:
             C = torch.empty((self.M, self.N), dtype=torch.float32, device=B.device)
-        _check(C, "C", torch.float32, (self.M, self.N))
-        B_.ag_gemm_run(self.handle, [s.data_ptr() for s in shards], B.data_ptr(), C.data_ptr(),
-                       _stream_handle(stream))
+        ldc = _check(C, "C", torch.float32, (self.M, self.N), pitched=True)
+        ptrs = [s.data_ptr() for s in shards]
+        if ldb == self.N and ldc == self.N:
+            B_.ag_gemm_run(self.handle, ptrs, B.data_ptr(), C.data_ptr(), _stream_handle(stream))
+        else:
+            B_.ag_gemm_run_ld(self.handle, ptrs, B.data_ptr(), ldb, C.data_ptr(), ldc,
+                              _stream_handle(stream))
         return C
 
     def dequant_run(self, shards, B, bias, scale, C_i32=None, D=None, stream=None):

@@ -39,6 +39,9 @@ class Workload:
     N: int
     dtype: str           # "f16", "bf16" or "i8"
     chunk_rows: int      # 0 = chosen by the library (64..128 chunks per source)
+    n_blocks: int = 1    # N-sharded layout: B and C have n_blocks * N columns and the
+                         # problem is rank `rank`'s column block (ring order from `rank`)
+    rank: int = 0
 
     @property
     def R(self) -> int:
@@ -51,7 +54,10 @@ class Workload:
 
 # The five workloads: a small parity case, two compute-bound fp16 cases, a
 # compute-bound int8 dequant case and a memory-bound skinny int8 case; 6 is the
-# 4096^3 fp16 case with bfloat16 operands.
+# 4096^3 fp16 case with bfloat16 operands; 7 is one rank of the N-sharded
+# collective matmul with the per-device shape of "Collective matrix
+# multiplication" (2 devices, 1024 rows per shard, K = 4096, 4096 columns of B
+# per device): rank 0's column block of B (K x 8192) and C.
 WORKLOADS = {
     1: Workload(1, "f16 2x128 rows, K=256, N=128, chunk 16", 2, 256, 256, 128, "f16", 16),
     2: Workload(2, "f16 2x2048 rows, K=4096, N=4096", 2, 4096, 4096, 4096, "f16", 0),
@@ -59,6 +65,8 @@ WORKLOADS = {
     4: Workload(4, "i8 dequant 4x4096 rows, K=27392, N=4096", 4, 16384, 27392, 4096, "i8", 0),
     5: Workload(5, "i8 dequant skinny 2x32 rows, K=16384, N=7168", 2, 64, 16384, 7168, "i8", 0),
     6: Workload(6, "bf16 2x2048 rows, K=4096, N=4096", 2, 4096, 4096, 4096, "bf16", 0),
+    7: Workload(7, "f16 N-sharded rank 0 of 2: 2x1024 rows, K=4096, 4096 of 8192 columns",
+                2, 2048, 4096, 4096, "f16", 0, n_blocks=2, rank=0),
 }
 
 
@@ -111,4 +119,8 @@ def make_inputs(S: int, R: int, K: int, N: int, dtype: str, seed: int):
 
 
 def workload_inputs(w: Workload):
-    return make_inputs(w.S, w.R, w.K, w.N, w.dtype, SEED_BASE + w.wid)
+    """Inputs of a workload; for an N-sharded one, B is the full K x (n_blocks * N)
+    matrix and ``B_rank`` the rank's column block (a view)."""
+    x = make_inputs(w.S, w.R, w.K, w.N * w.n_blocks, w.dtype, SEED_BASE + w.wid)
+    x["B_rank"] = x["B"][:, w.rank * w.N:(w.rank + 1) * w.N]
+    return x

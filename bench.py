@@ -199,11 +199,11 @@ def time_oracle(w, x, budget_s: float, row_block: int = 2):
         rr = np.repeat(rows, w.N)
         cc = np.tile(cols, row_block)
         if w.dtype == "f16":
-            oracle.ag_gemm_f16_at(x["shards"], x["B"], rr, cc)
+            oracle.ag_gemm_f16_at(x["shards"], x["B_rank"], rr, cc)
         elif w.dtype == "bf16":
-            oracle.ag_gemm_bf16_at(x["shards"], x["B"], rr, cc)
+            oracle.ag_gemm_bf16_at(x["shards"], x["B_rank"], rr, cc)
         else:
-            oracle.ag_gemm_dequant_at(x["shards"], x["B"], x["bias"], x["scale"], rr, cc)
+            oracle.ag_gemm_dequant_at(x["shards"], x["B_rank"], x["bias"], x["scale"], rr, cc)
         rows_done += row_block
         el = time.perf_counter() - t0
         if el >= budget_s:
@@ -247,10 +247,15 @@ def run_reference(args, w, rank):
 
 
 def workload_config(w, flush=True):
-    return {"workload": w.name, "n_shards": w.S, "M": w.M, "K": w.K, "N": w.N,
-            "dtype": w.dtype, "chunk_rows": w.chunk_rows or "auto",
-            "l2": ("flushed before each timed step (512 MiB written, then 512 MiB read)" if flush
-                   else "NOT flushed (analysis run; inputs may be L2-resident)")}
+    cfg = {"workload": w.name, "n_shards": w.S, "M": w.M, "K": w.K, "N": w.N,
+           "dtype": w.dtype, "chunk_rows": w.chunk_rows or "auto",
+           "l2": ("flushed before each timed step (512 MiB written, then 512 MiB read)" if flush
+                  else "NOT flushed (analysis run; inputs may be L2-resident)")}
+    if w.n_blocks > 1:
+        cfg["layout"] = (f"N-sharded: rank {w.rank} of {w.n_blocks} computes its column block of "
+                         f"C (B and C column blocks, ldb = ldc = {w.n_blocks * w.N}), row slices "
+                         f"in ring order from its own shard")
+    return cfg
 
 
 # ---------------------------------------------------------------------------
@@ -269,12 +274,16 @@ def run_ours(args, w, rank, world, local_rank):
     x = synth.workload_inputs(w)
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
     h_shards = [pin(s) for s in x["shards"]]
-    h_B = pin(x["B"])
+    h_B = pin(x["B_rank"])  # this rank's B (its column block, for the N-sharded layout)
     if w.dtype == "bf16":  # bit patterns (numpy has no bfloat16) -> bfloat16 tensors
         h_shards = [t.view(torch.int16).view(torch.bfloat16) for t in h_shards]
         h_B = h_B.view(torch.int16).view(torch.bfloat16)
     shards = [t.to(dev) for t in h_shards]
-    Bd = h_B.to(dev)
+    # B (and C below) at full width; the run takes the rank's column block
+    cols = slice(w.rank * w.N, (w.rank + 1) * w.N)
+    B_full = torch.empty((w.K, w.N * w.n_blocks), dtype=h_B.dtype, device=dev)
+    Bd = B_full[:, cols]
+    Bd.copy_(h_B)
     int8 = w.dtype == "i8"
     if int8:
         h_bias, h_scale = pin(x["bias"]), pin(x["scale"])
@@ -284,9 +293,12 @@ def run_ours(args, w, rank, world, local_rank):
         h_Ci = torch.empty((w.M, w.N), dtype=torch.int32).pin_memory()
         h_D = torch.empty((w.M, w.N), dtype=torch.float16).pin_memory()
     else:
-        C = torch.empty((w.M, w.N), dtype=torch.float32, device=dev)
+        C_full = torch.empty((w.M, w.N * w.n_blocks), dtype=torch.float32, device=dev)
+        C = C_full[:, cols]
         h_C = torch.empty((w.M, w.N), dtype=torch.float32).pin_memory()
     plan = Plan(w.S, w.M, w.K, w.N, w.dtype, w.chunk_rows)
+    if w.rank:
+        plan.set_local_rank(w.rank)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     flush_rd = torch.ones(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
@@ -445,7 +457,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=None,
                     help="timed steps (default: enough for ~2 s of timed GPU work, >= 20)")
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6])
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7])
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-step-seconds", type=float, default=4.0)

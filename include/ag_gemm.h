@@ -197,6 +197,25 @@ int ag_gemm_run(ag_gemm_plan *plan, const void *const *shard_ptrs,
                 const void *B, float *C, void *stream);
 
 /*
+ * ag_gemm_run with row pitches: B element (k, n) at B[k * ldb + n] and C
+ * element (m, n) at C[m * ldc + n] (ldb, ldc >= N; ldb % 8 == 0 and
+ * ldc % 4 == 0, i.e. 16-byte row pitches; the base pointers 16-byte aligned).
+ * Columns of a row past N are neither read nor written.
+ *
+ * This is the N-sharded layout of "Collective matrix multiplication"
+ * (sections 算法概述：Ring All-Gather and 将 kernel 与 JAX 集成): A is
+ * sharded by rows, B by columns, and rank d computes AllGather(A) x B_d, the
+ * column block d of C, taking the row slices of its output in ring order
+ * d, d+1, ..., d+D-1 (mod D) -- on this library, a plan with
+ * ag_gemm_plan_set_local_rank(plan, d).  With one GPU holding every rank,
+ * rank d passes B_d = B + d * n_shard and C_d = C + d * n_shard with
+ * ldb = ldc = D * n_shard (so n_shard % 8 == 0 for alignment).
+ * fp16 and bf16 plans only (AG_GEMM_ERR_INVALID otherwise).
+ */
+int ag_gemm_run_ld(ag_gemm_plan *plan, const void *const *shard_ptrs,
+                   const void *B, int64_t ldb, float *C, int64_t ldc, void *stream);
+
+/*
  * int8 AllGatherMatmulDequant.  shard_ptrs: n_shards device pointers to
  * R x K int8; B: K x N int8; bias: N int32; scale: N fp32; C_i32: M x N int32
  * and D_f16: M x N fp16, both written.  If |A x B + bias| reaches 2^31 the

@@ -16,6 +16,9 @@ Functions and what they state (page titles and sections):
 * ``ag_gemm_dequant`` -- "AllGather矩阵乘法反量化算子设计文档", 1.2 / 2.2:
   C_i32 = A x B + bias, D = fp16(fp32(C_i32) * scale).
 * ``*_at`` -- the same definitions evaluated at chosen output points.
+* ``collective_matmul_ring`` -- "Collective matrix multiplication",
+  算法概述：Ring All-Gather: rank d's column shard of C, built in the ring's
+  step order from the one-shard definition (index bookkeeping only).
 """
 from __future__ import annotations
 
@@ -317,4 +320,28 @@ def ag_gemm_bf16_at(shards, B, rows, cols) -> np.ndarray:
                                       _ptr(cols, ctypes.c_int64),
                                       _ptr(out, ctypes.c_double)),
            "ag_gemm_bf16_at")
+    return out
+
+
+# -- N-sharded collective matmul (ring order) -----------------------------------
+
+def collective_matmul_ring(shards, B_d, d, dtype="f16") -> np.ndarray:
+    """Rank d's output of the ring collective matmul: AllGather(shards) x B_d.
+
+    "Collective matrix multiplication", 算法概述：Ring All-Gather: with D ranks,
+    at step i (0 <= i < D) rank d holds shard A_{(d + i) % D}, multiplies it by
+    its own column shard B_d and writes the product into the output's row
+    slice (d + i) % D.  Each step is the one-shard definition (ag_gemm_f16 or
+    ag_gemm_bf16 with a single shard); this function only places the slices.
+    """
+    D = len(shards)
+    R = np.asarray(shards[0]).shape[0]
+    one = ag_gemm_f16 if dtype == "f16" else ag_gemm_bf16
+    out = None
+    for i in range(D):
+        src = (d + i) % D
+        part = one([shards[src]], B_d)
+        if out is None:
+            out = np.empty((D * R, part.shape[1]), dtype=np.float64)
+        out[src * R:(src + 1) * R] = part
     return out

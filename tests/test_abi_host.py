@@ -82,7 +82,8 @@ def test_validate_accepts_workloads(B):
 
 def test_geometry_of_workloads(B):
     from all_gather_gemm_chunked_gb300.synth import WORKLOADS
-    want = {1: (16, 8), 2: (32, 64), 3: (16, 64), 4: (64, 64), 5: (1, 32), 6: (32, 64)}
+    want = {1: (16, 8), 2: (32, 64), 3: (16, 64), 4: (64, 64), 5: (1, 32), 6: (32, 64),
+            7: (16, 64)}
     for wid, w in WORKLOADS.items():
         g = B.ag_gemm_geometry_of(w.S, w.M, w.K, w.N, _DT[w.dtype], w.chunk_rows)
         assert (g.chunk_rows, g.chunks_per_source) == want[wid]
@@ -157,6 +158,7 @@ def test_out_of_range_schedule_queries(B):
 def test_null_plan_is_rejected(B):
     lib = B.library_handle()
     assert lib.ag_gemm_run(None, None, None, None, None) == B.ERR_INVALID
+    assert lib.ag_gemm_run_ld(None, None, None, 0, None, 0, None) == B.ERR_INVALID
     assert lib.ag_gemm_plan_set_mode(None, 0) == B.ERR_INVALID
     assert lib.ag_gemm_plan_status(None) == B.ERR_INVALID
     assert lib.ag_gemm_plan_path(None) == B.ERR_INVALID

@@ -598,3 +598,86 @@ def test_oracle_bf16_at_matches_full(oracle):
     rows = rng.integers(0, 18, 50)
     cols = rng.integers(0, 9, 50)
     assert np.array_equal(oracle.ag_gemm_bf16_at(shards, B, rows, cols), C[rows, cols])
+
+
+# ---------------------------------------------------------------------------
+# N-sharded collective matmul: ring order ("Collective matrix multiplication",
+# 算法概述：Ring All-Gather)
+# ---------------------------------------------------------------------------
+
+def _ring_placement_pin(ring, D, d):
+    """Shards whose column 0 holds their rank index and B_d with a single row of
+    ones: row block s of rank d's output must be all s -- a closed form that
+    does not depend on the oracle's GEMM."""
+    R, K, ns = 3, 5, 4
+    shards = [np.zeros((R, K), np.float16) for _ in range(D)]
+    for s in range(D):
+        shards[s][:, 0] = s
+    B_d = np.zeros((K, ns), np.float16)
+    B_d[0, :] = 1
+    out = ring(shards, B_d, d)
+    want = np.repeat(np.arange(D, dtype=np.float64), R)[:, None] * np.ones((1, ns))
+    return out.shape == want.shape and np.array_equal(out, want)
+
+
+@pytest.mark.parametrize("D", [1, 2, 3, 4])
+def test_ring_places_each_step_in_its_row_slice(oracle, D):
+    for d in range(D):
+        assert _ring_placement_pin(oracle.collective_matmul_ring, D, d)
+
+
+@pytest.mark.parametrize("D,R,K,ns", [(2, 5, 7, 3), (3, 4, 16, 8), (4, 2, 9, 5)])
+def test_ring_column_shards_assemble_the_product(oracle, D, R, K, ns):
+    """Ranks 0..D-1, each with its column shard B_d, together give
+    AllGather(A) x B: checked against torch float64 matmul on the CPU."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(100 + D * 10 + K)
+    shards = [rng.standard_normal((R, K)).astype(np.float16) for _ in range(D)]
+    B = rng.standard_normal((K, D * ns)).astype(np.float16)
+    full = np.concatenate([oracle.collective_matmul_ring(shards, B[:, d * ns:(d + 1) * ns], d)
+                           for d in range(D)], axis=1)
+    A = np.concatenate(shards).astype(np.float64)
+    ref = (torch.from_numpy(A) @ torch.from_numpy(B.astype(np.float64))).numpy()
+    assert np.allclose(full, ref, rtol=1e-13, atol=1e-13)
+    # the same sums as the one-shot definition, element by element
+    assert np.array_equal(full, oracle.ag_gemm_f16(shards, B))
+
+
+def test_ring_bf16_matches_definition(oracle):
+    rng = np.random.default_rng(7)
+    D, R, K, ns = 3, 4, 24, 8
+    shards = [oracle.f64_to_bf16_bits(rng.standard_normal((R, K))) for _ in range(D)]
+    B = oracle.f64_to_bf16_bits(rng.standard_normal((K, D * ns)))
+    full = np.concatenate([oracle.collective_matmul_ring(shards, B[:, d * ns:(d + 1) * ns], d,
+                                                         dtype="bf16") for d in range(D)], axis=1)
+    assert np.array_equal(full, oracle.ag_gemm_bf16(shards, B))
+
+
+def test_ring_pin_catches_misplaced_steps(oracle):
+    """Planted mistakes in the ring's bookkeeping: step i written to slice i,
+    the ring walked backwards with the forward slice index, one step repeated."""
+    def to_step_index(shards, B_d, d):
+        D, R = len(shards), shards[0].shape[0]
+        out = np.empty((D * R, B_d.shape[1]))
+        for i in range(D):
+            out[i * R:(i + 1) * R] = oracle.ag_gemm_f16([shards[(d + i) % D]], B_d)
+        return out
+
+    def backwards(shards, B_d, d):
+        D, R = len(shards), shards[0].shape[0]
+        out = np.empty((D * R, B_d.shape[1]))
+        for i in range(D):
+            out[((d + i) % D) * R:((d + i) % D + 1) * R] = \
+                oracle.ag_gemm_f16([shards[(d - i) % D]], B_d)
+        return out
+
+    def repeated(shards, B_d, d):
+        D, R = len(shards), shards[0].shape[0]
+        out = np.empty((D * R, B_d.shape[1]))
+        for i in range(D):
+            src = (d + min(i, 1)) % D
+            out[((d + i) % D) * R:((d + i) % D + 1) * R] = oracle.ag_gemm_f16([shards[src]], B_d)
+        return out
+
+    for bad in (to_step_index, backwards, repeated):
+        assert not all(_ring_placement_pin(bad, 3, d) for d in range(3)), bad.__name__

@@ -455,6 +455,27 @@ def test_i8_skinny_modes_local_rank_and_repeats():
         assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])
 
 
+@pytest.mark.parametrize("S,R,K,N", [
+    (2, 16, 16384, 128),       # one n-tile of 64 units: 64 CTAs share it, the others hold none
+    (1, 8, 4096, 2048),        # 16 n-tiles of 16 units over 152 CTAs
+])
+def test_i8_skinny_shared_tiles_and_repeats(oracle, S, R, K, N):
+    """Split-K sums of one n-tile spread over many CTAs (some CTAs own no unit),
+    reduced by the CTA that stores the tile's last piece.  The per-tile counters
+    are monotonic across runs of one plan; a copy-only run leaves them alone."""
+    x = synth.make_inputs(S, R, K, N, "i8", 4000 + K + N)
+    Cref, Dref = oracle.ag_gemm_dequant(x["shards"], x["B"], x["bias"], x["scale"])
+    with Plan(S, S * R, K, N, "i8") as plan:
+        for i, mode in enumerate((B_.MODE_PIPELINED, B_.MODE_COPY_ONLY, B_.MODE_PIPELINED,
+                                  B_.MODE_COMPUTE_ONLY, B_.MODE_SEQUENTIAL, B_.MODE_PIPELINED)):
+            got = run_i8(x, S, R, K, N, plan=plan, mode=mode)
+            if mode != B_.MODE_COPY_ONLY:
+                _check_i8(got[0], got[1], Cref, Dref, f"run {i} mode {mode}")
+        plan.reset()
+        got = run_i8(x, S, R, K, N, plan=plan, mode=B_.MODE_PIPELINED)
+        _check_i8(got[0], got[1], Cref, Dref, "after reset")
+
+
 def test_i8_skinny_timeout_then_reset():
     S, R, K, N = 2, 32, 1024, 256
     x = synth.make_inputs(S, R, K, N, "i8", 92)
@@ -470,3 +491,82 @@ def test_i8_skinny_timeout_then_reset():
         plan.reset()
         got = run_i8(x, S, R, K, N, plan=plan)
         assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])
+
+
+# ---------------------------------------------------------------------------
+# N-sharded layout ("Collective matrix multiplication", Ring All-Gather): rank d
+# computes C[:, block d] = AllGather(A) x B[:, block d], its row slices taken
+# in ring order from d (the plan's local rank); B and C are column blocks of
+# the full matrices, passed with their row pitches (ag_gemm_run_ld).
+# ---------------------------------------------------------------------------
+
+def _nshard_inputs(dt, D, R, K, ns, seed):
+    x = synth.make_inputs(D, R, K, D * ns, dt, seed)
+    conv = _bf16_to_dev if dt == "bf16" else _to_dev
+    return x, [conv(s) for s in x["shards"]], conv(x["B"])
+
+
+@pytest.mark.parametrize("dt,D,R,K,ns", [
+    ("f16", 2, 256, 512, 256),
+    ("f16", 4, 96, 320, 72),     # n_shard not a multiple of 64: the 2-D B map
+    ("bf16", 3, 130, 256, 136),  # ragged rows per shard
+])
+def test_nshard_ranks_assemble_the_product(oracle, dt, D, R, K, ns):
+    x, shards, Bfull = _nshard_inputs(dt, D, R, K, ns, 5000 + D * 7 + K)
+    N = D * ns
+    C = torch.full((D * R, N), float("nan"), dtype=torch.float32, device=DEV)
+    with Plan(D, D * R, K, ns, dt) as plan:
+        for d in range(D):
+            plan.set_local_rank(d)
+            plan.run(shards, Bfull[:, d * ns:(d + 1) * ns], C[:, d * ns:(d + 1) * ns])
+            torch.cuda.synchronize()
+            assert plan.status() == 0, f"rank {d}: status word {plan.status_word():#x}"
+            if d + 1 < D:  # columns of later ranks untouched
+                assert torch.isnan(C[:, (d + 1) * ns:]).all()
+    got = C.cpu().numpy()
+    ref_fn = oracle.ag_gemm_f16 if dt == "f16" else oracle.ag_gemm_bf16
+    check_f16(got, ref_fn(x["shards"], x["B"]), K, f"{dt} N-sharded D={D}")
+    # each rank's block against the ring-order oracle of that rank
+    for d in range(D):
+        ring = oracle.collective_matmul_ring(x["shards"], x["B"][:, d * ns:(d + 1) * ns], d, dt)
+        check_f16(got[:, d * ns:(d + 1) * ns], ring, K, f"{dt} rank {d}")
+    # the same fp32 sums as one run over all columns with contiguous operands
+    with Plan(D, D * R, K, N, dt) as plan:
+        whole = plan.run(shards, Bfull)
+        torch.cuda.synchronize()
+    assert torch.equal(C, whole)
+
+
+def test_nshard_modes_bit_identical():
+    D, R, K, ns = 2, 128, 256, 128
+    _, shards, Bfull = _nshard_inputs("f16", D, R, K, ns, 77)
+    outs = []
+    with Plan(D, D * R, K, ns, "f16") as plan:
+        plan.set_local_rank(1)
+        for mode in (B_.MODE_PIPELINED, B_.MODE_SEQUENTIAL, B_.MODE_PIPELINED):
+            plan.set_mode(mode)
+            C = torch.full((D * R, D * ns), float("nan"), dtype=torch.float32, device=DEV)
+            plan.run(shards, Bfull[:, ns:], C[:, ns:])
+            torch.cuda.synchronize()
+            assert plan.status() == 0
+            outs.append(C)
+    assert all(torch.equal(outs[0][:, ns:], o[:, ns:]) for o in outs[1:])
+    assert not torch.isnan(outs[0][:, ns:]).any()
+    assert all(torch.isnan(o[:, :ns]).all() for o in outs)
+
+
+def test_nshard_pitch_checks():
+    D, R, K, ns = 2, 64, 128, 64
+    _, shards, Bfull = _nshard_inputs("f16", D, R, K, ns, 78)
+    C = torch.empty((D * R, D * ns), dtype=torch.float32, device=DEV)
+    ptrs = [s.data_ptr() for s in shards]
+    with Plan(D, D * R, K, ns, "f16") as plan:
+        for ldb, ldc in ((ns - 8, D * ns), (D * ns, ns - 4), (D * ns + 4, D * ns),
+                         (D * ns, D * ns + 2)):
+            with pytest.raises(B_.AgGemmError) as e:
+                B_.ag_gemm_run_ld(plan.handle, ptrs, Bfull.data_ptr(), ldb, C.data_ptr(), ldc)
+            assert e.value.code == B_.ERR_INVALID
+    with Plan(D, D * R, K, ns, "i8") as plan:
+        with pytest.raises(B_.AgGemmError) as e:
+            B_.ag_gemm_run_ld(plan.handle, ptrs, Bfull.data_ptr(), D * ns, C.data_ptr(), D * ns)
+        assert e.value.code == B_.ERR_INVALID
