@@ -46,7 +46,7 @@ class Geometry(ctypes.Structure):
         ("group_m", ctypes.c_int32), ("kseg_blocks", ctypes.c_int32),
         ("m_tiles", ctypes.c_int64), ("n_tiles", ctypes.c_int64), ("tiles", ctypes.c_int64),
         ("producer_items", ctypes.c_int64), ("staging_bytes", ctypes.c_int64),
-        ("workspace_bytes", ctypes.c_int64),
+        ("workspace_bytes", ctypes.c_int64), ("staging_slots", ctypes.c_int64),
     ]
 
     def as_dict(self):
@@ -68,6 +68,8 @@ def _load():
         "ag_gemm_tile_at": (i32, [geo_p, i32, i64, i64_arr]),
         "ag_gemm_item_at": (i32, [geo_p, i32, i64, i64_arr]),
         "ag_gemm_plan_create": (vp, [i32, i64, i64, i64, i32, i64]),
+        "ag_gemm_plan_create_bounded": (vp, [i32, i64, i64, i64, i32, i64, i32]),
+        "ag_gemm_choose_chunk_rows_bounded": (i64, [i64]),
         "ag_gemm_plan_destroy": (None, [vp]),
         "ag_gemm_plan_geometry": (i32, [vp, geo_p]),
         "ag_gemm_plan_chunk_rows": (i64, [vp]),
@@ -129,6 +131,10 @@ def ag_gemm_choose_chunk_rows(R: int) -> int:
     return _check(_lib.ag_gemm_choose_chunk_rows(R))
 
 
+def ag_gemm_choose_chunk_rows_bounded(R: int) -> int:
+    return _check(_lib.ag_gemm_choose_chunk_rows_bounded(R))
+
+
 def ag_gemm_validate(n_shards, M, K, N, dtype, chunk_rows) -> int:
     return _check(_lib.ag_gemm_validate(n_shards, M, K, N, dtype, chunk_rows))
 
@@ -153,6 +159,13 @@ def ag_gemm_item_at(geometry: Geometry, local_rank: int, i: int):
 
 def ag_gemm_plan_create(n_shards, M, K, N, dtype, chunk_rows=0) -> int:
     h = _lib.ag_gemm_plan_create(n_shards, M, K, N, dtype, chunk_rows)
+    if not h:
+        raise _err()
+    return h
+
+
+def ag_gemm_plan_create_bounded(n_shards, M, K, N, dtype, chunk_rows=0, staging_slots=0) -> int:
+    h = _lib.ag_gemm_plan_create_bounded(n_shards, M, K, N, dtype, chunk_rows, staging_slots)
     if not h:
         raise _err()
     return h

@@ -101,15 +101,50 @@ __device__ __forceinline__ void warp_widen16(const uint4* __restrict__ src, uint
   }
 }
 
+// Bounded staging: lane 0 waits until slot `slot` may take its next block
+// (the credits of the previous block's readers reached `target`).  Bounded by
+// the plan's timeout; false once another wait has failed or the time is up.
+__device__ bool wait_slot(const FusedParams& p, int64_t slot, uint32_t target, int lane) {
+  bool ok = true;
+  if (lane == 0 && ld_acquire_gpu(p.credits + slot) < target) {
+    const uint64_t deadline = globaltimer_ns() + p.timeout_ns;
+    uint32_t spins = 0;
+    while (ld_acquire_gpu(p.credits + slot) < target) {
+      __nanosleep(128);
+      if (++spins == 16) {
+        spins = 0;
+        if (*reinterpret_cast<volatile uint32_t*>(p.status) != 0u ||
+            globaltimer_ns() > deadline) {
+          ok = false;
+          break;
+        }
+      }
+    }
+    if (!ok) set_status(p.status, kStatusCreditTimeout, static_cast<uint32_t>(slot));
+  }
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
 template <bool kI8>
 __device__ void copy_warp(const FusedParams& p, int lane) {
   const Geometry& g = p.g;
+  // With bounded staging and the GEMM in the same launch, a block may only
+  // overwrite its slot after the slot's previous block has been read.  (A
+  // copy-only launch has no readers and writes freely.)
+  const bool credit = p.window > 0 && (p.flags & kFlagGemm) != 0;
+  int64_t ready_block = -1;  // the last block whose slot this warp saw released
   for (;;) {
     unsigned long long ticket = 0;
     if (lane == 0) ticket = atomicAdd(p.item_counter, 1ull);
     ticket = __shfl_sync(0xffffffffu, ticket, 0);
     const int64_t i = static_cast<int64_t>(ticket - p.item_base);
     if (i >= g.items) break;  // exactly one failing ticket per copy warp and run
+    if (i < 0) {
+      // tickets behind this run's base: the counters were not reset after a
+      // failed run; copy nothing (the readers time out and report it)
+      if (lane == 0) set_status(p.status, kStatusChunkTimeout, 0xFFFFFFu);
+      break;
+    }
     int pos, piece;
     int64_t q, v0, v1;
     item_coords(g, i, pos, q, piece, v0, v1);
@@ -117,8 +152,21 @@ __device__ void copy_warp(const FusedParams& p, int lane) {
     if (p.debug_delay_ns) __nanosleep(p.debug_delay_ns);
     const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.src[pos]) +
                                                       q * g.c * g.K * g.src_esize);
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.staging) +
-                                          ((int64_t)(pos - 1) * g.R + q * g.c) * g.K * 2);
+    int64_t drow = (int64_t)(pos - 1) * g.R + q * g.c;  // staging row of the chunk's first row
+    if (p.window > 0) {
+      // chunks never straddle a 256-row block (the plan requires 256 % c == 0)
+      const int64_t r = q * g.c, b = (int64_t)(pos - 1) * g.MT + r / kPairM;
+      const int64_t slot = b % p.window;
+      if (credit && b >= p.window && b != ready_block) {
+        // On a timeout the item is skipped (its chunk never becomes ready and
+        // its readers report the failure); the warp keeps drawing tickets so
+        // that it still draws exactly one failing ticket.
+        if (!wait_slot(p, slot, window_target(g, p.window, b, p.credit_epoch), lane)) continue;
+        ready_block = b;
+      }
+      drow = slot * kPairM + r % kPairM;
+    }
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.staging) + drow * g.K * 2);
     if (kI8)
       warp_widen16(src + v0, dst + 2 * v0, v1 - v0, lane);
     else
@@ -195,7 +243,11 @@ __device__ void tma_warp(const FusedParams& p, uint32_t rank, uint8_t* sA, uint8
         fence_acq_rel_gpu();
         fence_proxy_async_global();
       }
-      const int32_t y = static_cast<int32_t>(row0);
+      // A rows: the local shard at row0, or the staging: [S-1][R][K] at
+      // (row0, pos - 1), or the window's [W][256][K] at (this CTA's half, slot)
+      const bool win = pos > 0 && p.window > 0;
+      const int32_t y = win ? static_cast<int32_t>(rank * kBlockM) : static_cast<int32_t>(row0);
+      const int32_t z = win ? static_cast<int32_t>(((pos - 1) * g.MT + mt) % p.window) : pos - 1;
       const int32_t xb = static_cast<int32_t>(nt * g.BN + rank * half);
       for (int64_t kb = 0; kb < g.KB; ++kb) {
         if (!mbar_wait(&empty[stage], phase ^ 1u, p.pipe_timeout_ns, abort, gstatus)) {
@@ -209,7 +261,7 @@ __device__ void tma_warp(const FusedParams& p, uint32_t rank, uint8_t* sA, uint8
         if (pos == 0)
           tma_load_2d_pair(a_dst, &p.tm_a_local, bar, x, y);
         else
-          tma_load_3d_pair(a_dst, &p.tm_a_stage, bar, x, y, pos - 1);
+          tma_load_3d_pair(a_dst, &p.tm_a_stage, bar, x, y, z);
         uint8_t* b_dst = sB + stage * kBBytes;
         // One TMA instruction per operand and k-block where possible: the TMA
         // unit's per-instruction cost, not bandwidth, limits the ring on GB300.
@@ -258,10 +310,16 @@ __device__ void mma_warp(const FusedParams& p, const uint8_t* sA, const uint8_t*
   const int64_t nseg = ceil_div(g.KB, seg_len);
   const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
   const int64_t n_clusters = gridDim.x / 2, cluster = blockIdx.x / 2;
+  // bounded staging, pipelined launch: credit the slot a remote tile read
+  const bool credit = p.window > 0 && (p.flags & kFlagWait) != 0;
   int stage = 0;
   uint32_t phase = 0, unit = 0;
   bool ok = true;
   for (int64_t t = cluster; t < g.tiles && ok; t += n_clusters) {
+    int pos;
+    int64_t mt, nt;
+    tile_coords(g, t, pos, mt, nt);
+    const int64_t slot = credit && pos > 0 ? ((pos - 1) * g.MT + mt) % p.window : 0;
     for (int64_t seg = 0; seg < nseg && ok; ++seg) {
       const uint32_t buf = kI8 ? 0u : (unit & 1u);
       const uint32_t use = kI8 ? unit : (unit >> 1);
@@ -296,6 +354,12 @@ __device__ void mma_warp(const FusedParams& p, const uint8_t* sA, const uint8_t*
         if (++stage == kStages) {
           stage = 0;
           phase ^= 1u;
+        }
+        if (credit && pos > 0 && kb == g.KB - 1) {
+          // The last k-block of both CTAs' rows has landed (the pair's bytes
+          // are counted on this barrier): the staged rows are no longer read.
+          fence_proxy_async_global();
+          red_release_gpu_add(p.credits + slot, 1u);
         }
       }
       if (!ok) break;

@@ -15,6 +15,7 @@ enum : uint32_t {
   kStatusOk = 0,
   kStatusChunkTimeout = 1,     // a ready counter did not reach its target in time
   kStatusPipelineTimeout = 2,  // an mbarrier of the TMA/MMA/epilogue pipeline ran out
+  kStatusCreditTimeout = 3,    // bounded staging: a slot was not released by its readers in time
 };
 
 enum : int {
@@ -25,12 +26,12 @@ enum : int {
 
 struct FusedParams {
   CUtensorMap tm_a_local;   // fp16 [R][K] local shard (2D: K, R)
-  CUtensorMap tm_a_stage;   // fp16 [S-1][R][K] staging (3D: K, R, slot)
+  CUtensorMap tm_a_stage;   // fp16 staging (3D: K, rows, slot): [S-1][R][K], or [window][256][K]
   CUtensorMap tm_b;         // fp16 [K][N], loaded MN-major: 3D (64, K, N/64) when b3d, else 2D (N, K)
   CUtensorMap tm_c;         // fp16 path: fp32 C as [S][R][N] (3D: N, R, S), stored in 32x32 boxes
   Geometry g;
   const void* src[kMaxShards];  // shard pointers by consumption position
-  void* staging;                // fp16 [(S-1)][R][K]
+  void* staging;                // fp16 [(S-1)][R][K], or bounded: [window][256][K]
   uint32_t* counters;           // [(S-1)][Q] ready counters, monotonic
   unsigned long long* item_counter;  // copy items handed out so far (monotonic)
   unsigned long long item_base;      // item_counter value at the start of this run
@@ -49,6 +50,13 @@ struct FusedParams {
   uint64_t pipe_timeout_ns;     // limit of a wait on a pipeline mbarrier (longer)
   int64_t debug_skip_item;      // -1 = none
   uint32_t debug_delay_ns;
+  // Bounded staging (window > 0): remote row block b (256 rows: m-tile mt of
+  // position pos, b = (pos - 1) * MT + mt) lives in slot b % window.  Each
+  // remote tile that has loaded its rows adds one credit to the slot; block b
+  // may overwrite the slot once block b - window's NT tiles have all done so.
+  int window;                   // slots of 256 rows; 0 = every remote row has its own place
+  uint32_t* credits;            // [window] tiles done reading the slot, monotonic
+  uint32_t credit_epoch;        // pipelined runs of this plan since the last reset (>= 1)
 };
 
 constexpr int kThreads = 384;                         // 12 warps

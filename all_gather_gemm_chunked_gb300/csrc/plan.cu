@@ -204,6 +204,7 @@ void to_public(const Geometry& g, ag_gemm_geometry* out) {
   int64_t ws = out->staging_bytes + slots * g.Q * 4 + 64;
   if (g.dtype == AG_GEMM_I8) ws += (g.K * g.N + g.R * g.K) * 2;
   out->workspace_bytes = ws;
+  out->staging_slots = 0;
 }
 
 bool from_public(const ag_gemm_geometry* in, Geometry& g) {
@@ -266,6 +267,10 @@ struct ag_gemm_plan {
   bool skinny = false;
   int sk_grid = 0;
   int32_t* sk_ws = nullptr;      // piece sums, [n-tiles][sk_cmax][M][128] int32
+  // bounded staging of the fused path (window > 0): 256-row slots
+  int window = 0;
+  uint32_t* credits = nullptr;   // [window] tiles done reading each slot, monotonic
+  uint32_t credit_epoch = 0;     // pipelined runs since the last reset
   int64_t sk_tiles = 0;          // 128-column n-tiles
   int64_t sk_kq = 0;             // 4-k-block units per n-tile
   int64_t sk_cmax = 0;           // CTAs sharing an n-tile, at most
@@ -288,6 +293,7 @@ void free_plan(ag_gemm_plan* p) {
   cudaFree(p->b16);
   cudaFree(p->a16);
   cudaFree(p->sk_ws);
+  cudaFree(p->credits);
   if (p->done) cudaEventDestroy(p->done);
   delete p;
 }
@@ -417,6 +423,25 @@ int run_impl(ag_gemm_plan* p, const void* const* shard_ptrs, const void* B, int6
   const int mode = p->mode;
   const bool runs_gemm = mode != AG_GEMM_MODE_COPY_ONLY;
   const bool runs_copy = mode != AG_GEMM_MODE_COMPUTE_ONLY && g.S > 1;
+  if (p->window > 0) {
+    // a copy that runs ahead of the GEMM would need every remote row at once
+    if (mode == AG_GEMM_MODE_SEQUENTIAL)
+      return fail(AG_GEMM_ERR_UNSUPPORTED,
+                  "SEQUENTIAL mode needs the whole gather staged: use a plan without a staging "
+                  "window");
+    fp.window = p->window;
+    fp.credits = p->credits;
+    if (mode == AG_GEMM_MODE_PIPELINED) {
+      // after pipelined run e slot s holds e * uses(s) * NT credits: restart before overflow
+      const uint64_t per_run = static_cast<uint64_t>(agg::window_uses(g, p->window, 0)) * g.NT;
+      if ((static_cast<uint64_t>(p->credit_epoch) + 1) * per_run >= (1ull << 31)) {
+        e = cudaMemsetAsync(p->credits, 0, sizeof(uint32_t) * p->window, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "credit counter reset");
+        p->credit_epoch = 0;
+      }
+      fp.credit_epoch = ++p->credit_epoch;
+    }
+  }
   if (runs_copy && (p->debug_flags & AG_GEMM_DEBUG_POISON_STAGING)) {
     // fp16 0x7E7E is a NaN: a tile read before its chunk landed turns C into NaN.
     e = cudaMemsetAsync(p->staging, 0x7E, static_cast<size_t>(p->staging_bytes), stream);
@@ -577,9 +602,30 @@ int ag_gemm_item_at(const ag_gemm_geometry* geo, int local_rank, int64_t i, int6
 
 extern "C" {
 
-ag_gemm_plan* ag_gemm_plan_create(int n_shards, int64_t M, int64_t K, int64_t N, int dtype,
-                                  int64_t chunk_rows) {
+}  // extern "C"
+
+namespace {
+
+// staging_slots < 0: every remote row has its own place in the staging;
+// otherwise a bounded window of 256-row slots (0 = 2 swizzle groups).
+ag_gemm_plan* create_plan(int n_shards, int64_t M, int64_t K, int64_t N, int dtype,
+                          int64_t chunk_rows, int staging_slots) {
   if (check_problem(n_shards, M, K, N, dtype, chunk_rows) != AG_GEMM_OK) return nullptr;
+  const bool skinny = dtype == AG_GEMM_I8 && M <= agg::kSkMaxRows;
+  // the skinny path stages at most 127 x K bytes: it keeps the plain layout
+  const bool bounded = staging_slots >= 0 && !skinny && n_shards > 1;
+  if (staging_slots > 0 && staging_slots < agg::kGroupM) {
+    fail(AG_GEMM_ERR_INVALID,
+         "staging_slots must be 0 (default) or at least %d: the tiles of one swizzle group "
+         "read %d row blocks at once", agg::kGroupM, agg::kGroupM);
+    return nullptr;
+  }
+  if (bounded && chunk_rows > 0 && agg::kPairM % chunk_rows != 0) {
+    fail(AG_GEMM_ERR_INVALID, "bounded staging needs chunk_rows dividing %d (got %lld)",
+         agg::kPairM, (long long)chunk_rows);
+    return nullptr;
+  }
+  if (bounded && chunk_rows == 0) chunk_rows = agg::choose_chunk_rows_bounded(M / n_shards);
   ag_gemm_plan* p = new (std::nothrow) ag_gemm_plan();
   if (!p) {
     fail(AG_GEMM_ERR_OOM, "host allocation failed");
@@ -613,7 +659,14 @@ ag_gemm_plan* ag_gemm_plan_create(int n_shards, int64_t M, int64_t K, int64_t N,
   }
   p->grid = clusters * 2 < want ? clusters * 2 : want;
   const int64_t slots = g.S > 1 ? g.S - 1 : 1;
-  p->staging_bytes = slots * g.R * g.K * 2;
+  if (bounded) {
+    const int64_t blocks = static_cast<int64_t>(g.S - 1) * g.MT;
+    const int64_t w = staging_slots == 0 ? 2 * agg::kGroupM : staging_slots;
+    // a window as large as all remote row blocks is the plain layout
+    p->window = w < blocks ? static_cast<int>(w) : 0;
+  }
+  p->staging_bytes = p->window > 0 ? static_cast<int64_t>(p->window) * agg::kPairM * g.K * 2
+                                   : slots * g.R * g.K * 2;
   p->counter_count = slots * g.Q;
   if ((e = cudaMalloc(&p->staging, p->staging_bytes)) != cudaSuccess ||
       (e = cudaMalloc(&p->counters, sizeof(uint32_t) * p->counter_count)) != cudaSuccess ||
@@ -622,12 +675,15 @@ ag_gemm_plan* ag_gemm_plan_create(int n_shards, int64_t M, int64_t K, int64_t N,
       (e = cudaMalloc(&p->status, 2 * sizeof(uint32_t))) != cudaSuccess ||
       (e = cudaMemset(p->counters, 0, sizeof(uint32_t) * p->counter_count)) != cudaSuccess ||
       (e = cudaMemset(p->status, 0, 2 * sizeof(uint32_t))) != cudaSuccess ||
-      (e = cudaEventCreateWithFlags(&p->done, cudaEventDisableTiming)) != cudaSuccess) {
+      (e = cudaEventCreateWithFlags(&p->done, cudaEventDisableTiming)) != cudaSuccess ||
+      (p->window > 0 &&
+       ((e = cudaMalloc(&p->credits, sizeof(uint32_t) * p->window)) != cudaSuccess ||
+        (e = cudaMemset(p->credits, 0, sizeof(uint32_t) * p->window)) != cudaSuccess))) {
     cuda_fail(e, "plan allocation");
     free_plan(p);
     return nullptr;
   }
-  p->skinny = dtype == AG_GEMM_I8 && g.M <= agg::kSkMaxRows;
+  p->skinny = skinny;
   if (p->skinny) {
     p->sk_tiles = (g.N + 127) / 128;
     p->sk_grid = p->sm_count;
@@ -657,11 +713,36 @@ ag_gemm_plan* ag_gemm_plan_create(int n_shards, int64_t M, int64_t K, int64_t N,
       return nullptr;
     }
   }
-  if (encode_stage(&p->tm_stage, p->staging, slots, g.R, g.K) != AG_GEMM_OK) {
+  // staging map: [S-1][R][K], or the window's [W][256][K]
+  if ((p->window > 0 ? encode_stage(&p->tm_stage, p->staging, p->window, agg::kPairM, g.K)
+                     : encode_stage(&p->tm_stage, p->staging, slots, g.R, g.K)) != AG_GEMM_OK) {
     free_plan(p);
     return nullptr;
   }
   return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+ag_gemm_plan* ag_gemm_plan_create(int n_shards, int64_t M, int64_t K, int64_t N, int dtype,
+                                  int64_t chunk_rows) {
+  return create_plan(n_shards, M, K, N, dtype, chunk_rows, -1);
+}
+
+ag_gemm_plan* ag_gemm_plan_create_bounded(int n_shards, int64_t M, int64_t K, int64_t N,
+                                          int dtype, int64_t chunk_rows, int staging_slots) {
+  if (staging_slots < 0) {
+    fail(AG_GEMM_ERR_INVALID, "staging_slots must be >= 0 (got %d)", staging_slots);
+    return nullptr;
+  }
+  return create_plan(n_shards, M, K, N, dtype, chunk_rows, staging_slots);
+}
+
+int64_t ag_gemm_choose_chunk_rows_bounded(int64_t R) {
+  if (R < 1) return fail(AG_GEMM_ERR_INVALID, "R must be positive");
+  return agg::choose_chunk_rows_bounded(R);
 }
 
 void ag_gemm_plan_destroy(ag_gemm_plan* plan) {
@@ -673,6 +754,11 @@ void ag_gemm_plan_destroy(ag_gemm_plan* plan) {
 int ag_gemm_plan_geometry(const ag_gemm_plan* plan, ag_gemm_geometry* out) {
   if (!plan || !out) return fail(AG_GEMM_ERR_INVALID, "plan or out is NULL");
   to_public(plan->g, out);
+  if (plan->window > 0) {
+    out->workspace_bytes += plan->staging_bytes - out->staging_bytes + 4 * plan->window;
+    out->staging_bytes = plan->staging_bytes;
+    out->staging_slots = plan->window;
+  }
   return AG_GEMM_OK;
 }
 
@@ -751,8 +837,11 @@ int ag_gemm_plan_reset(ag_gemm_plan* plan, void* stream_v) {
   if ((e = cudaMemsetAsync(plan->counters, 0, sizeof(uint32_t) * plan->counter_count, stream)) != cudaSuccess ||
       (e = cudaMemsetAsync(plan->item_counter, 0, sizeof(unsigned long long), stream)) != cudaSuccess ||
       (e = cudaMemsetAsync(plan->status, 0, 2 * sizeof(uint32_t), stream)) != cudaSuccess ||
+      (plan->window > 0 && (e = cudaMemsetAsync(plan->credits, 0, sizeof(uint32_t) * plan->window,
+                                                stream)) != cudaSuccess) ||
       (e = cudaEventRecord(plan->done, stream)) != cudaSuccess)
     return cuda_fail(e, "plan reset");
+  plan->credit_epoch = 0;
   plan->epoch = 0;
   plan->item_base = 0;
   plan->last_stream = stream;

@@ -56,6 +56,19 @@ AGG_HD int64_t choose_chunk_rows(int64_t R) {
   return best;
 }
 
+// Chunk rule of a plan with bounded staging: a chunk must lie inside one
+// 256-row slot, so c divides 256 as well as R.  The unbounded rule's c when it
+// does; else the largest common divisor of R and 256 that keeps >= 64 chunks
+// per source; else 1.
+AGG_HD int64_t choose_chunk_rows_bounded(int64_t R) {
+  const int64_t c0 = choose_chunk_rows(R);
+  if (c0 < 1 || kPairM % c0 == 0) return c0;
+  int64_t best = 1;
+  for (int64_t c = 1; c <= kPairM && c <= R / 64; c *= 2)
+    if (R % c == 0) best = c;
+  return best;
+}
+
 AGG_HD void make_geometry(Geometry& g, int S, int64_t M, int64_t K, int64_t N,
                           int dtype, int64_t chunk_rows) {
   g.S = S; g.dtype = dtype; g.M = M; g.K = K; g.N = N;
@@ -108,6 +121,20 @@ AGG_HD void item_coords(const Geometry& g, int64_t i, int& pos, int64_t& q,
   int64_t vecs = g.c * g.K * g.src_esize / 16;
   v0 = vecs * piece / g.P;
   v1 = vecs * (piece + 1) / g.P;
+}
+
+// Bounded staging: row block b = (pos - 1) * MT + mt of the remote rows lives
+// in slot b % W; before its use u = b / W (u >= 1) the slot's credit counter
+// must reach base + u * NT, where base counts the credits of earlier runs:
+// (epoch - 1) * (uses of the slot per run) * NT.
+AGG_HD int64_t window_uses(const Geometry& g, int64_t W, int64_t slot) {
+  const int64_t nb = (int64_t)(g.S - 1) * g.MT;
+  return slot < nb ? (nb - slot + W - 1) / W : 0;
+}
+AGG_HD uint32_t window_target(const Geometry& g, int64_t W, int64_t b, uint32_t epoch) {
+  const int64_t slot = b % W, use = b / W;
+  return static_cast<uint32_t>((int64_t)(epoch - 1) * window_uses(g, W, slot) * g.NT +
+                               use * g.NT);
 }
 
 // Chunks [q0, q1] of a source that the 128 rows starting at row0 touch;

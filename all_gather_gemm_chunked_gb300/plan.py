@@ -39,12 +39,19 @@ class Plan:
     """One AllGather+GEMM problem: owns the library plan (staging, counters)."""
 
     def __init__(self, n_shards: int, M: int, K: int, N: int, dtype: str = "f16",
-                 chunk_rows: int = 0):
+                 chunk_rows: int = 0, staging_slots=None):
+        """staging_slots: None = every remote row staged (ag_gemm_plan_create);
+        an int = a bounded staging window of that many 256-row slots, 0 = the
+        default window (ag_gemm_plan_create_bounded)."""
         if dtype not in _DTYPES:
             raise ValueError("dtype must be 'f16', 'bf16' or 'i8'")
         self.n_shards, self.M, self.K, self.N, self.dtype = n_shards, M, K, N, dtype
         self.R = M // n_shards if n_shards else 0
-        self.handle = B_.ag_gemm_plan_create(n_shards, M, K, N, _DTYPES[dtype], chunk_rows)
+        if staging_slots is None:
+            self.handle = B_.ag_gemm_plan_create(n_shards, M, K, N, _DTYPES[dtype], chunk_rows)
+        else:
+            self.handle = B_.ag_gemm_plan_create_bounded(n_shards, M, K, N, _DTYPES[dtype],
+                                                         chunk_rows, int(staging_slots))
 
     # -- lifecycle
     def close(self):

@@ -21,6 +21,7 @@ buffers.  Seeds: ``0xA66E0000 + workload id``, then a fixed offset per tensor.
 from __future__ import annotations
 
 from dataclasses import dataclass
+from typing import Optional
 
 import numpy as np
 
@@ -42,6 +43,7 @@ class Workload:
     n_blocks: int = 1    # N-sharded layout: B and C have n_blocks * N columns and the
                          # problem is rank `rank`'s column block (ring order from `rank`)
     rank: int = 0
+    staging_slots: Optional[int] = None  # bounded staging window (256-row slots), None = plain
 
     @property
     def R(self) -> int:
@@ -57,7 +59,9 @@ class Workload:
 # 4096^3 fp16 case with bfloat16 operands; 7 is one rank of the N-sharded
 # collective matmul with the per-device shape of "Collective matrix
 # multiplication" (2 devices, 1024 rows per shard, K = 4096, 4096 columns of B
-# per device): rank 0's column block of B (K x 8192) and C.
+# per device): rank 0's column block of B (K x 8192) and C.  8 and 9 are
+# workloads 4 and 3 with the remote rows staged through a bounded window of 16
+# slots of 256 rows (two swizzle groups) instead of one place per remote row.
 WORKLOADS = {
     1: Workload(1, "f16 2x128 rows, K=256, N=128, chunk 16", 2, 256, 256, 128, "f16", 16),
     2: Workload(2, "f16 2x2048 rows, K=4096, N=4096", 2, 4096, 4096, 4096, "f16", 0),
@@ -67,6 +71,10 @@ WORKLOADS = {
     6: Workload(6, "bf16 2x2048 rows, K=4096, N=4096", 2, 4096, 4096, 4096, "bf16", 0),
     7: Workload(7, "f16 N-sharded rank 0 of 2: 2x1024 rows, K=4096, 4096 of 8192 columns",
                 2, 2048, 4096, 4096, "f16", 0, n_blocks=2, rank=0),
+    8: Workload(8, "i8 dequant 4x4096 rows, K=27392, N=4096, staging window 16 x 256 rows",
+                4, 16384, 27392, 4096, "i8", 0, staging_slots=16),
+    9: Workload(9, "f16 8x1024 rows, K=4096, N=4096, staging window 16 x 256 rows",
+                8, 8192, 4096, 4096, "f16", 0, staging_slots=16),
 }
 
 

@@ -76,6 +76,10 @@ typedef enum {
  *                   shards from an earlier run for C to be right).
  *   SEQUENTIAL   -- all chunk copies complete, then the GEMM runs.
  *   COPY_ONLY    -- chunk copies only; C is not written.
+ * A plan with a staging window (ag_gemm_plan_create_bounded) cannot run
+ * SEQUENTIAL (AG_GEMM_ERR_UNSUPPORTED): the copy would have to run ahead of
+ * the GEMM by the whole gather.  Its COMPUTE_ONLY runs read the window as it
+ * stands (timing only: earlier row blocks have been overwritten).
  */
 typedef enum {
     AG_GEMM_MODE_PIPELINED = 0,
@@ -118,6 +122,7 @@ typedef struct {
     int64_t producer_items;    /* (n_shards - 1) * Q * P */
     int64_t staging_bytes;     /* plan-owned staging workspace */
     int64_t workspace_bytes;   /* everything the plan allocates on the device */
+    int64_t staging_slots;     /* staging window in 256-row slots; 0 = one place per remote row */
 } ag_gemm_geometry;
 
 /*
@@ -178,6 +183,41 @@ int ag_gemm_item_at(const ag_gemm_geometry *g, int local_rank, int64_t i,
 ag_gemm_plan *ag_gemm_plan_create(int n_shards, int64_t M, int64_t K,
                                   int64_t N, int dtype, int64_t chunk_rows);
 
+/*
+ * Create a plan whose remote rows pass through a bounded staging window with
+ * back-pressure (the double-buffered workspace of "AllGather + GEMM 通算融合算子
+ * 示例" section 优化说明 and of "AllGather矩阵乘法反量化算子设计文档" 6.1: two
+ * workspace stages that the producer refills once the consumer is done).
+ *
+ * The remote rows, in consumption order, form row blocks of 256 rows (one
+ * m-tile of a shard; the last block of a shard may be shorter): block
+ * b = (p - 1) * m_tiles + mt for consumption position p >= 1.  Block b is
+ * staged in slot b % W of a [W][256][K] workspace.  Every tile that has read
+ * its rows adds one credit to the slot's counter; the producer writes block b
+ * only after the n_tiles tiles of block b - W have done so.  The tiles of a
+ * swizzle group (group_m = 8 m-tiles) read their blocks together, so W must
+ * be at least 8; staging_slots = 0 picks W = 16, two groups: one being read
+ * while the producer fills the other.  A window that covers every remote
+ * block is the plain layout (geometry.staging_slots = 0).  The staging then
+ * takes W * 256 * K * 2 bytes instead of (n_shards - 1) * R * K * 2.
+ *
+ * A chunk must not straddle a slot: chunk_rows must divide 256 (and R);
+ * chunk_rows = 0 picks ag_gemm_choose_chunk_rows_bounded(R).  int8 plans with
+ * M <= 128 (the skinny path, whose staging is at most 127 x K bytes) keep the
+ * plain layout.  Producer waits on a slot are bounded by the plan's timeout
+ * and end in the status kind 3 (credit timeout).
+ */
+ag_gemm_plan *ag_gemm_plan_create_bounded(int n_shards, int64_t M, int64_t K,
+                                          int64_t N, int dtype, int64_t chunk_rows,
+                                          int staging_slots);
+
+/*
+ * Chunk rule of a plan with a staging window: ag_gemm_choose_chunk_rows(R)
+ * when it divides 256; else the largest power of two dividing R and 256 with
+ * R / c >= 64; else 1.  Pure host function.
+ */
+int64_t ag_gemm_choose_chunk_rows_bounded(int64_t R);
+
 /* Wait for the plan's last run, then free everything the plan owns. NULL is a no-op. */
 void ag_gemm_plan_destroy(ag_gemm_plan *plan);
 
@@ -233,7 +273,8 @@ int ag_gemm_dequant_run(ag_gemm_plan *plan, const void *const *shard_ptrs,
  */
 int ag_gemm_plan_status(ag_gemm_plan *plan);
 
-/* Raw status word of the last run (0 = ok; low byte = kind; see the source). */
+/* Raw status word of the last run (0 = ok; low byte = kind: 1 a ready counter,
+ * 2 a pipeline barrier, 3 a staging-window slot ran out of time). */
 int64_t ag_gemm_plan_status_word(ag_gemm_plan *plan);
 
 /* Zero the ready counters and the status word on `stream`; the epoch restarts. */

@@ -83,7 +83,7 @@ def test_validate_accepts_workloads(B):
 def test_geometry_of_workloads(B):
     from all_gather_gemm_chunked_gb300.synth import WORKLOADS
     want = {1: (16, 8), 2: (32, 64), 3: (16, 64), 4: (64, 64), 5: (1, 32), 6: (32, 64),
-            7: (16, 64)}
+            7: (16, 64), 8: (64, 64), 9: (16, 64)}
     for wid, w in WORKLOADS.items():
         g = B.ag_gemm_geometry_of(w.S, w.M, w.K, w.N, _DT[w.dtype], w.chunk_rows)
         assert (g.chunk_rows, g.chunks_per_source) == want[wid]

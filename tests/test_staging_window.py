@@ -1,0 +1,86 @@
+"""Bounded staging window (back-pressure), host side, without a GPU.
+
+The plan stages the remote rows through W slots of 256 rows: row block b (an
+m-tile of a remote shard, in consumption order) lives in slot b % W, and the
+producer may write block b only once every tile of block b - W has read its
+rows.  These tests check the chunk rule such a plan uses, and -- by simulating
+the persistent schedule exactly as the kernel walks it (tile order from the
+library's own ag_gemm_tile_at, tiles dealt round-robin to the CTA pairs) --
+that a window of at least one swizzle group (group_m = 8 blocks) always
+finishes, while a smaller one can stall for good.
+"""
+import pytest
+
+from all_gather_gemm_chunked_gb300 import binding as B_
+
+
+def test_bounded_chunk_rule():
+    for R in list(range(1, 600)) + [1024, 2048, 3000, 4096, 4095, 6144, 10000]:
+        c = B_.ag_gemm_choose_chunk_rows_bounded(R)
+        assert R % c == 0 and 256 % c == 0, R
+        c0 = B_.ag_gemm_choose_chunk_rows(R)
+        if 256 % c0 == 0:
+            assert c == c0, R
+        else:
+            # the largest power of two dividing R with at least 64 chunks
+            best = max([d for d in (1, 2, 4, 8, 16, 32, 64, 128, 256)
+                        if R % d == 0 and R // d >= 64] or [1])
+            assert c == best, R
+    assert B_.ag_gemm_choose_chunk_rows_bounded(3000) == 8
+    assert B_.ag_gemm_choose_chunk_rows_bounded(4096) == 64
+
+
+def _simulate(g, local, W, pairs):
+    """True if every tile completes.  Producer: blocks in order, block b once
+    the NT tiles of block b - W have read their rows.  Consumers: pair p takes
+    tiles p, p + pairs, ... in order; a remote tile needs its block produced."""
+    S, MT, NT = g.n_shards, g.m_tiles, g.n_tiles
+    order = [B_.ag_gemm_tile_at(g, local, t) for t in range(g.tiles)]
+
+    def block(tile):
+        src, mt, _ = tile
+        pos = (src - local) % S
+        return None if pos == 0 else (pos - 1) * MT + mt
+
+    nblocks = (S - 1) * MT
+    produced, consumed = 0, [0] * nblocks
+    nxt = list(range(min(pairs, g.tiles)))  # next tile index per pair
+    done = 0
+    while True:
+        progress = False
+        while produced < nblocks and (produced < W or consumed[produced - W] == NT):
+            produced += 1
+            progress = True
+        for p in range(len(nxt)):
+            while nxt[p] < g.tiles:
+                b = block(order[nxt[p]])
+                if b is not None and b >= produced:
+                    break
+                if b is not None:
+                    consumed[b] += 1
+                nxt[p] += pairs
+                done += 1
+                progress = True
+        if done == g.tiles:
+            return True
+        if not progress:
+            return False
+
+
+@pytest.mark.parametrize("S,R,N", [(2, 4096, 4096), (4, 4096, 4096), (8, 1024, 4096),
+                                   (3, 600, 392), (5, 2560, 1024), (3, 8 * 256 + 7, 768)])
+def test_window_of_a_swizzle_group_always_finishes(S, R, N):
+    g = B_.ag_gemm_geometry_of(S, S * R, 256, N, 0, 0)
+    assert g.group_m == 8
+    for W in (8, 9, 16, 17):
+        for pairs in (1, 2, 7, 76):
+            for local in {0, S - 1}:
+                assert _simulate(g, local, W, pairs), (S, R, N, W, pairs, local)
+
+
+def test_window_below_a_swizzle_group_can_stall():
+    g = B_.ag_gemm_geometry_of(2, 2 * 8 * 256, 256, 512, 0, 0)  # 8 m-tiles, 2 n-tiles
+    assert g.m_tiles == 8 and g.n_tiles == 2
+    # one pair walks the group m-fastest: it needs block 4 before block 0 is done
+    assert not _simulate(g, 0, 4, 1)
+    assert _simulate(g, 0, 8, 1)
