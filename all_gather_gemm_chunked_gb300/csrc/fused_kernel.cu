@@ -316,10 +316,13 @@ __device__ void mma_warp(const FusedParams& p, const uint8_t* sA, const uint8_t*
   uint32_t phase = 0, unit = 0;
   bool ok = true;
   for (int64_t t = cluster; t < g.tiles && ok; t += n_clusters) {
-    int pos;
-    int64_t mt, nt;
-    tile_coords(g, t, pos, mt, nt);
-    const int64_t slot = credit && pos > 0 ? ((pos - 1) * g.MT + mt) % p.window : 0;
+    int64_t slot = -1;  // the window slot this remote tile reads (bounded staging)
+    if (credit) {
+      int pos;
+      int64_t mt, nt;
+      tile_coords(g, t, pos, mt, nt);
+      if (pos > 0) slot = ((pos - 1) * g.MT + mt) % p.window;
+    }
     for (int64_t seg = 0; seg < nseg && ok; ++seg) {
       const uint32_t buf = kI8 ? 0u : (unit & 1u);
       const uint32_t use = kI8 ? unit : (unit >> 1);
@@ -355,14 +358,16 @@ __device__ void mma_warp(const FusedParams& p, const uint8_t* sA, const uint8_t*
           stage = 0;
           phase ^= 1u;
         }
-        if (credit && pos > 0 && kb == g.KB - 1) {
-          // The last k-block of both CTAs' rows has landed (the pair's bytes
-          // are counted on this barrier): the staged rows are no longer read.
-          fence_proxy_async_global();
-          red_release_gpu_add(p.credits + slot, 1u);
-        }
       }
       if (!ok) break;
+      if (slot >= 0 && seg == nseg - 1) {
+        // The tile's last k-block of both CTAs' rows has landed (the pair's
+        // bytes are counted on the full barrier): the staged rows are no
+        // longer read.  (Kept out of the k-block loop: code there, even when
+        // not taken, slows the MMA issue.)
+        fence_proxy_async_global();
+        red_release_gpu_add(p.credits + slot, 1u);
+      }
       mma_commit_pair_both(&tfull[buf]);  // accumulator ready for both epilogues
       ++unit;
     }
