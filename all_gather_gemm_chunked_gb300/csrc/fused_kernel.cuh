@@ -75,16 +75,16 @@ constexpr int kCopyWarpsPerCta = 2;
 constexpr int kSkMaxRows = 128;   // the gathered rows are the MMA's N operand (N <= 128 here)
 
 struct SkinnyParams {
-  CUtensorMap tm_b8;        // int8 B (2D: N, K), box 128 x 256, 128-byte swizzle
-  CUtensorMap tm_a8_local;  // int8 local shard (2D: K, R), box 256 x R, unswizzled
-  CUtensorMap tm_a8_stage;  // int8 staging (3D: K, R, S - 1), box 256 x R x (S - 1)
+  CUtensorMap tm_b8;        // int8 B (2D: N, K), box 128 x 128, 128-byte swizzle
+  CUtensorMap tm_a8_local;  // int8 local shard (2D: K, R), box 128 x R, unswizzled
+  CUtensorMap tm_a8_stage;  // int8 staging (3D: K, R, S - 1), box 128 x R x (S - 1)
   Geometry g;
   const void* src[kMaxShards];  // shard pointers by consumption position
   int8_t* staging;              // int8 [S-1][R][K]
   uint32_t* counters;           // [(S-1)][Q] ready counters, monotonic
   unsigned long long* item_counter;
   unsigned long long item_base;
-  int32_t* ws;                  // [n_tiles][cmax][M][128] int32 piece sums
+  int32_t* ws;                  // [n_tiles][cmax][M][256] int32 piece sums
   uint32_t* status;
   const int32_t* bias;
   const float* scale;
@@ -97,8 +97,8 @@ struct SkinnyParams {
   uint64_t pipe_timeout_ns;
   int64_t debug_skip_item;
   uint32_t debug_delay_ns;
-  int64_t n_tiles;              // ceil(N / 128)
-  int64_t kq;                   // 4-k-block units per n-tile: ceil(KB / 4)
+  int64_t n_tiles;              // ceil(N / 256)
+  int64_t kq;                   // 2-k-block units per n-tile: ceil(KB / 2)
   int64_t cmax;                 // workspace slots per n-tile
 };
 constexpr int kSkCopyWarpsPerCta = 2;

@@ -79,27 +79,27 @@ int encode_f16(CUtensorMap* map, const void* base, int rank, const cuuint64_t* d
   return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, base, rank, dims, strides_bytes, box);
 }
 
-// int8 B (N, K) of the skinny path in 128 x 256 boxes (four k-blocks, 32 KB) with
-// 128-byte swizzle; rows past K read as zero.
+// int8 B (N, K) of the skinny path in 128 x 128 boxes (two k-blocks, 16 KB) with
+// 128-byte swizzle; rows past K and columns past N read as zero.
 int encode_b8(CUtensorMap* map, const void* base, int64_t K, int64_t N) {
   cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)K};
   cuuint64_t strides[1] = {(cuuint64_t)N};
-  cuuint32_t box[2] = {128, 4 * agg::kBlockK};
+  cuuint32_t box[2] = {128, 2 * agg::kBlockK};
   return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, 2, dims, strides, box);
 }
-// int8 gathered rows of the skinny path, 256 k at a time, unswizzled: a shard
-// (K, R) in 256 x R boxes, the staging (K, R, S - 1) in 256 x R x (S - 1) boxes.
+// int8 gathered rows of the skinny path, 128 k at a time, unswizzled: a shard
+// (K, R) in 128 x R boxes, the staging (K, R, S - 1) in 128 x R x (S - 1) boxes.
 int encode_a8(CUtensorMap* map, const void* base, int64_t R, int64_t K) {
   cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)R};
   cuuint64_t strides[1] = {(cuuint64_t)K};
-  cuuint32_t box[2] = {4 * agg::kBlockK, (cuuint32_t)R};
+  cuuint32_t box[2] = {2 * agg::kBlockK, (cuuint32_t)R};
   return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, 2, dims, strides, box,
                       CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 int encode_stage8(CUtensorMap* map, const void* base, int64_t slots, int64_t R, int64_t K) {
   cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)R, (cuuint64_t)slots};
   cuuint64_t strides[2] = {(cuuint64_t)K, (cuuint64_t)R * K};
-  cuuint32_t box[3] = {4 * agg::kBlockK, (cuuint32_t)R, (cuuint32_t)slots};
+  cuuint32_t box[3] = {2 * agg::kBlockK, (cuuint32_t)R, (cuuint32_t)slots};
   return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, 3, dims, strides, box,
                       CU_TENSOR_MAP_SWIZZLE_NONE);
 }
@@ -266,13 +266,13 @@ struct ag_gemm_plan {
   // int8 with at most 128 gathered rows: the skinny kernel
   bool skinny = false;
   int sk_grid = 0;
-  int32_t* sk_ws = nullptr;      // piece sums, [n-tiles][sk_cmax][M][128] int32
+  int32_t* sk_ws = nullptr;      // piece sums, [n-tiles][sk_cmax][M][256] int32
   // bounded staging of the fused path (window > 0): 256-row slots
   int window = 0;
   uint32_t* credits = nullptr;   // [window] tiles done reading each slot, monotonic
   uint32_t credit_epoch = 0;     // pipelined runs since the last reset
-  int64_t sk_tiles = 0;          // 128-column n-tiles
-  int64_t sk_kq = 0;             // 4-k-block units per n-tile
+  int64_t sk_tiles = 0;          // 256-column n-tiles
+  int64_t sk_kq = 0;             // 2-k-block units per n-tile
   int64_t sk_cmax = 0;           // CTAs sharing an n-tile, at most
   const void* cached_b8 = nullptr;
   CUtensorMap tm_b8_cached{};
@@ -685,12 +685,12 @@ ag_gemm_plan* create_plan(int n_shards, int64_t M, int64_t K, int64_t N, int dty
   }
   p->skinny = skinny;
   if (p->skinny) {
-    p->sk_tiles = (g.N + 127) / 128;
+    p->sk_tiles = (g.N + 255) / 256;
     p->sk_grid = p->sm_count;
-    p->sk_kq = (g.KB + 3) / 4;
+    p->sk_kq = (g.KB + 1) / 2;
     p->sk_cmax = agg::skinny_max_sharers(p->sk_tiles, p->sk_kq, p->sk_grid);
     if ((e = agg::skinny_prepare()) != cudaSuccess ||
-        (e = cudaMalloc(&p->sk_ws, static_cast<size_t>(p->sk_tiles * p->sk_cmax * g.M * 128 * 4))) !=
+        (e = cudaMalloc(&p->sk_ws, static_cast<size_t>(p->sk_tiles * p->sk_cmax * g.M * 256 * 4))) !=
             cudaSuccess) {
       cuda_fail(e, "plan allocation (skinny int8 path)");
       free_plan(p);

@@ -10,41 +10,42 @@
 // (1024 k), which keeps every fp32 partial an integer below 2^24; segments are
 // folded into an int32 sum in TMEM.
 //
-// The MMA computes the transposed tile, C^T (128 columns of C x M rows) =
-// B^T x A^T: the widened 128-column B tile is the M = 128 operand (MN-major),
-// the gathered rows are the N = round16(M) operand (K-major).  With few rows
-// this halves the tensor work of a 128 x 128 tile, leaves the A operand in
-// shared memory where any warp may write it, and puts one column of C on each
-// TMEM lane, so the epilogue stores whole 128-byte row segments.
+// The MMA computes the tile as it stands: the gathered rows are the M operand
+// (M = 64 for up to 64 rows, else 128; K-major), 256 columns of the widened B
+// are the N operand (MN-major).  On GB300 one tcgen05.mma of K = 16 occupies
+// the tensor pipe for ~200 cycles at any shape up to 128 x 256, so the count
+// of instructions, not their size, sets the rate: 64 x 256 per instruction is
+// twice the work of the transposed 128-column x 64-row tile.  The fp32
+// accumulator (256 TMEM columns) and the int32 running sums (256 more) fill
+// TMEM, so the accumulator is single-buffered: at the end of each segment the
+// MMA waits until the epilogue has folded it into the sums.
 //
-// B moves in 32 KB TMA boxes (128 columns x 256 k-rows, four k-blocks): a TMA
-// box carries a fixed cost of several hundred cycles, and on GB300 machines of
-// 8 KB cap a one-box-per-k-block stream near 2.6 TB/s while 32 KB boxes run at
-// the read bandwidth of HBM.  The same raw stage takes the unit's gathered rows
-// (M x 256 int8, two more boxes: the local shard and all staged shards), so A
-// arrives with B; loads issued thread by thread queued behind the B stream for
-// microseconds.  The rows land in consumption order (local shard first), which
-// the epilogue maps back to global rows.
+// B moves in 16 KB TMA boxes (128 columns x 128 k-rows, 128-byte swizzled),
+// two per unit (2 k-blocks of one 256-column n-tile); a TMA box carries a
+// fixed cost of several hundred cycles, which is why the boxes are not
+// smaller.  The same raw stage takes the unit's gathered rows (M x 128 int8,
+// two more boxes: the local shard and all staged shards), so A arrives with
+// B.  The rows land in consumption order (local shard first), which the
+// epilogue maps back to global rows.
 //
-// Work: the (128-column n-tile, 4-k-block unit) pairs, n-tile major, are cut
+// Work: the (256-column n-tile, 2-k-block unit) pairs, n-tile major, are cut
 // into one contiguous range per CTA (stream-K), so a CTA holds at most a few
-// pieces of n-tiles.  At the end of a piece its exact int32 sums (M rows x 128
-// columns) go to a workspace slot of their own (plain coalesced stores, no
-// atomics); ag_skinny_finish_kernel then adds the slots of each n-tile in a
-// fixed order, adds the bias and writes C_i32 and the fp16 dequant D.  The
-// workspace needs no clearing: every slot the finish kernel reads is written
-// by the same run.
+// pieces of n-tiles.  At the end of a piece its exact int32 sums (M rows x 256
+// columns) go to a workspace slot of their own (plain stores, no atomics);
+// ag_skinny_finish_kernel then adds the slots of each n-tile in a fixed order,
+// adds the bias and writes C_i32 and the fp16 dequant D.  The workspace needs
+// no clearing: every slot the finish kernel reads is written by the same run.
 //
 // Roles (20 warps).  The scheduler of warp w is w % 4; the MMA issue thread
 // shares scheduler 0 only with warps that mostly sleep, and the widening work
 // is spread over schedulers 1-3.  TMEM lane quadrant q is reachable only from
 // warps w with w % 4 == q, hence the epilogue warps 16, 1, 2, 3.
-//   warp 0                 MMA: one thread issues tcgen05.mma (M = 128,
-//                          N = round16(M), K = 16).
-//   warp 4                 TMA: streams the CTA's units (B box + row boxes)
-//                          into a raw ring; the B boxes of the first stages go
-//                          out before the warp waits once for every remote
-//                          chunk.
+//   warp 0                 MMA: one thread issues tcgen05.mma (M = 64 or 128,
+//                          N = 256, K = 16).
+//   warp 4                 TMA: streams the CTA's units (two B boxes + row
+//                          boxes) into a raw ring; the B boxes of the first
+//                          stages go out before the warp waits once for every
+//                          remote chunk.
 //   warps 8, 12            copy: remote chunks, in 1/8-piece parts, into the
 //                          int8 staging workspace; release their ready counters.
 //   warps 16, 1, 2, 3      epilogue: fold fp32 segments into the int32 sums in
@@ -66,21 +67,23 @@ namespace {
 
 constexpr int kSkWarps = 20;
 constexpr int kSkThreads = kSkWarps * 32;
-constexpr int kSkN = 128;              // n-tile (the MMA's M)
-constexpr int kSkUnitBlocks = 4;       // k-blocks per B box (256 k-rows)
-constexpr int kSkRaw = 2;              // raw stages (B box + rows)
-constexpr int kSkFpMax = 5;            // fp16 stages (B + A, one k-block each; 3 when M > 64)
+constexpr int kSkN = 256;              // n-tile (the MMA's N)
+constexpr int kSkHalf = 128;           // columns of one B box
+constexpr int kSkUnitBlocks = 2;       // k-blocks per unit (128 k-rows)
+constexpr int kSkRawMax = 3;           // raw stages (B boxes + rows), at most
+constexpr int kSkFpMax = 3;            // fp16 stages (B + A, one k-block each), at most
 constexpr int kSkBwThreads = 256;      // 8 B-widening warps
 constexpr int kSkAwThreads = 128;      // 4 A-widening warps
-constexpr int kSkRawB = kSkN * kBlockK * kSkUnitBlocks;      // 32 KB int8 B per raw stage
-constexpr int kSkARow = kBlockK * kSkUnitBlocks;             // 256 bytes of a row per unit
-constexpr int kSkFpStage = kSkN * kBlockK * 2;               // 16 KB fp16
-// M <= 64: fp16 5 x (16 + 8) KB, raw 2 x (32 + 16) KB = 216 KB;
-// M <= 128: fp16 3 x (16 + 16) KB, raw 2 x (32 + 32) KB = 224 KB.
-constexpr int kSkDataBytes = 224 * 1024;
+constexpr int kSkBoxB = kSkHalf * kBlockK * kSkUnitBlocks;   // 16 KB: one int8 B box
+constexpr int kSkRawB = 2 * kSkBoxB;                         // 32 KB int8 B per raw stage
+constexpr int kSkARow = kBlockK * kSkUnitBlocks;             // 128 bytes of a row per unit
+constexpr int kSkFpB = kSkN * kBlockK * 2;                   // 32 KB: one fp16 k-block of B
+// M <= 64: raw 2 x (32 + 8) KB, fp16 3 x (32 + 8) KB = 200 KB;
+// M <= 128: raw 2 x (32 + 16) KB, fp16 2 x (32 + 16) KB = 192 KB.
+constexpr int kSkDataBytes = 200 * 1024;
 constexpr int kSkSmem = kSkDataBytes + 1024 + 1024;
-constexpr uint32_t kSkDcol = 0;        // TMEM columns [0, 256): two fp32 accumulators
-constexpr uint32_t kSkScol = 256;      // [256, 384): int32 running sums
+constexpr uint32_t kSkDcol = 0;        // TMEM columns [0, 256): the fp32 accumulator
+constexpr uint32_t kSkScol = 256;      // [256, 512): int32 running sums
 
 enum SkRole { kRoleMma, kRoleTma, kRoleCopy, kRoleEpi, kRoleBw, kRoleAw };
 
@@ -107,6 +110,22 @@ struct Ring {
       s = 0;
       ph ^= 1u;
     }
+  }
+};
+
+// Shared-memory plan, from the row count: the MMA's M, the A stage, the depth
+// of both rings.
+struct SkLayout {
+  int mm;         // rows of the MMA (64 or 128)
+  int a_stage;    // bytes of one fp16 A stage (mm rows x 128 bytes)
+  int n_raw, n_fp;
+  int raw_stage;  // two B boxes, then mm rows x 128 bytes
+  __device__ __forceinline__ explicit SkLayout(int64_t M) {
+    mm = M <= 64 ? 64 : 128;
+    a_stage = mm * 128;
+    n_raw = 2;
+    n_fp = mm == 64 ? 3 : 2;
+    raw_stage = kSkRawB + mm * kSkARow;
   }
 };
 
@@ -211,8 +230,15 @@ __device__ bool sk_wait_all_chunks(const SkinnyParams& p, int lane, volatile int
 }
 
 // ------------------------------------------------------------------ TMA warp
-// Rows of unit u into the raw stage at `a`: the local shard, then every
-// staged shard (consumption order).
+// Unit u (n-tile nt, unit q within it) into the raw stage at `st`: the two
+// B boxes, then the rows (the local shard, then every staged shard:
+// consumption order).
+__device__ __forceinline__ void sk_issue_b(const SkinnyParams& p, uint8_t* st, uint64_t* bar,
+                                           int64_t nt, int64_t q) {
+  const int32_t y = static_cast<int32_t>(q * kSkARow);
+  tma_load_2d(st, &p.tm_b8, bar, static_cast<int32_t>(nt * kSkN), y);
+  tma_load_2d(st + kSkBoxB, &p.tm_b8, bar, static_cast<int32_t>(nt * kSkN + kSkHalf), y);
+}
 __device__ __forceinline__ void sk_issue_rows(const SkinnyParams& p, uint8_t* a, uint64_t* bar,
                                               int64_t q) {
   const int32_t x = static_cast<int32_t>(q * kSkARow);
@@ -220,7 +246,7 @@ __device__ __forceinline__ void sk_issue_rows(const SkinnyParams& p, uint8_t* a,
   if (p.g.S > 1) tma_load_3d(a + p.g.R * kSkARow, &p.tm_a8_stage, bar, x, 0, 0);
 }
 
-__device__ void sk_tma_warp(const SkinnyParams& p, uint8_t* sRaw, int n_raw, int raw_stage,
+__device__ void sk_tma_warp(const SkinnyParams& p, uint8_t* sRaw, const SkLayout& L,
                             uint64_t* raw_full, uint64_t* raw_empty, int lane,
                             volatile int* abort) {
   const Geometry& g = p.g;
@@ -229,7 +255,7 @@ __device__ void sk_tma_warp(const SkinnyParams& p, uint8_t* sRaw, int n_raw, int
   int64_t u0, u1;
   skinny_cta_range(p.n_tiles * KQ, blockIdx.x, gridDim.x, u0, u1);
   const int64_t n = u1 - u0;
-  const int head = static_cast<int>(n < n_raw ? n : n_raw);
+  const int head = static_cast<int>(n < L.n_raw ? n : L.n_raw);
   const uint32_t tx = static_cast<uint32_t>(kSkRawB + g.M * kSkARow);
   if (lane == 0) {
     tma_prefetch_desc(&p.tm_b8);
@@ -237,10 +263,9 @@ __device__ void sk_tma_warp(const SkinnyParams& p, uint8_t* sRaw, int n_raw, int
     if (g.S > 1) tma_prefetch_desc(&p.tm_a8_stage);
     // B of the first stages before the remote rows are known to have landed
     for (int i = 0; i < head; ++i) {
-      const int64_t u = u0 + i, nt = u / KQ, q = u - nt * KQ;
+      const int64_t u = u0 + i, nt = u / KQ;
       mbar_arrive_expect_tx(&raw_full[i], tx);
-      tma_load_2d(sRaw + i * raw_stage, &p.tm_b8, &raw_full[i], static_cast<int32_t>(nt * kSkN),
-                  static_cast<int32_t>(q * kSkARow));
+      sk_issue_b(p, sRaw + i * L.raw_stage, &raw_full[i], nt, u - nt * KQ);
     }
   }
   __syncwarp();
@@ -255,8 +280,8 @@ __device__ void sk_tma_warp(const SkinnyParams& p, uint8_t* sRaw, int n_raw, int
   uint32_t issued = (1u << head) - 1u, issued_phase = 0;
   if (ok)
     for (int i = 0; i < head; ++i)
-      sk_issue_rows(p, sRaw + i * raw_stage + kSkRawB, &raw_full[i], (u0 + i) % KQ);
-  Ring r(n_raw);
+      sk_issue_rows(p, sRaw + i * L.raw_stage + kSkRawB, &raw_full[i], (u0 + i) % KQ);
+  Ring r(L.n_raw);
   for (int i = 0; i < head; ++i) r.next();
   for (int64_t u = u0 + head; u < u1 && ok; ++u, r.next()) {
     if (!mbar_wait(&raw_empty[r.s], r.ph ^ 1u, p.pipe_timeout_ns, abort, gstatus)) {
@@ -264,10 +289,9 @@ __device__ void sk_tma_warp(const SkinnyParams& p, uint8_t* sRaw, int n_raw, int
       break;
     }
     const int64_t nt = u / KQ, q = u - nt * KQ;
-    uint8_t* st = sRaw + r.s * raw_stage;
+    uint8_t* st = sRaw + r.s * L.raw_stage;
     mbar_arrive_expect_tx(&raw_full[r.s], tx);
-    tma_load_2d(st, &p.tm_b8, &raw_full[r.s], static_cast<int32_t>(nt * kSkN),
-                static_cast<int32_t>(q * kSkARow));
+    sk_issue_b(p, st, &raw_full[r.s], nt, q);
     sk_issue_rows(p, st + kSkRawB, &raw_full[r.s], q);
     issued |= 1u << r.s;
     issued_phase = (issued_phase & ~(1u << r.s)) | (r.ph << r.s);
@@ -279,30 +303,30 @@ __device__ void sk_tma_warp(const SkinnyParams& p, uint8_t* sRaw, int n_raw, int
     // were never issued cannot complete; their B boxes land well within the
     // bounded waits below.
     volatile int never = 0;
-    for (int s = 0; s < n_raw; ++s)
+    for (int s = 0; s < L.n_raw; ++s)
       if (issued & (1u << s))
         mbar_wait(&raw_full[s], (issued_phase >> s) & 1u, 20000000ull, &never);
   }
 }
 
 // ------------------------------------------------------------------ B widening (8 warps)
-// Thread t widens 32 bytes of one k-row: columns qt * 32 .. +31 (half of one
+// Per k-block and box half h (columns 128h .. 128h + 127), thread t widens 32
+// bytes of one k-row: columns qt * 32 .. +31 of the half (half of one
 // 64-column swizzle group of the MN-major fp16 tile) of k-row krow.  The 8
 // lanes of a shared-memory phase take 8 consecutive k-rows of one quarter qt,
 // so both the swizzled raw reads and the swizzled fp16 writes hit 8 distinct
 // 16-byte bank groups.
-__device__ void sk_bwiden(const SkinnyParams& p, const uint8_t* sRaw, int n_raw, int raw_stage,
-                          int n_fp, uint8_t* sFp,
-                          uint64_t* raw_full, uint64_t* raw_empty, uint64_t* fp_full,
-                          uint64_t* fp_empty, int t, volatile int* abort) {
+__device__ void sk_bwiden(const SkinnyParams& p, const uint8_t* sRaw, const SkLayout& L,
+                          uint8_t* sFp, uint64_t* raw_full, uint64_t* raw_empty,
+                          uint64_t* fp_full, uint64_t* fp_empty, int t, volatile int* abort) {
   const Geometry& g = p.g;
   const volatile uint32_t* gstatus = p.status;
   const int lane = t & 31, krow = 8 * (t >> 5) + (t & 7), qt = (t >> 3) & 3;
-  const int grp = qt >> 1, cb = (qt & 1) * 4;  // fp16 64-column group, first 16-byte chunk
+  const int cb = (qt & 1) * 4;  // first 16-byte chunk within the 64-column group
   const int64_t KQ = p.kq;
   int64_t u0, u1;
   skinny_cta_range(p.n_tiles * KQ, blockIdx.x, gridDim.x, u0, u1);
-  Ring rr(n_raw), fr(n_fp);
+  Ring rr(L.n_raw), fr(L.n_fp);
   for (int64_t u = u0; u < u1; ++u, rr.next()) {
     if (!mbar_wait(&raw_full[rr.s], rr.ph, p.pipe_timeout_ns, abort, gstatus)) {
       if (lane == 0) {
@@ -313,7 +337,7 @@ __device__ void sk_bwiden(const SkinnyParams& p, const uint8_t* sRaw, int n_raw,
     }
     int64_t kb0, kb1;
     unit_blocks(g, KQ, u, kb0, kb1);
-    const uint8_t* raw = sRaw + rr.s * raw_stage;
+    const uint8_t* raw = sRaw + rr.s * L.raw_stage;
     for (int b = 0; b < static_cast<int>(kb1 - kb0); ++b, fr.next()) {
       if (!mbar_wait(&fp_empty[fr.s], fr.ph ^ 1u, p.pipe_timeout_ns, abort, gstatus)) {
         if (lane == 0) {
@@ -324,17 +348,25 @@ __device__ void sk_bwiden(const SkinnyParams& p, const uint8_t* sRaw, int n_raw,
       }
       // raw B arrives 128-byte swizzled: 16-byte chunk c of box row r sits at c ^ (r % 8)
       const int r = b * kBlockK + krow;
-      const uint8_t* src = raw + r * kSkN;
-      const uint4 v0 = *reinterpret_cast<const uint4*>(src + (((2 * qt) ^ (r & 7)) * 16));
-      const uint4 v1 = *reinterpret_cast<const uint4*>(src + (((2 * qt + 1) ^ (r & 7)) * 16));
-      uint8_t* dst = sFp + fr.s * kSkFpStage + grp * (64 * kBlockK * 2) + krow * 128;
-      uint4 a, c;
-      widen16x(v0, a, c);
-      *reinterpret_cast<uint4*>(dst + (((cb + 0) ^ (krow & 7)) * 16)) = a;
-      *reinterpret_cast<uint4*>(dst + (((cb + 1) ^ (krow & 7)) * 16)) = c;
-      widen16x(v1, a, c);
-      *reinterpret_cast<uint4*>(dst + (((cb + 2) ^ (krow & 7)) * 16)) = a;
-      *reinterpret_cast<uint4*>(dst + (((cb + 3) ^ (krow & 7)) * 16)) = c;
+      uint4 v[4];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint8_t* src = raw + h * kSkBoxB + r * kSkHalf;
+        v[2 * h] = *reinterpret_cast<const uint4*>(src + (((2 * qt) ^ (r & 7)) * 16));
+        v[2 * h + 1] = *reinterpret_cast<const uint4*>(src + (((2 * qt + 1) ^ (r & 7)) * 16));
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        // 64-column group 2h + qt / 2 of the fp16 k-block
+        uint8_t* dst = sFp + fr.s * kSkFpB + (2 * h + (qt >> 1)) * (64 * kBlockK * 2) + krow * 128;
+        uint4 a, c;
+        widen16x(v[2 * h], a, c);
+        *reinterpret_cast<uint4*>(dst + (((cb + 0) ^ (krow & 7)) * 16)) = a;
+        *reinterpret_cast<uint4*>(dst + (((cb + 1) ^ (krow & 7)) * 16)) = c;
+        widen16x(v[2 * h + 1], a, c);
+        *reinterpret_cast<uint4*>(dst + (((cb + 2) ^ (krow & 7)) * 16)) = a;
+        *reinterpret_cast<uint4*>(dst + (((cb + 3) ^ (krow & 7)) * 16)) = c;
+      }
       fence_proxy_async_shared();
       __syncwarp();
       if (lane == 0) mbar_arrive(&fp_full[fr.s]);
@@ -347,12 +379,12 @@ __device__ void sk_bwiden(const SkinnyParams& p, const uint8_t* sRaw, int n_raw,
 // ------------------------------------------------------------------ A widening (4 warps)
 // Thread t widens the 16 k at k-offset (t % 4) * 16 of rows t / 4 + 32 e,
 // e < NE (NE = 2 for M <= 64, 4 for M <= 128), from the raw stage's rows
-// (256 bytes each, consumption order) into fp16 A stages: K-major, 128-byte
-// rows, 16-byte chunk c of row j at c ^ (j % 8).
+// (128 bytes each, consumption order) into fp16 A stages: K-major, 128-byte
+// rows, 16-byte chunk c of row j at c ^ (j % 8).  Rows M .. mm - 1 are left
+// as they are: they only reach rows of the accumulator nobody reads.
 template <int NE>
-__device__ void sk_awiden(const SkinnyParams& p, const uint8_t* sRaw, int n_raw, int raw_stage,
-                          int n_fp,
-                          uint8_t* sA, int a_stage, uint64_t* raw_full, uint64_t* raw_empty,
+__device__ void sk_awiden(const SkinnyParams& p, const uint8_t* sRaw, const SkLayout& L,
+                          uint8_t* sA, uint64_t* raw_full, uint64_t* raw_empty,
                           uint64_t* a_full, uint64_t* a_empty, int t, volatile int* abort) {
   const Geometry& g = p.g;
   const volatile uint32_t* gstatus = p.status;
@@ -360,7 +392,7 @@ __device__ void sk_awiden(const SkinnyParams& p, const uint8_t* sRaw, int n_raw,
   const int64_t KQ = p.kq;
   int64_t u0, u1;
   skinny_cta_range(p.n_tiles * KQ, blockIdx.x, gridDim.x, u0, u1);
-  Ring rr(n_raw), ar(n_fp);
+  Ring rr(L.n_raw), ar(L.n_fp);
   for (int64_t u = u0; u < u1; ++u, rr.next()) {
     if (!mbar_wait(&raw_full[rr.s], rr.ph, p.pipe_timeout_ns, abort, gstatus)) {
       if (lane == 0) {
@@ -371,7 +403,7 @@ __device__ void sk_awiden(const SkinnyParams& p, const uint8_t* sRaw, int n_raw,
     }
     int64_t kb0, kb1;
     unit_blocks(g, KQ, u, kb0, kb1);
-    const uint8_t* raw = sRaw + rr.s * raw_stage + kSkRawB;
+    const uint8_t* raw = sRaw + rr.s * L.raw_stage + kSkRawB;
     for (int b = 0; b < static_cast<int>(kb1 - kb0); ++b, ar.next()) {
       if (!mbar_wait(&a_empty[ar.s], ar.ph ^ 1u, p.pipe_timeout_ns, abort, gstatus)) {
         if (lane == 0) {
@@ -388,7 +420,7 @@ __device__ void sk_awiden(const SkinnyParams& p, const uint8_t* sRaw, int n_raw,
               *reinterpret_cast<const uint4*>(raw + j * kSkARow + b * kBlockK + h * 16);
           uint4 lo, hi;
           widen16x(v, lo, hi);
-          uint8_t* dst = sA + ar.s * a_stage + j * 128;
+          uint8_t* dst = sA + ar.s * L.a_stage + j * 128;
           *reinterpret_cast<uint4*>(dst + (((2 * h) ^ (j & 7)) * 16)) = lo;
           *reinterpret_cast<uint4*>(dst + (((2 * h + 1) ^ (j & 7)) * 16)) = hi;
         }
@@ -404,56 +436,58 @@ __device__ void sk_awiden(const SkinnyParams& p, const uint8_t* sRaw, int n_raw,
 
 // ------------------------------------------------------------------ MMA warp
 // Pieces: maximal runs of this CTA's units inside one n-tile; segments: at most
-// kSegBlocks k-blocks of a piece, each accumulated into one fp32 buffer.
-__device__ void sk_mma(const SkinnyParams& p, const uint8_t* sFp, const uint8_t* sA, int a_stage,
-                       int n_fp,
-                       uint64_t* st_full, uint64_t* st_empty,
+// kSegBlocks k-blocks of a piece, accumulated into the fp32 accumulator, which
+// the epilogue folds into the int32 sums before the next segment starts.
+__device__ void sk_mma(const SkinnyParams& p, const uint8_t* sFp, const uint8_t* sA,
+                       const SkLayout& L, uint64_t* st_full, uint64_t* st_empty,
                        uint64_t* dfull, uint64_t* dempty, uint32_t tmem, volatile int* abort) {
   const Geometry& g = p.g;
   const volatile uint32_t* gstatus = p.status;
-  const int np = static_cast<int>((g.M + 15) / 16) * 16;  // rows padded to the MMA's N step
-  // D^T fp32; A operand = B^T tile (MN-major), B operand = gathered rows (K-major)
-  const uint32_t idesc = idesc_f16_f32(kSkN, np, /*a_mn=*/true, /*b_mn=*/false);
+  // D fp32 (mm rows x 256 columns); A operand = gathered rows (K-major),
+  // B operand = the widened B tile (MN-major)
+  const uint32_t idesc = idesc_f16_f32(L.mm, kSkN, /*a_mn=*/false, /*b_mn=*/true);
   // Descriptors of stage 0, k-step 0; the start address sits in the low bits
   // (16-byte units), so other stages and k-steps are plain additions.
-  const uint64_t ad0 = smem_desc_sw128(smem_u32(sFp), 64 * kBlockK * 2, 1024);
-  const uint64_t bd0 = smem_desc_sw128(smem_u32(sA), 16, 1024);
+  // Rows: 8-row groups 1 KB apart.  B: 64-column groups 8 KB apart (LBO),
+  // 8-k-row groups 1 KB apart (SBO).
+  const uint64_t ad0 = smem_desc_sw128(smem_u32(sA), 16, 1024);
+  const uint64_t bd0 = smem_desc_sw128(smem_u32(sFp), 64 * kBlockK * 2, 1024);
   const int64_t KQ = p.kq;
   int64_t u0, u1;
   skinny_cta_range(p.n_tiles * KQ, blockIdx.x, gridDim.x, u0, u1);
-  Ring kr(n_fp);
-  uint32_t seg = 0;  // segment sequence index (accumulator buffer = seg & 1)
+  Ring kr(L.n_fp);
+  uint32_t seg = 0;  // segment sequence index
   bool ok = true;
   for (int64_t u = u0; u < u1 && ok;) {
     int64_t nt, ue, kb0, kb1;
     piece_at(g, KQ, u, u1, nt, ue, kb0, kb1);
     for (int64_t s0 = kb0; s0 < kb1 && ok; s0 += kSegBlocks, ++seg) {
       const int n = static_cast<int>((s0 + kSegBlocks < kb1 ? s0 + kSegBlocks : kb1) - s0);
-      const uint32_t buf = seg & 1u, use = seg >> 1;
-      if (!mbar_wait(&dempty[buf], (use & 1u) ^ 1u, p.pipe_timeout_ns, abort, gstatus)) {
+      // the epilogue has read the previous segment's accumulator
+      if (!mbar_wait(dempty, (seg & 1u) ^ 1u, p.pipe_timeout_ns, abort, gstatus)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t d = tmem + kSkDcol + buf * 128;
+      const uint32_t d = tmem + kSkDcol;
       for (int b = 0; b < n; ++b, kr.next()) {
         if (!mbar_wait(&st_full[kr.s], kr.ph, p.pipe_timeout_ns, abort, gstatus)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint64_t ad = ad0 + static_cast<uint64_t>((kr.s * kSkFpStage) >> 4);
-        const uint64_t bd = bd0 + static_cast<uint64_t>((kr.s * a_stage) >> 4);
+        const uint64_t ad = ad0 + static_cast<uint64_t>((kr.s * L.a_stage) >> 4);
+        const uint64_t bd = bd0 + static_cast<uint64_t>((kr.s * kSkFpB) >> 4);
 #pragma unroll
         for (int k = 0; k < kBlockK / kUmmaK; ++k)
-          // B^T: +16 k-rows = two 8-row groups (2048 bytes); rows: +16 k = 32 bytes
-          mma_f16(d, ad + static_cast<uint64_t>((k * kUmmaK * 128) >> 4),
-                  bd + static_cast<uint64_t>((k * kUmmaK * 2) >> 4), idesc,
+          // rows: +16 k = 32 bytes; B: +16 k-rows = two 8-row groups (2048 bytes)
+          mma_f16(d, ad + static_cast<uint64_t>((k * kUmmaK * 2) >> 4),
+                  bd + static_cast<uint64_t>((k * kUmmaK * 128) >> 4), idesc,
                   (b > 0 || k > 0) ? 1u : 0u);
         mma_commit(&st_empty[kr.s]);
       }
       if (!ok) break;
-      mma_commit(&dfull[buf]);
+      mma_commit(dfull);
     }
     u = ue;
   }
@@ -464,14 +498,26 @@ __device__ void sk_mma(const SkinnyParams& p, const uint8_t* sFp, const uint8_t*
 }
 
 // ------------------------------------------------------------------ epilogue (4 warps)
-// TMEM lane = column of the n-tile, TMEM column = row of C.
-__device__ void sk_epilogue(const SkinnyParams& p, uint64_t* dfull, uint64_t* dempty,
-                            uint32_t tmem, int quad, int lane, volatile int* abort) {
+// TMEM lane = row of the tile, TMEM column = column of the n-tile.  With
+// mm = 128, gathered row j sits on lane j; with mm = 64, rows 16q .. 16q + 15
+// sit on lanes 32q .. 32q + 15 of quadrant q (lanes 32q + 16 .. 32q + 31 are
+// not written by the MMA and their values are never stored).  The kernel runs
+// this one for mm = 128 and sk_epilogue64 below for mm = 64.
+__device__ void sk_epilogue(const SkinnyParams& p, const SkLayout& L, uint64_t* dfull,
+                            uint64_t* dempty, uint32_t tmem, int quad, int lane,
+                            volatile int* abort) {
   const Geometry& g = p.g;
   const volatile uint32_t* gstatus = p.status;
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-  const int nl = quad * 32 + lane;  // column within the n-tile
-  const int chunks = static_cast<int>((g.M + 31) / 32);
+  // gathered row of this thread (consumption order), -1 for none
+  const int jr = L.mm == 128 ? quad * 32 + lane : (lane < 16 ? quad * 16 + lane : -1);
+  const bool row_ok = jr >= 0 && jr < g.M;
+  // its C row: row r of the shard at position jr / R, s = (local + position) % S
+  int64_t crow = 0;
+  if (row_ok) {
+    const int R = static_cast<int>(g.R), pos = jr / R;
+    crow = static_cast<int64_t>((p.local + pos) % g.S) * R + (jr - pos * R);
+  }
   const int64_t KQ = p.kq, U = p.n_tiles * KQ;
   int64_t u0, u1;
   skinny_cta_range(U, blockIdx.x, gridDim.x, u0, u1);
@@ -480,12 +526,10 @@ __device__ void sk_epilogue(const SkinnyParams& p, uint64_t* dfull, uint64_t* de
     int64_t nt, ue, kb0, kb1;
     piece_at(g, KQ, u, u1, nt, ue, kb0, kb1);
     const int64_t slot = nt * p.cmax + (blockIdx.x - skinny_owner(nt * KQ, U, gridDim.x));
-    const bool col_ok = nt * kSkN + nl < g.N;
-    int32_t* out = p.ws + slot * g.M * kSkN + nl;
+    int4* out = reinterpret_cast<int4*>(p.ws + (slot * g.M + crow) * kSkN);
     for (int64_t s0 = kb0; s0 < kb1; s0 += kSegBlocks, ++seg) {
       const bool first = s0 == kb0, last = s0 + kSegBlocks >= kb1;
-      const uint32_t buf = seg & 1u, use = seg >> 1;
-      const bool mine = mbar_wait(&dfull[buf], use & 1u, p.pipe_timeout_ns, abort, gstatus);
+      const bool mine = mbar_wait(dfull, seg & 1u, p.pipe_timeout_ns, abort, gstatus);
       // the four epilogue warps decide together
       uint32_t all_ok;
       asm volatile(
@@ -502,16 +546,16 @@ __device__ void sk_epilogue(const SkinnyParams& p, uint64_t* dfull, uint64_t* de
         return;
       }
       tc_fence_after();
-      for (int j = 0; j < chunks; ++j) {
+      for (int j = 0; j < kSkN / 32; ++j) {
         uint32_t f[32], s[32];
-        tmem_ld32(lane_base + kSkDcol + buf * 128 + j * 32, f);
+        tmem_ld32(lane_base + kSkDcol + j * 32, f);
         if (!first) tmem_ld32(lane_base + kSkScol + j * 32, s);
         tmem_ld_wait();
-        if (j == chunks - 1) {
-          // the fp32 buffer has been read: the MMA may reuse it
+        if (j == kSkN / 32 - 1) {
+          // the accumulator has been read: the MMA may start the next segment
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&dempty[buf]);
+          if (lane == 0) mbar_arrive(dempty);
         }
         uint32_t acc[32];
 #pragma unroll
@@ -522,23 +566,97 @@ __device__ void sk_epilogue(const SkinnyParams& p, uint64_t* dfull, uint64_t* de
           tmem_st32(lane_base + kSkScol + j * 32, acc);
           continue;
         }
-        // TMEM column jj holds gathered row jj in consumption order: row r of
-        // the shard at position jj / R, i.e. C row s * R + r with
-        // s = (local + position) % S.  32 lanes store 128 consecutive bytes.
-        if (col_ok) {
-          const int R = static_cast<int>(g.R);
-          int pos = (j * 32) / R;
-          int r = j * 32 - pos * R;
-          int s = (p.local + pos) % g.S;
+        // columns 32j .. 32j + 31 of the thread's row: 128 contiguous bytes
+        if (row_ok) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            if (j * 32 + e < g.M)
-              out[(static_cast<int64_t>(s) * R + r) * kSkN] = static_cast<int32_t>(acc[e]);
-            if (++r == R) {
-              r = 0;
-              s = s + 1 == g.S ? 0 : s + 1;
-            }
-          }
+          for (int e = 0; e < 8; ++e)
+            out[j * 8 + e] = make_int4(static_cast<int32_t>(acc[4 * e]),
+                                       static_cast<int32_t>(acc[4 * e + 1]),
+                                       static_cast<int32_t>(acc[4 * e + 2]),
+                                       static_cast<int32_t>(acc[4 * e + 3]));
+        }
+      }
+      if (!last) tmem_st_wait();
+    }
+    u = ue;
+  }
+}
+
+// The epilogue for mm = 64: the accumulator fills lanes 32q .. 32q + 15 of
+// each quadrant, which the 16x256b shape reads without the 16 idle lanes:
+// thread t holds rows 16q + t / 4 and 16q + t / 4 + 8, columns 8i + 2(t % 4)
+// and +1 of each 8-column block i of a 64-column chunk.
+__device__ void sk_epilogue64(const SkinnyParams& p, uint64_t* dfull, uint64_t* dempty,
+                              uint32_t tmem, int quad, int lane, volatile int* abort) {
+  const Geometry& g = p.g;
+  const volatile uint32_t* gstatus = p.status;
+  const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+  const int R = static_cast<int>(g.R);
+  // C row of gathered row j (consumption order): row j % R of the shard at
+  // position j / R, i.e. shard (local + position) % S
+  auto c_row = [&](int j) -> int64_t {
+    const int pos = j / R;
+    return static_cast<int64_t>((p.local + pos) % g.S) * R + (j - pos * R);
+  };
+  const int ja = quad * 16 + (lane >> 2), jb = ja + 8;
+  const bool oka = ja < g.M, okb = jb < g.M;
+  const int64_t cra = oka ? c_row(ja) : 0, crb = okb ? c_row(jb) : 0;
+  const int cp = 2 * (lane & 3);
+  const int64_t KQ = p.kq, U = p.n_tiles * KQ;
+  int64_t u0, u1;
+  skinny_cta_range(U, blockIdx.x, gridDim.x, u0, u1);
+  uint32_t seg = 0;
+  for (int64_t u = u0; u < u1;) {
+    int64_t nt, ue, kb0, kb1;
+    piece_at(g, KQ, u, u1, nt, ue, kb0, kb1);
+    const int64_t slot = nt * p.cmax + (blockIdx.x - skinny_owner(nt * KQ, U, gridDim.x));
+    int32_t* out_a = p.ws + (slot * g.M + cra) * kSkN + cp;
+    int32_t* out_b = p.ws + (slot * g.M + crb) * kSkN + cp;
+    for (int64_t s0 = kb0; s0 < kb1; s0 += kSegBlocks, ++seg) {
+      const bool first = s0 == kb0, last = s0 + kSegBlocks >= kb1;
+      const bool mine = mbar_wait(dfull, seg & 1u, p.pipe_timeout_ns, abort, gstatus);
+      uint32_t all_ok;
+      asm volatile(
+          "{\n\t.reg .pred q, r;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+          "bar.red.and.pred r, 1, 128, q;\n\tselp.u32 %0, 1, 0, r;\n\t}"
+          : "=r"(all_ok)
+          : "r"(mine ? 1u : 0u)
+          : "memory");
+      if (!all_ok) {
+        if (lane == 0) {
+          sk_set_status(p.status, kStatusPipelineTimeout, 0x1500u);
+          *abort = 1;
+        }
+        return;
+      }
+      tc_fence_after();
+      for (int j = 0; j < kSkN / 64; ++j) {
+        uint32_t f[32], s[32];
+        tmem_ld16x64(lane_base + kSkDcol + j * 64, f);
+        if (!first) tmem_ld16x64(lane_base + kSkScol + j * 64, s);
+        tmem_ld_wait();
+        if (j == kSkN / 64 - 1) {
+          // the accumulator has been read: the MMA may start the next segment
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(dempty);
+        }
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          s[e] = (first ? 0u : s[e]) +
+                 static_cast<uint32_t>(__float2int_rn(__uint_as_float(f[e])));
+        if (!last) {
+          tmem_st16x64(lane_base + kSkScol + j * 64, s);
+          continue;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (oka)
+            *reinterpret_cast<int2*>(out_a + j * 64 + 8 * i) =
+                make_int2(static_cast<int32_t>(s[4 * i]), static_cast<int32_t>(s[4 * i + 1]));
+          if (okb)
+            *reinterpret_cast<int2*>(out_b + j * 64 + 8 * i) =
+                make_int2(static_cast<int32_t>(s[4 * i + 2]), static_cast<int32_t>(s[4 * i + 3]));
         }
       }
       if (!last) tmem_st_wait();
@@ -551,32 +669,27 @@ __global__ void __launch_bounds__(kSkThreads, 1) ag_skinny_kernel(const __grid_c
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  // M <= 64: five fp16 stages with 8 KB of rows; else three with 16 KB.
-  const bool small = p.g.M <= 64;
-  const int a_stage = small ? 8 * 1024 : 16 * 1024;
-  const int n_fp = small ? kSkFpMax : 3;
-  const int n_raw = kSkRaw;
-  const int raw_stage = kSkRawB + (small ? 64 : 128) * kSkARow;
-  uint8_t* sFp = smem;                                   // 1024-aligned swizzled fp16 B stages
-  uint8_t* sA = sFp + n_fp * kSkFpStage;                 // swizzled fp16 A stages
-  uint8_t* sRaw = sA + n_fp * a_stage;                   // raw ring: B box, then the rows
+  const SkLayout L(p.g.M);
+  uint8_t* sFp = smem;                          // 1024-aligned swizzled fp16 B stages
+  uint8_t* sA = sFp + L.n_fp * kSkFpB;          // swizzled fp16 A stages
+  uint8_t* sRaw = sA + L.n_fp * L.a_stage;      // raw ring: two B boxes, then the rows
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kSkDataBytes);
   uint64_t* raw_full = bars;
-  uint64_t* raw_empty = raw_full + kSkRaw;
+  uint64_t* raw_empty = raw_full + kSkRawMax;
   // One full/empty pair per fp16 stage: the B and the A half of stage s are
   // written by the two widening roles (12 arrivals) and released by one commit.
-  uint64_t* st_full = raw_empty + kSkRaw;
+  uint64_t* st_full = raw_empty + kSkRawMax;
   uint64_t* st_empty = st_full + kSkFpMax;
   uint64_t* dfull = st_empty + kSkFpMax;
-  uint64_t* dempty = dfull + 2;
-  uint64_t* drain = dempty + 2;
+  uint64_t* dempty = dfull + 1;
+  uint64_t* drain = dempty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool gemm = (p.flags & kFlagGemm) != 0;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kSkRaw; ++s) {
+    for (int s = 0; s < kSkRawMax; ++s) {
       mbar_init(&raw_full[s], 1);
       mbar_init(&raw_empty[s], (kSkBwThreads + kSkAwThreads) / 32);  // both widening roles
     }
@@ -584,10 +697,8 @@ __global__ void __launch_bounds__(kSkThreads, 1) ag_skinny_kernel(const __grid_c
       mbar_init(&st_full[s], (kSkBwThreads + kSkAwThreads) / 32);
       mbar_init(&st_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&dfull[b], 1);
-      mbar_init(&dempty[b], 4);
-    }
+    mbar_init(dfull, 1);
+    mbar_init(dempty, 4);
     mbar_init(drain, 1);
     *tmem_slot = 0;
     *abort = 0;
@@ -609,27 +720,28 @@ __global__ void __launch_bounds__(kSkThreads, 1) ag_skinny_kernel(const __grid_c
   } else if (gemm) {
     switch (role) {
       case kRoleMma:
-        if (lane == 0)
-          sk_mma(p, sFp, sA, a_stage, n_fp, st_full, st_empty, dfull, dempty, tmem,
-                 abort);
+        if (lane == 0) sk_mma(p, sFp, sA, L, st_full, st_empty, dfull, dempty, tmem, abort);
         break;
       case kRoleTma:
-        sk_tma_warp(p, sRaw, n_raw, raw_stage, raw_full, raw_empty, lane, abort);
+        sk_tma_warp(p, sRaw, L, raw_full, raw_empty, lane, abort);
         break;
       case kRoleEpi:
-        sk_epilogue(p, dfull, dempty, tmem, warp & 3, lane, abort);
+        if (L.mm == 64)
+          sk_epilogue64(p, dfull, dempty, tmem, warp & 3, lane, abort);
+        else
+          sk_epilogue(p, L, dfull, dempty, tmem, warp & 3, lane, abort);
         break;
       case kRoleBw:
-        sk_bwiden(p, sRaw, n_raw, raw_stage, n_fp, sFp, raw_full, raw_empty, st_full, st_empty,
-                  rank * 32 + lane, abort);
+        sk_bwiden(p, sRaw, L, sFp, raw_full, raw_empty, st_full, st_empty, rank * 32 + lane,
+                  abort);
         break;
       default:
-        if (small)
-          sk_awiden<2>(p, sRaw, n_raw, raw_stage, n_fp, sA, a_stage, raw_full, raw_empty, st_full,
-                       st_empty, rank * 32 + lane, abort);
+        if (L.mm == 64)
+          sk_awiden<2>(p, sRaw, L, sA, raw_full, raw_empty, st_full, st_empty, rank * 32 + lane,
+                       abort);
         else
-          sk_awiden<4>(p, sRaw, n_raw, raw_stage, n_fp, sA, a_stage, raw_full, raw_empty, st_full,
-                       st_empty, rank * 32 + lane, abort);
+          sk_awiden<4>(p, sRaw, L, sA, raw_full, raw_empty, st_full, st_empty, rank * 32 + lane,
+                       abort);
         break;
     }
   }

@@ -401,13 +401,15 @@ def test_i8_full_size_workload(oracle, wid):
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("S,R,K,N,c", [
-    (2, 32, 1056, 208, 0),     # two K segments + a K tail, a ragged 128-column n-tile
+    (2, 32, 1056, 208, 0),     # two K segments + a K tail, a ragged 256-column n-tile
+    (2, 24, 768, 400, 0),      # two n-tiles, the second ragged inside its second B box
     (4, 8, 64, 16, 0),         # one k-block, one tiny n-tile
     (2, 64, 2048, 384, 16),    # 128 rows (every TMEM lane)
     (1, 40, 512, 128, 0),      # a single shard
     (3, 16, 4096, 256, 2),
     (3, 13, 1040, 144, 0),     # rows of a shard not a multiple of 8, 3 lane quadrants
-    (2, 20, 112, 48, 0),       # K below one 256-row B box, two k-blocks
+    (2, 20, 112, 48, 0),       # K below one 128-row B box, two k-blocks; the second box of
+                               # the n-tile lies past N (zero fill)
     (1, 128, 320, 128, 0),     # 128 rows of one shard, a 1-k-block last unit
 ])
 def test_i8_skinny_full(oracle, S, R, K, N, c):
@@ -456,8 +458,8 @@ def test_i8_skinny_modes_local_rank_and_repeats():
 
 
 @pytest.mark.parametrize("S,R,K,N", [
-    (2, 16, 16384, 128),       # one n-tile of 64 units: 64 CTAs share it, the others hold none
-    (1, 8, 4096, 2048),        # 16 n-tiles of 16 units over 152 CTAs
+    (2, 16, 16384, 128),       # one n-tile of 128 units: 128 CTAs share it, the others hold none
+    (1, 8, 4096, 2048),        # 8 n-tiles of 32 units over 152 CTAs
 ])
 def test_i8_skinny_shared_tiles_and_repeats(oracle, S, R, K, N):
     """Split-K sums of one n-tile spread over many CTAs (some CTAs own no unit),
