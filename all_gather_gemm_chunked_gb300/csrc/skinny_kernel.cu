@@ -767,6 +767,9 @@ __global__ void __launch_bounds__(256) ag_skinny_finish_kernel(
     const int32_t* __restrict__ ws, const int32_t* __restrict__ bias,
     const float* __restrict__ scale, int32_t* __restrict__ C_i32, uint16_t* __restrict__ D,
     int64_t M, int64_t N, int64_t n_tiles, int64_t KQ, int64_t cmax, int grid) {
+  // launched as a programmatic dependent of the skinny kernel: wait for it to
+  // complete (all of its workspace stores visible)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t groups = M * N / 8, U = n_tiles * KQ;
   for (int64_t gi = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; gi < groups;
        gi += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -819,10 +822,24 @@ cudaError_t launch_skinny(const SkinnyParams& p, int grid, cudaStream_t stream) 
   ag_skinny_kernel<<<grid, kSkThreads, kSkSmem, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !(p.flags & kFlagGemm)) return e;
-  ag_skinny_finish_kernel<<<grid * 2, 256, 0, stream>>>(p.ws, p.bias, p.scale, p.C_i32, p.D_f16,
-                                                        p.g.M, p.g.N, p.n_tiles, p.kq, p.cmax,
-                                                        grid);
-  return cudaGetLastError();
+  // Programmatic dependent launch: the finish grid's launch is processed while
+  // the skinny kernel runs, and its griddepcontrol.wait holds it until the
+  // skinny grid has completed.  The skinny kernel triggers nothing early: a
+  // trigger at its start let the finish grid in sooner and measured slower
+  // (59.4 us against 55.3 us on 2 x 32 rows, K = 16384, N = 7168).
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid * 2);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, ag_skinny_finish_kernel, static_cast<const int32_t*>(p.ws),
+                            p.bias, p.scale, p.C_i32, p.D_f16, p.g.M, p.g.N, p.n_tiles, p.kq,
+                            p.cmax, grid);
 }
 
 }  // namespace agg
