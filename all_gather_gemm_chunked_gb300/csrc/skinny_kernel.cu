@@ -778,15 +778,29 @@ __global__ void __launch_bounds__(256) ag_skinny_finish_kernel(
     const int64_t b_lo = skinny_owner(nt * KQ, U, grid);
     const int64_t b_hi = skinny_owner((nt + 1) * KQ - 1, U, grid);
     int32_t c[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    for (int64_t b = b_lo; b <= b_hi; ++b) {
-      int64_t lo, hi;
-      skinny_cta_range(U, b, grid, lo, hi);
-      if (lo == hi) continue;  // a CTA without units wrote no slot
-      const int4* sp = reinterpret_cast<const int4*>(
-          ws + ((nt * cmax + (b - b_lo)) * M + m) * kSkN + nl);
-      const int4 x0 = __ldcg(sp), x1 = __ldcg(sp + 1);
-      c[0] += x0.x; c[1] += x0.y; c[2] += x0.z; c[3] += x0.w;
-      c[4] += x1.x; c[5] += x1.y; c[6] += x1.z; c[7] += x1.w;
+    // four slots per step: their eight 16-byte loads are issued before any is
+    // used (a CTA without units wrote no slot: its loads are skipped)
+    for (int64_t b0 = b_lo; b0 <= b_hi; b0 += 4) {
+      int4 x[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int64_t b = b0 + i;
+        int64_t lo = 0, hi = 0;
+        if (b <= b_hi) skinny_cta_range(U, b, grid, lo, hi);
+        x[2 * i] = x[2 * i + 1] = make_int4(0, 0, 0, 0);
+        if (lo < hi) {
+          const int4* sp = reinterpret_cast<const int4*>(
+              ws + ((nt * cmax + (b - b_lo)) * M + m) * kSkN + nl);
+          x[2 * i] = __ldcg(sp);
+          x[2 * i + 1] = __ldcg(sp + 1);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int4 x0 = x[2 * i], x1 = x[2 * i + 1];
+        c[0] += x0.x; c[1] += x0.y; c[2] += x0.z; c[3] += x0.w;
+        c[4] += x1.x; c[5] += x1.y; c[6] += x1.z; c[7] += x1.w;
+      }
     }
     const int4 b0 = __ldg(reinterpret_cast<const int4*>(bias + n));
     const int4 b1 = __ldg(reinterpret_cast<const int4*>(bias + n + 4));
