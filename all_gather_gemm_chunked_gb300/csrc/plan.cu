@@ -754,6 +754,17 @@ void ag_gemm_plan_destroy(ag_gemm_plan* plan) {
 int ag_gemm_plan_geometry(const ag_gemm_plan* plan, ag_gemm_geometry* out) {
   if (!plan || !out) return fail(AG_GEMM_ERR_INVALID, "plan or out is NULL");
   to_public(plan->g, out);
+  if (plan->skinny) {
+    // the skinny kernel's own tiling and allocations
+    out->block_m = plan->g.M <= 64 ? 64 : 128;
+    out->block_n = 256;
+    out->m_tiles = 1;
+    out->n_tiles = plan->sk_tiles;
+    out->tiles = plan->sk_tiles;
+    out->workspace_bytes = plan->staging_bytes +
+                           static_cast<int64_t>(sizeof(uint32_t)) * plan->counter_count + 64 +
+                           plan->sk_tiles * plan->sk_cmax * plan->g.M * 256 * 4;
+  }
   if (plan->window > 0) {
     out->workspace_bytes += plan->staging_bytes - out->staging_bytes + 4 * plan->window;
     out->staging_bytes = plan->staging_bytes;

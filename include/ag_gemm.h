@@ -221,7 +221,13 @@ int64_t ag_gemm_choose_chunk_rows_bounded(int64_t R);
 /* Wait for the plan's last run, then free everything the plan owns. NULL is a no-op. */
 void ag_gemm_plan_destroy(ag_gemm_plan *plan);
 
-/* The derived sizes of a plan. */
+/*
+ * The derived sizes of a plan.  For a plan on the skinny int8 path
+ * (AG_GEMM_PATH_SKINNY_I8) the tile fields describe that kernel: block_m = 64
+ * or 128 (the MMA's rows: M rounded up), block_n = 256, m_tiles = 1,
+ * n_tiles = tiles = ceil(N / 256), and workspace_bytes counts its split-K
+ * slots instead of fp16 copies of B and the local shard.
+ */
 int ag_gemm_plan_geometry(const ag_gemm_plan *plan, ag_gemm_geometry *out);
 
 /* c actually used by the plan, or a negative status. */

@@ -430,6 +430,19 @@ def test_plan_path_and_grid():
         assert p.path == B_.PATH_FUSED_F16 and p.grid % 2 == 0 and 0 < p.grid <= sms
 
 
+def test_skinny_plan_geometry():
+    """A skinny plan reports its own kernel's tiling (rows x 256-column n-tiles) and
+    what it allocates (split-K slots, no fp16 copy of B)."""
+    with Plan(2, 64, 16384, 7168, "i8") as p:
+        g = p.geometry
+        assert (g["block_m"], g["block_n"], g["m_tiles"]) == (64, 256, 1)
+        assert g["n_tiles"] == g["tiles"] == 28
+        assert g["workspace_bytes"] < 64 * 1024 * 1024    # fp16 B alone would be 235 MB
+    with Plan(2, 128, 1024, 400, "i8") as p:
+        g = p.geometry
+        assert (g["block_m"], g["block_n"], g["n_tiles"]) == (128, 256, 2)
+
+
 def test_i8_skinny_worst_case_magnitudes_exact(oracle):
     S, R, K, N = 2, 32, 16384, 256
     rng = np.random.default_rng(6)
