@@ -40,8 +40,10 @@
 // the fp16 tensor path: int8 values are exact in fp16, products of two int8
 // values are exact in fp32, and K is cut into segments of 1024 so every fp32
 // partial sum is an integer below 2^24 (exact).  After each segment the
-// epilogue converts the fp32 accumulator to int32 and adds it to an int32
-// running sum kept in the other half of TMEM.
+// epilogue converts the fp32 accumulator to int32 and adds it to the int32
+// running sums it keeps in registers (one row x 128 columns per thread), so
+// the two TMEM accumulators alternate as on the fp16 path and the MMA never
+// waits for a fold.
 
 #include <cuda_fp16.h>
 
@@ -324,8 +326,7 @@ __device__ void mma_warp(const FusedParams& p, const uint8_t* sA, const uint8_t*
       if (pos > 0) slot = ((pos - 1) * g.MT + mt) % p.window;
     }
     for (int64_t seg = 0; seg < nseg && ok; ++seg) {
-      const uint32_t buf = kI8 ? 0u : (unit & 1u);
-      const uint32_t use = kI8 ? unit : (unit >> 1);
+      const uint32_t buf = unit & 1u, use = unit >> 1;
       if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, p.pipe_timeout_ns, abort, gstatus)) {
         ok = false;
         break;
@@ -399,6 +400,9 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
   const int nchunks = g.BN / 64;                      // 32-column chunks in this warp's half
   const int chunk0 = half * nchunks;
   uint8_t* box = sEpi + (half * 4 + quad) * kEpiBoxBytes;  // this warp's staging box
+  // int8: the running int32 sums of this thread's row over the warp's columns
+  // (at most 4 chunks of 32), kept in registers across the tile's segments
+  uint32_t sums[kI8 ? 128 : 1];
   uint32_t unit = 0;
   for (int64_t t = cluster; t < g.tiles; t += n_clusters) {
     int pos;
@@ -409,8 +413,7 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
     const bool row_ok = r < g.R;
     const int64_t grow = static_cast<int64_t>(src) * g.R + r;
     for (int64_t seg = 0; seg < nseg; ++seg) {
-      const uint32_t buf = kI8 ? 0u : (unit & 1u);
-      const uint32_t use = kI8 ? unit : (unit >> 1);
+      const uint32_t buf = unit & 1u, use = unit >> 1;
       if (!mbar_wait(&tfull[buf], use & 1u, p.pipe_timeout_ns, abort, gstatus)) {
         if (lane == 0) {
           set_status(p.status, kStatusPipelineTimeout, 0x300u | rank);
@@ -465,23 +468,30 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
         }
       } else {
         const bool first = seg == 0, last = seg == nseg - 1;
-        for (int jj = 0; jj < nchunks; ++jj) {
-          const int j = chunk0 + jj;
-          uint32_t f[32], s[32];
-          tmem_ld32(lane_base + j * 32, f);
-          if (!first) tmem_ld32(lane_base + 256u + j * 32, s);
-          tmem_ld_wait();
-          if (jj == nchunks - 1) release();
-          // fp32 partial (an exact integer) -> int32, added to the running sum
-          uint32_t acc[32];
+        // fp32 partials (exact integers) -> int32, added to the running sums;
+        // 16 columns per TMEM load keep the sums in registers
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            acc[e] = (first ? 0u : s[e]) +
-                     static_cast<uint32_t>(__float2int_rn(__uint_as_float(f[e])));
-          if (!last) {
-            tmem_st32(lane_base + 256u + j * 32, acc);
-          } else if (row_ok) {
-            const int64_t n0 = nt * g.BN + j * 32;
+        for (int jj = 0; jj < 4; ++jj) {
+          if (jj < nchunks) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              uint32_t f[16];
+              tmem_ld16(lane_base + buf * 256u + (chunk0 + jj) * 32 + hh * 16, f);
+              tmem_ld_wait();
+              if (jj == nchunks - 1 && hh == 1) release();
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const uint32_t v = static_cast<uint32_t>(__float2int_rn(__uint_as_float(f[e])));
+                if (kI8) sums[jj * 32 + hh * 16 + e] = first ? v : sums[jj * 32 + hh * 16 + e] + v;
+              }
+            }
+          }
+        }
+        if (last && row_ok) {
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            if (jj >= nchunks) continue;
+            const int64_t n0 = nt * g.BN + (chunk0 + jj) * 32;
 #pragma unroll
             for (int e = 0; e < 32; e += 8) {
               if (n0 + e >= g.N) continue;
@@ -495,7 +505,8 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
               uint32_t h[4];
 #pragma unroll
               for (int u = 0; u < 8; ++u) {
-                const int32_t cv = static_cast<int32_t>(acc[e + u] + static_cast<uint32_t>(bb[u]));
+                const int32_t cv =
+                    static_cast<int32_t>((kI8 ? sums[jj * 32 + e + u] : 0u) + static_cast<uint32_t>(bb[u]));
                 c[u] = static_cast<uint32_t>(cv);
                 const float dv = __fmul_rn(__int2float_rn(cv), ss[u]);
                 const uint32_t hb = __half_as_ushort(__float2half_rn(dv));
@@ -511,8 +522,6 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
             }
           }
         }
-        // the int32 sums must be in TMEM before this warp's next fold reads them
-        if (!last) tmem_st_wait();
       }
       ++unit;
     }
