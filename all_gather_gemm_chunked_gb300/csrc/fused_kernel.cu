@@ -436,7 +436,7 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
             mbar_arrive_cluster(tempty0 + buf * 8);
         }
       };
-      if (!kI8) {
+      if constexpr (!kI8) {
         // 32 rows (one per lane) x 32 columns at a time: registers -> swizzled
         // shared box -> one TMA store of 32 full 128-byte row segments.  Rows
         // past the shard and columns past N are clipped by the descriptor.
@@ -482,7 +482,7 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
 #pragma unroll
               for (int e = 0; e < 16; ++e) {
                 const uint32_t v = static_cast<uint32_t>(__float2int_rn(__uint_as_float(f[e])));
-                if (kI8) sums[jj * 32 + hh * 16 + e] = first ? v : sums[jj * 32 + hh * 16 + e] + v;
+                sums[jj * 32 + hh * 16 + e] = first ? v : sums[jj * 32 + hh * 16 + e] + v;
               }
             }
           }
@@ -506,7 +506,7 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
 #pragma unroll
               for (int u = 0; u < 8; ++u) {
                 const int32_t cv =
-                    static_cast<int32_t>((kI8 ? sums[jj * 32 + e + u] : 0u) + static_cast<uint32_t>(bb[u]));
+                    static_cast<int32_t>(sums[jj * 32 + e + u] + static_cast<uint32_t>(bb[u]));
                 c[u] = static_cast<uint32_t>(cv);
                 const float dv = __fmul_rn(__int2float_rn(cv), ss[u]);
                 const uint32_t hb = __half_as_ushort(__float2half_rn(dv));
