@@ -101,3 +101,30 @@ def test_sweep_bf16(oracle, S, R, K, N, c):
     x = synth.make_inputs(S, R, K, N, "bf16", 9500 + S * 131 + R * 17 + K + N)
     C = run_bf16(x, S, R, K, N, c)
     check_f16(C, oracle.ag_gemm_bf16(x["shards"], x["B"]), K, f"bf16 S={S} R={R} K={K} N={N} c={c}")
+
+
+# Many shards, down to one row per shard (chunk = row), on every path.
+MANY = [
+    (8, 1, 1040, 272, "i8"),      # 8 rows: skinny, M = 64 MMA rows, one row per shard
+    (7, 18, 2064, 528, "i8"),     # 126 rows: skinny, M = 128 MMA rows
+    (6, 30, 1024, 160, "i8"),     # 180 rows: fused int8
+    (8, 1, 200, 72, "f16"),       # one row per shard
+    (8, 3, 520, 136, "f16"),
+    (5, 61, 64, 264, "bf16"),
+]
+
+
+@pytest.mark.parametrize("S,R,K,N,dtype", MANY,
+                         ids=["S{}R{}K{}N{}{}".format(*c) for c in MANY])
+def test_sweep_many_shards(oracle, S, R, K, N, dtype):
+    x = synth.make_inputs(S, R, K, N, dtype, 9900 + S * 131 + R * 17 + K + N)
+    if dtype == "i8":
+        Ci, D = run_i8(x, S, R, K, N)
+        Cref, Dref = oracle.ag_gemm_dequant(x["shards"], x["B"], x["bias"], x["scale"])
+        _check_i8(Ci, D, Cref, Dref, f"int8 S={S} R={R} K={K} N={N}")
+    elif dtype == "f16":
+        check_f16(run_f16(x, S, R, K, N), oracle.ag_gemm_f16(x["shards"], x["B"]), K,
+                  f"f16 S={S} R={R} K={K} N={N}")
+    else:
+        check_f16(run_bf16(x, S, R, K, N), oracle.ag_gemm_bf16(x["shards"], x["B"]), K,
+                  f"bf16 S={S} R={R} K={K} N={N}")
