@@ -212,6 +212,80 @@ def time_oracle(w, x, budget_s: float, row_block: int = 2):
     return ops / el * 1e-12, rows_done, el
 
 
+_START_BARRIER = None
+
+
+def _oracle_worker_init(barrier):
+    global _START_BARRIER
+    _START_BARRIER = barrier
+
+
+def _oracle_rows_worker(task):
+    """One process of the all-cores CPU figure (started with spawn): time the
+    oracle on whole rows of C for `budget_s`, from row `row0` of one shard.
+    Only that shard and B (plus bias and scale) are generated here, from the
+    same seeded streams as the workload; the rows' arithmetic is the same as
+    in the full problem (the oracle over the one-shard list)."""
+    wid, row0, budget_s = task
+    import oracle
+    from all_gather_gemm_chunked_gb300 import synth
+    w = synth.WORKLOADS[wid]
+    seed = synth.SEED_BASE + w.wid
+    s = (row0 // w.R) % w.S
+    gen = {"f16": synth.normal_f16, "bf16": synth.normal_bf16_bits, "i8": synth.uniform_i8}[w.dtype]
+    shard = gen(seed + s, (w.R, w.K))
+    B = gen(seed + synth.OFF_B, (w.K, w.N * w.n_blocks))[:, w.rank * w.N:(w.rank + 1) * w.N]
+    B = np.ascontiguousarray(B)
+    if w.dtype == "i8":
+        bias = synth.uniform_i32(seed + synth.OFF_BIAS, (w.N * w.n_blocks,))[:w.N]
+        scale = synth.uniform_f32(seed + synth.OFF_SCALE, (w.N * w.n_blocks,))[:w.N]
+    oracle.build()
+    cols = np.arange(w.N, dtype=np.int64)
+    r, rows_done = row0 % w.R, 0
+    if _START_BARRIER is not None:
+        try:  # every process starts its timed rows together
+            _START_BARRIER.wait(timeout=300)
+        except Exception:
+            pass
+    t0 = time.time()
+    while True:
+        rows = np.arange(r, r + 2) % w.R
+        rr, cc = np.repeat(rows, w.N), np.tile(cols, 2)
+        if w.dtype == "f16":
+            oracle.ag_gemm_f16_at([shard], B, rr, cc)
+        elif w.dtype == "bf16":
+            oracle.ag_gemm_bf16_at([shard], B, rr, cc)
+        else:
+            oracle.ag_gemm_dequant_at([shard], B, bias, scale, rr, cc)
+        rows_done += 2
+        r += 2
+        if time.time() - t0 >= budget_s:
+            break
+    return rows_done, t0, time.time()
+
+
+def time_oracle_all_cores(w, budget_s: float):
+    """The same oracle on every host core as separate processes (spawn), each on
+    its own rows for `budget_s`: (value, rows, cores, wall seconds), or None."""
+    import multiprocessing as mp
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    cores = max(1, int(cores or 1))
+    tasks = [(w.wid, (i * w.M) // cores, budget_s) for i in range(cores)]
+    ctx = mp.get_context("spawn")
+    pool = ctx.Pool(cores, initializer=_oracle_worker_init, initargs=(ctx.Barrier(cores),))
+    try:
+        res = pool.map_async(_oracle_rows_worker, tasks).get(timeout=budget_s * 4 + 300)
+        pool.close()
+    except Exception:  # a failed or stuck worker costs the figure, never the bench line
+        pool.terminate()
+        return None
+    finally:
+        pool.join()
+    rows = sum(r for r, _, _ in res)
+    wall = max(t1 for _, _, t1 in res) - min(t0 for _, t0, _ in res)
+    return 2.0 * rows * w.N * w.K / wall * 1e-12, rows, cores, wall
+
+
 def run_reference(args, w, rank):
     if rank != 0:
         return 0
@@ -444,6 +518,12 @@ def run_ours(args, w, rank, world, local_rank):
         cpu = {"value": v, "unit": unit, "cores": 1, "kind": "oracle",
                "sample": f"{rows} whole rows of C ({rows * w.N} outputs), {el:.1f} s",
                "cpu": cpu_model()}
+        par = time_oracle_all_cores(w, args.cpu_seconds)
+        if par is not None:
+            pv, prow, pcores, pwall = par
+            cpu["all_cores"] = {"value": pv, "unit": unit, "cores": pcores,
+                                "sample": f"{prow} whole rows of C over {pcores} processes "
+                                          f"(one per core, spawn), {pwall:.1f} s wall"}
 
     plan.close()
     if rank != 0:
