@@ -147,7 +147,7 @@ AGG_HD bool rows_chunks(const Geometry& g, int64_t row0, int64_t& q0, int64_t& q
   return true;
 }
 
-// Skinny int8 path: the U (n-tile, 4-k-block) units are cut into G contiguous
+// Skinny int8 path: the U (n-tile, 2-k-block) units are cut into G contiguous
 // per-CTA ranges; CTA b takes [U b / G, U (b + 1) / G).
 AGG_HD void skinny_cta_range(int64_t U, int64_t b, int64_t G, int64_t& lo, int64_t& hi) {
   lo = U * b / G;

@@ -1,23 +1,33 @@
 """Benchmark of the streamed AllGather+GEMM on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 2] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 4]
+                    [--extra-workloads 2,3,5] [--impl ours|reference]
 
 Metric: streamed gather+GEMM throughput 2*M*N*K / t in TFLOP/s (TOP/s for the
 int8 workloads), where t is the device time of one run (PIPELINED mode: chunk
-copies and GEMM concurrently, one cooperative launch for fp16) on inputs
-already resident in HBM.  L2 is flushed before every timed step, outside the
-timed events: a 512 MiB buffer is written, then a second 512 MiB buffer is
-read, so that the written lines are back in HBM and L2 holds no data of the
-run and no dirty lines whose write-back would land in the timed step.  One
-JSON line is printed by rank 0.
+copies and GEMM concurrently in one persistent launch) on inputs already
+resident in HBM.  The headline workload is the largest one: int8
+AllGatherMatmulDequant, 4 shards of 4096 rows, K = 27392, N = 4096 (the first
+test shape of "AllGather矩阵乘法反量化算子设计文档", 8.3).  The fp16 workloads
+2 and 3 and the HBM-bound skinny int8 workload 5 are measured in the same call
+and reported under "workloads", each with its own roofline.
+
+L2 is flushed before every timed step, outside the timed events: a 512 MiB
+buffer is written, then a second 512 MiB buffer is read, so that the written
+lines are back in HBM and L2 holds no data of the run and no dirty lines whose
+write-back would land in the timed step.  Each batch of timed steps is
+enqueued behind a GPU spin, so the host has queued every event and launch of
+the batch before the GPU reaches the first one (host latency never falls
+inside a timed event).  One JSON line is printed by rank 0.
 
 N > 1 (torchrun): every rank runs its own full replica of the workload on its
 own GPU (the shards are simulated ranks inside one GPU, so nothing is
 exchanged between GPUs); the step time is the max over ranks and `value` is
-the whole-job throughput N * flops / t_max ("scaling": "weak").
+the whole-job throughput N * flops / t_max ("scaling": "weak").  The extra
+workloads are measured at N = 1 only.
 
 --impl reference times the CPU oracle (plain single-threaded C loops) on a
-bounded sample of the same workload.
+bounded sample of the same workload: a step is one sample of whole rows of C.
 """
 from __future__ import annotations
 
@@ -291,28 +301,32 @@ def run_reference(args, w, rank):
         return 0
     from all_gather_gemm_chunked_gb300 import synth
     x = synth.workload_inputs(w)
-    per_step = []
+    per_step_s, per_row_s = [], []
     rows_total = 0
-    # one untimed warm-up sample, then K bounded samples
+    # one untimed warm-up sample, then K bounded samples; a step is one sample
     for i in range(args.warmup + args.steps):
         v, rows, el = time_oracle(w, x, budget_s=args.ref_step_seconds)
         if i >= args.warmup:
-            per_step.append(el / rows)
+            per_step_s.append(el)
+            per_row_s.append(el / rows)
             rows_total += rows
-    s_per_row = float(np.mean(per_step))
+    s_per_row = float(np.mean(per_row_s))
     value = 2.0 * w.N * w.K / s_per_row * 1e-12
     unit = "TOP/s" if w.dtype == "i8" else "TFLOP/s"
-    full_ms = s_per_row * w.M * 1e3
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": unit,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": full_ms, "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": float(np.mean(per_step_s)) * 1e3,
+        "ms_per_step_median": float(np.median(per_step_s)) * 1e3,
+        "full_workload_ms_extrapolated": s_per_row * w.M * 1e3,
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int64" if w.dtype == "i8" else "f64",
         "data": "synthetic", "config": workload_config(w),
         "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
                          "sample": f"{rows_total} whole rows of C over {args.steps} steps "
-                                   f"(~{args.ref_step_seconds:.0f} s each); ms_per_step is "
-                                   f"the extrapolated full-workload time",
+                                   f"(~{args.ref_step_seconds:.0f} s each); a step is one such "
+                                   f"sample, full_workload_ms_extrapolated scales it to all "
+                                   f"{w.M} rows",
                          "cpu": cpu_model()},
         "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -339,77 +353,241 @@ def workload_config(w, flush=True):
 # GPU arm
 # ---------------------------------------------------------------------------
 
+def timed_events(torch, stream, dev, n, body, before=None, batch=64, gate_ms=20.0):
+    """Device times (ms) of n calls of body(), each bracketed by CUDA events on
+    `stream` and preceded, outside the events, by before().
+
+    Every batch of up to `batch` steps is enqueued behind a GPU spin of
+    `gate_ms`, so that the host has enqueued all events and launches of the
+    batch before the GPU reaches the first of them: host latency (Python,
+    ctypes, the clock sampler starting) cannot leave the GPU idle inside a
+    timed event.  If the spin had already ended when the host finished
+    enqueueing, the batch is timed again behind a longer spin."""
+    times, late_batches, redone = [], 0, 0
+    while len(times) < n:
+        b = min(batch, n - len(times))
+        for attempt in range(4):
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(b)]
+            gate = torch.cuda.Event()
+            torch.cuda._sleep(int(gate_ms * 2.1e6))  # ~gate_ms at <= 2.1 GHz SM clock
+            gate.record(stream)
+            t0 = time.perf_counter()
+            for a, e in evs:
+                if before is not None:
+                    before()
+                a.record(stream)
+                body()
+                e.record(stream)
+            host_ms = (time.perf_counter() - t0) * 1e3
+            late = gate.query()
+            torch.cuda.synchronize(dev)
+            if not late:
+                break
+            redone += 1
+            gate_ms = max(2.0 * gate_ms, 2.0 * host_ms)
+        else:
+            late_batches += 1
+        times += [a.elapsed_time(e) for a, e in evs]
+    return times, {"batches_redone": redone, "batches_host_bound": late_batches,
+                   "gate_ms": gate_ms}
+
+
+class Runner:
+    """One workload on one GPU: inputs resident in HBM, a plan, the run and
+    (optionally) the end-to-end run from pinned host buffers."""
+
+    def __init__(self, torch, w, dev, args, host=False):
+        from all_gather_gemm_chunked_gb300 import synth
+        from all_gather_gemm_chunked_gb300.plan import Plan
+        self.torch, self.w, self.dev, self.args = torch, w, dev, args
+        x = synth.workload_inputs(w)
+        self.x = x
+        pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+        h_shards = [pin(s) for s in x["shards"]]
+        h_B = pin(x["B_rank"])  # this rank's B (its column block, for the N-sharded layout)
+        if w.dtype == "bf16":  # bit patterns (numpy has no bfloat16) -> bfloat16 tensors
+            h_shards = [t.view(torch.int16).view(torch.bfloat16) for t in h_shards]
+            h_B = h_B.view(torch.int16).view(torch.bfloat16)
+        self.shards = [t.to(dev) for t in h_shards]
+        # B (and C below) at full width; the run takes the rank's column block
+        cols = slice(w.rank * w.N, (w.rank + 1) * w.N)
+        B_full = torch.empty((w.K, w.N * w.n_blocks), dtype=h_B.dtype, device=dev)
+        self.Bd = B_full[:, cols]
+        self.Bd.copy_(h_B)
+        self.int8 = w.dtype == "i8"
+        if self.int8:
+            h_bias, h_scale = pin(x["bias"]), pin(x["scale"])
+            self.bias, self.scale = h_bias.to(dev), h_scale.to(dev)
+            self.Ci = torch.empty((w.M, w.N), dtype=torch.int32, device=dev)
+            self.D = torch.empty((w.M, w.N), dtype=torch.float16, device=dev)
+        else:
+            C_full = torch.empty((w.M, w.N * w.n_blocks), dtype=torch.float32, device=dev)
+            self.C = C_full[:, cols]
+        self.plan = Plan(w.S, w.M, w.K, w.N, w.dtype, w.chunk_rows, staging_slots=w.staging_slots)
+        self.geometry = self.plan.geometry  # the plan's own sizes (staging window included)
+        self.path = self.plan.path
+        if w.rank:
+            self.plan.set_local_rank(w.rank)
+        self.stream = torch.cuda.current_stream(dev)
+        self.host = host
+        if host:
+            self.h_shards, self.h_B = h_shards, h_B
+            if self.int8:
+                self.h_bias, self.h_scale = h_bias, h_scale
+                self.h_Ci = torch.empty((w.M, w.N), dtype=torch.int32).pin_memory()
+                self.h_D = torch.empty((w.M, w.N), dtype=torch.float16).pin_memory()
+            else:
+                self.h_C = torch.empty((w.M, w.N), dtype=torch.float32).pin_memory()
+
+    def step(self):
+        if self.int8:
+            self.plan.dequant_run(self.shards, self.Bd, self.bias, self.scale, self.Ci, self.D)
+        else:
+            self.plan.run(self.shards, self.Bd, self.C)
+
+    def e2e_step(self):
+        for hs, ds in zip(self.h_shards, self.shards):
+            ds.copy_(hs, non_blocking=True)
+        self.Bd.copy_(self.h_B, non_blocking=True)
+        if self.int8:
+            self.bias.copy_(self.h_bias, non_blocking=True)
+            self.scale.copy_(self.h_scale, non_blocking=True)
+        self.step()
+        if self.int8:
+            self.h_Ci.copy_(self.Ci, non_blocking=True)
+            self.h_D.copy_(self.D, non_blocking=True)
+        else:
+            self.h_C.copy_(self.C, non_blocking=True)
+
+    def e2e_bytes(self):
+        h2d = (sum(t.numel() * t.element_size() for t in self.h_shards)
+               + self.h_B.numel() * self.h_B.element_size())
+        if self.int8:
+            return h2d + self.h_bias.numel() * 4 + self.h_scale.numel() * 4, \
+                self.h_Ci.numel() * 4 + self.h_D.numel() * 2
+        return h2d, self.h_C.numel() * 4
+
+    def timed(self, n, mode, flush, fn=None):
+        from all_gather_gemm_chunked_gb300 import binding as B_
+        self.plan.set_mode(mode)
+        try:
+            return timed_events(self.torch, self.stream, self.dev, n, fn or self.step, flush)
+        finally:
+            self.plan.set_mode(B_.MODE_PIPELINED)
+
+    def warm(self, n):
+        for _ in range(n):
+            self.step()
+        self.torch.cuda.synchronize(self.dev)
+        if self.plan.status() != 0:
+            raise RuntimeError(f"{self.w.name}: warm-up run failed: status "
+                               f"{self.plan.status_word():#x}")
+
+    def check_status(self, what):
+        if self.plan.status() != 0:
+            raise RuntimeError(f"{self.w.name}: {what} failed: status {self.plan.status_word():#x}")
+
+    def modes(self, n, flush, t_pipe):
+        from all_gather_gemm_chunked_gb300 import binding as B_
+        t_compute = float(np.median(self.timed(n, B_.MODE_COMPUTE_ONLY, flush)[0]))
+        t_copy = float(np.median(self.timed(n, B_.MODE_COPY_ONLY, flush)[0]))
+        # a staging window cannot hold the whole gather: no SEQUENTIAL run
+        t_seq = (float(np.median(self.timed(n, B_.MODE_SEQUENTIAL, flush)[0]))
+                 if self.w.staging_slots is None else None)
+        self.check_status("mode runs")
+        overlap = (t_copy + t_compute - t_pipe) / max(min(t_copy, t_compute), 1e-9)
+        return {"pipelined_ms": t_pipe, "compute_only_ms": t_compute, "copy_only_ms": t_copy,
+                "sequential_ms": t_seq, "overlap_efficiency": overlap,
+                "speedup_vs_sequential": t_seq / t_pipe if t_seq is not None else None}
+
+    def close(self):
+        self.plan.close()
+
+
+def roofline_of(w, path_id, kernel_ms, clk, peaks, peak_src):
+    """Roofline of one run's device time against the measured peak of its bound."""
+    from all_gather_gemm_chunked_gb300 import binding as B_
+    traffic = profiled_traffic(w.wid, path_id)
+    if path_id == B_.PATH_SKINNY_I8:
+        # bound by HBM: algorithmic bytes of one run = B once, the gathered rows
+        # once, the remote shards copied (read + write), bias, scale, C_i32, D
+        algo = (w.K * w.N + w.M * w.K + 2 * (w.S - 1) * w.R * w.K + 8 * w.N
+                + 6 * w.M * w.N)
+        peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        achieved = algo / (kernel_ms * 1e-3) * 1e-9
+        return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic, "algorithmic_bytes": algo,
+                "peak_source": f"{peak_src} HBM copy bandwidth",
+                "kernel": "ag_skinny_kernel + ag_skinny_finish_kernel (one run)"}
+    # a dense fp16 contraction: its peak is the measured dense bf16 figure
+    # (fp16 and bf16 share the same nominal dense rate): the burst figure, or
+    # the sustained one (cuBLAS back to back under the power cap) when the
+    # clock samples of this timed region saw sw_power_cap
+    capped = bool(clk) and "sw_power_cap" in (clk.get("reasons") or [])
+    key = "bf16_tflops_sustained" if capped else "bf16_tflops"
+    peak = float(peaks.get(key, FALLBACK_PEAKS[key]))
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    achieved = w.flops / (kernel_ms * 1e-3) * 1e-12
+    int8 = w.dtype == "i8"
+    r = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+         "frac": achieved / peak, "traffic": traffic,
+         "peak_source": f"{peak_src} bf16 dense "
+                        + ("sustained (the timed region ran under sw_power_cap)" if capped
+                           else "burst")
+                        + " (fp16 dense = bf16 dense nominal; int8 runs exactly on the fp16 "
+                          "tensor path)",
+         "kernel": "ag_fused_kernel" + ("<int8> + widen_kernel (one run)" if int8 else "<fp16>")}
+    if capped:
+        r["frac_of_burst"] = achieved / burst
+    return r
+
+
+def measure_extra(torch, w, dev, args, flush_fn, peaks, peak_src):
+    """A compact record of one more workload, timed like the headline one."""
+    r = Runner(torch, w, dev, args)
+    try:
+        r.warm(max(args.warmup, 3))
+        from all_gather_gemm_chunked_gb300 import binding as B_
+        steps = args.steps if args.steps is not None else 20
+        times, gate = r.timed(steps, B_.MODE_PIPELINED, flush_fn)
+        r.check_status("timed runs")
+        mean_ms, med_ms = float(np.mean(times)), float(np.median(times))
+        unit = "TOP/s" if w.dtype == "i8" else "TFLOP/s"
+        rec = {"workload": w.name, "value": w.flops / (mean_ms * 1e-3) * 1e-12, "unit": unit,
+               "steps": steps, "ms_per_step": mean_ms, "ms_per_step_median": med_ms,
+               "roofline": roofline_of(w, r.path, mean_ms, None, peaks, peak_src),
+               "config": workload_config(w, flush_fn is not None), "enqueue": gate}
+        if not args.no_modes:
+            rec["modes"] = r.modes(max(3, min(steps, 10)), flush_fn, med_ms)
+        return rec
+    finally:
+        r.close()
+
+
 def run_ours(args, w, rank, world, local_rank):
     import torch
 
     from all_gather_gemm_chunked_gb300 import binding as B_
     from all_gather_gemm_chunked_gb300 import synth
-    from all_gather_gemm_chunked_gb300.plan import Plan
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    x = synth.workload_inputs(w)
-    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
-    h_shards = [pin(s) for s in x["shards"]]
-    h_B = pin(x["B_rank"])  # this rank's B (its column block, for the N-sharded layout)
-    if w.dtype == "bf16":  # bit patterns (numpy has no bfloat16) -> bfloat16 tensors
-        h_shards = [t.view(torch.int16).view(torch.bfloat16) for t in h_shards]
-        h_B = h_B.view(torch.int16).view(torch.bfloat16)
-    shards = [t.to(dev) for t in h_shards]
-    # B (and C below) at full width; the run takes the rank's column block
-    cols = slice(w.rank * w.N, (w.rank + 1) * w.N)
-    B_full = torch.empty((w.K, w.N * w.n_blocks), dtype=h_B.dtype, device=dev)
-    Bd = B_full[:, cols]
-    Bd.copy_(h_B)
-    int8 = w.dtype == "i8"
-    if int8:
-        h_bias, h_scale = pin(x["bias"]), pin(x["scale"])
-        bias, scale = h_bias.to(dev), h_scale.to(dev)
-        Ci = torch.empty((w.M, w.N), dtype=torch.int32, device=dev)
-        D = torch.empty((w.M, w.N), dtype=torch.float16, device=dev)
-        h_Ci = torch.empty((w.M, w.N), dtype=torch.int32).pin_memory()
-        h_D = torch.empty((w.M, w.N), dtype=torch.float16).pin_memory()
-    else:
-        C_full = torch.empty((w.M, w.N * w.n_blocks), dtype=torch.float32, device=dev)
-        C = C_full[:, cols]
-        h_C = torch.empty((w.M, w.N), dtype=torch.float32).pin_memory()
-    plan = Plan(w.S, w.M, w.K, w.N, w.dtype, w.chunk_rows, staging_slots=w.staging_slots)
-    geometry = plan.geometry  # the plan's own sizes (staging window included)
-    if w.rank:
-        plan.set_local_rank(w.rank)
-    stream = torch.cuda.current_stream(dev)
-    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    r = Runner(torch, w, dev, args, host=True)
+    flush_buf = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     flush_rd = torch.ones(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     flush_sink = torch.empty((), dtype=torch.float32, device=dev)
 
-    def step():
-        if int8:
-            plan.dequant_run(shards, Bd, bias, scale, Ci, D)
-        else:
-            plan.run(shards, Bd, C)
+    def flush():
+        flush_buf.fill_(1.0)
+        torch.sum(flush_rd, dim=0, out=flush_sink)
 
-    def timed(n, mode, fn=step):
-        plan.set_mode(mode)
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(n)]
-        for a, b in evs:
-            if not args.no_flush:
-                flush.fill_(1.0)
-                torch.sum(flush_rd, dim=0, out=flush_sink)
-            a.record(stream)
-            fn()
-            b.record(stream)
-        torch.cuda.synchronize(dev)
-        return [a.elapsed_time(b) for a, b in evs]
+    flush_fn = None if args.no_flush else flush
 
-    for _ in range(max(args.warmup, 3)):
-        step()
-    torch.cuda.synchronize(dev)
-    if plan.status() != 0:
-        raise RuntimeError(f"warm-up run failed: status {plan.status_word():#x}")
+    r.warm(max(args.warmup, 3))
     if args.steps is None:
         # size the timed region so that the clock sampler sees it for ~2 s
-        est = float(np.median(timed(5, B_.MODE_PIPELINED))) * 1e-3 + 1e-4  # + flush
+        est = float(np.median(r.timed(5, B_.MODE_PIPELINED, flush_fn)[0])) * 1e-3 + 1e-4
         args.steps = int(min(20000, max(20, np.ceil(2.0 / est))))
         args.steps = int(reduce_max(args.steps, dev))
 
@@ -417,13 +595,11 @@ def run_ours(args, w, rank, world, local_rank):
     barrier()
     torch.cuda.synchronize(dev)
     clocks.start()
-    times_ms = timed(args.steps, B_.MODE_PIPELINED)
+    times_ms, gate = r.timed(args.steps, B_.MODE_PIPELINED, flush_fn)
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
     barrier()
-    status = plan.status()
-    if status != 0:
-        raise RuntimeError(f"timed runs failed: status {plan.status_word():#x}")
+    r.check_status("timed runs")
     t_local = float(np.sum(times_ms)) / 1e3
     t_max = reduce_max(t_local, dev)
     ms_per_step = t_max / args.steps * 1e3          # the mean step (max over ranks)
@@ -433,89 +609,30 @@ def run_ours(args, w, rank, world, local_rank):
     # the other run modes (context: overlap of copy and GEMM)
     modes = {}
     if not args.no_modes:
-        nm = max(3, min(args.steps, 10))
-        t_compute = float(np.median(timed(nm, B_.MODE_COMPUTE_ONLY)))
-        t_copy = float(np.median(timed(nm, B_.MODE_COPY_ONLY)))
-        # a staging window cannot hold the whole gather: no SEQUENTIAL run
-        t_seq = (float(np.median(timed(nm, B_.MODE_SEQUENTIAL))) if w.staging_slots is None
-                 else None)
-        t_pipe = float(np.median(times_ms))
-        overlap = (t_copy + t_compute - t_pipe) / max(min(t_copy, t_compute), 1e-9)
-        modes = {"pipelined_ms": t_pipe, "compute_only_ms": t_compute, "copy_only_ms": t_copy,
-                 "sequential_ms": t_seq, "overlap_efficiency": overlap,
-                 "speedup_vs_sequential": t_seq / t_pipe if t_seq is not None else None}
-        plan.set_mode(B_.MODE_PIPELINED)
+        modes = r.modes(max(3, min(args.steps, 10)), flush_fn, float(np.median(times_ms)))
 
-    # end to end through the C ABI with host buffers
-    def e2e_step():
-        for hs, ds in zip(h_shards, shards):
-            ds.copy_(hs, non_blocking=True)
-        Bd.copy_(h_B, non_blocking=True)
-        if int8:
-            bias.copy_(h_bias, non_blocking=True)
-            scale.copy_(h_scale, non_blocking=True)
-        step()
-        if int8:
-            h_Ci.copy_(Ci, non_blocking=True)
-            h_D.copy_(D, non_blocking=True)
-        else:
-            h_C.copy_(C, non_blocking=True)
-
+    # end to end through the C ABI with host buffers: every step copies its
+    # inputs from pinned host memory and reads its outputs back
     ne = max(3, min(args.steps, 10))
-    e2e_ms = timed(ne, B_.MODE_PIPELINED, e2e_step)
+    e2e_ms, _ = r.timed(ne, B_.MODE_PIPELINED, None, fn=r.e2e_step)
+    r.check_status("end-to-end runs")
     e2e_t = reduce_max(float(np.sum(e2e_ms)) / 1e3, dev)
-    h2d = sum(t.numel() * t.element_size() for t in h_shards) + h_B.numel() * h_B.element_size()
-    if int8:
-        h2d += h_bias.numel() * 4 + h_scale.numel() * 4
-        d2h = h_Ci.numel() * 4 + h_D.numel() * 2
-    else:
-        d2h = h_C.numel() * 4
-    unit = "TOP/s" if int8 else "TFLOP/s"
+    h2d, d2h = r.e2e_bytes()
+    unit = "TOP/s" if r.int8 else "TFLOP/s"
     e2e = {"value": whole_job_value(w.flops * ne, world, e2e_t), "unit": unit,
            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
     peaks, peak_src = load_peaks()
-    path_id = plan.path
+    path_id = r.path
     tensor_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     # kernels launched by one PIPELINED run: the fused kernel (fp16); the widening
     # kernel and the fused kernel (int8); the skinny and the finish kernel (skinny)
     launches_per_run = 1 if path_id == B_.PATH_FUSED_F16 else 2
-    traffic = profiled_traffic(w.wid, path_id)
-    # device time of one run (events around each run): the dominant kernel plus,
-    # for int8, the small kernel that runs with it
-    kernel_ms = float(np.mean(times_ms))
-    if path_id == B_.PATH_SKINNY_I8:
-        # bound by HBM: algorithmic bytes of one run = B once, the gathered rows
-        # once, the remote shards copied (read + write), bias, scale, C_i32, D
-        algo = (w.K * w.N + w.M * w.K + 2 * (w.S - 1) * w.R * w.K + 8 * w.N
-                + 6 * w.M * w.N)
-        peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-        achieved = algo / (kernel_ms * 1e-3) * 1e-9
-        roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                    "frac": achieved / peak, "traffic": traffic, "algorithmic_bytes": algo,
-                    "peak_source": f"{peak_src} HBM copy bandwidth",
-                    "kernel": "ag_skinny_kernel + ag_skinny_finish_kernel (one run)"}
-    else:
-        # a dense fp16 contraction: its peak is the measured dense bf16 figure
-        # (fp16 and bf16 share the same nominal dense rate): the burst figure,
-        # or the sustained one (cuBLAS back to back under the power cap) when
-        # the clock samples of this timed region saw sw_power_cap
-        capped = bool(clk) and "sw_power_cap" in (clk.get("reasons") or [])
-        key = "bf16_tflops_sustained" if capped else "bf16_tflops"
-        peak = float(peaks.get(key, FALLBACK_PEAKS[key]))
-        achieved = w.flops / (kernel_ms * 1e-3) * 1e-12
-        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak, "traffic": traffic,
-                    "peak_source": f"{peak_src} bf16 dense "
-                                   + ("sustained (the timed region ran under sw_power_cap)"
-                                      if capped else "burst")
-                                   + " (fp16 dense = bf16 dense nominal)",
-                    "kernel": "ag_fused_kernel" + ("<int8> + widen_kernel (one run)" if int8
-                                                   else "<fp16>")}
+    roofline = roofline_of(w, path_id, float(np.mean(times_ms)), clk, peaks, peak_src)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        v, rows, el = time_oracle(w, x, budget_s=args.cpu_seconds)
+        v, rows, el = time_oracle(w, r.x, budget_s=args.cpu_seconds)
         cpu = {"value": v, "unit": unit, "cores": 1, "kind": "oracle",
                "sample": f"{rows} whole rows of C ({rows * w.N} outputs), {el:.1f} s",
                "cpu": cpu_model()}
@@ -525,8 +642,18 @@ def run_ours(args, w, rank, world, local_rank):
             cpu["all_cores"] = {"value": pv, "unit": unit, "cores": pcores,
                                 "sample": f"{prow} whole rows of C over {pcores} processes "
                                           f"(one per core, spawn), {pwall:.1f} s wall"}
+    geometry = r.geometry
+    r.close()
+    del r
 
-    plan.close()
+    # the other workloads of the suite, measured in the same call (rank 0 reports)
+    extras = {}
+    for wid in (args.extra_workloads if world == 1 else []):
+        if wid == w.wid:
+            continue
+        extras[str(wid)] = measure_extra(torch, synth.WORKLOADS[wid], dev, args, flush_fn,
+                                         peaks, peak_src)
+
     if rank != 0:
         return 0
     line = {
@@ -539,7 +666,7 @@ def run_ours(args, w, rank, world, local_rank):
         "pct_of_peak": 100.0 * value / world / tensor_peak,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
         "gpu_launches": launches_per_run * args.steps, "modes": modes,
-        "grid": geometry,
+        "enqueue": gate, "grid": geometry, "workloads": extras,
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -551,7 +678,10 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=None,
                     help="timed steps (default: enough for ~2 s of timed GPU work, >= 20)")
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", type=int, default=2, choices=list(range(1, 10)))
+    ap.add_argument("--workload", type=int, default=4, choices=list(range(1, 10)))
+    ap.add_argument("--extra-workloads", default="2,3,5",
+                    help="comma-separated workloads measured after the headline one in the same "
+                         "call and reported under 'workloads' ('' for none)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-step-seconds", type=float, default=4.0)
@@ -560,6 +690,10 @@ def main(argv=None):
     ap.add_argument("--no-flush", action="store_true",
                     help="analysis only: keep inputs L2-resident between timed steps")
     args = ap.parse_args(argv)
+    args.extra_workloads = [int(s) for s in args.extra_workloads.split(",") if s.strip()]
+    for wid in args.extra_workloads:
+        if wid not in range(1, 10):
+            ap.error(f"unknown workload {wid} in --extra-workloads")
 
     from all_gather_gemm_chunked_gb300 import synth
     w = synth.WORKLOADS[args.workload]

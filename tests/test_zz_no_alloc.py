@@ -7,7 +7,10 @@ device) are not allowed.  Its staging workspace, counters and status word live
 in a fixed array inside the library, shared by every call.  These tests call it
 through the C ABI and require its C to match ag_gemm_run's within the fp16
 tolerance used by the other GPU tests, on two calls in a row with different
-inputs (the second call starts from the first call's leftovers in the array).
+inputs (the second call starts from the first call's leftovers in the array), and
+compare the small cases with the CPU oracle as well.  A further test checks that
+a call allocates nothing: the device's free memory is the same before and after
+a second call on buffers that already exist.
 """
 import numpy as np
 import pytest
@@ -58,7 +61,7 @@ def _noalloc_result(x, S, R, K, N, c):
     (3, 200, 328, 392, 0),    # ragged tiles, K and N tails
     (2, 2048, 4096, 4096, 0), # the 2 x 2048-row, K = N = 4096 workload (16 MiB of staging)
 ])
-def test_noalloc_matches_plan_on_two_calls_in_a_row(S, R, K, N, c):
+def test_noalloc_matches_plan_on_two_calls_in_a_row(S, R, K, N, c, oracle):
     x1 = synth.make_inputs(S, R, K, N, "f16", 4100 + S + K)
     x2 = synth.make_inputs(S, R, K, N, "f16", 4200 + S + K)
     ref1 = _plan_result(x1, S, R, K, N, c)
@@ -67,6 +70,36 @@ def test_noalloc_matches_plan_on_two_calls_in_a_row(S, R, K, N, c):
     got2 = _noalloc_result(x2, S, R, K, N, c)
     check_f16(got1, ref1, K, "first no-allocation call vs ag_gemm_run")
     check_f16(got2, ref2, K, "second no-allocation call vs ag_gemm_run")
+    if S * R * K * N <= 64 * 1024 * 1024:
+        # small enough for the fp64 CPU oracle: the same tolerance against it
+        check_f16(got1, oracle.ag_gemm_f16(x1["shards"], x1["B"]), K,
+                  "first no-allocation call vs the oracle")
+        check_f16(got2, oracle.ag_gemm_f16(x2["shards"], x2["B"]), K,
+                  "second no-allocation call vs the oracle")
+
+
+def test_noalloc_call_allocates_no_device_memory():
+    S, R, K, N = 2, 512, 1024, 512
+    x = synth.make_inputs(S, R, K, N, "f16", 4300)
+    shards = [_dev(s) for s in x["shards"]]
+    Bd = _dev(x["B"])
+    C = torch.empty((S * R, N), dtype=torch.float32, device=DEV)
+    status = torch.zeros((2,), dtype=torch.int32, device=DEV)
+    stream = torch.cuda.current_stream().cuda_stream
+    ptrs = [s.data_ptr() for s in shards]
+
+    def call():
+        B_.ag_gemm_run_noalloc(S, S * R, K, N, 0, ptrs, Bd.data_ptr(), C.data_ptr(),
+                               status.data_ptr(), stream)
+        torch.cuda.synchronize()
+
+    call()  # the first call on the device looks up the array (and may load the module)
+    free_before, _ = torch.cuda.mem_get_info(DEV)
+    call()
+    free_after, _ = torch.cuda.mem_get_info(DEV)
+    assert status.cpu().tolist() == [0, 0]
+    assert free_after == free_before, (
+        f"device free memory changed across a no-allocation call: {free_before} -> {free_after}")
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
