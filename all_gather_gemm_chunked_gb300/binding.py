@@ -21,6 +21,9 @@ F16, I8, BF16 = 0, 1, 2
 MODE_PIPELINED, MODE_COMPUTE_ONLY, MODE_SEQUENTIAL, MODE_COPY_ONLY = 0, 1, 2, 3
 DEBUG_POISON_STAGING, DEBUG_SKIP_ITEM, DEBUG_DELAY_NS = 1, 2, 4
 PATH_FUSED_F16, PATH_FUSED_I8, PATH_SKINNY_I8 = 0, 1, 2
+(TRACE_CTA_START, TRACE_CTA_END, TRACE_LANDED, TRACE_WAIT_START, TRACE_WAIT_END, TRACE_TILE_DONE,
+ TRACE_UNIT_ISSUED, TRACE_UNIT_LANDED, TRACE_KB_WIDENED, TRACE_KB_MMA,
+ TRACE_PIECE_DONE) = range(1, 12)
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_OOM, ERR_TIMEOUT, ERR_STATE = 0, -1, -2, -3, -4, -5, -6
 ERROR_NAMES = {ERR_INVALID: "INVALID", ERR_UNSUPPORTED: "UNSUPPORTED", ERR_CUDA: "CUDA",
                ERR_OOM: "OOM", ERR_TIMEOUT: "TIMEOUT", ERR_STATE: "STATE"}
@@ -51,6 +54,12 @@ class Geometry(ctypes.Structure):
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class TraceEvent(ctypes.Structure):
+    """ag_gemm_trace_event."""
+    _fields_ = [("t_ns", ctypes.c_uint64), ("kind", ctypes.c_uint32), ("cta", ctypes.c_uint32),
+                ("warp", ctypes.c_uint32), ("id", ctypes.c_uint32), ("aux", ctypes.c_uint64)]
 
 
 def _load():
@@ -86,6 +95,8 @@ def _load():
         "ag_gemm_plan_grid": (i32, [vp]),
         "ag_gemm_plan_path": (i32, [vp]),
         "ag_gemm_run_noalloc": (i32, [i32, i64, i64, i64, i64, ctypes.POINTER(vp), vp, vp, vp, vp]),
+        "ag_gemm_plan_set_trace": (i32, [vp, i64]),
+        "ag_gemm_plan_trace": (i64, [vp, ctypes.POINTER(TraceEvent), i64]),
         "ag_gemm_last_error": (i32, []),
         "ag_gemm_last_error_message": (ctypes.c_char_p, []),
     }
@@ -245,6 +256,22 @@ def ag_gemm_run_noalloc(n_shards, M, K, N, chunk_rows, shard_ptrs, B: int, C: in
     p, _keep = _ptrs(shard_ptrs)
     return _check(_lib.ag_gemm_run_noalloc(n_shards, M, K, N, chunk_rows, p, B, C,
                                            status_out or None, stream))
+
+
+def ag_gemm_plan_set_trace(plan: int, capacity: int) -> int:
+    return _check(_lib.ag_gemm_plan_set_trace(plan, capacity))
+
+
+def ag_gemm_plan_trace(plan: int, max_events: int):
+    """(events recorded by the last run, numpy structured array of the kept ones)."""
+    import numpy as np
+    buf = (TraceEvent * max(max_events, 1))()
+    n = _check(_lib.ag_gemm_plan_trace(plan, buf, max_events))
+    kept = min(n, max_events)
+    dt = np.dtype([("t_ns", "<u8"), ("kind", "<u4"), ("cta", "<u4"), ("warp", "<u4"),
+                   ("id", "<u4"), ("aux", "<u8")])
+    arr = np.frombuffer(bytes(buf), dtype=dt, count=kept).copy()
+    return n, arr
 
 
 def ag_gemm_last_error() -> int:

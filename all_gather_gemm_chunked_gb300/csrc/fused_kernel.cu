@@ -127,7 +127,7 @@ __device__ bool wait_slot(const FusedParams& p, int64_t slot, uint32_t target, i
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
-template <bool kI8>
+template <bool kI8, bool kTrace>
 __device__ void copy_warp(const FusedParams& p, int lane) {
   const Geometry& g = p.g;
   // With bounded staging and the GEMM in the same launch, a block may only
@@ -175,7 +175,11 @@ __device__ void copy_warp(const FusedParams& p, int lane) {
       warp_copy16(src + v0, dst + v0, v1 - v0, lane);
     __threadfence();
     __syncwarp();
-    if (lane == 0) red_release_gpu_add(p.counters + (int64_t)(pos - 1) * g.Q + q, 1u);
+    if (lane == 0) {
+      const int64_t ci = (int64_t)(pos - 1) * g.Q + q;
+      if constexpr (kTrace) trace_emit(p.trace, kTrLanded, static_cast<uint32_t>(ci), i);
+      red_release_gpu_add(p.counters + ci, 1u);
+    }
   }
 }
 
@@ -216,7 +220,7 @@ __device__ bool wait_chunks(const FusedParams& p, int pos, int64_t row0, int lan
   return ok;
 }
 
-template <bool kI8>
+template <bool kI8, bool kTrace>
 __device__ void tma_warp(const FusedParams& p, uint32_t rank, uint8_t* sA, uint8_t* sB,
                          uint64_t* full, uint64_t* empty, int lane, volatile int* abort) {
   const Geometry& g = p.g;
@@ -239,7 +243,18 @@ __device__ void tma_warp(const FusedParams& p, uint32_t rank, uint8_t* sA, uint8
     int64_t mt, nt;
     tile_coords(g, t, pos, mt, nt);
     const int64_t row0 = mt * kPairM + rank * kBlockM;
-    if (pos > 0 && wait && !wait_chunks(p, pos, row0, lane, abort)) break;
+    if constexpr (kTrace) {
+      int64_t q0 = 0, q1 = -1;
+      const bool rows = pos > 0 && wait && rows_chunks(g, row0, q0, q1);
+      const uint64_t aux = (static_cast<uint64_t>(pos) << 48) |
+                           (static_cast<uint64_t>(q0 & 0xFFFFFF) << 24) |
+                           static_cast<uint64_t>(q1 & 0xFFFFFF);
+      if (rows && lane == 0) trace_emit(p.trace, kTrWaitStart, static_cast<uint32_t>(t), aux);
+      if (pos > 0 && wait && !wait_chunks(p, pos, row0, lane, abort)) break;
+      if (rows && lane == 0) trace_emit(p.trace, kTrWaitEnd, static_cast<uint32_t>(t), aux);
+    } else {
+      if (pos > 0 && wait && !wait_chunks(p, pos, row0, lane, abort)) break;
+    }
     if (lane == 0) {
       if (pos > 0) {
         fence_acq_rel_gpu();
@@ -386,7 +401,7 @@ __device__ __forceinline__ void st_v4(void* ptr, uint32_t a, uint32_t b, uint32_
                : "memory");
 }
 
-template <bool kI8>
+template <bool kI8, bool kTrace>
 __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int half, int lane,
                               uint64_t* tfull, uint64_t* tempty, uint32_t tmem, uint8_t* sEpi,
                               volatile int* abort) {
@@ -525,13 +540,16 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
       }
       ++unit;
     }
+    if constexpr (kTrace)
+      if (quad == 0 && half == 0 && lane == 0)
+        trace_emit(p.trace, kTrTileDone, static_cast<uint32_t>(t), 0);
   }
   if (lane == 0) bulk_wait_group_all();  // every C store performed before the CTA exits
   __syncwarp();
 }
 
 // ------------------------------------------------------------------ kernel
-template <bool kI8>
+template <bool kI8, bool kTrace>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ag_fused_kernel(const __grid_constant__ FusedParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -576,17 +594,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  if constexpr (kTrace)
+    if (threadIdx.x == 0) trace_emit(p.trace, kTrCtaStart, 0, 0);
   if (warp == 0) {
-    if (gemm) tma_warp<kI8>(p, rank, sA, sB, full, empty, lane, abort);
+    if (gemm) tma_warp<kI8, kTrace>(p, rank, sA, sB, full, empty, lane, abort);
   } else if (warp == 1) {
     if (gemm && rank == 0 && lane == 0)
       mma_warp<kI8>(p, sA, sB, full, empty, tfull, tempty, tmem, abort);
   } else if (warp < 2 + kCopyWarpsPerCta) {
-    if (p.flags & kFlagCopy) copy_warp<kI8>(p, lane);
+    if (p.flags & kFlagCopy) copy_warp<kI8, kTrace>(p, lane);
   } else {
     if (gemm)
-      epilogue_warp<kI8>(p, rank, warp & 3, (warp - 4) >> 2, lane, tfull, tempty, tmem, sEpi,
-                         abort);
+      epilogue_warp<kI8, kTrace>(p, rank, warp & 3, (warp - 4) >> 2, lane, tfull, tempty, tmem,
+                                 sEpi, abort);
   }
 
   tc_fence_before();
@@ -610,6 +630,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc_pair(tmem, 512);
   }
+  if constexpr (kTrace)
+    if (threadIdx.x == 0) trace_emit(p.trace, kTrCtaEnd, 0, 0);
 }
 
 // ------------------------------------------------------------------ int8 widening
@@ -634,14 +656,20 @@ __global__ void __launch_bounds__(256) widen_kernel(const uint4* __restrict__ s0
 }
 
 // ------------------------------------------------------------------ launchers
-static const void* fused_fn(int dtype) {
-  return dtype == 1 ? reinterpret_cast<const void*>(&ag_fused_kernel<true>)
-                    : reinterpret_cast<const void*>(&ag_fused_kernel<false>);
+static const void* fused_fn(int dtype, bool trace) {
+  if (trace)
+    return dtype == 1 ? reinterpret_cast<const void*>(&ag_fused_kernel<true, true>)
+                      : reinterpret_cast<const void*>(&ag_fused_kernel<false, true>);
+  return dtype == 1 ? reinterpret_cast<const void*>(&ag_fused_kernel<true, false>)
+                    : reinterpret_cast<const void*>(&ag_fused_kernel<false, false>);
 }
 
 cudaError_t fused_max_clusters(int dtype, int grid, int* clusters) {
-  const void* fn = fused_fn(dtype);
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(fused_fn(dtype, true),
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const void* fn = fused_fn(dtype, false);
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -656,8 +684,12 @@ cudaError_t launch_fused(const FusedParams& p, int grid, cudaStream_t stream) {
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
-  if (p.g.dtype == 1) return cudaLaunchKernelEx(&cfg, ag_fused_kernel<true>, p);
-  return cudaLaunchKernelEx(&cfg, ag_fused_kernel<false>, p);
+  if (p.trace.count) {
+    if (p.g.dtype == 1) return cudaLaunchKernelEx(&cfg, ag_fused_kernel<true, true>, p);
+    return cudaLaunchKernelEx(&cfg, ag_fused_kernel<false, true>, p);
+  }
+  if (p.g.dtype == 1) return cudaLaunchKernelEx(&cfg, ag_fused_kernel<true, false>, p);
+  return cudaLaunchKernelEx(&cfg, ag_fused_kernel<false, false>, p);
 }
 
 cudaError_t launch_widen(const int8_t* src0, uint16_t* dst0, int64_t n0, const int8_t* src1,

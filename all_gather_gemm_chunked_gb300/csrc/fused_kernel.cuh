@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include "schedule.h"
+#include "trace.cuh"
 
 namespace agg {
 
@@ -57,6 +58,7 @@ struct FusedParams {
   int window;                   // slots of 256 rows; 0 = every remote row has its own place
   uint32_t* credits;            // [window] tiles done reading the slot, monotonic
   uint32_t credit_epoch;        // pipelined runs of this plan since the last reset (>= 1)
+  TraceBuf trace;               // event trace (count == nullptr: off)
 };
 
 constexpr int kThreads = 384;                         // 12 warps
@@ -81,7 +83,7 @@ struct SkinnyParams {
   Geometry g;
   const void* src[kMaxShards];  // shard pointers by consumption position
   int8_t* staging;              // int8 [S-1][R][K]
-  uint32_t* counters;           // [(S-1)][Q] ready counters, monotonic
+  uint32_t* counters;           // [np][S-1][Q] ready counters, one release per task, monotonic
   unsigned long long* item_counter;
   unsigned long long item_base;
   int32_t* ws;                  // [n_tiles][cmax][M][256] int32 piece sums
@@ -100,9 +102,10 @@ struct SkinnyParams {
   int64_t n_tiles;              // ceil(N / 256)
   int64_t kq;                   // 2-k-block units per n-tile: ceil(KB / 2)
   int64_t cmax;                 // workspace slots per n-tile
+  int np;                       // k-parts of the remote rows (copy tasks and counters per chunk)
+  TraceBuf trace;               // event trace (count == nullptr: off)
 };
 constexpr int kSkCopyWarpsPerCta = 2;
-constexpr int kSkCopyParts = 8;   // tickets (and counter releases) per copy item
 
 // Launchers (fused_kernel.cu, skinny_kernel.cu).
 cudaError_t launch_fused(const FusedParams& p, int grid, cudaStream_t stream);

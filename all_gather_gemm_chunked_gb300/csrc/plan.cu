@@ -274,6 +274,10 @@ struct ag_gemm_plan {
   int64_t sk_tiles = 0;          // 256-column n-tiles
   int64_t sk_kq = 0;             // 2-k-block units per n-tile
   int64_t sk_cmax = 0;           // CTAs sharing an n-tile, at most
+  int sk_np = 1;                 // k-parts of the remote rows (copy tasks per chunk)
+  // event trace (ag_gemm_plan_set_trace): [0] count, then the events
+  unsigned long long* trace_buf = nullptr;
+  int64_t trace_cap = 0;
   const void* cached_b8 = nullptr;
   CUtensorMap tm_b8_cached{};
   const void* cached_a8 = nullptr;
@@ -294,6 +298,7 @@ void free_plan(ag_gemm_plan* p) {
   cudaFree(p->a16);
   cudaFree(p->sk_ws);
   cudaFree(p->credits);
+  cudaFree(p->trace_buf);
   if (p->done) cudaEventDestroy(p->done);
   delete p;
 }
@@ -303,8 +308,9 @@ int launch_skinny(ag_gemm_plan* p, agg::SkinnyParams& sp, int flags, cudaStream_
   sp.item_base = p->item_base;
   cudaError_t e = agg::launch_skinny(sp, p->sk_grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "skinny kernel launch");
+  // Each copy warp draws every task's ticket plus one failing ticket.
   if (flags & agg::kFlagCopy)
-    p->item_base += static_cast<unsigned long long>(p->g.items) * agg::kSkCopyParts +
+    p->item_base += static_cast<unsigned long long>((p->g.S - 1) * p->g.Q * p->sk_np) +
                     static_cast<unsigned long long>(p->sk_grid) * agg::kSkCopyWarpsPerCta;
   return AG_GEMM_OK;
 }
@@ -357,9 +363,9 @@ int run_impl(ag_gemm_plan* p, const void* const* shard_ptrs, const void* B, int6
     e = cudaStreamWaitEvent(stream, p->done, 0);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent");
   }
-  // Counters are monotonic: after run e each holds e * P (times the copy parts per
-  // item on the skinny path).  Restart before overflow.
-  const uint64_t releases = static_cast<uint64_t>(g.P) * (p->skinny ? agg::kSkCopyParts : 1);
+  // Counters are monotonic: after run e each holds e * P (e on the skinny path,
+  // whose counters take one release per copy task).  Restart before overflow.
+  const uint64_t releases = p->skinny ? 1u : static_cast<uint64_t>(g.P);
   if (static_cast<uint64_t>(p->epoch + 1) * releases >= (1ull << 31)) {
     e = cudaMemsetAsync(p->counters, 0, sizeof(uint32_t) * p->counter_count, stream);
     if (e != cudaSuccess) return cuda_fail(e, "counter reset");
@@ -419,6 +425,14 @@ int run_impl(ag_gemm_plan* p, const void* const* shard_ptrs, const void* B, int6
   fp.debug_delay_ns = (p->debug_flags & AG_GEMM_DEBUG_DELAY_NS)
                           ? static_cast<uint32_t>(p->debug_arg > 1000000 ? 1000000 : p->debug_arg)
                           : 0u;
+  if (p->trace_buf) {
+    // the run's events replace the previous run's
+    e = cudaMemsetAsync(p->trace_buf, 0, sizeof(unsigned long long), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "trace reset");
+    fp.trace.count = p->trace_buf;
+    fp.trace.ev = reinterpret_cast<agg::TraceEvent*>(p->trace_buf + 4);
+    fp.trace.cap = static_cast<uint32_t>(p->trace_cap);
+  }
 
   const int mode = p->mode;
   const bool runs_gemm = mode != AG_GEMM_MODE_COPY_ONLY;
@@ -483,6 +497,8 @@ int run_impl(ag_gemm_plan* p, const void* const* shard_ptrs, const void* B, int6
     sp.n_tiles = p->sk_tiles;
     sp.kq = p->sk_kq;
     sp.cmax = p->sk_cmax;
+    sp.np = p->sk_np;
+    sp.trace = fp.trace;
     using namespace agg;
     switch (mode) {
       case AG_GEMM_MODE_PIPELINED:
@@ -667,7 +683,14 @@ ag_gemm_plan* create_plan(int n_shards, int64_t M, int64_t K, int64_t N, int dty
   }
   p->staging_bytes = p->window > 0 ? static_cast<int64_t>(p->window) * agg::kPairM * g.K * 2
                                    : slots * g.R * g.K * 2;
-  p->counter_count = slots * g.Q;
+  p->skinny = skinny;
+  if (skinny) {
+    p->sk_tiles = (g.N + 255) / 256;
+    p->sk_kq = (g.KB + 1) / 2;
+    p->sk_np = agg::skinny_parts(g, p->sk_kq);
+  }
+  // one counter per chunk; on the skinny path one per (k-part, chunk)
+  p->counter_count = slots * g.Q * (skinny ? p->sk_np : 1);
   if ((e = cudaMalloc(&p->staging, p->staging_bytes)) != cudaSuccess ||
       (e = cudaMalloc(&p->counters, sizeof(uint32_t) * p->counter_count)) != cudaSuccess ||
       (e = cudaMalloc(&p->item_counter, sizeof(unsigned long long))) != cudaSuccess ||
@@ -683,11 +706,8 @@ ag_gemm_plan* create_plan(int n_shards, int64_t M, int64_t K, int64_t N, int dty
     free_plan(p);
     return nullptr;
   }
-  p->skinny = skinny;
   if (p->skinny) {
-    p->sk_tiles = (g.N + 255) / 256;
     p->sk_grid = p->sm_count;
-    p->sk_kq = (g.KB + 1) / 2;
     p->sk_cmax = agg::skinny_max_sharers(p->sk_tiles, p->sk_kq, p->sk_grid);
     if ((e = agg::skinny_prepare()) != cudaSuccess ||
         (e = cudaMalloc(&p->sk_ws, static_cast<size_t>(p->sk_tiles * p->sk_cmax * g.M * 256 * 4))) !=
@@ -893,6 +913,54 @@ int ag_gemm_plan_set_debug(ag_gemm_plan* plan, int flags, int64_t arg) {
   plan->debug_flags = flags;
   plan->debug_arg = arg;
   return AG_GEMM_OK;
+}
+
+int ag_gemm_plan_set_trace(ag_gemm_plan* plan, int64_t capacity) {
+  if (!plan) return fail(AG_GEMM_ERR_INVALID, "plan is NULL");
+  if (capacity < 0 || capacity > (int64_t{1} << 26))
+    return fail(AG_GEMM_ERR_INVALID, "trace capacity must be in [0, 2^26] events (got %lld)",
+                (long long)capacity);
+  DeviceGuard dg(plan->device);
+  cudaError_t e;
+  // the buffer may still be written by the last run
+  if (plan->has_run && (e = cudaEventSynchronize(plan->done)) != cudaSuccess)
+    return cuda_fail(e, "cudaEventSynchronize");
+  if ((e = cudaFree(plan->trace_buf)) != cudaSuccess) return cuda_fail(e, "cudaFree (trace)");
+  plan->trace_buf = nullptr;
+  plan->trace_cap = 0;
+  if (capacity == 0) return AG_GEMM_OK;
+  static_assert(sizeof(agg::TraceEvent) == sizeof(ag_gemm_trace_event), "trace event layout");
+  void* buf = nullptr;
+  const size_t bytes = 32 + static_cast<size_t>(capacity) * sizeof(agg::TraceEvent);
+  if ((e = cudaMalloc(&buf, bytes)) != cudaSuccess) return cuda_fail(e, "trace allocation");
+  if ((e = cudaMemset(buf, 0, 32)) != cudaSuccess) {
+    cudaFree(buf);
+    return cuda_fail(e, "trace allocation");
+  }
+  plan->trace_buf = static_cast<unsigned long long*>(buf);
+  plan->trace_cap = capacity;
+  return AG_GEMM_OK;
+}
+
+int64_t ag_gemm_plan_trace(ag_gemm_plan* plan, ag_gemm_trace_event* out, int64_t max_events) {
+  if (!plan) return fail(AG_GEMM_ERR_INVALID, "plan is NULL");
+  if (!plan->trace_buf) return fail(AG_GEMM_ERR_STATE, "tracing is off (ag_gemm_plan_set_trace)");
+  if (max_events < 0 || (max_events > 0 && !out))
+    return fail(AG_GEMM_ERR_INVALID, "out is NULL or max_events < 0");
+  DeviceGuard dg(plan->device);
+  cudaError_t e;
+  if (plan->has_run && (e = cudaEventSynchronize(plan->done)) != cudaSuccess)
+    return cuda_fail(e, "cudaEventSynchronize");
+  unsigned long long count = 0;
+  if ((e = cudaMemcpy(&count, plan->trace_buf, sizeof(count), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "trace read");
+  int64_t n = static_cast<int64_t>(count);
+  if (n > plan->trace_cap) n = plan->trace_cap;
+  if (n > max_events) n = max_events;
+  if (n > 0 && (e = cudaMemcpy(out, plan->trace_buf + 4, static_cast<size_t>(n) * sizeof(agg::TraceEvent),
+                               cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "trace read");
+  return static_cast<int64_t>(count);
 }
 
 int ag_gemm_last_error(void) { return g_last_error; }

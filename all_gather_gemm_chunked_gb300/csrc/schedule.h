@@ -157,6 +157,38 @@ AGG_HD void skinny_cta_range(int64_t U, int64_t b, int64_t G, int64_t& lo, int64
 AGG_HD int64_t skinny_owner(int64_t x, int64_t U, int64_t G) {
   return ((x + 1) * G + U - 1) / U - 1;
 }
+// Skinny int8 path, streamed gather: every unit reads all gathered rows, but
+// only 128 k of them, so the remote rows are copied and released in k-parts
+// and a unit waits only for the part that holds its k-slice.  np parts split
+// the KQ units of an n-tile: part j covers units [KQ j / np, KQ (j + 1) / np)
+// (k in [128 KQ j / np, 128 KQ (j + 1) / np), clipped at K).  A copy task is
+// (part j, consumption position pos >= 1, chunk q): the c rows of the chunk
+// over the part's k-range, released on counter (j (S - 1) + pos - 1) Q + q.
+// Tasks are numbered part-major, then by position, then by chunk.
+AGG_HD int skinny_parts(const Geometry& g, int64_t KQ) {
+  int64_t np = ceil_div(g.c * g.K, 2048);  // ~2 KB of source per task
+  if (np > 32) np = 32;
+  if (np > KQ) np = KQ;
+  return np < 1 ? 1 : static_cast<int>(np);
+}
+AGG_HD int skinny_part_of(int64_t qu, int64_t KQ, int np) {
+  return static_cast<int>(((qu + 1) * np + KQ - 1) / KQ - 1);
+}
+AGG_HD void skinny_task(const Geometry& g, int64_t KQ, int np, int64_t t, int& j, int& pos,
+                        int64_t& q, int64_t& k0, int64_t& k1) {
+  const int64_t per_part = (int64_t)(g.S - 1) * g.Q;
+  j = static_cast<int>(t / per_part);
+  const int64_t r = t - (int64_t)j * per_part;
+  pos = 1 + static_cast<int>(r / g.Q);
+  q = r - (int64_t)(pos - 1) * g.Q;
+  k0 = 128 * (KQ * j / np);
+  k1 = 128 * (KQ * (j + 1) / np);
+  if (k1 > g.K) k1 = g.K;
+}
+AGG_HD int64_t skinny_counter(const Geometry& g, int j, int pos, int64_t q) {
+  return ((int64_t)j * (g.S - 1) + (pos - 1)) * g.Q + q;
+}
+
 // Most CTAs that share one n-tile of KQ units: the workspace slots per n-tile.
 inline int64_t skinny_max_sharers(int64_t n_tiles, int64_t KQ, int64_t G) {
   const int64_t U = n_tiles * KQ;

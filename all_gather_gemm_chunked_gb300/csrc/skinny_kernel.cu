@@ -43,11 +43,12 @@
 //   warp 0                 MMA: one thread issues tcgen05.mma (M = 64 or 128,
 //                          N = 256, K = 16).
 //   warp 4                 TMA: streams the CTA's units (two B boxes + row
-//                          boxes) into a raw ring; the B boxes of the first
-//                          stages go out before the warp waits once for every
-//                          remote chunk.
-//   warps 8, 12            copy: remote chunks, in 1/8-piece parts, into the
-//                          int8 staging workspace; release their ready counters.
+//                          boxes) into a raw ring; B and the local rows go out
+//                          at once, the staged rows once the unit's k-part of
+//                          every remote chunk has landed.
+//   warps 8, 12            copy: remote chunks, one k-part at a time, into the
+//                          int8 staging workspace; one ready counter per
+//                          (k-part, chunk).
 //   warps 16, 1, 2, 3      epilogue: fold fp32 segments into the int32 sums in
 //                          TMEM; store each finished piece to its workspace slot.
 //   warps 5-7, 9-11, 13,14 B widening: raw int8 B -> fp16 in the MN-major
@@ -158,58 +159,72 @@ __device__ __forceinline__ void piece_at(const Geometry& g, int64_t KQ, int64_t 
 }
 
 // ------------------------------------------------------------------ copy warps
-// Copy item i (a piece of a chunk) is split into kSkCopyParts parts, one
-// ticket each; the chunk's counter gets one release per part.
+// Copy task t = (k-part j, position pos, chunk q): the chunk's c rows over the
+// part's k-range, from the source shard into the int8 staging, then one
+// release of the task's own counter.  Tasks are taken from a grid-wide ticket
+// counter in part-major order.
+template <bool kTrace>
 __device__ void sk_copy_warp(const SkinnyParams& p, int lane) {
   const Geometry& g = p.g;
-  const int64_t parts = g.items * kSkCopyParts;
+  const int64_t tasks = (int64_t)(g.S - 1) * g.Q * p.np;
   for (;;) {
     unsigned long long ticket = 0;
     if (lane == 0) ticket = atomicAdd(p.item_counter, 1ull);
     ticket = __shfl_sync(0xffffffffu, ticket, 0);
     const int64_t t = static_cast<int64_t>(ticket - p.item_base);
-    if (t >= parts) break;
-    const int64_t i = t / kSkCopyParts;
-    const int part = static_cast<int>(t - i * kSkCopyParts);
-    int pos, piece;
-    int64_t q, v0, v1;
-    item_coords(g, i, pos, q, piece, v0, v1);
-    if (i == p.debug_skip_item) continue;
-    if (p.debug_delay_ns) __nanosleep(p.debug_delay_ns);
-    const int64_t w0 = v0 + (v1 - v0) * part / kSkCopyParts;
-    const int64_t w1 = v0 + (v1 - v0) * (part + 1) / kSkCopyParts;
-    const uint4* src =
-        reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.src[pos]) + q * g.c * g.K);
-    uint4* dst = reinterpret_cast<uint4*>(p.staging + ((int64_t)(pos - 1) * g.R + q * g.c) * g.K);
-    // 8 independent 16-byte loads in flight per lane
-    int64_t v = w0 + lane;
-    for (; v + 7 * 32 < w1; v += 8 * 32) {
-      uint4 x[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) x[u] = ld_nc_v4(src + v + u * 32);
-#pragma unroll
-      for (int u = 0; u < 8; ++u) dst[v + u * 32] = x[u];
+    if (t >= tasks) break;  // exactly one failing ticket per copy warp and run
+    if (t < 0) {
+      // tickets behind this run's base: the counters were not reset after a
+      // failed run; copy nothing (the readers time out and report it)
+      if (lane == 0) sk_set_status(p.status, kStatusChunkTimeout, 0xFFFFFFu);
+      break;
     }
-    for (; v < w1; v += 32) dst[v] = ld_nc_v4(src + v);
+    int j, pos;
+    int64_t q, k0, k1;
+    skinny_task(g, p.kq, p.np, t, j, pos, q, k0, k1);
+    if (t == p.debug_skip_item) continue;  // failure injection: this part never lands
+    if (p.debug_delay_ns) __nanosleep(p.debug_delay_ns);
+    const int64_t n = (k1 - k0) / 16;  // 16-byte vectors of one row
+    for (int64_t r = q * g.c; r < (q + 1) * g.c; ++r) {
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.src[pos]) +
+                                                        r * g.K + k0);
+      uint4* dst = reinterpret_cast<uint4*>(p.staging + ((int64_t)(pos - 1) * g.R + r) * g.K + k0);
+      // 8 independent 16-byte loads in flight per lane
+      int64_t v = lane;
+      for (; v + 7 * 32 < n; v += 8 * 32) {
+        uint4 x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) x[u] = ld_nc_v4(src + v + u * 32);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) dst[v + u * 32] = x[u];
+      }
+      for (; v < n; v += 32) dst[v] = ld_nc_v4(src + v);
+    }
     __threadfence();
     __syncwarp();
-    if (lane == 0) red_release_gpu_add(p.counters + (int64_t)(pos - 1) * g.Q + q, 1u);
+    if (lane == 0) {
+      const int64_t ci = skinny_counter(g, j, pos, q);
+      if constexpr (kTrace) trace_emit(p.trace, kTrLanded, static_cast<uint32_t>(ci), t);
+      red_release_gpu_add(p.counters + ci, 1u);
+    }
   }
 }
 
-// Every lane acquires a share of the ready counters; true once all chunks of
-// this epoch have landed (false on timeout / abort, with the status set).
-__device__ bool sk_wait_all_chunks(const SkinnyParams& p, int lane, volatile int* abort) {
+// All lanes acquire the counters of part j (every remote chunk's slice of the
+// part's k-range); true once all have landed in this epoch (false on timeout
+// or abort, with the status set).
+__device__ bool sk_wait_part(const SkinnyParams& p, int j, int lane, volatile int* abort) {
   const Geometry& g = p.g;
-  const int64_t total = (int64_t)(g.S - 1) * g.Q;
-  const uint32_t target = p.epoch * static_cast<uint32_t>(g.P * kSkCopyParts);
+  const int64_t per_part = (int64_t)(g.S - 1) * g.Q;
+  const uint32_t* cnt = p.counters + (int64_t)j * per_part;
+  const uint32_t target = p.epoch;
   bool ok = true;
-  for (int64_t q = lane; q < total && ok; q += 32) {
-    if (ld_acquire_gpu(p.counters + q) >= target) continue;
+  for (int64_t q = lane; q < per_part && ok; q += 32) {
+    if (ld_acquire_gpu(cnt + q) >= target) continue;
     const uint64_t deadline = globaltimer_ns() + p.timeout_ns;
     uint32_t spins = 0;
-    while (ld_acquire_gpu(p.counters + q) < target) {
-      __nanosleep(256);
+    while (ld_acquire_gpu(cnt + q) < target) {
+      __nanosleep(64);
       if (++spins == 16) {
         spins = 0;
         if (*abort || *reinterpret_cast<volatile uint32_t*>(p.status) != 0u ||
@@ -222,7 +237,7 @@ __device__ bool sk_wait_all_chunks(const SkinnyParams& p, int lane, volatile int
   }
   ok = __all_sync(0xffffffffu, ok);
   if (!ok && lane == 0) {
-    sk_set_status(p.status, kStatusChunkTimeout, 0x10000u);
+    sk_set_status(p.status, kStatusChunkTimeout, 0x10000u | static_cast<uint32_t>(j));
     *abort = 1;
   }
   __syncwarp();
@@ -239,13 +254,14 @@ __device__ __forceinline__ void sk_issue_b(const SkinnyParams& p, uint8_t* st, u
   tma_load_2d(st, &p.tm_b8, bar, static_cast<int32_t>(nt * kSkN), y);
   tma_load_2d(st + kSkBoxB, &p.tm_b8, bar, static_cast<int32_t>(nt * kSkN + kSkHalf), y);
 }
-__device__ __forceinline__ void sk_issue_rows(const SkinnyParams& p, uint8_t* a, uint64_t* bar,
-                                              int64_t q) {
-  const int32_t x = static_cast<int32_t>(q * kSkARow);
-  tma_load_2d(a, &p.tm_a8_local, bar, x, 0);
-  if (p.g.S > 1) tma_load_3d(a + p.g.R * kSkARow, &p.tm_a8_stage, bar, x, 0, 0);
-}
 
+// The streamed gather: for each unit, B and the local shard's rows go out at
+// once (no wait: the local row group comes first, "AllGather + GEMM 通算融合
+// 算子示例", 流式流水线); the staged rows of the other shards go out as soon as
+// the k-part the unit reads has landed for every remote chunk, which the
+// warp's 32 lanes check together on the part's ready counters.  A part that
+// has been checked once stays checked for the rest of the run.
+template <bool kTrace>
 __device__ void sk_tma_warp(const SkinnyParams& p, uint8_t* sRaw, const SkLayout& L,
                             uint64_t* raw_full, uint64_t* raw_empty, int lane,
                             volatile int* abort) {
@@ -254,59 +270,74 @@ __device__ void sk_tma_warp(const SkinnyParams& p, uint8_t* sRaw, const SkLayout
   const int64_t KQ = p.kq;
   int64_t u0, u1;
   skinny_cta_range(p.n_tiles * KQ, blockIdx.x, gridDim.x, u0, u1);
-  const int64_t n = u1 - u0;
-  const int head = static_cast<int>(n < L.n_raw ? n : L.n_raw);
   const uint32_t tx = static_cast<uint32_t>(kSkRawB + g.M * kSkARow);
+  const bool remote = g.S > 1;
+  const bool wait = remote && (p.flags & kFlagWait) != 0;
   if (lane == 0) {
     tma_prefetch_desc(&p.tm_b8);
     tma_prefetch_desc(&p.tm_a8_local);
-    if (g.S > 1) tma_prefetch_desc(&p.tm_a8_stage);
-    // B of the first stages before the remote rows are known to have landed
-    for (int i = 0; i < head; ++i) {
-      const int64_t u = u0 + i, nt = u / KQ;
-      mbar_arrive_expect_tx(&raw_full[i], tx);
-      sk_issue_b(p, sRaw + i * L.raw_stage, &raw_full[i], nt, u - nt * KQ);
-    }
+    if (remote) tma_prefetch_desc(&p.tm_a8_stage);
   }
-  __syncwarp();
-  const bool ok0 = !((p.flags & kFlagWait) && g.S > 1) || sk_wait_all_chunks(p, lane, abort);
-  if (lane != 0) return;
-  bool ok = ok0;
-  if (ok && g.S > 1) {
-    // the staged rows were written by other SMs' generic stores; TMA reads them
-    fence_acq_rel_gpu();
-    fence_proxy_async_global();
-  }
-  uint32_t issued = (1u << head) - 1u, issued_phase = 0;
-  if (ok)
-    for (int i = 0; i < head; ++i)
-      sk_issue_rows(p, sRaw + i * L.raw_stage + kSkRawB, &raw_full[i], (u0 + i) % KQ);
+  uint32_t ready = 0;                       // bit j: part j checked in this run
+  uint32_t issued = 0, issued_phase = 0;    // bit s: stage s used / parity of its last use
+  bool ok = true, wait_failed = false;
   Ring r(L.n_raw);
-  for (int i = 0; i < head; ++i) r.next();
-  for (int64_t u = u0 + head; u < u1 && ok; ++u, r.next()) {
-    if (!mbar_wait(&raw_empty[r.s], r.ph ^ 1u, p.pipe_timeout_ns, abort, gstatus)) {
-      ok = false;
-      break;
-    }
+  int64_t i = 0;
+  for (int64_t u = u0; u < u1; ++u, ++i, r.next()) {
     const int64_t nt = u / KQ, q = u - nt * KQ;
     uint8_t* st = sRaw + r.s * L.raw_stage;
-    mbar_arrive_expect_tx(&raw_full[r.s], tx);
-    sk_issue_b(p, st, &raw_full[r.s], nt, q);
-    sk_issue_rows(p, st + kSkRawB, &raw_full[r.s], q);
-    issued |= 1u << r.s;
-    issued_phase = (issued_phase & ~(1u << r.s)) | (r.ph << r.s);
+    const int32_t x = static_cast<int32_t>(q * kSkARow);
+    if (lane == 0) {
+      if (i >= L.n_raw &&
+          !mbar_wait(&raw_empty[r.s], r.ph ^ 1u, p.pipe_timeout_ns, abort, gstatus))
+        ok = false;
+      if (ok) {
+        mbar_arrive_expect_tx(&raw_full[r.s], tx);
+        sk_issue_b(p, st, &raw_full[r.s], nt, q);
+        tma_load_2d(st + kSkRawB, &p.tm_a8_local, &raw_full[r.s], x, 0);
+        issued |= 1u << r.s;
+        issued_phase = (issued_phase & ~(1u << r.s)) | (r.ph << r.s);
+      }
+    }
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    if (!ok) break;
+    if (remote) {
+      const int j = skinny_part_of(q, KQ, p.np);
+      if (wait && !((ready >> j) & 1u)) {
+        if constexpr (kTrace)
+          if (lane == 0) trace_emit(p.trace, kTrWaitStart, static_cast<uint32_t>(u), j);
+        if (!sk_wait_part(p, j, lane, abort)) {
+          ok = false;
+          wait_failed = true;
+          break;
+        }
+        if constexpr (kTrace)
+          if (lane == 0) trace_emit(p.trace, kTrWaitEnd, static_cast<uint32_t>(u), j);
+        ready |= 1u << j;
+        if (lane == 0) {
+          // the staged rows were written by other SMs' generic stores; TMA reads them
+          fence_acq_rel_gpu();
+          fence_proxy_async_global();
+        }
+      }
+      if (lane == 0)
+        tma_load_3d(st + kSkRawB + g.R * kSkARow, &p.tm_a8_stage, &raw_full[r.s], x, 0, 0);
+    }
+    if constexpr (kTrace)
+      if (lane == 0) trace_emit(p.trace, kTrUnitIssued, static_cast<uint32_t>(u), 0);
   }
-  if (!ok) {
-    if (ok0) sk_set_status(p.status, kStatusPipelineTimeout, 0x1100u);
+  if (!ok && lane == 0) {
+    if (!wait_failed) sk_set_status(p.status, kStatusPipelineTimeout, 0x1100u);
     *abort = 1;
-    // Loads already issued must land before the CTA exits.  Stages whose rows
-    // were never issued cannot complete; their B boxes land well within the
-    // bounded waits below.
+    // Loads already issued must land before the CTA exits.  A stage whose
+    // staged rows were never issued cannot complete; its B boxes and local
+    // rows land well within the bounded waits below.
     volatile int never = 0;
     for (int s = 0; s < L.n_raw; ++s)
       if (issued & (1u << s))
         mbar_wait(&raw_full[s], (issued_phase >> s) & 1u, 20000000ull, &never);
   }
+  __syncwarp();
 }
 
 // ------------------------------------------------------------------ B widening (8 warps)
@@ -316,6 +347,7 @@ __device__ void sk_tma_warp(const SkinnyParams& p, uint8_t* sRaw, const SkLayout
 // lanes of a shared-memory phase take 8 consecutive k-rows of one quarter qt,
 // so both the swizzled raw reads and the swizzled fp16 writes hit 8 distinct
 // 16-byte bank groups.
+template <bool kTrace>
 __device__ void sk_bwiden(const SkinnyParams& p, const uint8_t* sRaw, const SkLayout& L,
                           uint8_t* sFp, uint64_t* raw_full, uint64_t* raw_empty,
                           uint64_t* fp_full, uint64_t* fp_empty, int t, volatile int* abort) {
@@ -335,6 +367,8 @@ __device__ void sk_bwiden(const SkinnyParams& p, const uint8_t* sRaw, const SkLa
       }
       return;
     }
+    if constexpr (kTrace)
+      if (t == 0) trace_emit(p.trace, kTrUnitLanded, static_cast<uint32_t>(u), 0);
     int64_t kb0, kb1;
     unit_blocks(g, KQ, u, kb0, kb1);
     const uint8_t* raw = sRaw + rr.s * L.raw_stage;
@@ -370,6 +404,8 @@ __device__ void sk_bwiden(const SkinnyParams& p, const uint8_t* sRaw, const SkLa
       fence_proxy_async_shared();
       __syncwarp();
       if (lane == 0) mbar_arrive(&fp_full[fr.s]);
+      if constexpr (kTrace)
+        if (t == 0) trace_emit(p.trace, kTrKbWidened, static_cast<uint32_t>(kb0 + b), u);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&raw_empty[rr.s]);
@@ -438,6 +474,7 @@ __device__ void sk_awiden(const SkinnyParams& p, const uint8_t* sRaw, const SkLa
 // Pieces: maximal runs of this CTA's units inside one n-tile; segments: at most
 // kSegBlocks k-blocks of a piece, accumulated into the fp32 accumulator, which
 // the epilogue folds into the int32 sums before the next segment starts.
+template <bool kTrace>
 __device__ void sk_mma(const SkinnyParams& p, const uint8_t* sFp, const uint8_t* sA,
                        const SkLayout& L, uint64_t* st_full, uint64_t* st_empty,
                        uint64_t* dfull, uint64_t* dempty, uint32_t tmem, volatile int* abort) {
@@ -485,6 +522,8 @@ __device__ void sk_mma(const SkinnyParams& p, const uint8_t* sFp, const uint8_t*
                   bd + static_cast<uint64_t>((k * kUmmaK * 128) >> 4), idesc,
                   (b > 0 || k > 0) ? 1u : 0u);
         mma_commit(&st_empty[kr.s]);
+        if constexpr (kTrace)
+          trace_emit(p.trace, kTrKbMma, static_cast<uint32_t>(s0 + b), static_cast<uint64_t>(nt));
       }
       if (!ok) break;
       mma_commit(dfull);
@@ -503,6 +542,7 @@ __device__ void sk_mma(const SkinnyParams& p, const uint8_t* sFp, const uint8_t*
 // sit on lanes 32q .. 32q + 15 of quadrant q (lanes 32q + 16 .. 32q + 31 are
 // not written by the MMA and their values are never stored).  The kernel runs
 // this one for mm = 128 and sk_epilogue64 below for mm = 64.
+template <bool kTrace>
 __device__ void sk_epilogue(const SkinnyParams& p, const SkLayout& L, uint64_t* dfull,
                             uint64_t* dempty, uint32_t tmem, int quad, int lane,
                             volatile int* abort) {
@@ -578,6 +618,8 @@ __device__ void sk_epilogue(const SkinnyParams& p, const SkLayout& L, uint64_t* 
       }
       if (!last) tmem_st_wait();
     }
+    if constexpr (kTrace)
+      if (quad == 0 && lane == 0) trace_emit(p.trace, kTrPieceDone, static_cast<uint32_t>(nt), u);
     u = ue;
   }
 }
@@ -586,6 +628,7 @@ __device__ void sk_epilogue(const SkinnyParams& p, const SkLayout& L, uint64_t* 
 // each quadrant, which the 16x256b shape reads without the 16 idle lanes:
 // thread t holds rows 16q + t / 4 and 16q + t / 4 + 8, columns 8i + 2(t % 4)
 // and +1 of each 8-column block i of a 64-column chunk.
+template <bool kTrace>
 __device__ void sk_epilogue64(const SkinnyParams& p, uint64_t* dfull, uint64_t* dempty,
                               uint32_t tmem, int quad, int lane, volatile int* abort) {
   const Geometry& g = p.g;
@@ -661,10 +704,13 @@ __device__ void sk_epilogue64(const SkinnyParams& p, uint64_t* dfull, uint64_t* 
       }
       if (!last) tmem_st_wait();
     }
+    if constexpr (kTrace)
+      if (quad == 0 && lane == 0) trace_emit(p.trace, kTrPieceDone, static_cast<uint32_t>(nt), u);
     u = ue;
   }
 }
 
+template <bool kTrace>
 __global__ void __launch_bounds__(kSkThreads, 1) ag_skinny_kernel(const __grid_constant__ SkinnyParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -713,27 +759,30 @@ __global__ void __launch_bounds__(kSkThreads, 1) ag_skinny_kernel(const __grid_c
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  if constexpr (kTrace)
+    if (threadIdx.x == 0) trace_emit(p.trace, kTrCtaStart, 0, 0);
   int role, rank;
   sk_role(warp, role, rank);
   if (role == kRoleCopy) {
-    if (p.flags & kFlagCopy) sk_copy_warp(p, lane);
+    if (p.flags & kFlagCopy) sk_copy_warp<kTrace>(p, lane);
   } else if (gemm) {
     switch (role) {
       case kRoleMma:
-        if (lane == 0) sk_mma(p, sFp, sA, L, st_full, st_empty, dfull, dempty, tmem, abort);
+        if (lane == 0)
+          sk_mma<kTrace>(p, sFp, sA, L, st_full, st_empty, dfull, dempty, tmem, abort);
         break;
       case kRoleTma:
-        sk_tma_warp(p, sRaw, L, raw_full, raw_empty, lane, abort);
+        sk_tma_warp<kTrace>(p, sRaw, L, raw_full, raw_empty, lane, abort);
         break;
       case kRoleEpi:
         if (L.mm == 64)
-          sk_epilogue64(p, dfull, dempty, tmem, warp & 3, lane, abort);
+          sk_epilogue64<kTrace>(p, dfull, dempty, tmem, warp & 3, lane, abort);
         else
-          sk_epilogue(p, L, dfull, dempty, tmem, warp & 3, lane, abort);
+          sk_epilogue<kTrace>(p, L, dfull, dempty, tmem, warp & 3, lane, abort);
         break;
       case kRoleBw:
-        sk_bwiden(p, sRaw, L, sFp, raw_full, raw_empty, st_full, st_empty, rank * 32 + lane,
-                  abort);
+        sk_bwiden<kTrace>(p, sRaw, L, sFp, raw_full, raw_empty, st_full, st_empty,
+                          rank * 32 + lane, abort);
         break;
       default:
         if (L.mm == 64)
@@ -758,6 +807,8 @@ __global__ void __launch_bounds__(kSkThreads, 1) ag_skinny_kernel(const __grid_c
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  if constexpr (kTrace)
+    if (threadIdx.x == 0) trace_emit(p.trace, kTrCtaEnd, 0, 0);
 }
 
 // C_i32 = (sum of the n-tile's workspace slots) + bias,
@@ -828,12 +879,18 @@ __global__ void __launch_bounds__(256) ag_skinny_finish_kernel(
 }  // namespace
 
 cudaError_t skinny_prepare() {
-  return cudaFuncSetAttribute(reinterpret_cast<const void*>(&ag_skinny_kernel),
+  cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&ag_skinny_kernel<false>),
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSkSmem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(reinterpret_cast<const void*>(&ag_skinny_kernel<true>),
                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSkSmem);
 }
 
 cudaError_t launch_skinny(const SkinnyParams& p, int grid, cudaStream_t stream) {
-  ag_skinny_kernel<<<grid, kSkThreads, kSkSmem, stream>>>(p);
+  if (p.trace.count)
+    ag_skinny_kernel<true><<<grid, kSkThreads, kSkSmem, stream>>>(p);
+  else
+    ag_skinny_kernel<false><<<grid, kSkThreads, kSkSmem, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !(p.flags & kFlagGemm)) return e;
   // Programmatic dependent launch: the finish grid's launch is processed while

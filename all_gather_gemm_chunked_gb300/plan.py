@@ -101,6 +101,15 @@ class Plan:
     def set_debug(self, flags: int, arg: int = 0):
         B_.ag_gemm_plan_set_debug(self.handle, flags, arg)
 
+    def set_trace(self, capacity: int):
+        """Record an event trace of every later run (capacity events; 0 = off)."""
+        self.trace_capacity = int(capacity)
+        B_.ag_gemm_plan_set_trace(self.handle, self.trace_capacity)
+
+    def trace(self):
+        """(events the last run recorded, numpy structured array of the kept events)."""
+        return B_.ag_gemm_plan_trace(self.handle, getattr(self, "trace_capacity", 0))
+
     def status(self) -> int:
         return B_.ag_gemm_plan_status(self.handle)
 

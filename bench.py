@@ -153,6 +153,18 @@ class ClockSampler:
         except (OSError, FileNotFoundError):
             self.proc = None
 
+    def wait_ready(self, timeout_s: float = 5.0):
+        """Return once nvidia-smi has written its first sample (its start-up can
+        stall CUDA calls of this process for up to a second), or after timeout_s."""
+        t0 = time.time()
+        while self.proc is not None and time.time() - t0 < timeout_s:
+            try:
+                if os.path.getsize(self.path) > 0:
+                    return
+            except OSError:
+                return
+            time.sleep(0.05)
+
     def stop(self):
         if self.proc is None:
             return None
@@ -595,6 +607,7 @@ def run_ours(args, w, rank, world, local_rank):
     barrier()
     torch.cuda.synchronize(dev)
     clocks.start()
+    clocks.wait_ready()
     times_ms, gate = r.timed(args.steps, B_.MODE_PIPELINED, flush_fn)
     torch.cuda.synchronize(dev)
     clk = clocks.stop()

@@ -301,6 +301,76 @@ int ag_gemm_plan_set_timeout_ns(ag_gemm_plan *plan, int64_t ns);
 /* OR of ag_gemm_debug_flag values; `arg` is the item index or the delay. */
 int ag_gemm_plan_set_debug(ag_gemm_plan *plan, int flags, int64_t arg);
 
+/*
+ * Per-run event trace (opt-in): when each chunk landed in the staging, when
+ * each consumer started and stopped waiting for remote rows, and a few
+ * pipeline milestones, stamped with the GPU's global nanosecond timer.  It
+ * shows the overlap of the copy and the GEMM, the measurement the PTO example
+ * ships as its overlap analysis ("AllGather + GEMM 通算融合算子示例", section
+ * 目录结构, prof_analysis).  A plan with tracing on runs the trace-enabled
+ * instantiation of its kernels (slower: every event is a global atomic); with
+ * tracing off the kernels contain no trace code.
+ *
+ * Event kinds and the meaning of id / aux:
+ *   CTA_START, CTA_END    thread 0 of a CTA (id = aux = 0)
+ *   LANDED                a copy warp finished a copy item and is about to
+ *                         release its ready counter: id = counter index,
+ *                         aux = item index.  Fused paths: counter
+ *                         (p - 1) * Q + q of chunk q at consumption position
+ *                         p, item as ag_gemm_item_at.  Skinny path: a copy
+ *                         task (k-part j, position p, chunk q) with counter
+ *                         (j * (n_shards - 1) + p - 1) * Q + q.
+ *   WAIT_START, WAIT_END  the TMA warp before / after acquiring remote rows.
+ *                         Fused: id = tile, aux = p << 48 | q0 << 24 | q1
+ *                         (chunks q0..q1 of position p; one pair per CTA of a
+ *                         pair tile).  Skinny: id = unit, aux = k-part j.
+ *   TILE_DONE             fused: an epilogue warp issued its last store of a tile (id = tile)
+ *   UNIT_ISSUED           skinny: a unit's loads issued (id = unit)
+ *   UNIT_LANDED           skinny: a unit's operands in shared memory (id = unit)
+ *   KB_WIDENED            skinny: a k-block of B widened to fp16 (id = k-block of the n-tile, aux = unit)
+ *   KB_MMA                skinny: a k-block's MMAs issued (id = k-block of the n-tile, aux = n-tile)
+ *   PIECE_DONE            skinny: a CTA's split-K sums of one n-tile stored (id = n-tile, aux = next unit)
+ */
+typedef enum {
+    AG_GEMM_TRACE_CTA_START = 1,
+    AG_GEMM_TRACE_CTA_END = 2,
+    AG_GEMM_TRACE_LANDED = 3,
+    AG_GEMM_TRACE_WAIT_START = 4,
+    AG_GEMM_TRACE_WAIT_END = 5,
+    AG_GEMM_TRACE_TILE_DONE = 6,
+    AG_GEMM_TRACE_UNIT_ISSUED = 7,
+    AG_GEMM_TRACE_UNIT_LANDED = 8,
+    AG_GEMM_TRACE_KB_WIDENED = 9,
+    AG_GEMM_TRACE_KB_MMA = 10,
+    AG_GEMM_TRACE_PIECE_DONE = 11
+} ag_gemm_trace_kind;
+
+typedef struct {
+    uint64_t t_ns;   /* the GPU's global nanosecond timer (%globaltimer) */
+    uint32_t kind;   /* ag_gemm_trace_kind */
+    uint32_t cta;    /* CTA index within its launch */
+    uint32_t warp;   /* warp index within the CTA */
+    uint32_t id;     /* per kind, see above */
+    uint64_t aux;    /* per kind, see above */
+} ag_gemm_trace_event;
+
+/*
+ * Turn tracing on (capacity > 0 events, at most 2^26; allocates
+ * 32 + 32 * capacity bytes on the device) or off (capacity = 0, frees the
+ * buffer).  Waits for the plan's last run.  Every later run clears the trace
+ * and records its own events; events past the capacity are dropped (counted).
+ */
+int ag_gemm_plan_set_trace(ag_gemm_plan *plan, int64_t capacity);
+
+/*
+ * Wait for the plan's last run and copy up to max_events of its events (in
+ * the order they were recorded, which is not strictly time order) to the
+ * HOST array out.  Returns the number of events the run tried to record
+ * (more than were kept if the capacity was exceeded), or a negative status
+ * (AG_GEMM_ERR_STATE when tracing is off).
+ */
+int64_t ag_gemm_plan_trace(ag_gemm_plan *plan, ag_gemm_trace_event *out, int64_t max_events);
+
 /* Number of CTAs the plan's main kernel launches (one per SM). */
 int ag_gemm_plan_grid(const ag_gemm_plan *plan);
 
