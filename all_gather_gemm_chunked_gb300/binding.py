@@ -23,7 +23,7 @@ DEBUG_POISON_STAGING, DEBUG_SKIP_ITEM, DEBUG_DELAY_NS = 1, 2, 4
 PATH_FUSED_F16, PATH_FUSED_I8, PATH_SKINNY_I8 = 0, 1, 2
 (TRACE_CTA_START, TRACE_CTA_END, TRACE_LANDED, TRACE_WAIT_START, TRACE_WAIT_END, TRACE_TILE_DONE,
  TRACE_UNIT_ISSUED, TRACE_UNIT_LANDED, TRACE_KB_WIDENED, TRACE_KB_MMA,
- TRACE_PIECE_DONE) = range(1, 12)
+ TRACE_PIECE_DONE, TRACE_COPY_START, TRACE_ACC_READY, TRACE_PARTS_READY) = range(1, 15)
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_OOM, ERR_TIMEOUT, ERR_STATE = 0, -1, -2, -3, -4, -5, -6
 ERROR_NAMES = {ERR_INVALID: "INVALID", ERR_UNSUPPORTED: "UNSUPPORTED", ERR_CUDA: "CUDA",
                ERR_OOM: "OOM", ERR_TIMEOUT: "TIMEOUT", ERR_STATE: "STATE"}
@@ -50,6 +50,7 @@ class Geometry(ctypes.Structure):
         ("m_tiles", ctypes.c_int64), ("n_tiles", ctypes.c_int64), ("tiles", ctypes.c_int64),
         ("producer_items", ctypes.c_int64), ("staging_bytes", ctypes.c_int64),
         ("workspace_bytes", ctypes.c_int64), ("staging_slots", ctypes.c_int64),
+        ("split_tiles", ctypes.c_int64), ("split_parts", ctypes.c_int64),
     ]
 
     def as_dict(self):
@@ -96,6 +97,7 @@ def _load():
         "ag_gemm_plan_path": (i32, [vp]),
         "ag_gemm_run_noalloc": (i32, [i32, i64, i64, i64, i64, ctypes.POINTER(vp), vp, vp, vp, vp]),
         "ag_gemm_plan_set_trace": (i32, [vp, i64]),
+        "ag_gemm_plan_set_grid": (i32, [vp, i32]),
         "ag_gemm_plan_trace": (i64, [vp, ctypes.POINTER(TraceEvent), i64]),
         "ag_gemm_last_error": (i32, []),
         "ag_gemm_last_error_message": (ctypes.c_char_p, []),
@@ -240,6 +242,10 @@ def ag_gemm_plan_set_timeout_ns(plan: int, ns: int) -> int:
 
 def ag_gemm_plan_set_debug(plan: int, flags: int, arg: int = 0) -> int:
     return _check(_lib.ag_gemm_plan_set_debug(plan, flags, arg))
+
+
+def ag_gemm_plan_set_grid(plan: int, ctas: int) -> int:
+    return _check(_lib.ag_gemm_plan_set_grid(plan, ctas))
 
 
 def ag_gemm_plan_grid(plan: int) -> int:

@@ -130,6 +130,7 @@ __device__ bool wait_slot(const FusedParams& p, int64_t slot, uint32_t target, i
 template <bool kI8, bool kTrace>
 __device__ void copy_warp(const FusedParams& p, int lane) {
   const Geometry& g = p.g;
+  [[maybe_unused]] uint32_t tn = 0;  // trace events of this warp
   // With bounded staging and the GEMM in the same launch, a block may only
   // overwrite its slot after the slot's previous block has been read.  (A
   // copy-only launch has no readers and writes freely.)
@@ -152,6 +153,10 @@ __device__ void copy_warp(const FusedParams& p, int lane) {
     item_coords(g, i, pos, q, piece, v0, v1);
     if (i == p.debug_skip_item) continue;  // failure injection: this chunk never completes
     if (p.debug_delay_ns) __nanosleep(p.debug_delay_ns);
+    if constexpr (kTrace)
+      if (lane == 0)
+        trace_emit(p.trace, tn, threadIdx.x >> 5, kTrCopyStart,
+                   static_cast<uint32_t>((int64_t)(pos - 1) * g.Q + q), i);
     const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.src[pos]) +
                                                       q * g.c * g.K * g.src_esize);
     int64_t drow = (int64_t)(pos - 1) * g.R + q * g.c;  // staging row of the chunk's first row
@@ -173,14 +178,68 @@ __device__ void copy_warp(const FusedParams& p, int lane) {
       warp_widen16(src + v0, dst + 2 * v0, v1 - v0, lane);
     else
       warp_copy16(src + v0, dst + v0, v1 - v0, lane);
-    __threadfence();
+    // the warp barrier orders every lane's stores before lane 0's release
+    // (release is cumulative), which publishes them at GPU scope
     __syncwarp();
     if (lane == 0) {
       const int64_t ci = (int64_t)(pos - 1) * g.Q + q;
-      if constexpr (kTrace) trace_emit(p.trace, kTrLanded, static_cast<uint32_t>(ci), i);
+      if constexpr (kTrace) trace_emit(p.trace, tn, threadIdx.x >> 5, kTrLanded, static_cast<uint32_t>(ci), i);
       red_release_gpu_add(p.counters + ci, 1u);
     }
   }
+}
+
+// ------------------------------------------------------------------ tile ring
+// Tiles are handed out dynamically: the even CTA's TMA warp draws pair tiles
+// from a grid-wide ticket counter, in schedule order, and publishes each index
+// (or -1 once none is left) in a kTq-deep ring in the shared memory of both
+// CTAs of the pair.  So whichever pairs are resident always take the lowest
+// tiles not yet taken: no tile waits on a pair that has not started, which
+// keeps the staging window's credits live even when fewer pairs are resident
+// than were launched.
+struct TileRing {
+  int32_t* tq;         // this CTA's ring of tile indices
+  uint64_t* full;      // this CTA's "published" barriers (one arrival: the producer)
+  uint64_t* empty;     // the even CTA's "read" barriers (kTqReaders arrivals)
+  uint32_t empty0;     // shared::cluster address of the even CTA's empty[0]
+};
+
+// A reader's n-th tile (the caller's single thread): false on timeout/abort.
+__device__ __forceinline__ bool ring_read(const TileRing& r, uint32_t n, int64_t& t,
+                                          uint64_t timeout_ns, volatile int* abort,
+                                          const volatile uint32_t* gstatus) {
+  const uint32_t slot = n % kTq, ph = (n / kTq) & 1u;
+  if (!mbar_wait_cluster(&r.full[slot], ph, timeout_ns, abort, gstatus)) return false;
+  t = *reinterpret_cast<volatile int32_t*>(&r.tq[slot]);
+  mbar_arrive_cluster(r.empty0 + slot * 8);  // the slot may be refilled
+  return true;
+}
+
+// The producer's side (even CTA, one thread).  A ticket is drawn from the
+// grid-wide counter (ring_draw) well before it is needed and published as the
+// pair's n-th tile once the slot is free (ring_put): into both CTAs' rings.
+// Pair k's first item is item k when k < static_items (a whole tile of the
+// local shard: it waits for nothing, so a pair that starts late holds up no
+// other pair); every other item comes from the ticket counter: ticket i is
+// item static_items + i.
+__device__ __forceinline__ int64_t ring_draw(const FusedParams& p) {
+  const unsigned long long ticket = atomicAdd(p.tile_counter, 1ull);
+  const int64_t i = static_cast<int64_t>(ticket - p.tile_base);
+  // exactly one failing ticket per pair and run; a negative one means the
+  // counters were not reset after a failed run: take nothing
+  return (i >= 0 && p.static_items + i < p.work_items) ? p.static_items + i : -1;
+}
+__device__ __forceinline__ bool ring_put(const FusedParams& p, const TileRing& r, uint32_t n,
+                                         int64_t t, volatile int* abort,
+                                         const volatile uint32_t* gstatus) {
+  const uint32_t slot = n % kTq, ph = (n / kTq) & 1u;
+  if (!mbar_wait_cluster(&r.empty[slot], ph ^ 1u, p.pipe_timeout_ns, abort, gstatus))
+    return false;
+  r.tq[slot] = static_cast<int32_t>(t);
+  st_shared_cluster_u32(mapa_shared(smem_u32(&r.tq[slot]), 1), static_cast<uint32_t>(t));
+  mbar_arrive(&r.full[slot]);
+  mbar_arrive_cluster(mapa_shared(smem_u32(&r.full[slot]), 1));
+  return true;
 }
 
 // ------------------------------------------------------------------ TMA warp
@@ -195,10 +254,10 @@ __device__ bool wait_chunks(const FusedParams& p, int pos, int64_t row0, int lan
   const uint32_t* cnt = p.counters + (int64_t)(pos - 1) * g.Q;
   bool ok = true;
   for (int64_t q = q0 + lane; q <= q1 && ok; q += 32) {
-    if (ld_acquire_gpu(cnt + q) >= target) continue;
+    if (ld_relaxed_gpu(cnt + q) >= target) continue;
     const uint64_t deadline = globaltimer_ns() + p.timeout_ns;
     uint32_t spins = 0;
-    while (ld_acquire_gpu(cnt + q) < target) {
+    while (ld_relaxed_gpu(cnt + q) < target) {
       __nanosleep(64);
       if (++spins == 16) {
         spins = 0;
@@ -210,6 +269,7 @@ __device__ bool wait_chunks(const FusedParams& p, int pos, int64_t row0, int lan
       }
     }
   }
+  fence_acq_rel_gpu();  // with the relaxed reads above: an acquire of every counter seen
   ok = __all_sync(0xffffffffu, ok);
   if (!ok && lane == 0) {
     set_status(p.status, kStatusChunkTimeout,
@@ -222,14 +282,15 @@ __device__ bool wait_chunks(const FusedParams& p, int pos, int64_t row0, int lan
 
 template <bool kI8, bool kTrace>
 __device__ void tma_warp(const FusedParams& p, uint32_t rank, uint8_t* sA, uint8_t* sB,
-                         uint64_t* full, uint64_t* empty, int lane, volatile int* abort) {
+                         uint64_t* full, uint64_t* empty, const TileRing& ring, int lane,
+                         volatile int* abort) {
   const Geometry& g = p.g;
+  [[maybe_unused]] uint32_t tn = 0;  // trace events of this warp
   const volatile uint32_t* gstatus = p.status;
   const bool wait = (p.flags & kFlagWait) != 0;
   const int half = g.BN / 2;                                   // B columns this CTA stages
   const uint32_t pair_tx = static_cast<uint32_t>(2 * (kABytes + half * kBlockK * 2));
   const uint32_t full0 = mapa_shared(smem_u32(full), 0);       // the even CTA's barriers
-  const int64_t n_clusters = gridDim.x / 2, cluster = blockIdx.x / 2;
   int stage = 0;
   uint32_t phase = 0, issued = 0, issued_phase = 0;  // bit s: stage s used / parity of last use
   if (lane == 0) {
@@ -238,10 +299,45 @@ __device__ void tma_warp(const FusedParams& p, uint32_t rank, uint8_t* sA, uint8
     tma_prefetch_desc(&p.tm_b);
   }
   bool ok = true;
-  for (int64_t t = cluster; t < g.tiles && ok; t += n_clusters) {
+  // Even CTA: the ticket for item seq + 1 is requested when item seq starts and
+  // published once item seq's loads have been issued, so the ticket's round
+  // trip to L2 never holds up a load.
+  uint32_t published = 0;  // items published so far
+  bool drawn_all = false;  // the end marker (-1) has been published
+  if (rank == 0 && lane == 0) {
+    const int64_t pair = blockIdx.x / 2;
+    const int64_t first = pair < p.static_items ? pair : ring_draw(p);
+    ok = ring_put(p, ring, published, first, abort, gstatus);
+    ++published;
+    drawn_all = first < 0;
+  }
+  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  for (uint32_t seq = 0; ok; ++seq) {
+    // the pair's next tile: published by the even CTA, read by the odd one
+    int64_t t = -1, ahead = -1;
+    bool got = true;
+    if (lane == 0) {
+      if (rank == 0) {
+        t = *reinterpret_cast<volatile int32_t*>(&ring.tq[seq % kTq]);
+        if (t >= 0 && !drawn_all) ahead = ring_draw(p);
+      } else {
+        got = ring_read(ring, seq, t, p.pipe_timeout_ns, abort, gstatus);
+      }
+    }
+    got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+    t = __shfl_sync(0xffffffffu, t, 0);
+    if (!got) {
+      ok = false;
+      break;
+    }
+    if (t < 0) break;
+    // work item t: tile `tile`, k-blocks [kbs, kbe) (the whole K unless the tile is split)
+    int64_t tile, kbs, kbe;
+    int part, parts;
+    work_item(g, p.full_tiles, p.split, t, tile, part, parts, kbs, kbe);
     int pos;
     int64_t mt, nt;
-    tile_coords(g, t, pos, mt, nt);
+    tile_coords(g, tile, pos, mt, nt);
     const int64_t row0 = mt * kPairM + rank * kBlockM;
     if constexpr (kTrace) {
       int64_t q0 = 0, q1 = -1;
@@ -249,9 +345,9 @@ __device__ void tma_warp(const FusedParams& p, uint32_t rank, uint8_t* sA, uint8
       const uint64_t aux = (static_cast<uint64_t>(pos) << 48) |
                            (static_cast<uint64_t>(q0 & 0xFFFFFF) << 24) |
                            static_cast<uint64_t>(q1 & 0xFFFFFF);
-      if (rows && lane == 0) trace_emit(p.trace, kTrWaitStart, static_cast<uint32_t>(t), aux);
+      if (rows && lane == 0) trace_emit(p.trace, tn, threadIdx.x >> 5, kTrWaitStart, static_cast<uint32_t>(tile), aux);
       if (pos > 0 && wait && !wait_chunks(p, pos, row0, lane, abort)) break;
-      if (rows && lane == 0) trace_emit(p.trace, kTrWaitEnd, static_cast<uint32_t>(t), aux);
+      if (rows && lane == 0) trace_emit(p.trace, tn, threadIdx.x >> 5, kTrWaitEnd, static_cast<uint32_t>(tile), aux);
     } else {
       if (pos > 0 && wait && !wait_chunks(p, pos, row0, lane, abort)) break;
     }
@@ -266,7 +362,7 @@ __device__ void tma_warp(const FusedParams& p, uint32_t rank, uint8_t* sA, uint8
       const int32_t y = win ? static_cast<int32_t>(rank * kBlockM) : static_cast<int32_t>(row0);
       const int32_t z = win ? static_cast<int32_t>(((pos - 1) * g.MT + mt) % p.window) : pos - 1;
       const int32_t xb = static_cast<int32_t>(nt * g.BN + rank * half);
-      for (int64_t kb = 0; kb < g.KB; ++kb) {
+      for (int64_t kb = kbs; kb < kbe; ++kb) {
         if (!mbar_wait(&empty[stage], phase ^ 1u, p.pipe_timeout_ns, abort, gstatus)) {
           ok = false;
           break;
@@ -294,6 +390,11 @@ __device__ void tma_warp(const FusedParams& p, uint32_t rank, uint8_t* sA, uint8
           phase ^= 1u;
         }
       }
+      if (ok && rank == 0 && !drawn_all) {
+        ok = ring_put(p, ring, published, ahead, abort, gstatus);
+        ++published;
+        drawn_all = ahead < 0;
+      }
     }
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
   }
@@ -318,26 +419,35 @@ __device__ void tma_warp(const FusedParams& p, uint32_t rank, uint8_t* sA, uint8
 template <bool kI8>
 __device__ void mma_warp(const FusedParams& p, const uint8_t* sA, const uint8_t* sB,
                          uint64_t* full, uint64_t* empty, uint64_t* tfull, uint64_t* tempty,
-                         uint32_t tmem, volatile int* abort) {
+                         const TileRing& ring, uint32_t tmem, volatile int* abort) {
   const Geometry& g = p.g;
   const volatile uint32_t* gstatus = p.status;
   const uint32_t idesc = idesc_f16_f32(kPairM, g.BN, /*a_mn=*/false, /*b_mn=*/true) |
                          (p.bf16 ? kIdescAbBf16 : 0u);
-  const int64_t seg_len = kI8 ? kSegBlocks : g.KB;
-  const int64_t nseg = ceil_div(g.KB, seg_len);
   const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
-  const int64_t n_clusters = gridDim.x / 2, cluster = blockIdx.x / 2;
   // bounded staging, pipelined launch: credit the slot a remote tile read
   const bool credit = p.window > 0 && (p.flags & kFlagWait) != 0;
   int stage = 0;
   uint32_t phase = 0, unit = 0;
   bool ok = true;
-  for (int64_t t = cluster; t < g.tiles && ok; t += n_clusters) {
+  for (uint32_t seq = 0; ok; ++seq) {
+    int64_t t = -1;
+    if (!ring_read(ring, seq, t, p.pipe_timeout_ns, abort, gstatus)) {
+      ok = false;
+      break;
+    }
+    if (t < 0) break;
+    int64_t tile, kbs, kbe;
+    int part, parts;
+    work_item(g, p.full_tiles, p.split, t, tile, part, parts, kbs, kbe);
+    // fp32 accumulation spans the whole item (fp16), or segments of kSegBlocks (int8)
+    const int64_t seg_len = kI8 ? kSegBlocks : kbe - kbs;
+    const int64_t nseg = ceil_div(kbe - kbs, seg_len);
     int64_t slot = -1;  // the window slot this remote tile reads (bounded staging)
     if (credit) {
       int pos;
       int64_t mt, nt;
-      tile_coords(g, t, pos, mt, nt);
+      tile_coords(g, tile, pos, mt, nt);
       if (pos > 0) slot = ((pos - 1) * g.MT + mt) % p.window;
     }
     for (int64_t seg = 0; seg < nseg && ok; ++seg) {
@@ -348,8 +458,8 @@ __device__ void mma_warp(const FusedParams& p, const uint8_t* sA, const uint8_t*
       }
       tc_fence_after();
       const uint32_t d = tmem + buf * 256u;
-      const int64_t kb0 = seg * seg_len;
-      const int64_t kb1 = kb0 + seg_len < g.KB ? kb0 + seg_len : g.KB;
+      const int64_t kb0 = kbs + seg * seg_len;
+      const int64_t kb1 = kb0 + seg_len < kbe ? kb0 + seg_len : kbe;
       for (int64_t kb = kb0; kb < kb1; ++kb) {
         if (!mbar_wait(&full[stage], phase, p.pipe_timeout_ns, abort, gstatus)) {
           ok = false;
@@ -401,17 +511,53 @@ __device__ __forceinline__ void st_v4(void* ptr, uint32_t a, uint32_t b, uint32_
                : "memory");
 }
 
+// A split tile's last part: lane 0 waits (bounded) until every warp of the
+// earlier parts has stored its partial sums; then every lane acquires the flag,
+// which orders its reads of the partials after those stores.
+__device__ bool wait_parts(const FusedParams& p, int64_t tail, uint32_t rank, int lane,
+                           volatile int* abort) {
+  const uint32_t* flag = p.part_flags + tail;
+  bool ok = true;
+  if (lane == 0 && ld_acquire_gpu(flag) < p.part_target) {
+    const uint64_t deadline = globaltimer_ns() + p.pipe_timeout_ns;
+    uint32_t spins = 0;
+    while (ld_acquire_gpu(flag) < p.part_target) {
+      __nanosleep(128);
+      if (++spins == 16) {
+        spins = 0;
+        if (*abort || *reinterpret_cast<volatile uint32_t*>(p.status) != 0u ||
+            globaltimer_ns() > deadline) {
+          ok = false;
+          break;
+        }
+      }
+    }
+    if (!ok) {
+      set_status(p.status, kStatusPipelineTimeout, 0x500u | rank);
+      *abort = 1;
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  if (ok) (void)ld_acquire_gpu(flag);
+  return ok;
+}
+
+// An earlier part has stored this warp's share of its partial sums: the warp
+// barrier orders every lane's stores before lane 0's (cumulative) release.
+__device__ __forceinline__ void signal_part(const FusedParams& p, int64_t tail, int lane) {
+  __syncwarp();
+  if (lane == 0) red_release_gpu_add(p.part_flags + tail, 1u);
+}
+
 template <bool kI8, bool kTrace>
 __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int half, int lane,
-                              uint64_t* tfull, uint64_t* tempty, uint32_t tmem, uint8_t* sEpi,
-                              volatile int* abort) {
+                              uint64_t* tfull, uint64_t* tempty, const TileRing& ring,
+                              uint32_t tmem, uint8_t* sEpi, volatile int* abort) {
   const Geometry& g = p.g;
+  [[maybe_unused]] uint32_t tn = 0;  // trace events of this warp
   const volatile uint32_t* gstatus = p.status;
-  const int64_t seg_len = kI8 ? kSegBlocks : g.KB;
-  const int64_t nseg = ceil_div(g.KB, seg_len);
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
   const uint32_t tempty0 = mapa_shared(smem_u32(tempty), 0);  // the even CTA's barriers
-  const int64_t n_clusters = gridDim.x / 2, cluster = blockIdx.x / 2;
   const int nchunks = g.BN / 64;                      // 32-column chunks in this warp's half
   const int chunk0 = half * nchunks;
   uint8_t* box = sEpi + (half * 4 + quad) * kEpiBoxBytes;  // this warp's staging box
@@ -419,10 +565,45 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
   // (at most 4 chunks of 32), kept in registers across the tile's segments
   uint32_t sums[kI8 ? 128 : 1];
   uint32_t unit = 0;
-  for (int64_t t = cluster; t < g.tiles; t += n_clusters) {
+  for (uint32_t seq = 0;; ++seq) {
+    int64_t t = -1;
+    bool got = true;
+    if (lane == 0) got = ring_read(ring, seq, t, p.pipe_timeout_ns, abort, gstatus);
+    got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+    t = __shfl_sync(0xffffffffu, t, 0);
+    if (!got) {
+      if (lane == 0) {
+        set_status(p.status, kStatusPipelineTimeout, 0x400u | rank);
+        *abort = 1;
+        bulk_wait_group_all();
+      }
+      return;
+    }
+    if (t < 0) break;
+    int64_t tile, kbs, kbe;
+    int part, parts;
+    work_item(g, p.full_tiles, p.split, t, tile, part, parts, kbs, kbe);
+    const int64_t seg_len = kI8 ? kSegBlocks : kbe - kbs;
+    const int64_t nseg = ceil_div(kbe - kbs, seg_len);
+    // a split tile: earlier parts store partial sums, the last part adds them
+    const bool store_part = parts > 1 && part < parts - 1;
+    const bool add_parts = parts > 1 && part == parts - 1;
+    const int64_t tail = tile - p.full_tiles;
+    // Partial sums of part j of this tail tile, laid out for this warp: 16-byte
+    // vector c of every lane of the warp is contiguous (512 bytes), so each
+    // store and load of the warp moves whole lines.  Vector c (c < BN / 8) of
+    // a lane holds its row's columns 4c .. 4c + 3 of the warp's half of the
+    // tile; a (tile, part) takes 2 CTAs x 8 warps x BN / 8 x 32 lanes x 16 B
+    // = 2 x 128 rows x BN x 4 bytes, the size the plan allocates per part.
+    const int64_t vecs = g.BN / 8;
+    auto part_vec = [&](int j, int c) -> uint4* {
+      return static_cast<uint4*>(p.partials) +
+             (((((tail * (p.split - 1) + j) * 2 + rank) * kEpiWarps + half * 4 + quad) * vecs +
+               c) * 32 + lane);
+    };
     int pos;
     int64_t mt, nt;
-    tile_coords(g, t, pos, mt, nt);
+    tile_coords(g, tile, pos, mt, nt);
     const int src = source_of(g, p.local, pos);
     const int64_t r = mt * kPairM + rank * kBlockM + quad * 32 + lane;
     const bool row_ok = r < g.R;
@@ -438,6 +619,10 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
         return;
       }
       tc_fence_after();
+      if constexpr (kTrace)
+        if (quad == 0 && half == 0 && lane == 0 && seg == nseg - 1)
+          trace_emit(p.trace, tn, threadIdx.x >> 5, kTrAccReady, static_cast<uint32_t>(tile),
+                     static_cast<uint64_t>(part) | (static_cast<uint64_t>(parts) << 8));
       // Called once this warp has read its last accumulator column of the
       // unit: the pair leader's MMA may then overwrite the buffer while this
       // warp finishes converting and storing.
@@ -456,12 +641,53 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
         // shared box -> one TMA store of 32 full 128-byte row segments.  Rows
         // past the shard and columns past N are clipped by the descriptor.
         const int64_t r0 = mt * kPairM + rank * kBlockM + quad * 32;
+        if (add_parts && !wait_parts(p, tail, rank, lane, abort)) {
+          if (lane == 0) bulk_wait_group_all();
+          return;
+        }
+        if constexpr (kTrace)
+          if (add_parts && quad == 0 && half == 0 && lane == 0)
+            trace_emit(p.trace, tn, threadIdx.x >> 5, kTrPartsReady, static_cast<uint32_t>(tile), 0);
         for (int jj = 0; jj < nchunks; ++jj) {
           const int j = chunk0 + jj;
           uint32_t v[32];
           tmem_ld32(lane_base + buf * 256u + j * 32, v);
           tmem_ld_wait();
           if (jj == nchunks - 1) release();
+          if (store_part) {
+            // this part's fp32 sums of the thread's row, 32 columns
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              *part_vec(part, jj * 8 + c) =
+                  make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+            continue;
+          }
+          if (add_parts) {
+            // (part 0 + part 1 + ...) + this part, in that order
+            uint4 x[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) x[c] = __ldcg(part_vec(0, jj * 8 + c));
+            for (int pj = 1; pj < parts - 1; ++pj) {
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                const uint4 y = __ldcg(part_vec(pj, jj * 8 + c));
+                x[c].x = __float_as_uint(__fadd_rn(__uint_as_float(x[c].x), __uint_as_float(y.x)));
+                x[c].y = __float_as_uint(__fadd_rn(__uint_as_float(x[c].y), __uint_as_float(y.y)));
+                x[c].z = __float_as_uint(__fadd_rn(__uint_as_float(x[c].z), __uint_as_float(y.z)));
+                x[c].w = __float_as_uint(__fadd_rn(__uint_as_float(x[c].w), __uint_as_float(y.w)));
+              }
+            }
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              v[4 * c] = __float_as_uint(__fadd_rn(__uint_as_float(x[c].x), __uint_as_float(v[4 * c])));
+              v[4 * c + 1] =
+                  __float_as_uint(__fadd_rn(__uint_as_float(x[c].y), __uint_as_float(v[4 * c + 1])));
+              v[4 * c + 2] =
+                  __float_as_uint(__fadd_rn(__uint_as_float(x[c].z), __uint_as_float(v[4 * c + 2])));
+              v[4 * c + 3] =
+                  __float_as_uint(__fadd_rn(__uint_as_float(x[c].w), __uint_as_float(v[4 * c + 3])));
+            }
+          }
           const int64_t n0 = nt * g.BN + j * 32;
           if (r0 >= g.R || n0 >= g.N) continue;  // warp-uniform: nothing of this box exists
           if (lane == 0) bulk_wait_group_read<0>();  // the previous store has read the box
@@ -481,6 +707,7 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
             bulk_commit_group();
           }
         }
+        if (store_part) signal_part(p, tail, lane);
       } else {
         const bool first = seg == 0, last = seg == nseg - 1;
         // fp32 partials (exact integers) -> int32, added to the running sums;
@@ -502,7 +729,42 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
             }
           }
         }
-        if (last && row_ok) {
+        if (last && store_part) {
+          // this part's exact int32 sums of the thread's row
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (c < nchunks * 8)
+              *part_vec(part, c) =
+                  make_uint4(sums[4 * c], sums[4 * c + 1], sums[4 * c + 2], sums[4 * c + 3]);
+          signal_part(p, tail, lane);
+        }
+        if (last && add_parts) {
+          if (!wait_parts(p, tail, rank, lane, abort)) {
+            if (lane == 0) bulk_wait_group_all();
+            return;
+          }
+          if constexpr (kTrace)
+            if (quad == 0 && half == 0 && lane == 0)
+              trace_emit(p.trace, tn, threadIdx.x >> 5, kTrPartsReady, static_cast<uint32_t>(tile), 0);
+          // integer sums: exact in any order; 8 vectors in flight at a time
+          for (int pj = 0; pj < parts - 1; ++pj) {
+#pragma unroll
+            for (int c0 = 0; c0 < 32; c0 += 8) {
+              if (c0 >= nchunks * 8) break;
+              uint4 x[8];
+#pragma unroll
+              for (int c = 0; c < 8; ++c) x[c] = __ldcg(part_vec(pj, c0 + c));
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                sums[4 * (c0 + c)] += x[c].x;
+                sums[4 * (c0 + c) + 1] += x[c].y;
+                sums[4 * (c0 + c) + 2] += x[c].z;
+                sums[4 * (c0 + c) + 3] += x[c].w;
+              }
+            }
+          }
+        }
+        if (last && row_ok && !store_part) {
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {
             if (jj >= nchunks) continue;
@@ -542,7 +804,8 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
     }
     if constexpr (kTrace)
       if (quad == 0 && half == 0 && lane == 0)
-        trace_emit(p.trace, kTrTileDone, static_cast<uint32_t>(t), 0);
+        trace_emit(p.trace, tn, threadIdx.x >> 5, kTrTileDone, static_cast<uint32_t>(tile),
+                   static_cast<uint64_t>(part) | (static_cast<uint64_t>(parts) << 8));
   }
   if (lane == 0) bulk_wait_group_all();  // every C store performed before the CTA exits
   __syncwarp();
@@ -552,6 +815,7 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
 template <bool kI8, bool kTrace>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ag_fused_kernel(const __grid_constant__ FusedParams p) {
+  [[maybe_unused]] uint32_t tc = 0;  // trace events of the CTA slot
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -564,7 +828,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t* tfull = bars + 2 * kStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* tq_full = drain + 1;
+  uint64_t* tq_empty = tq_full + kTq;
+  int32_t* tq = reinterpret_cast<int32_t*>(tq_empty + kTq);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tq + kTq);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -581,6 +848,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&tempty[b], 2 * kEpiWarps);  // the epilogue warps of both CTAs of the pair
     }
     mbar_init(drain, 1);
+    for (int i = 0; i < kTq; ++i) {
+      mbar_init(&tq_full[i], 1);
+      mbar_init(&tq_empty[i], kTqReaders);
+      tq[i] = -1;
+    }
     *tmem_slot = 0;
     *abort = 0;
     fence_mbar_init();
@@ -593,20 +865,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();  // barriers initialised and TMEM allocated in both CTAs
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const TileRing ring{tq, tq_full, tq_empty, mapa_shared(smem_u32(tq_empty), 0)};
 
   if constexpr (kTrace)
-    if (threadIdx.x == 0) trace_emit(p.trace, kTrCtaStart, 0, 0);
+    if (threadIdx.x == 0) trace_emit(p.trace, tc, kTrCtaSlot, kTrCtaStart, 0, 0);
   if (warp == 0) {
-    if (gemm) tma_warp<kI8, kTrace>(p, rank, sA, sB, full, empty, lane, abort);
+    if (gemm) tma_warp<kI8, kTrace>(p, rank, sA, sB, full, empty, ring, lane, abort);
   } else if (warp == 1) {
     if (gemm && rank == 0 && lane == 0)
-      mma_warp<kI8>(p, sA, sB, full, empty, tfull, tempty, tmem, abort);
+      mma_warp<kI8>(p, sA, sB, full, empty, tfull, tempty, ring, tmem, abort);
   } else if (warp < 2 + kCopyWarpsPerCta) {
     if (p.flags & kFlagCopy) copy_warp<kI8, kTrace>(p, lane);
   } else {
     if (gemm)
-      epilogue_warp<kI8, kTrace>(p, rank, warp & 3, (warp - 4) >> 2, lane, tfull, tempty, tmem,
-                                 sEpi, abort);
+      epilogue_warp<kI8, kTrace>(p, rank, warp & 3, (warp - 4) >> 2, lane, tfull, tempty, ring,
+                                 tmem, sEpi, abort);
   }
 
   tc_fence_before();
@@ -631,27 +904,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tmem_dealloc_pair(tmem, 512);
   }
   if constexpr (kTrace)
-    if (threadIdx.x == 0) trace_emit(p.trace, kTrCtaEnd, 0, 0);
+    if (threadIdx.x == 0) trace_emit(p.trace, tc, kTrCtaSlot, kTrCtaEnd, 0, 0);
 }
 
 // ------------------------------------------------------------------ int8 widening
-// fp16 copies of B and of the local shard for the int8 path (exact).
+// fp16 copies of B and of the local shard for the int8 path (exact).  Each
+// thread keeps four 16-byte loads in flight before widening and storing them:
+// the copy is bound by memory latency otherwise.
 __global__ void __launch_bounds__(256) widen_kernel(const uint4* __restrict__ s0,
                                                     uint4* __restrict__ d0, int64_t n0,
                                                     const uint4* __restrict__ s1,
                                                     uint4* __restrict__ d1, int64_t n1) {
+  constexpr int U = 4;
   const int64_t total = n0 + n1;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-       i += stride) {
-    const bool first = i < n0;
-    const int64_t j = first ? i : i - n0;
-    const uint4 v = ld_nc_v4((first ? s0 : s1) + j);
-    uint4 a, b;
-    widen16(v, a, b);
-    uint4* d = (first ? d0 : d1) + 2 * j;
-    d[0] = a;
-    d[1] = b;
+  for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i0 < total;
+       i0 += U * stride) {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t i = i0 + u * stride;
+      if (i < total) v[u] = ld_nc_v4(i < n0 ? s0 + i : s1 + (i - n0));
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t i = i0 + u * stride;
+      if (i >= total) break;
+      uint4 a, b;
+      widen16(v[u], a, b);
+      uint4* d = i < n0 ? d0 + 2 * i : d1 + 2 * (i - n0);
+      d[0] = a;
+      d[1] = b;
+    }
   }
 }
 
@@ -684,7 +968,7 @@ cudaError_t launch_fused(const FusedParams& p, int grid, cudaStream_t stream) {
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
-  if (p.trace.count) {
+  if (p.trace.ev) {
     if (p.g.dtype == 1) return cudaLaunchKernelEx(&cfg, ag_fused_kernel<true, true>, p);
     return cudaLaunchKernelEx(&cfg, ag_fused_kernel<false, true>, p);
   }

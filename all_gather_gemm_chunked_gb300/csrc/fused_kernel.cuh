@@ -36,6 +36,20 @@ struct FusedParams {
   uint32_t* counters;           // [(S-1)][Q] ready counters, monotonic
   unsigned long long* item_counter;  // copy items handed out so far (monotonic)
   unsigned long long item_base;      // item_counter value at the start of this run
+  unsigned long long* tile_counter;  // work items handed out so far (monotonic)
+  unsigned long long tile_base;      // tile_counter value at the start of this run
+  // Work items: tiles [0, full_tiles) whole, the others in `split` K-parts.
+  // Every part but the last stores its partial sums (fp32, or int32 on the
+  // int8 path) to `partials` and counts its 16 epilogue warps on the tile's
+  // flag; the last part waits for the flag to reach part_target, adds the
+  // partials in part order and writes the outputs.
+  int64_t full_tiles;
+  int64_t work_items;
+  int64_t static_items;      // pair k < static_items takes item k first, without a ticket
+  int split;
+  void* partials;            // [tail tiles][split - 1][2 CTAs][128 rows][BN] 4-byte sums
+  uint32_t* part_flags;      // [tail tiles], monotonic
+  uint32_t part_target;      // flag value once every earlier part of this run has stored
   uint32_t* status;             // [2]: status word, detail
   float* C;                     // f16 path output, M x N fp32
   int32_t* C_i32;               // i8 path outputs
@@ -72,6 +86,10 @@ constexpr int kEpiBytes = kEpiWarps * kEpiBoxBytes;  // 32 KB
 constexpr int kSmemBytes =
     kStages * (kABytes + kBBytes) + kEpiBytes + 1024 /*barriers*/ + 1024 /*align*/;
 constexpr int kCopyWarpsPerCta = 2;
+// The pair's tile ring: tile indices drawn by the even CTA's TMA warp, read by
+// the odd CTA's TMA warp, the MMA thread and the 16 epilogue warps of the pair.
+constexpr int kTq = 4;
+constexpr int kTqReaders = 2 + 2 * kEpiWarps;
 
 // ---------------------------------------------------------------- skinny int8 path
 constexpr int kSkMaxRows = 128;   // the gathered rows are the MMA's N operand (N <= 128 here)

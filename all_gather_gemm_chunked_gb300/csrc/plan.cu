@@ -4,11 +4,13 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <vector>
 
 #include "ag_gemm.h"
 #include "fused_kernel.cuh"
@@ -205,6 +207,8 @@ void to_public(const Geometry& g, ag_gemm_geometry* out) {
   if (g.dtype == AG_GEMM_I8) ws += (g.K * g.N + g.R * g.K) * 2;
   out->workspace_bytes = ws;
   out->staging_slots = 0;
+  out->split_tiles = 0;
+  out->split_parts = 1;
 }
 
 bool from_public(const ag_gemm_geometry* in, Geometry& g) {
@@ -236,6 +240,7 @@ struct ag_gemm_plan {
   int device = 0;
   int sm_count = 0;
   int grid = 0;
+  int grid_override = 0;  // ag_gemm_plan_set_grid (fused kernel), 0 = grid
   int mode = AG_GEMM_MODE_PIPELINED;
   int local = 0;
   uint64_t timeout_ns = 1000000000ull;
@@ -247,6 +252,8 @@ struct ag_gemm_plan {
   int64_t counter_count = 0;
   unsigned long long* item_counter = nullptr;  // copy items handed out (monotonic)
   unsigned long long item_base = 0;
+  unsigned long long* tile_counter = nullptr;  // fused kernel: pair tiles handed out (monotonic)
+  unsigned long long tile_base = 0;
   uint32_t* status = nullptr;
   uint16_t* b16 = nullptr;  // int8 path: fp16 copy of B
   uint16_t* a16 = nullptr;  // int8 path: fp16 copy of the local shard
@@ -275,6 +282,14 @@ struct ag_gemm_plan {
   int64_t sk_kq = 0;             // 2-k-block units per n-tile
   int64_t sk_cmax = 0;           // CTAs sharing an n-tile, at most
   int sk_np = 1;                 // k-parts of the remote rows (copy tasks per chunk)
+  // fused kernel: the last round's tiles split into K-parts (split > 1)
+  int split = 1;
+  int64_t full_tiles = 0;        // tiles computed whole
+  int64_t work_items = 0;        // full_tiles + split tiles x split
+  void* partials = nullptr;      // partial sums of the earlier parts
+  int64_t partials_bytes = 0;
+  uint32_t* part_flags = nullptr;
+  uint32_t part_epoch = 0;       // runs of the GEMM since the last reset
   // event trace (ag_gemm_plan_set_trace): [0] count, then the events
   unsigned long long* trace_buf = nullptr;
   int64_t trace_cap = 0;
@@ -293,12 +308,15 @@ void free_plan(ag_gemm_plan* p) {
   cudaFree(p->staging);
   cudaFree(p->counters);
   cudaFree(p->item_counter);
+  cudaFree(p->tile_counter);
   cudaFree(p->status);
   cudaFree(p->b16);
   cudaFree(p->a16);
   cudaFree(p->sk_ws);
   cudaFree(p->credits);
   cudaFree(p->trace_buf);
+  cudaFree(p->partials);
+  cudaFree(p->part_flags);
   if (p->done) cudaEventDestroy(p->done);
   delete p;
 }
@@ -308,22 +326,55 @@ int launch_skinny(ag_gemm_plan* p, agg::SkinnyParams& sp, int flags, cudaStream_
   sp.item_base = p->item_base;
   cudaError_t e = agg::launch_skinny(sp, p->sk_grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "skinny kernel launch");
-  // Each copy warp draws every task's ticket plus one failing ticket.
-  if (flags & agg::kFlagCopy)
-    p->item_base += static_cast<unsigned long long>((p->g.S - 1) * p->g.Q * p->sk_np) +
-                    static_cast<unsigned long long>(p->sk_grid) * agg::kSkCopyWarpsPerCta;
+  // The W copy warps take the first W tasks without a ticket; the rest are
+  // drawn, and every copy warp draws one failing ticket.
+  if (flags & agg::kFlagCopy) {
+    const int64_t tasks = (p->g.S - 1) * p->g.Q * p->sk_np;
+    const int64_t W = static_cast<int64_t>(p->sk_grid) * agg::kSkCopyWarpsPerCta;
+    p->item_base += static_cast<unsigned long long>((tasks > W ? tasks - W : 0) + W);
+  }
   return AG_GEMM_OK;
 }
 
 int launch_fused(ag_gemm_plan* p, agg::FusedParams& fp, int flags, cudaStream_t stream) {
   fp.flags = flags;
   fp.item_base = p->item_base;
-  cudaError_t e = agg::launch_fused(fp, p->grid, stream);
+  fp.tile_counter = p->tile_counter;
+  fp.tile_base = p->tile_base;
+  fp.full_tiles = p->full_tiles;
+  fp.work_items = p->work_items;
+  fp.split = p->split;
+  fp.partials = p->partials;
+  fp.part_flags = p->part_flags;
+  if ((flags & agg::kFlagGemm) && p->split > 1) {
+    // every earlier part's 16 epilogue warps count once on the tile's flag per
+    // run: restart the flags before they would overflow
+    const uint64_t per_run = static_cast<uint64_t>(p->split - 1) * 2 * agg::kEpiWarps;
+    if ((static_cast<uint64_t>(p->part_epoch) + 1) * per_run >= (1ull << 31)) {
+      cudaError_t e = cudaMemsetAsync(p->part_flags, 0,
+                                      sizeof(uint32_t) * (p->g.tiles - p->full_tiles), stream);
+      if (e != cudaSuccess) return cuda_fail(e, "split-tile flag reset");
+      p->part_epoch = 0;
+    }
+    ++p->part_epoch;
+    fp.part_target = static_cast<uint32_t>(p->part_epoch * per_run);
+  }
+  const int grid = p->grid_override > 0 ? p->grid_override : p->grid;
+  // the first item of each pair without a ticket: whole tiles of the local shard
+  int64_t stat = grid / 2;
+  if (stat > p->full_tiles) stat = p->full_tiles;
+  if (stat > p->g.MT * p->g.NT) stat = p->g.MT * p->g.NT;
+  fp.static_items = stat;
+  cudaError_t e = agg::launch_fused(fp, grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "fused kernel launch");
-  // Each copy warp draws every item's ticket plus one failing ticket.
+  // Each copy warp draws every item's ticket plus one failing ticket; each
+  // pair draws every tile it computes plus one failing ticket.
   if (flags & agg::kFlagCopy)
     p->item_base += static_cast<unsigned long long>(p->g.items) +
-                    static_cast<unsigned long long>(p->grid) * agg::kCopyWarpsPerCta;
+                    static_cast<unsigned long long>(grid) * agg::kCopyWarpsPerCta;
+  if (flags & agg::kFlagGemm)
+    p->tile_base += static_cast<unsigned long long>(p->work_items - stat) +
+                    static_cast<unsigned long long>(grid / 2);
   return AG_GEMM_OK;
 }
 
@@ -426,12 +477,15 @@ int run_impl(ag_gemm_plan* p, const void* const* shard_ptrs, const void* B, int6
                           ? static_cast<uint32_t>(p->debug_arg > 1000000 ? 1000000 : p->debug_arg)
                           : 0u;
   if (p->trace_buf) {
-    // the run's events replace the previous run's
-    e = cudaMemsetAsync(p->trace_buf, 0, sizeof(unsigned long long), stream);
+    // the run's events replace the previous run's: a cleared buffer cut into
+    // one region per (CTA, warp slot) of the launch
+    e = cudaMemsetAsync(p->trace_buf, 0, 32 + static_cast<size_t>(p->trace_cap) * 32, stream);
     if (e != cudaSuccess) return cuda_fail(e, "trace reset");
-    fp.trace.count = p->trace_buf;
+    const int64_t ctas = p->skinny ? p->sk_grid
+                                   : (p->grid_override > 0 ? p->grid_override : p->grid);
     fp.trace.ev = reinterpret_cast<agg::TraceEvent*>(p->trace_buf + 4);
-    fp.trace.cap = static_cast<uint32_t>(p->trace_cap);
+    fp.trace.dropped = p->trace_buf;
+    fp.trace.per_slot = static_cast<uint32_t>(p->trace_cap / (ctas * agg::kTrSlots));
   }
 
   const int mode = p->mode;
@@ -681,6 +735,15 @@ ag_gemm_plan* create_plan(int n_shards, int64_t M, int64_t K, int64_t N, int dty
     // a window as large as all remote row blocks is the plain layout
     p->window = w < blocks ? static_cast<int>(w) : 0;
   }
+  // The last round's tiles of the fused kernel, split along K over the pairs
+  // that would otherwise idle (not with a staging window, whose slot credits
+  // count whole tiles).  Chosen for the full grid, so a smaller or larger grid
+  // (ag_gemm_plan_set_grid) computes the same sums.
+  p->split = (skinny || p->window > 0) ? 1 : agg::choose_split(g, p->grid / 2);
+  const int64_t tail = p->split > 1 ? g.tiles % (p->grid / 2) : 0;
+  p->full_tiles = g.tiles - tail;
+  p->work_items = p->full_tiles + tail * p->split;
+  p->partials_bytes = tail * (p->split - 1) * 2 * agg::kBlockM * g.BN * 4;
   p->staging_bytes = p->window > 0 ? static_cast<int64_t>(p->window) * agg::kPairM * g.K * 2
                                    : slots * g.R * g.K * 2;
   p->skinny = skinny;
@@ -695,13 +758,19 @@ ag_gemm_plan* create_plan(int n_shards, int64_t M, int64_t K, int64_t N, int dty
       (e = cudaMalloc(&p->counters, sizeof(uint32_t) * p->counter_count)) != cudaSuccess ||
       (e = cudaMalloc(&p->item_counter, sizeof(unsigned long long))) != cudaSuccess ||
       (e = cudaMemset(p->item_counter, 0, sizeof(unsigned long long))) != cudaSuccess ||
+      (e = cudaMalloc(&p->tile_counter, sizeof(unsigned long long))) != cudaSuccess ||
+      (e = cudaMemset(p->tile_counter, 0, sizeof(unsigned long long))) != cudaSuccess ||
       (e = cudaMalloc(&p->status, 2 * sizeof(uint32_t))) != cudaSuccess ||
       (e = cudaMemset(p->counters, 0, sizeof(uint32_t) * p->counter_count)) != cudaSuccess ||
       (e = cudaMemset(p->status, 0, 2 * sizeof(uint32_t))) != cudaSuccess ||
       (e = cudaEventCreateWithFlags(&p->done, cudaEventDisableTiming)) != cudaSuccess ||
       (p->window > 0 &&
        ((e = cudaMalloc(&p->credits, sizeof(uint32_t) * p->window)) != cudaSuccess ||
-        (e = cudaMemset(p->credits, 0, sizeof(uint32_t) * p->window)) != cudaSuccess))) {
+        (e = cudaMemset(p->credits, 0, sizeof(uint32_t) * p->window)) != cudaSuccess)) ||
+      (tail > 0 &&
+       ((e = cudaMalloc(&p->partials, static_cast<size_t>(p->partials_bytes))) != cudaSuccess ||
+        (e = cudaMalloc(&p->part_flags, sizeof(uint32_t) * tail)) != cudaSuccess ||
+        (e = cudaMemset(p->part_flags, 0, sizeof(uint32_t) * tail)) != cudaSuccess))) {
     cuda_fail(e, "plan allocation");
     free_plan(p);
     return nullptr;
@@ -785,6 +854,11 @@ int ag_gemm_plan_geometry(const ag_gemm_plan* plan, ag_gemm_geometry* out) {
                            static_cast<int64_t>(sizeof(uint32_t)) * plan->counter_count + 64 +
                            plan->sk_tiles * plan->sk_cmax * plan->g.M * 256 * 4;
   }
+  if (!plan->skinny) {
+    out->split_tiles = plan->g.tiles - plan->full_tiles;
+    out->split_parts = plan->split;
+    out->workspace_bytes += plan->partials_bytes + 4 * out->split_tiles;
+  }
   if (plan->window > 0) {
     out->workspace_bytes += plan->staging_bytes - out->staging_bytes + 4 * plan->window;
     out->staging_bytes = plan->staging_bytes;
@@ -800,7 +874,8 @@ int64_t ag_gemm_plan_chunk_rows(const ag_gemm_plan* plan) {
 
 int ag_gemm_plan_grid(const ag_gemm_plan* plan) {
   if (!plan) return fail(AG_GEMM_ERR_INVALID, "plan is NULL");
-  return plan->skinny ? plan->sk_grid : plan->grid;
+  if (plan->skinny) return plan->sk_grid;
+  return plan->grid_override > 0 ? plan->grid_override : plan->grid;
 }
 
 int ag_gemm_plan_path(const ag_gemm_plan* plan) {
@@ -867,14 +942,20 @@ int ag_gemm_plan_reset(ag_gemm_plan* plan, void* stream_v) {
     return cuda_fail(e, "cudaStreamWaitEvent");
   if ((e = cudaMemsetAsync(plan->counters, 0, sizeof(uint32_t) * plan->counter_count, stream)) != cudaSuccess ||
       (e = cudaMemsetAsync(plan->item_counter, 0, sizeof(unsigned long long), stream)) != cudaSuccess ||
+      (e = cudaMemsetAsync(plan->tile_counter, 0, sizeof(unsigned long long), stream)) != cudaSuccess ||
       (e = cudaMemsetAsync(plan->status, 0, 2 * sizeof(uint32_t), stream)) != cudaSuccess ||
       (plan->window > 0 && (e = cudaMemsetAsync(plan->credits, 0, sizeof(uint32_t) * plan->window,
                                                 stream)) != cudaSuccess) ||
+      (plan->part_flags &&
+       (e = cudaMemsetAsync(plan->part_flags, 0,
+                            sizeof(uint32_t) * (plan->g.tiles - plan->full_tiles), stream)) != cudaSuccess) ||
       (e = cudaEventRecord(plan->done, stream)) != cudaSuccess)
     return cuda_fail(e, "plan reset");
   plan->credit_epoch = 0;
+  plan->part_epoch = 0;
   plan->epoch = 0;
   plan->item_base = 0;
+  plan->tile_base = 0;
   plan->last_stream = stream;
   plan->has_run = true;
   return AG_GEMM_OK;
@@ -900,6 +981,18 @@ int ag_gemm_plan_set_timeout_ns(ag_gemm_plan* plan, int64_t ns) {
   if (!plan) return fail(AG_GEMM_ERR_INVALID, "plan is NULL");
   if (ns <= 0) return fail(AG_GEMM_ERR_INVALID, "timeout must be positive");
   plan->timeout_ns = static_cast<uint64_t>(ns);
+  return AG_GEMM_OK;
+}
+
+int ag_gemm_plan_set_grid(ag_gemm_plan* plan, int ctas) {
+  if (!plan) return fail(AG_GEMM_ERR_INVALID, "plan is NULL");
+  if (plan->skinny)
+    return fail(AG_GEMM_ERR_UNSUPPORTED,
+                "the skinny int8 path keeps one CTA per SM (its split-K slots are sized for it)");
+  if (ctas != 0 && (ctas < 2 || ctas % 2 != 0 || ctas > 4 * plan->sm_count))
+    return fail(AG_GEMM_ERR_INVALID, "ctas must be 0 or an even number in [2, %d] (got %d)",
+                4 * plan->sm_count, ctas);
+  plan->grid_override = ctas;
   return AG_GEMM_OK;
 }
 
@@ -951,16 +1044,28 @@ int64_t ag_gemm_plan_trace(ag_gemm_plan* plan, ag_gemm_trace_event* out, int64_t
   cudaError_t e;
   if (plan->has_run && (e = cudaEventSynchronize(plan->done)) != cudaSuccess)
     return cuda_fail(e, "cudaEventSynchronize");
-  unsigned long long count = 0;
-  if ((e = cudaMemcpy(&count, plan->trace_buf, sizeof(count), cudaMemcpyDeviceToHost)) != cudaSuccess)
+  // the dropped count, then every region; recorded events have a non-zero time
+  std::vector<agg::TraceEvent> all;
+  unsigned long long dropped = 0;
+  try {
+    all.resize(static_cast<size_t>(plan->trace_cap));
+  } catch (...) {
+    return fail(AG_GEMM_ERR_OOM, "host allocation for the trace failed");
+  }
+  if ((e = cudaMemcpy(&dropped, plan->trace_buf, sizeof(dropped), cudaMemcpyDeviceToHost)) != cudaSuccess ||
+      (e = cudaMemcpy(all.data(), plan->trace_buf + 4, all.size() * sizeof(agg::TraceEvent),
+                      cudaMemcpyDeviceToHost)) != cudaSuccess)
     return cuda_fail(e, "trace read");
-  int64_t n = static_cast<int64_t>(count);
-  if (n > plan->trace_cap) n = plan->trace_cap;
-  if (n > max_events) n = max_events;
-  if (n > 0 && (e = cudaMemcpy(out, plan->trace_buf + 4, static_cast<size_t>(n) * sizeof(agg::TraceEvent),
-                               cudaMemcpyDeviceToHost)) != cudaSuccess)
-    return cuda_fail(e, "trace read");
-  return static_cast<int64_t>(count);
+  size_t kept = 0;
+  for (size_t i = 0; i < all.size(); ++i)
+    if (all[i].t_ns != 0) all[kept++] = all[i];
+  all.resize(kept);
+  std::stable_sort(all.begin(), all.end(), [](const agg::TraceEvent& a, const agg::TraceEvent& b) {
+    return a.t_ns < b.t_ns;
+  });
+  const size_t n = kept < static_cast<size_t>(max_events) ? kept : static_cast<size_t>(max_events);
+  if (n > 0) std::memcpy(out, all.data(), n * sizeof(agg::TraceEvent));
+  return static_cast<int64_t>(kept + dropped);
 }
 
 int ag_gemm_last_error(void) { return g_last_error; }
@@ -977,7 +1082,7 @@ const char* ag_gemm_last_error_message(void) { return g_last_msg; }
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = 64ull << 20;  // 64 MiB, held on every device that loads the library
-constexpr size_t kNoAllocCtrlBytes = 512;              // status (8 B) + item counter (8 B), padded
+constexpr size_t kNoAllocCtrlBytes = 512;              // status, item and tile counters (8 B each), padded
 constexpr int kNoAllocMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -1062,6 +1167,7 @@ extern "C" int ag_gemm_run_noalloc(int n_shards, int64_t M, int64_t K, int64_t N
   unsigned char* ctrl = d->scratch;
   uint32_t* status = reinterpret_cast<uint32_t*>(ctrl);
   unsigned long long* item_counter = reinterpret_cast<unsigned long long*>(ctrl + 256);
+  unsigned long long* tile_counter = reinterpret_cast<unsigned long long*>(ctrl + 384);
   uint32_t* counters = reinterpret_cast<uint32_t*>(ctrl + kNoAllocCtrlBytes);
   unsigned char* staging = ctrl + kNoAllocCtrlBytes + counter_bytes;
 
@@ -1078,6 +1184,12 @@ extern "C" int ag_gemm_run_noalloc(int n_shards, int64_t M, int64_t K, int64_t N
   fp.counters = counters;
   fp.item_counter = item_counter;
   fp.item_base = 0;
+  fp.tile_counter = tile_counter;
+  fp.tile_base = 0;
+  fp.full_tiles = g.tiles;  // whole tiles only: no partial-sum workspace
+  fp.work_items = g.tiles;
+  fp.split = 1;
+  fp.static_items = 0;      // every tile from the ticket counter
   fp.status = status;
   fp.C = C;
   fp.local = 0;
@@ -1088,7 +1200,7 @@ extern "C" int ag_gemm_run_noalloc(int n_shards, int64_t M, int64_t K, int64_t N
   fp.debug_skip_item = -1;
   fp.flags = agg::kFlagGemm | agg::kFlagWait | (g.S > 1 ? agg::kFlagCopy : 0);
   // Every call shares the array and finds the previous call's values in it:
-  // the status word, the item counter and the ready counters must start at zero.
+  // the status word, the item and tile counters and the ready counters must start at zero.
   if ((e = cudaMemsetAsync(ctrl, 0, kNoAllocCtrlBytes + counter_bytes, stream)) != cudaSuccess)
     return cuda_fail(e, "clearing the no-allocation scratch");
   if ((e = agg::launch_fused(fp, d->grid, stream)) != cudaSuccess)

@@ -105,6 +105,39 @@ AGG_HD void tile_coords(const Geometry& g, int64_t t, int& pos, int64_t& mt,
   nt = w / gm;
 }
 
+// Work items of the fused kernel: the first `full` tiles whole, then the
+// remaining (tail) tiles in `split` parts along K -- the tiles that would
+// leave most CTA pairs idle in the last round.  Tail items go part-major (the
+// first part of every tail tile, then the second ...), so the last part of a
+// tile, which adds the others' partial sums, is handed out after all of them.
+// Item i -> tile t, part j of `parts`, and the part's k-blocks [kb0, kb1).
+AGG_HD void work_item(const Geometry& g, int64_t full, int split, int64_t i, int64_t& t,
+                      int& part, int& parts, int64_t& kb0, int64_t& kb1) {
+  if (i < full) {
+    t = i;
+    part = 0;
+    parts = 1;
+  } else {
+    const int64_t tail = g.tiles - full, r = i - full;
+    part = static_cast<int>(r / tail);
+    t = full + (r - static_cast<int64_t>(part) * tail);
+    parts = split;
+  }
+  kb0 = g.KB * part / parts;
+  kb1 = g.KB * (part + 1) / parts;
+}
+
+// Parts per tail tile for `pairs` CTA pairs: tiles % pairs tiles are left for
+// the last round.  When they fill at most half of the pairs, each is split in
+// two along K (at least 8 k-blocks a part), which halves that round; the last
+// part's addition of the first part's sums costs far less than the half tile.
+inline int choose_split(const Geometry& g, int64_t pairs) {
+  if (pairs < 2) return 1;
+  const int64_t tail = g.tiles % pairs;
+  if (tail == 0 || 2 * tail > pairs || g.KB < 16) return 1;
+  return 2;
+}
+
 AGG_HD int source_of(const Geometry& g, int local, int pos) {
   return (local + pos) % g.S;
 }
@@ -174,15 +207,17 @@ AGG_HD int skinny_parts(const Geometry& g, int64_t KQ) {
 AGG_HD int skinny_part_of(int64_t qu, int64_t KQ, int np) {
   return static_cast<int>(((qu + 1) * np + KQ - 1) / KQ - 1);
 }
+// (32-bit arithmetic: a skinny plan has at most 127 remote rows, K <= 133000.)
 AGG_HD void skinny_task(const Geometry& g, int64_t KQ, int np, int64_t t, int& j, int& pos,
                         int64_t& q, int64_t& k0, int64_t& k1) {
-  const int64_t per_part = (int64_t)(g.S - 1) * g.Q;
-  j = static_cast<int>(t / per_part);
-  const int64_t r = t - (int64_t)j * per_part;
-  pos = 1 + static_cast<int>(r / g.Q);
-  q = r - (int64_t)(pos - 1) * g.Q;
-  k0 = 128 * (KQ * j / np);
-  k1 = 128 * (KQ * (j + 1) / np);
+  const uint32_t Q = static_cast<uint32_t>(g.Q), per_part = static_cast<uint32_t>(g.S - 1) * Q;
+  const uint32_t t32 = static_cast<uint32_t>(t), kq = static_cast<uint32_t>(KQ);
+  j = static_cast<int>(t32 / per_part);
+  const uint32_t r = t32 - static_cast<uint32_t>(j) * per_part;
+  pos = 1 + static_cast<int>(r / Q);
+  q = r - static_cast<uint32_t>(pos - 1) * Q;
+  k0 = 128 * static_cast<int64_t>(kq * static_cast<uint32_t>(j) / static_cast<uint32_t>(np));
+  k1 = 128 * static_cast<int64_t>(kq * static_cast<uint32_t>(j + 1) / static_cast<uint32_t>(np));
   if (k1 > g.K) k1 = g.K;
 }
 AGG_HD int64_t skinny_counter(const Geometry& g, int j, int pos, int64_t q) {

@@ -106,6 +106,38 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
 }
+// 32-bit store to a shared::cluster address (possibly in the peer CTA).
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+// try_wait whose acquire covers the cluster: it orders this thread's later
+// reads after writes that the peer CTA released with its arrive.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity,
+                                                      uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+// mbar_wait with cluster-scope acquire (bounded in the same way).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity,
+                                                  uint64_t timeout_ns, volatile int* abort,
+                                                  const volatile uint32_t* gstatus) {
+  if (mbar_try_wait_cluster(bar, parity, 0)) return true;
+  const uint64_t start = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait_cluster(bar, parity, kWaitSliceNs)) return true;
+    if (*abort) return false;
+    const uint64_t waited = globaltimer_ns() - start;
+    if (waited > timeout_ns) return false;
+    if (waited > kSlowWaitNs && gstatus && *gstatus) return false;
+  }
+}
 
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
@@ -190,6 +222,14 @@ __device__ __forceinline__ void fence_acq_rel_gpu() {
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// A relaxed load at GPU scope: several can be in flight at once.  A reader
+// that saw a released value follows it with fence_acq_rel_gpu() (together an
+// acquire) before it touches the data the release published.
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p));
   return v;
 }
 __device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {

@@ -39,28 +39,41 @@ enum : uint32_t {
   kTrKbWidened = 9,  // skinny: one k-block of B widened into an fp16 stage
   kTrKbMma = 10,     // skinny: the MMAs of one k-block issued and committed
   kTrPieceDone = 11, // skinny: a piece's int32 sums stored to its workspace slot
+  kTrCopyStart = 12, // a copy warp starts a copy item / task (before its loads)
+  kTrAccReady = 13,  // fused: the accumulator of a work item's last segment is ready
+  kTrPartsReady = 14,// fused: a split tile's last part saw every earlier part stored
 };
+
+// The buffer is cut into one region per (CTA, warp slot): 32 slots per CTA,
+// slot = the emitting warp, or kTrCtaSlot for the CTA-wide events of thread 0.
+// Each emitter keeps its own event count, so an event is one plain 32-byte
+// store: no atomics that would stall the pipeline being observed.  The host
+// clears the buffer before a traced run and keeps the slots whose time is
+// non-zero; an emitter whose region is full counts the event as dropped.
+constexpr uint32_t kTrSlots = 32;
+constexpr uint32_t kTrCtaSlot = 31;
 
 struct TraceBuf {
-  unsigned long long* count;  // events attempted (may exceed cap)
-  TraceEvent* ev;
-  uint32_t cap;
+  TraceEvent* ev;                 // nullptr: tracing off
+  unsigned long long* dropped;    // events that did not fit their region
+  uint32_t per_slot;              // events per (CTA, slot) region
 };
 
-__device__ __forceinline__ void trace_emit(const TraceBuf& tb, uint32_t kind, uint32_t id,
-                                           uint64_t aux) {
-  const uint64_t t = globaltimer_ns();
-  const unsigned long long i = atomicAdd(tb.count, 1ull);
-  if (i < tb.cap) {
+__device__ __forceinline__ void trace_emit(const TraceBuf& tb, uint32_t& n, uint32_t slot,
+                                           uint32_t kind, uint32_t id, uint64_t aux) {
+  if (n < tb.per_slot) {
     TraceEvent e;
-    e.t_ns = t;
+    e.t_ns = globaltimer_ns();
     e.kind = kind;
     e.cta = blockIdx.x;
     e.warp = threadIdx.x >> 5;
     e.id = id;
     e.aux = aux;
-    tb.ev[i] = e;
+    tb.ev[(static_cast<uint64_t>(blockIdx.x) * kTrSlots + slot) * tb.per_slot + n] = e;
+  } else {
+    atomicAdd(tb.dropped, 1ull);
   }
+  ++n;
 }
 
 }  // namespace agg

@@ -98,6 +98,10 @@ class Plan:
     def set_timeout_ns(self, ns: int):
         B_.ag_gemm_plan_set_timeout_ns(self.handle, ns)
 
+    def set_grid(self, ctas: int):
+        """CTAs of the fused kernel (0 = one per SM, the default; even otherwise)."""
+        B_.ag_gemm_plan_set_grid(self.handle, ctas)
+
     def set_debug(self, flags: int, arg: int = 0):
         B_.ag_gemm_plan_set_debug(self.handle, flags, arg)
 

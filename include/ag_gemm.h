@@ -92,7 +92,9 @@ typedef enum {
 typedef enum {
     AG_GEMM_DEBUG_NONE = 0,
     AG_GEMM_DEBUG_POISON_STAGING = 1, /* fill staging with NaN / 0x7E before each run */
-    AG_GEMM_DEBUG_SKIP_ITEM = 2,      /* producer skips copy item `arg` (its chunk never becomes ready) */
+    AG_GEMM_DEBUG_SKIP_ITEM = 2,      /* producer skips copy item `arg` (its chunk never becomes
+                                         ready); on the skinny path copy task `arg`, one k-part
+                                         of one chunk (see AG_GEMM_TRACE_LANDED) */
     AG_GEMM_DEBUG_DELAY_NS = 4        /* producer sleeps `arg` ns before each copy item */
 } ag_gemm_debug_flag;
 
@@ -123,6 +125,9 @@ typedef struct {
     int64_t staging_bytes;     /* plan-owned staging workspace */
     int64_t workspace_bytes;   /* everything the plan allocates on the device */
     int64_t staging_slots;     /* staging window in 256-row slots; 0 = one place per remote row */
+    int64_t split_tiles;       /* fused kernel: tiles computed in K-parts by several CTA pairs
+                                  (the last round's tiles; ag_gemm_plan_geometry only) */
+    int64_t split_parts;       /* parts per split tile (1 = no split) */
 } ag_gemm_geometry;
 
 /*
@@ -324,12 +329,18 @@ int ag_gemm_plan_set_debug(ag_gemm_plan *plan, int flags, int64_t arg);
  *                         Fused: id = tile, aux = p << 48 | q0 << 24 | q1
  *                         (chunks q0..q1 of position p; one pair per CTA of a
  *                         pair tile).  Skinny: id = unit, aux = k-part j.
- *   TILE_DONE             fused: an epilogue warp issued its last store of a tile (id = tile)
+ *   TILE_DONE             fused: an epilogue warp issued its last store of a work item
+ *                         (id = tile, aux = part | parts << 8; parts = 1 for a whole tile)
+ *   ACC_READY             fused: the accumulator of a work item's last segment is ready
+ *                         for the epilogue (id, aux as for TILE_DONE)
+ *   PARTS_READY           fused: the last part of a split tile saw every earlier part's
+ *                         partial sums stored (id = tile)
  *   UNIT_ISSUED           skinny: a unit's loads issued (id = unit)
  *   UNIT_LANDED           skinny: a unit's operands in shared memory (id = unit)
  *   KB_WIDENED            skinny: a k-block of B widened to fp16 (id = k-block of the n-tile, aux = unit)
  *   KB_MMA                skinny: a k-block's MMAs issued (id = k-block of the n-tile, aux = n-tile)
  *   PIECE_DONE            skinny: a CTA's split-K sums of one n-tile stored (id = n-tile, aux = next unit)
+ *   COPY_START            a copy warp starts a copy item (id, aux as for LANDED)
  */
 typedef enum {
     AG_GEMM_TRACE_CTA_START = 1,
@@ -342,7 +353,10 @@ typedef enum {
     AG_GEMM_TRACE_UNIT_LANDED = 8,
     AG_GEMM_TRACE_KB_WIDENED = 9,
     AG_GEMM_TRACE_KB_MMA = 10,
-    AG_GEMM_TRACE_PIECE_DONE = 11
+    AG_GEMM_TRACE_PIECE_DONE = 11,
+    AG_GEMM_TRACE_COPY_START = 12,
+    AG_GEMM_TRACE_ACC_READY = 13,
+    AG_GEMM_TRACE_PARTS_READY = 14
 } ag_gemm_trace_kind;
 
 typedef struct {
@@ -358,20 +372,34 @@ typedef struct {
  * Turn tracing on (capacity > 0 events, at most 2^26; allocates
  * 32 + 32 * capacity bytes on the device) or off (capacity = 0, frees the
  * buffer).  Waits for the plan's last run.  Every later run clears the trace
- * and records its own events; events past the capacity are dropped (counted).
+ * and records its own events.  The capacity is split evenly between the
+ * launch's CTAs, 32 warp slots each (an event is a plain store into its
+ * warp's region, so tracing does not serialise the kernel on atomics); events
+ * past a region's share are dropped and counted.
  */
 int ag_gemm_plan_set_trace(ag_gemm_plan *plan, int64_t capacity);
 
 /*
- * Wait for the plan's last run and copy up to max_events of its events (in
- * the order they were recorded, which is not strictly time order) to the
- * HOST array out.  Returns the number of events the run tried to record
- * (more than were kept if the capacity was exceeded), or a negative status
+ * Wait for the plan's last run and copy up to max_events of its events,
+ * sorted by time, to the HOST array out.  Returns the number of events the
+ * run tried to record (kept + dropped), or a negative status
  * (AG_GEMM_ERR_STATE when tracing is off).
  */
 int64_t ag_gemm_plan_trace(ag_gemm_plan *plan, ag_gemm_trace_event *out, int64_t max_events);
 
-/* Number of CTAs the plan's main kernel launches (one per SM). */
+/*
+ * Number of CTAs the fused kernel launches (fp16, bf16 and int8 plans with
+ * M > 128): 0 = the default, one CTA per SM in CTA pairs; otherwise an even
+ * number in [2, 4 * SMs].  Pair tiles are handed out at run time in schedule
+ * order, so any grid computes the same C: a smaller grid simply has fewer
+ * pairs, and a grid larger than the GPU holds at once leaves the extra pairs
+ * to start as others finish (they find the tiles taken and exit) -- the
+ * partial residency a GPU shared with other work can also cause.
+ * AG_GEMM_ERR_UNSUPPORTED on the skinny int8 path (one CTA per SM, fixed).
+ */
+int ag_gemm_plan_set_grid(ag_gemm_plan *plan, int ctas);
+
+/* Number of CTAs the plan's main kernel launches (one per SM unless set). */
 int ag_gemm_plan_grid(const ag_gemm_plan *plan);
 
 /* The ag_gemm_path the plan runs (fixed at creation by dtype and M); a

@@ -585,3 +585,55 @@ def test_nshard_pitch_checks():
         with pytest.raises(B_.AgGemmError) as e:
             B_.ag_gemm_run_ld(plan.handle, ptrs, Bfull.data_ptr(), D * ns, C.data_ptr(), D * ns)
         assert e.value.code == B_.ERR_INVALID
+
+
+# ---------------------------------------------------------------------------
+# the last round's tiles split along K over otherwise idle CTA pairs: earlier
+# parts store partial sums, the last part adds them in part order
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dt,S,R,K,N", [
+    ("f16", 2, 512, 2048, 1024),   # 16 tiles, 2 parts each
+    ("bf16", 3, 300, 1024, 520),   # 18 tiles (ragged rows and columns), 2 parts each
+    ("i8", 2, 384, 2080, 512),     # 8 tiles, 2 parts of 16 and 17 k-blocks (int32 partials)
+])
+def test_split_tail_parity_modes_and_repeats(oracle, dt, S, R, K, N):
+    x = synth.make_inputs(S, R, K, N, dt, 7000 + S * 17 + K)
+    run = {"f16": run_f16, "bf16": run_bf16, "i8": run_i8}[dt]
+    with Plan(S, S * R, K, N, dt) as plan:
+        g = plan.geometry
+        assert g["split_parts"] > 1 and g["split_tiles"] > 0, g
+        first = run(x, S, R, K, N, plan=plan)
+        if dt == "i8":
+            Cref, Dref = oracle.ag_gemm_dequant(x["shards"], x["B"], x["bias"], x["scale"])
+            _check_i8(first[0], first[1], Cref, Dref, "split tail")
+        else:
+            ref = (oracle.ag_gemm_f16 if dt == "f16" else oracle.ag_gemm_bf16)(x["shards"], x["B"])
+            check_f16(first, ref, K, f"split tail {dt}")
+        # the part flags are monotonic across runs and modes; a reset restarts them
+        for mode in (B_.MODE_PIPELINED, B_.MODE_COMPUTE_ONLY, B_.MODE_SEQUENTIAL,
+                     B_.MODE_PIPELINED):
+            again = run(x, S, R, K, N, plan=plan, mode=mode)
+            same = (np.array_equal(again[0], first[0]) and np.array_equal(again[1], first[1])
+                    if dt == "i8" else np.array_equal(again, first))
+            assert same, f"mode {mode}"
+        plan.reset()
+        again = run(x, S, R, K, N, plan=plan, mode=B_.MODE_PIPELINED)
+        assert (np.array_equal(again[0], first[0]) if dt == "i8" else np.array_equal(again, first))
+
+
+def test_split_tail_plan_geometry():
+    """The split is chosen for the device's full grid: when the last round's
+    tiles fill at most half of the CTA pairs, each is split in two along K
+    (each part >= 8 k-blocks)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    pairs = sms // 2
+    with Plan(2, 4096, 4096, 4096, "f16") as p:      # 256 pair tiles
+        g = p.geometry
+        assert g["split_tiles"] == 256 % pairs and g["split_parts"] == 2
+    with Plan(8, 8192, 4096, 4096, "f16") as p:      # 512 tiles: the last round is too full
+        assert p.geometry["split_parts"] == 1
+    with Plan(2, 512, 256, 512, "f16") as p:         # 4 k-blocks: too short to split
+        assert p.geometry["split_parts"] == 1 and p.geometry["split_tiles"] == 0
+    with Plan(4, 4096, 2048, 2048, "f16", staging_slots=8) as p:   # a staging window
+        assert p.geometry["split_parts"] == 1

@@ -5,9 +5,13 @@ m-tile of a remote shard, in consumption order) lives in slot b % W, and the
 producer may write block b only once every tile of block b - W has read its
 rows.  These tests check the chunk rule such a plan uses, and -- by simulating
 the persistent schedule exactly as the kernel walks it (tile order from the
-library's own ag_gemm_tile_at, tiles dealt round-robin to the CTA pairs) --
-that a window of at least one swizzle group (group_m = 8 blocks) always
-finishes, while a smaller one can stall for good.
+library's own ag_gemm_tile_at, tiles handed out by a ticket counter in that
+order to whichever CTA pairs are running) -- that a window of at least one
+swizzle group (group_m = 8 blocks) always finishes, also when fewer pairs are
+resident than were launched, while a smaller window can stall for good.  A
+static deal of tiles to pairs (pair p takes tiles p, p + pairs, ...) is
+simulated too: under partial residency it can stall, which is why the kernel
+hands tiles out at run time.
 """
 import pytest
 
@@ -28,6 +32,90 @@ def test_bounded_chunk_rule():
             assert c == best, R
     assert B_.ag_gemm_choose_chunk_rows_bounded(3000) == 8
     assert B_.ag_gemm_choose_chunk_rows_bounded(4096) == 64
+
+
+def _block_of(g, local):
+    S, MT = g.n_shards, g.m_tiles
+
+    def block(t):
+        src, mt, _ = B_.ag_gemm_tile_at(g, local, t)
+        pos = (src - local) % S
+        return None if pos == 0 else (pos - 1) * MT + mt
+    return [block(t) for t in range(g.tiles)]
+
+
+def _simulate_tickets(g, local, W, resident):
+    """True if every tile completes when `resident` pairs run at once and take
+    tiles from a ticket counter in schedule order (a pair holds its tile until
+    the tile's block is produced).  Producer: blocks in order, block b once the
+    NT tiles of block b - W have read their rows."""
+    blocks = _block_of(g, local)
+    nblocks = (g.n_shards - 1) * g.m_tiles
+    produced, consumed = 0, [0] * nblocks
+    holding = [None] * resident   # tile each running pair works on
+    ticket, done = 0, 0
+    while True:
+        progress = False
+        while produced < nblocks and (produced < W or consumed[produced - W] == g.n_tiles):
+            produced += 1
+            progress = True
+        for p in range(resident):
+            while True:
+                if holding[p] is None:
+                    if ticket == g.tiles:
+                        break
+                    holding[p] = ticket
+                    ticket += 1
+                    progress = True
+                b = blocks[holding[p]]
+                if b is not None and b >= produced:
+                    break
+                if b is not None:
+                    consumed[b] += 1
+                holding[p] = None
+                done += 1
+                progress = True
+        if done == g.tiles:
+            return True
+        if not progress:
+            return False
+
+
+def _simulate_static(g, local, W, pairs, resident):
+    """The static deal: pair p takes tiles p, p + pairs, ...; only the first
+    `resident` pairs run, a later pair starts when a running one has finished
+    all of its tiles."""
+    blocks = _block_of(g, local)
+    nblocks = (g.n_shards - 1) * g.m_tiles
+    produced, consumed = 0, [0] * nblocks
+    nxt = list(range(min(pairs, g.tiles)))
+    running = list(range(min(resident, len(nxt))))
+    waiting = list(range(len(running), len(nxt)))
+    done = 0
+    while True:
+        progress = False
+        while produced < nblocks and (produced < W or consumed[produced - W] == g.n_tiles):
+            produced += 1
+            progress = True
+        for p in list(running):
+            while nxt[p] < g.tiles:
+                b = blocks[nxt[p]]
+                if b is not None and b >= produced:
+                    break
+                if b is not None:
+                    consumed[b] += 1
+                nxt[p] += pairs
+                done += 1
+                progress = True
+            if nxt[p] >= g.tiles:
+                running.remove(p)
+                if waiting:
+                    running.append(waiting.pop(0))
+                progress = True
+        if done == g.tiles:
+            return True
+        if not progress:
+            return False
 
 
 def _simulate(g, local, W, pairs):
@@ -78,9 +166,29 @@ def test_window_of_a_swizzle_group_always_finishes(S, R, N):
                 assert _simulate(g, local, W, pairs), (S, R, N, W, pairs, local)
 
 
+@pytest.mark.parametrize("S,R,N", [(4, 4096, 4096), (8, 1024, 4096), (3, 600, 392),
+                                   (5, 2560, 1024)])
+def test_window_with_tickets_finishes_under_partial_residency(S, R, N):
+    g = B_.ag_gemm_geometry_of(S, S * R, 256, N, 0, 0)
+    for W in (8, 16):
+        for resident in (1, 7, 38, 76):
+            for local in {0, S - 1}:
+                assert _simulate_tickets(g, local, W, resident), (S, R, N, W, resident, local)
+
+
+def test_static_deal_can_stall_under_partial_residency():
+    # workload 4's shape with a window of 16 slots: 76 pairs launched, 7 resident
+    g = B_.ag_gemm_geometry_of(4, 4 * 4096, 256, 4096, 0, 0)
+    assert _simulate_static(g, 0, 16, 76, 76)
+    assert not _simulate_static(g, 0, 16, 76, 7)
+    assert _simulate_tickets(g, 0, 16, 7)
+
+
 def test_window_below_a_swizzle_group_can_stall():
     g = B_.ag_gemm_geometry_of(2, 2 * 8 * 256, 256, 512, 0, 0)  # 8 m-tiles, 2 n-tiles
     assert g.m_tiles == 8 and g.n_tiles == 2
     # one pair walks the group m-fastest: it needs block 4 before block 0 is done
     assert not _simulate(g, 0, 4, 1)
     assert _simulate(g, 0, 8, 1)
+    assert not _simulate_tickets(g, 0, 4, 1)
+    assert _simulate_tickets(g, 0, 8, 1)

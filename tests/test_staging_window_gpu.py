@@ -137,3 +137,31 @@ def test_window_plan_checks():
         with pytest.raises(B_.AgGemmError) as e:
             Plan(4, 4 * 3072, 256, 256, "f16", chunk, staging_slots=slots)
         assert e.value.code == B_.ERR_INVALID
+
+
+GRID_CASES = [
+    # dt, S, R, K, N, W (None = plain staging)
+    ("f16", 4, 600, 256, 384, 8),
+    ("i8", 5, 520, 1056, 208, 9),
+    ("f16", 3, 1000, 512, 520, None),
+    ("f16", 2, 1536, 2048, 2048, None),   # 96 tiles: the last round's 20 split in two along K
+    ("i8", 3, 512, 1024, 768, None),      # 18 tiles split in parts (int32 partial sums)
+]
+
+
+@pytest.mark.parametrize("dt,S,R,K,N,W", GRID_CASES)
+def test_any_grid_gives_the_same_result(dt, S, R, K, N, W):
+    """Pair tiles are handed out at run time in schedule order, so the grid does
+    not change C: one pair, a few pairs, and four times the pairs the GPU holds
+    at once (the extra pairs start only as earlier ones finish -- the partial
+    residency of a shared GPU -- and must never be waited for)."""
+    x = _inputs(dt, S, R, K, N, 6500 + S * 7 + K)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    with Plan(S, S * R, K, N, dt, staging_slots=W) as plan:
+        ref = _run(plan, x, dt)
+        for ctas in (2, 6, 4 * sms - (4 * sms) % 2, 0):
+            plan.set_grid(ctas)
+            assert plan.grid == (ctas or plan.grid)
+            assert _same(_run(plan, x, dt), ref), f"grid {ctas}"
+        with pytest.raises(B_.AgGemmError):
+            plan.set_grid(3)

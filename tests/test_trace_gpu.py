@@ -98,7 +98,10 @@ def test_trace_fused_f16_waits_follow_landings(S, R, K, N, c):
     tiles = geo["tiles"]
     local_tiles = tiles // S
     assert set(ends["id"].tolist()) == set(range(local_tiles, tiles))
-    assert np.count_nonzero(ev["kind"] == B_.TRACE_TILE_DONE) == tiles * 2
+    done = ev[ev["kind"] == B_.TRACE_TILE_DONE]
+    final = (done["aux"] & 0xFF) == (done["aux"] >> 8) - 1   # whole tiles and last parts
+    assert np.count_nonzero(final) == tiles * 2
+    assert sorted(set(done["id"][final].tolist())) == list(range(tiles))
 
 
 @pytest.mark.parametrize("S,R,K,N", [
@@ -184,10 +187,10 @@ def test_trace_off_and_capacity():
         with pytest.raises(B_.AgGemmError) as e:
             plan.trace()
         assert e.value.code == B_.ERR_STATE
-        plan.set_trace(4)           # far too small: events are counted, 4 kept
+        plan.set_trace(4)           # far too small: events are counted, at most 4 kept
         _run(plan, x, "f16")
         n, ev = plan.trace()
-        assert n > 4 and len(ev) == 4
+        assert n > 4 and len(ev) <= 4
         plan.set_trace(0)
         with pytest.raises(B_.AgGemmError):
             plan.trace()
