@@ -189,46 +189,71 @@ __device__ void copy_warp(const FusedParams& p, int lane) {
   }
 }
 
-// ------------------------------------------------------------------ tile ring
-// Tiles are handed out dynamically: the even CTA's TMA warp draws pair tiles
-// from a grid-wide ticket counter, in schedule order, and publishes each index
-// (or -1 once none is left) in a kTq-deep ring in the shared memory of both
-// CTAs of the pair.  So whichever pairs are resident always take the lowest
-// tiles not yet taken: no tile waits on a pair that has not started, which
-// keeps the staging window's credits live even when fewer pairs are resident
-// than were launched.
+// ------------------------------------------------------------------ work items
+// A pair's items: first the whole tiles dealt round-robin -- pair k takes
+// items k, k + pairs, ... below static_items -- then items handed out at run
+// time.  The dealt items wait on no other pair (plain staging), so they need
+// no coordination; the rest -- the split parts of the last round's tiles, and
+// every item when a staging window's credits tie tiles to one another -- are
+// drawn from a grid-wide ticket counter in schedule order.  Whichever pairs
+// are resident therefore always take the lowest items left: no item waits on
+// a pair that has not started (the window's credits and a split tile's
+// partial sums come only from items drawn earlier), even when fewer pairs are
+// resident than were launched.
+//
+// The even CTA's TMA warp (lane 1) draws the tickets and publishes the drawn
+// items, two ahead of use, in a kTq-deep ring in the shared memory of both
+// CTAs of the pair.  The TMA warps and the MMA thread read the ring; the 16
+// epilogue warps read it after the MMA has finished the item's first segment
+// and are the ones that free a slot: by then both TMA warps and the MMA
+// thread have read the item (their reads precede the loads and MMAs the
+// epilogue waited for).
 struct TileRing {
-  int32_t* tq;         // this CTA's ring of tile indices
+  int32_t* tq;         // this CTA's ring of items
   uint64_t* full;      // this CTA's "published" barriers (one arrival: the producer)
   uint64_t* empty;     // the even CTA's "read" barriers (kTqReaders arrivals)
   uint32_t empty0;     // shared::cluster address of the even CTA's empty[0]
 };
 
-// A reader's n-th tile (the caller's single thread): false on timeout/abort.
+struct PairItems {
+  int64_t pair, pairs, n_static;  // this pair, all pairs, this pair's dealt items
+  bool drawn;                     // does the plan have drawn items at all?
+  __device__ __forceinline__ explicit PairItems(const FusedParams& p) {
+    pair = blockIdx.x / 2;
+    pairs = gridDim.x / 2;
+    n_static = pair < p.static_items ? (p.static_items - pair + pairs - 1) / pairs : 0;
+    drawn = p.work_items > p.static_items;
+  }
+  __device__ __forceinline__ bool dealt(uint32_t seq) const { return seq < n_static; }
+  // Every item dealt: the pair is done after its own, with no ring traffic.
+  __device__ __forceinline__ bool done(uint32_t seq) const { return !drawn && seq >= n_static; }
+  __device__ __forceinline__ int64_t dealt_item(uint32_t seq) const { return pair + seq * pairs; }
+  __device__ __forceinline__ uint32_t ring_index(uint32_t seq) const {
+    return seq - static_cast<uint32_t>(n_static);
+  }
+};
+
+// Ring entry n (the caller's single thread); `release` frees the slot.
+// false on timeout/abort.
 __device__ __forceinline__ bool ring_read(const TileRing& r, uint32_t n, int64_t& t,
                                           uint64_t timeout_ns, volatile int* abort,
-                                          const volatile uint32_t* gstatus) {
+                                          const volatile uint32_t* gstatus, bool release) {
   const uint32_t slot = n % kTq, ph = (n / kTq) & 1u;
   if (!mbar_wait_cluster(&r.full[slot], ph, timeout_ns, abort, gstatus)) return false;
   t = *reinterpret_cast<volatile int32_t*>(&r.tq[slot]);
-  mbar_arrive_cluster(r.empty0 + slot * 8);  // the slot may be refilled
+  if (release) mbar_arrive_cluster(r.empty0 + slot * 8);
   return true;
 }
 
-// The producer's side (even CTA, one thread).  A ticket is drawn from the
-// grid-wide counter (ring_draw) well before it is needed and published as the
-// pair's n-th tile once the slot is free (ring_put): into both CTAs' rings.
-// Pair k's first item is item k when k < static_items (a whole tile of the
-// local shard: it waits for nothing, so a pair that starts late holds up no
-// other pair); every other item comes from the ticket counter: ticket i is
-// item static_items + i.
-__device__ __forceinline__ int64_t ring_draw(const FusedParams& p) {
-  const unsigned long long ticket = atomicAdd(p.tile_counter, 1ull);
+// The producer's side (even CTA, lane 1 of the TMA warp).  Ticket i is item
+// static_items + i; exactly one failing ticket per pair and run (a negative
+// one means the counters were not reset after a failed run: take nothing).
+__device__ __forceinline__ int64_t ring_item(const FusedParams& p, unsigned long long ticket) {
   const int64_t i = static_cast<int64_t>(ticket - p.tile_base);
-  // exactly one failing ticket per pair and run; a negative one means the
-  // counters were not reset after a failed run: take nothing
   return (i >= 0 && p.static_items + i < p.work_items) ? p.static_items + i : -1;
 }
+
+// Publish item t as ring entry n in both CTAs' rings once the slot is free.
 __device__ __forceinline__ bool ring_put(const FusedParams& p, const TileRing& r, uint32_t n,
                                          int64_t t, volatile int* abort,
                                          const volatile uint32_t* gstatus) {
@@ -254,10 +279,10 @@ __device__ bool wait_chunks(const FusedParams& p, int pos, int64_t row0, int lan
   const uint32_t* cnt = p.counters + (int64_t)(pos - 1) * g.Q;
   bool ok = true;
   for (int64_t q = q0 + lane; q <= q1 && ok; q += 32) {
-    if (ld_relaxed_gpu(cnt + q) >= target) continue;
+    if (ld_acquire_gpu(cnt + q) >= target) continue;
     const uint64_t deadline = globaltimer_ns() + p.timeout_ns;
     uint32_t spins = 0;
-    while (ld_relaxed_gpu(cnt + q) < target) {
+    while (ld_acquire_gpu(cnt + q) < target) {
       __nanosleep(64);
       if (++spins == 16) {
         spins = 0;
@@ -269,7 +294,6 @@ __device__ bool wait_chunks(const FusedParams& p, int pos, int64_t row0, int lan
       }
     }
   }
-  fence_acq_rel_gpu();  // with the relaxed reads above: an acquire of every counter seen
   ok = __all_sync(0xffffffffu, ok);
   if (!ok && lane == 0) {
     set_status(p.status, kStatusChunkTimeout,
@@ -299,33 +323,39 @@ __device__ void tma_warp(const FusedParams& p, uint32_t rank, uint8_t* sA, uint8
     tma_prefetch_desc(&p.tm_b);
   }
   bool ok = true;
-  // Even CTA: the ticket for item seq + 1 is requested when item seq starts and
-  // published once item seq's loads have been issued, so the ticket's round
-  // trip to L2 never holds up a load.
-  uint32_t published = 0;  // items published so far
-  bool drawn_all = false;  // the end marker (-1) has been published
-  if (rank == 0 && lane == 0) {
-    const int64_t pair = blockIdx.x / 2;
-    const int64_t first = pair < p.static_items ? pair : ring_draw(p);
-    ok = ring_put(p, ring, published, first, abort, gstatus);
-    ++published;
-    drawn_all = first < 0;
+  const PairItems items(p);
+  // Even CTA, lane 1: ring entries published so far, and whether the end
+  // marker (-1) is among them.  Entries go out two ahead of use: while item
+  // seq runs, entries up to seq + 2 - n_static are drawn.
+  int64_t published = 0;
+  bool drawn_all = false;
+  if (rank == 0 && lane == 1 && items.drawn && items.n_static == 0) {
+    // a pair with no dealt item publishes its first item before any load
+    // (one ticket: every pair takes exactly one failing ticket per run, the
+    // count the host advances the ticket base by); the loop below keeps two
+    // entries ahead from the first item on
+    const int64_t t = ring_item(p, atomicAdd(p.tile_counter, 1ull));
+    ok = ring_put(p, ring, 0u, t, abort, gstatus);
+    published = 1;
+    drawn_all = t < 0;
   }
-  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-  for (uint32_t seq = 0; ok; ++seq) {
-    // the pair's next tile: published by the even CTA, read by the odd one
-    int64_t t = -1, ahead = -1;
+  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 1) != 0;
+  for (uint32_t seq = 0; ok && !items.done(seq); ++seq) {
+    int64_t t = -1;
     bool got = true;
-    if (lane == 0) {
-      if (rank == 0) {
-        t = *reinterpret_cast<volatile int32_t*>(&ring.tq[seq % kTq]);
-        if (t >= 0 && !drawn_all) ahead = ring_draw(p);
-      } else {
-        got = ring_read(ring, seq, t, p.pipe_timeout_ns, abort, gstatus);
-      }
+    if (items.dealt(seq)) {
+      t = items.dealt_item(seq);
+    } else if (lane == 0) {
+      got = ring_read(ring, items.ring_index(seq), t, p.pipe_timeout_ns, abort, gstatus, false);
     }
     got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
     t = __shfl_sync(0xffffffffu, t, 0);
+    // lane 1 of the even CTA draws one more ticket during this item?
+    const bool draw = rank == 0 && items.drawn &&
+                      __shfl_sync(0xffffffffu,
+                                  (!drawn_all && published < static_cast<int64_t>(seq) + 3 -
+                                                                 items.n_static) ? 1 : 0,
+                                  1) != 0;
     if (!got) {
       ok = false;
       break;
@@ -351,6 +381,8 @@ __device__ void tma_warp(const FusedParams& p, uint32_t rank, uint8_t* sA, uint8
     } else {
       if (pos > 0 && wait && !wait_chunks(p, pos, row0, lane, abort)) break;
     }
+    unsigned long long ticket = 0;
+    if (lane == 1 && draw) ticket = atomicAdd(p.tile_counter, 1ull);
     if (lane == 0) {
       if (pos > 0) {
         fence_acq_rel_gpu();
@@ -390,13 +422,15 @@ __device__ void tma_warp(const FusedParams& p, uint32_t rank, uint8_t* sA, uint8
           phase ^= 1u;
         }
       }
-      if (ok && rank == 0 && !drawn_all) {
-        ok = ring_put(p, ring, published, ahead, abort, gstatus);
-        ++published;
-        drawn_all = ahead < 0;
-      }
     }
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    if (lane == 1 && ok && draw) {
+      const int64_t ahead = ring_item(p, ticket);
+      ok = ring_put(p, ring, static_cast<uint32_t>(published), ahead, abort, gstatus);
+      ++published;
+      drawn_all = ahead < 0;
+    }
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 1) != 0;
   }
   if (lane == 0) {
     if (!ok) {
@@ -430,13 +464,29 @@ __device__ void mma_warp(const FusedParams& p, const uint8_t* sA, const uint8_t*
   int stage = 0;
   uint32_t phase = 0, unit = 0;
   bool ok = true;
-  for (uint32_t seq = 0; ok; ++seq) {
+  const PairItems items(p);
+  for (uint32_t seq = 0; ok && !items.done(seq); ++seq) {
     int64_t t = -1;
-    if (!ring_read(ring, seq, t, p.pipe_timeout_ns, abort, gstatus)) {
+    if (items.dealt(seq)) {
+      t = items.dealt_item(seq);
+    } else if (!ring_read(ring, items.ring_index(seq), t, p.pipe_timeout_ns, abort, gstatus,
+                          false)) {
       ok = false;
       break;
     }
-    if (t < 0) break;
+    if (t < 0) {
+      // no more items: complete one more accumulator phase without MMAs, so
+      // that the epilogue, which reads the ring only after an accumulator is
+      // ready, can read the end marker
+      const uint32_t buf = unit & 1u, use = unit >> 1;
+      if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, p.pipe_timeout_ns, abort, gstatus)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      mma_commit_pair_both(&tfull[buf]);
+      break;
+    }
     int64_t tile, kbs, kbe;
     int part, parts;
     work_item(g, p.full_tiles, p.split, t, tile, part, parts, kbs, kbe);
@@ -549,7 +599,7 @@ __device__ __forceinline__ void signal_part(const FusedParams& p, int64_t tail, 
   if (lane == 0) red_release_gpu_add(p.part_flags + tail, 1u);
 }
 
-template <bool kI8, bool kTrace>
+template <bool kI8, bool kTrace, bool kSplit>
 __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int half, int lane,
                               uint64_t* tfull, uint64_t* tempty, const TileRing& ring,
                               uint32_t tmem, uint8_t* sEpi, volatile int* abort) {
@@ -565,12 +615,22 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
   // (at most 4 chunks of 32), kept in registers across the tile's segments
   uint32_t sums[kI8 ? 128 : 1];
   uint32_t unit = 0;
-  for (uint32_t seq = 0;; ++seq) {
+  const PairItems items(p);
+  for (uint32_t seq = 0; !items.done(seq); ++seq) {
     int64_t t = -1;
     bool got = true;
-    if (lane == 0) got = ring_read(ring, seq, t, p.pipe_timeout_ns, abort, gstatus);
-    got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
-    t = __shfl_sync(0xffffffffu, t, 0);
+    if (items.dealt(seq)) {
+      t = items.dealt_item(seq);
+    } else {
+      // a drawn item: read it (and free its slot) once its first accumulator
+      // is ready -- or the MMA's closing phase, if there is no item left
+      const uint32_t buf = unit & 1u, use = unit >> 1;
+      got = mbar_wait(&tfull[buf], use & 1u, p.pipe_timeout_ns, abort, gstatus);
+      if (lane == 0 && got)
+        got = ring_read(ring, items.ring_index(seq), t, p.pipe_timeout_ns, abort, gstatus, true);
+      got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+      t = __shfl_sync(0xffffffffu, t, 0);
+    }
     if (!got) {
       if (lane == 0) {
         set_status(p.status, kStatusPipelineTimeout, 0x400u | rank);
@@ -586,8 +646,10 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
     const int64_t seg_len = kI8 ? kSegBlocks : kbe - kbs;
     const int64_t nseg = ceil_div(kbe - kbs, seg_len);
     // a split tile: earlier parts store partial sums, the last part adds them
-    const bool store_part = parts > 1 && part < parts - 1;
-    const bool add_parts = parts > 1 && part == parts - 1;
+    // (compiled only into the kernel a splitting plan launches: the split
+    // paths would raise the register count of every tile's epilogue)
+    const bool store_part = kSplit && parts > 1 && part < parts - 1;
+    const bool add_parts = kSplit && parts > 1 && part == parts - 1;
     const int64_t tail = tile - p.full_tiles;
     // Partial sums of part j of this tail tile, laid out for this warp: 16-byte
     // vector c of every lane of the warp is contiguous (512 bytes), so each
@@ -595,12 +657,15 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
     // a lane holds its row's columns 4c .. 4c + 3 of the warp's half of the
     // tile; a (tile, part) takes 2 CTAs x 8 warps x BN / 8 x 32 lanes x 16 B
     // = 2 x 128 rows x BN x 4 bytes, the size the plan allocates per part.
+    // (part j's vector c of this lane: base + j * part_stride + c * 32)
     const int64_t vecs = g.BN / 8;
-    auto part_vec = [&](int j, int c) -> uint4* {
-      return static_cast<uint4*>(p.partials) +
-             (((((tail * (p.split - 1) + j) * 2 + rank) * kEpiWarps + half * 4 + quad) * vecs +
-               c) * 32 + lane);
-    };
+    const int64_t part_stride = 2 * kEpiWarps * vecs * 32;
+    uint4* const part_base =
+        parts > 1 ? static_cast<uint4*>(p.partials) +
+                        ((((tail * (p.split - 1)) * 2 + rank) * kEpiWarps + half * 4 + quad) * vecs *
+                             32 + lane)
+                  : nullptr;
+    auto part_vec = [&](int j, int c) -> uint4* { return part_base + j * part_stride + c * 32; };
     int pos;
     int64_t mt, nt;
     tile_coords(g, tile, pos, mt, nt);
@@ -663,29 +728,31 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
             continue;
           }
           if (add_parts) {
-            // (part 0 + part 1 + ...) + this part, in that order
-            uint4 x[8];
+            // (part 0 + part 1 + ...) + this part, in that order; 4 vectors
+            // of the partials in flight at a time
 #pragma unroll
-            for (int c = 0; c < 8; ++c) x[c] = __ldcg(part_vec(0, jj * 8 + c));
-            for (int pj = 1; pj < parts - 1; ++pj) {
+            for (int c0 = 0; c0 < 8; c0 += 4) {
+              uint4 x[4];
 #pragma unroll
-              for (int c = 0; c < 8; ++c) {
-                const uint4 y = __ldcg(part_vec(pj, jj * 8 + c));
-                x[c].x = __float_as_uint(__fadd_rn(__uint_as_float(x[c].x), __uint_as_float(y.x)));
-                x[c].y = __float_as_uint(__fadd_rn(__uint_as_float(x[c].y), __uint_as_float(y.y)));
-                x[c].z = __float_as_uint(__fadd_rn(__uint_as_float(x[c].z), __uint_as_float(y.z)));
-                x[c].w = __float_as_uint(__fadd_rn(__uint_as_float(x[c].w), __uint_as_float(y.w)));
+              for (int c = 0; c < 4; ++c) x[c] = __ldcg(part_vec(0, jj * 8 + c0 + c));
+              for (int pj = 1; pj < parts - 1; ++pj) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                  const uint4 y = __ldcg(part_vec(pj, jj * 8 + c0 + c));
+                  x[c].x = __float_as_uint(__fadd_rn(__uint_as_float(x[c].x), __uint_as_float(y.x)));
+                  x[c].y = __float_as_uint(__fadd_rn(__uint_as_float(x[c].y), __uint_as_float(y.y)));
+                  x[c].z = __float_as_uint(__fadd_rn(__uint_as_float(x[c].z), __uint_as_float(y.z)));
+                  x[c].w = __float_as_uint(__fadd_rn(__uint_as_float(x[c].w), __uint_as_float(y.w)));
+                }
               }
-            }
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              v[4 * c] = __float_as_uint(__fadd_rn(__uint_as_float(x[c].x), __uint_as_float(v[4 * c])));
-              v[4 * c + 1] =
-                  __float_as_uint(__fadd_rn(__uint_as_float(x[c].y), __uint_as_float(v[4 * c + 1])));
-              v[4 * c + 2] =
-                  __float_as_uint(__fadd_rn(__uint_as_float(x[c].z), __uint_as_float(v[4 * c + 2])));
-              v[4 * c + 3] =
-                  __float_as_uint(__fadd_rn(__uint_as_float(x[c].w), __uint_as_float(v[4 * c + 3])));
+              for (int c = 0; c < 4; ++c) {
+                uint32_t* vv = v + 4 * (c0 + c);
+                vv[0] = __float_as_uint(__fadd_rn(__uint_as_float(x[c].x), __uint_as_float(vv[0])));
+                vv[1] = __float_as_uint(__fadd_rn(__uint_as_float(x[c].y), __uint_as_float(vv[1])));
+                vv[2] = __float_as_uint(__fadd_rn(__uint_as_float(x[c].z), __uint_as_float(vv[2])));
+                vv[3] = __float_as_uint(__fadd_rn(__uint_as_float(x[c].w), __uint_as_float(vv[3])));
+              }
             }
           }
           const int64_t n0 = nt * g.BN + j * 32;
@@ -812,7 +879,7 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
 }
 
 // ------------------------------------------------------------------ kernel
-template <bool kI8, bool kTrace>
+template <bool kI8, bool kTrace, bool kSplit>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ag_fused_kernel(const __grid_constant__ FusedParams p) {
   [[maybe_unused]] uint32_t tc = 0;  // trace events of the CTA slot
@@ -878,7 +945,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (p.flags & kFlagCopy) copy_warp<kI8, kTrace>(p, lane);
   } else {
     if (gemm)
-      epilogue_warp<kI8, kTrace>(p, rank, warp & 3, (warp - 4) >> 2, lane, tfull, tempty, ring,
+      epilogue_warp<kI8, kTrace, kSplit>(p, rank, warp & 3, (warp - 4) >> 2, lane, tfull, tempty,
+                                         ring,
                                  tmem, sEpi, abort);
   }
 
@@ -940,21 +1008,27 @@ __global__ void __launch_bounds__(256) widen_kernel(const uint4* __restrict__ s0
 }
 
 // ------------------------------------------------------------------ launchers
-static const void* fused_fn(int dtype, bool trace) {
-  if (trace)
-    return dtype == 1 ? reinterpret_cast<const void*>(&ag_fused_kernel<true, true>)
-                      : reinterpret_cast<const void*>(&ag_fused_kernel<false, true>);
-  return dtype == 1 ? reinterpret_cast<const void*>(&ag_fused_kernel<true, false>)
-                    : reinterpret_cast<const void*>(&ag_fused_kernel<false, false>);
+template <bool kI8, bool kTrace, bool kSplit>
+static const void* fused_fn_t() {
+  return reinterpret_cast<const void*>(&ag_fused_kernel<kI8, kTrace, kSplit>);
+}
+static const void* fused_fn(int dtype, bool trace, bool split) {
+  const bool i8 = dtype == 1;
+  if (i8) {
+    if (trace) return split ? fused_fn_t<true, true, true>() : fused_fn_t<true, true, false>();
+    return split ? fused_fn_t<true, false, true>() : fused_fn_t<true, false, false>();
+  }
+  if (trace) return split ? fused_fn_t<false, true, true>() : fused_fn_t<false, true, false>();
+  return split ? fused_fn_t<false, false, true>() : fused_fn_t<false, false, false>();
 }
 
 cudaError_t fused_max_clusters(int dtype, int grid, int* clusters) {
-  cudaError_t e = cudaFuncSetAttribute(fused_fn(dtype, true),
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e != cudaSuccess) return e;
-  const void* fn = fused_fn(dtype, false);
-  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e != cudaSuccess) return e;
+  for (int v = 0; v < 4; ++v) {
+    cudaError_t e = cudaFuncSetAttribute(fused_fn(dtype, (v & 1) != 0, (v & 2) != 0),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+  }
+  const void* fn = fused_fn(dtype, false, false);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(kThreads);
@@ -968,12 +1042,9 @@ cudaError_t launch_fused(const FusedParams& p, int grid, cudaStream_t stream) {
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
-  if (p.trace.ev) {
-    if (p.g.dtype == 1) return cudaLaunchKernelEx(&cfg, ag_fused_kernel<true, true>, p);
-    return cudaLaunchKernelEx(&cfg, ag_fused_kernel<false, true>, p);
-  }
-  if (p.g.dtype == 1) return cudaLaunchKernelEx(&cfg, ag_fused_kernel<true, false>, p);
-  return cudaLaunchKernelEx(&cfg, ag_fused_kernel<false, false>, p);
+  const void* fn = fused_fn(p.g.dtype, p.trace.ev != nullptr, p.split > 1);
+  void* args[] = {const_cast<FusedParams*>(&p)};
+  return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 cudaError_t launch_widen(const int8_t* src0, uint16_t* dst0, int64_t n0, const int8_t* src1,

@@ -45,7 +45,7 @@ struct FusedParams {
   // partials in part order and writes the outputs.
   int64_t full_tiles;
   int64_t work_items;
-  int64_t static_items;      // pair k < static_items takes item k first, without a ticket
+  int64_t static_items;      // items below this are dealt round-robin: pair k takes k, k + pairs, ...
   int split;
   void* partials;            // [tail tiles][split - 1][2 CTAs][128 rows][BN] 4-byte sums
   uint32_t* part_flags;      // [tail tiles], monotonic
@@ -86,10 +86,11 @@ constexpr int kEpiBytes = kEpiWarps * kEpiBoxBytes;  // 32 KB
 constexpr int kSmemBytes =
     kStages * (kABytes + kBBytes) + kEpiBytes + 1024 /*barriers*/ + 1024 /*align*/;
 constexpr int kCopyWarpsPerCta = 2;
-// The pair's tile ring: tile indices drawn by the even CTA's TMA warp, read by
-// the odd CTA's TMA warp, the MMA thread and the 16 epilogue warps of the pair.
-constexpr int kTq = 4;
-constexpr int kTqReaders = 2 + 2 * kEpiWarps;
+// The pair's ring of drawn work items: published by the even CTA's TMA warp
+// (lane 1), read by both TMA warps and the MMA thread, and freed by the 16
+// epilogue warps of the pair, which read each entry last.
+constexpr int kTq = 8;
+constexpr int kTqReaders = 2 * kEpiWarps;
 
 // ---------------------------------------------------------------- skinny int8 path
 constexpr int kSkMaxRows = 128;   // the gathered rows are the MMA's N operand (N <= 128 here)

@@ -360,19 +360,19 @@ int launch_fused(ag_gemm_plan* p, agg::FusedParams& fp, int flags, cudaStream_t 
     fp.part_target = static_cast<uint32_t>(p->part_epoch * per_run);
   }
   const int grid = p->grid_override > 0 ? p->grid_override : p->grid;
-  // the first item of each pair without a ticket: whole tiles of the local shard
-  int64_t stat = grid / 2;
-  if (stat > p->full_tiles) stat = p->full_tiles;
-  if (stat > p->g.MT * p->g.NT) stat = p->g.MT * p->g.NT;
+  // Whole tiles are dealt round-robin (they wait on no other pair), unless a
+  // staging window's credits tie tiles together: then every item is drawn.
+  const int64_t stat = p->window > 0 ? 0 : p->full_tiles;
   fp.static_items = stat;
   cudaError_t e = agg::launch_fused(fp, grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "fused kernel launch");
-  // Each copy warp draws every item's ticket plus one failing ticket; each
-  // pair draws every tile it computes plus one failing ticket.
+  // Each copy warp draws every item's ticket plus one failing ticket; when
+  // the plan has drawn work items, each pair draws every drawn item it
+  // computes plus one failing ticket (with every item dealt, none at all).
   if (flags & agg::kFlagCopy)
     p->item_base += static_cast<unsigned long long>(p->g.items) +
                     static_cast<unsigned long long>(grid) * agg::kCopyWarpsPerCta;
-  if (flags & agg::kFlagGemm)
+  if ((flags & agg::kFlagGemm) && p->work_items > stat)
     p->tile_base += static_cast<unsigned long long>(p->work_items - stat) +
                     static_cast<unsigned long long>(grid / 2);
   return AG_GEMM_OK;
@@ -1189,7 +1189,7 @@ extern "C" int ag_gemm_run_noalloc(int n_shards, int64_t M, int64_t K, int64_t N
   fp.full_tiles = g.tiles;  // whole tiles only: no partial-sum workspace
   fp.work_items = g.tiles;
   fp.split = 1;
-  fp.static_items = 0;      // every tile from the ticket counter
+  fp.static_items = g.tiles;  // every tile dealt round-robin
   fp.status = status;
   fp.C = C;
   fp.local = 0;

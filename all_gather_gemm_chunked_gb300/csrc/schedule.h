@@ -129,12 +129,14 @@ AGG_HD void work_item(const Geometry& g, int64_t full, int split, int64_t i, int
 
 // Parts per tail tile for `pairs` CTA pairs: tiles % pairs tiles are left for
 // the last round.  When they fill at most half of the pairs, each is split in
-// two along K (at least 8 k-blocks a part), which halves that round; the last
-// part's addition of the first part's sums costs far less than the half tile.
+// two along K, which halves that round -- worth it when a tile is long: the
+// partial sums' store and addition cost a few microseconds whatever K, a half
+// tile of 64 k-blocks only ~10 us (measured on 4096^3 fp16: no gain), so
+// only tiles of at least 128 k-blocks (K >= 8192) are split.
 inline int choose_split(const Geometry& g, int64_t pairs) {
   if (pairs < 2) return 1;
   const int64_t tail = g.tiles % pairs;
-  if (tail == 0 || 2 * tail > pairs || g.KB < 16) return 1;
+  if (tail == 0 || 2 * tail > pairs || g.KB < 128) return 1;
   return 2;
 }
 

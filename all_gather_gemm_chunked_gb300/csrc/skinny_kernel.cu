@@ -862,9 +862,8 @@ __global__ void __launch_bounds__(kSkThreads, 1) ag_skinny_kernel(const __grid_c
 }
 
 // C_i32 = (sum of the n-tile's workspace slots) + bias,
-// D = fp16(fp32(C_i32) * scale): one thread per 4 consecutive outputs of a row
-// (N % 16 == 0, so they never straddle a row or an n-tile), the loads of up to
-// eight slots in flight before any is added.
+// D = fp16(fp32(C_i32) * scale): one thread per 8 consecutive outputs of a row
+// (N % 16 == 0, so they never straddle a row or an n-tile).
 __global__ void __launch_bounds__(256) ag_skinny_finish_kernel(
     const int32_t* __restrict__ ws, const int32_t* __restrict__ bias,
     const float* __restrict__ scale, int32_t* __restrict__ C_i32, uint16_t* __restrict__ D,
@@ -872,52 +871,73 @@ __global__ void __launch_bounds__(256) ag_skinny_finish_kernel(
   // launched as a programmatic dependent of the skinny kernel: wait for it to
   // complete (all of its workspace stores visible)
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int64_t groups = M * N / 4, U = n_tiles * KQ;
+  const int64_t groups = M * N / 8, U = n_tiles * KQ;
+  // the CTA ranges U b / G in 32-bit arithmetic when U and G allow it
+  const bool narrow =
+      static_cast<uint64_t>(U + 1) * static_cast<uint64_t>(grid) + static_cast<uint64_t>(U) <
+      (1ull << 32);
+  const uint32_t U32 = static_cast<uint32_t>(U), G32 = static_cast<uint32_t>(grid);
+  auto owner = [&](int64_t x) -> int64_t {
+    if (narrow)
+      return static_cast<int64_t>((static_cast<uint32_t>(x + 1) * G32 + U32 - 1) / U32) - 1;
+    return skinny_owner(x, U, grid);
+  };
+  auto has_units = [&](int64_t b) -> bool {
+    if (narrow)
+      return U32 * static_cast<uint32_t>(b) / G32 < U32 * static_cast<uint32_t>(b + 1) / G32;
+    int64_t lo, hi;
+    skinny_cta_range(U, b, grid, lo, hi);
+    return lo < hi;
+  };
   for (int64_t gi = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; gi < groups;
        gi += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t off = gi * 4, m = off / N, n = off - m * N;
+    const int64_t off = gi * 8, m = off / N, n = off - m * N;
     const int64_t nt = n / kSkN, nl = n - nt * kSkN;
-    const int64_t b_lo = skinny_owner(nt * KQ, U, grid);
-    const int64_t b_hi = skinny_owner((nt + 1) * KQ - 1, U, grid);
-    uint32_t c[4] = {0u, 0u, 0u, 0u};
-    for (int64_t b0 = b_lo; b0 <= b_hi; b0 += 8) {
+    const int64_t b_lo = owner(nt * KQ);
+    const int64_t b_hi = owner((nt + 1) * KQ - 1);
+    int32_t c[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    // four slots per step: their eight 16-byte loads are issued before any is
+    // used (a CTA without units wrote no slot: its loads are skipped)
+    for (int64_t b0 = b_lo; b0 <= b_hi; b0 += 4) {
       int4 x[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < 4; ++i) {
         const int64_t b = b0 + i;
-        int64_t lo = 0, hi = 0;
-        if (b <= b_hi) skinny_cta_range(U, b, grid, lo, hi);
-        // a CTA without units wrote no slot: its loads are skipped
-        x[i] = lo < hi ? __ldcg(reinterpret_cast<const int4*>(
-                             ws + ((nt * cmax + (b - b_lo)) * M + m) * kSkN + nl))
-                       : make_int4(0, 0, 0, 0);
+        x[2 * i] = x[2 * i + 1] = make_int4(0, 0, 0, 0);
+        if (b <= b_hi && has_units(b)) {
+          const int4* sp = reinterpret_cast<const int4*>(
+              ws + ((nt * cmax + (b - b_lo)) * M + m) * kSkN + nl);
+          x[2 * i] = __ldcg(sp);
+          x[2 * i + 1] = __ldcg(sp + 1);
+        }
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        c[0] += static_cast<uint32_t>(x[i].x);
-        c[1] += static_cast<uint32_t>(x[i].y);
-        c[2] += static_cast<uint32_t>(x[i].z);
-        c[3] += static_cast<uint32_t>(x[i].w);
+      for (int i = 0; i < 4; ++i) {
+        const int4 x0 = x[2 * i], x1 = x[2 * i + 1];
+        c[0] += x0.x; c[1] += x0.y; c[2] += x0.z; c[3] += x0.w;
+        c[4] += x1.x; c[5] += x1.y; c[6] += x1.z; c[7] += x1.w;
       }
     }
-    const int4 bb = __ldg(reinterpret_cast<const int4*>(bias + n));
-    const float4 ss = __ldg(reinterpret_cast<const float4*>(scale + n));
-    const int32_t bv[4] = {bb.x, bb.y, bb.z, bb.w};
-    const float sv[4] = {ss.x, ss.y, ss.z, ss.w};
-    int32_t cv[4];
-    uint32_t h[2];
+    const int4 b0 = __ldg(reinterpret_cast<const int4*>(bias + n));
+    const int4 b1 = __ldg(reinterpret_cast<const int4*>(bias + n + 4));
+    const float4 s0 = __ldg(reinterpret_cast<const float4*>(scale + n));
+    const float4 s1 = __ldg(reinterpret_cast<const float4*>(scale + n + 4));
+    const int32_t bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+    const float ss[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+    uint32_t h[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      cv[e] = static_cast<int32_t>(c[e] + static_cast<uint32_t>(bv[e]));
+    for (int e = 0; e < 8; ++e) {
+      c[e] = static_cast<int32_t>(static_cast<uint32_t>(c[e]) + static_cast<uint32_t>(bb[e]));
       const uint32_t hb =
-          __half_as_ushort(__float2half_rn(__fmul_rn(__int2float_rn(cv[e]), sv[e])));
+          __half_as_ushort(__float2half_rn(__fmul_rn(__int2float_rn(c[e]), ss[e])));
       if (e & 1)
         h[e >> 1] |= hb << 16;
       else
         h[e >> 1] = hb;
     }
-    *reinterpret_cast<int4*>(C_i32 + off) = make_int4(cv[0], cv[1], cv[2], cv[3]);
-    *reinterpret_cast<uint2*>(D + off) = make_uint2(h[0], h[1]);
+    *reinterpret_cast<int4*>(C_i32 + off) = make_int4(c[0], c[1], c[2], c[3]);
+    *reinterpret_cast<int4*>(C_i32 + off + 4) = make_int4(c[4], c[5], c[6], c[7]);
+    *reinterpret_cast<uint4*>(D + off) = make_uint4(h[0], h[1], h[2], h[3]);
   }
 }
 
@@ -944,9 +964,7 @@ cudaError_t launch_skinny(const SkinnyParams& p, int grid, cudaStream_t stream) 
   // trigger at its start let the finish grid in sooner and measured slower
   // (59.4 us against 55.3 us on 2 x 32 rows, K = 16384, N = 7168).
   cudaLaunchConfig_t cfg{};
-  // one thread per 4 outputs, all of them in one pass up to 8 CTAs per SM
-  const int64_t need = (p.g.M * p.g.N / 4 + 255) / 256;
-  cfg.gridDim = dim3(static_cast<unsigned>(need < 8 * grid ? need : 8 * grid));
+  cfg.gridDim = dim3(grid * 2);
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;

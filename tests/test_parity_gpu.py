@@ -593,9 +593,9 @@ def test_nshard_pitch_checks():
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("dt,S,R,K,N", [
-    ("f16", 2, 512, 2048, 1024),   # 16 tiles, 2 parts each
-    ("bf16", 3, 300, 1024, 520),   # 18 tiles (ragged rows and columns), 2 parts each
-    ("i8", 2, 384, 2080, 512),     # 8 tiles, 2 parts of 16 and 17 k-blocks (int32 partials)
+    ("f16", 2, 384, 8192, 512),    # 8 tiles, 2 parts of 64 k-blocks each
+    ("bf16", 3, 300, 8192, 264),   # 12 tiles (ragged rows and columns), 2 parts each
+    ("i8", 2, 384, 8256, 512),     # 4 tiles, 2 parts of 64 and 65 k-blocks (int32 partials)
 ])
 def test_split_tail_parity_modes_and_repeats(oracle, dt, S, R, K, N):
     x = synth.make_inputs(S, R, K, N, dt, 7000 + S * 17 + K)
@@ -624,13 +624,15 @@ def test_split_tail_parity_modes_and_repeats(oracle, dt, S, R, K, N):
 
 def test_split_tail_plan_geometry():
     """The split is chosen for the device's full grid: when the last round's
-    tiles fill at most half of the CTA pairs, each is split in two along K
-    (each part >= 8 k-blocks)."""
+    tiles fill at most half of the CTA pairs and a tile has at least 128
+    k-blocks, each is split in two along K."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     pairs = sms // 2
-    with Plan(2, 4096, 4096, 4096, "f16") as p:      # 256 pair tiles
+    with Plan(2, 4096, 8192, 4096, "f16") as p:      # 256 pair tiles, 128 k-blocks
         g = p.geometry
         assert g["split_tiles"] == 256 % pairs and g["split_parts"] == 2
+    with Plan(2, 4096, 4096, 4096, "f16") as p:      # 64 k-blocks: the split would not pay
+        assert p.geometry["split_parts"] == 1
     with Plan(8, 8192, 4096, 4096, "f16") as p:      # 512 tiles: the last round is too full
         assert p.geometry["split_parts"] == 1
     with Plan(2, 512, 256, 512, "f16") as p:         # 4 k-blocks: too short to split

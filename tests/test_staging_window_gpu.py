@@ -144,8 +144,8 @@ GRID_CASES = [
     ("f16", 4, 600, 256, 384, 8),
     ("i8", 5, 520, 1056, 208, 9),
     ("f16", 3, 1000, 512, 520, None),
-    ("f16", 2, 1536, 2048, 2048, None),   # 96 tiles: the last round's 20 split in two along K
-    ("i8", 3, 512, 1024, 768, None),      # 18 tiles split in parts (int32 partial sums)
+    ("f16", 2, 1536, 8192, 512, None),    # 24 tiles split in two along K (fp32 partial sums)
+    ("i8", 3, 512, 8192, 768, None),      # 18 tiles split in two (int32 partial sums)
 ]
 
 
