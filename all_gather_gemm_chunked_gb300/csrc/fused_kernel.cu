@@ -192,10 +192,11 @@ __device__ void copy_warp(const FusedParams& p, int lane) {
 // ------------------------------------------------------------------ work items
 // A pair's items: first the whole tiles dealt round-robin -- pair k takes
 // items k, k + pairs, ... below static_items -- then items handed out at run
-// time.  The dealt items wait on no other pair (plain staging), so they need
-// no coordination; the rest -- the split parts of the last round's tiles, and
-// every item when a staging window's credits tie tiles to one another -- are
-// drawn from a grid-wide ticket counter in schedule order.  Whichever pairs
+// time.  The dealt items wait on no other pair (plain staging, or the local
+// shard's tiles of a plan with a staging window), so they need no
+// coordination; the rest -- the split parts of the last round's tiles, and
+// the remote tiles when a staging window's credits tie tiles to one another
+// -- are drawn from a grid-wide ticket counter in schedule order.  Whichever pairs
 // are resident therefore always take the lowest items left: no item waits on
 // a pair that has not started (the window's credits and a split tile's
 // partial sums come only from items drawn earlier), even when fewer pairs are

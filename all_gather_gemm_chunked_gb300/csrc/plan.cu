@@ -360,9 +360,12 @@ int launch_fused(ag_gemm_plan* p, agg::FusedParams& fp, int flags, cudaStream_t 
     fp.part_target = static_cast<uint32_t>(p->part_epoch * per_run);
   }
   const int grid = p->grid_override > 0 ? p->grid_override : p->grid;
-  // Whole tiles are dealt round-robin (they wait on no other pair), unless a
-  // staging window's credits tie tiles together: then every item is drawn.
-  const int64_t stat = p->window > 0 ? 0 : p->full_tiles;
+  // Whole tiles are dealt round-robin (they wait on no other pair).  With a
+  // staging window the remote tiles' credits tie them together, so only the
+  // local shard's tiles (consumption position 0: the first MT x NT in schedule
+  // order, which neither wait for rows nor add credits) are dealt and every
+  // remote tile is drawn.
+  const int64_t stat = p->window > 0 ? p->g.MT * p->g.NT : p->full_tiles;
   fp.static_items = stat;
   cudaError_t e = agg::launch_fused(fp, grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "fused kernel launch");

@@ -5,13 +5,14 @@ m-tile of a remote shard, in consumption order) lives in slot b % W, and the
 producer may write block b only once every tile of block b - W has read its
 rows.  These tests check the chunk rule such a plan uses, and -- by simulating
 the persistent schedule exactly as the kernel walks it (tile order from the
-library's own ag_gemm_tile_at, tiles handed out by a ticket counter in that
-order to whichever CTA pairs are running) -- that a window of at least one
-swizzle group (group_m = 8 blocks) always finishes, also when fewer pairs are
-resident than were launched, while a smaller window can stall for good.  A
-static deal of tiles to pairs (pair p takes tiles p, p + pairs, ...) is
-simulated too: under partial residency it can stall, which is why the kernel
-hands tiles out at run time.
+library's own ag_gemm_tile_at; the local shard's tiles dealt round-robin, the
+remote tiles handed out by a ticket counter in that order to whichever CTA
+pairs are running) -- that a window of at least one swizzle group (group_m =
+8 blocks) always finishes, also when fewer pairs are resident than were
+launched, while a smaller window can stall for good.  A static deal of every
+tile to pairs (pair p takes tiles p, p + pairs, ...) is simulated too: under
+partial residency it can stall, which is why the kernel hands the remote
+tiles out at run time.
 """
 import pytest
 
@@ -44,35 +45,53 @@ def _block_of(g, local):
     return [block(t) for t in range(g.tiles)]
 
 
-def _simulate_tickets(g, local, W, resident):
-    """True if every tile completes when `resident` pairs run at once and take
-    tiles from a ticket counter in schedule order (a pair holds its tile until
-    the tile's block is produced).  Producer: blocks in order, block b once the
-    NT tiles of block b - W have read their rows."""
+def _simulate_tickets(g, local, W, resident, pairs=None, dealt=0):
+    """True if every tile completes when `pairs` pairs are launched, `resident`
+    of them run at once (a waiting pair starts when a running one exits), and
+    each pair first computes the tiles dealt to it (pair k: tiles k, k + pairs,
+    ... below `dealt`), then takes tiles from a ticket counter in schedule
+    order, starting at `dealt` (a pair holds its tile until the tile's block
+    is produced, and exits when the tickets run out).  Producer: blocks in
+    order, block b once the NT tiles of block b - W have read their rows."""
+    pairs = resident if pairs is None else pairs
     blocks = _block_of(g, local)
     nblocks = (g.n_shards - 1) * g.m_tiles
     produced, consumed = 0, [0] * nblocks
-    holding = [None] * resident   # tile each running pair works on
-    ticket, done = 0, 0
+    nxt = list(range(pairs))             # next dealt tile per pair
+    holding = {}                         # running pair -> drawn tile it holds
+    running = list(range(min(resident, pairs)))
+    waiting = list(range(len(running), pairs))
+    ticket, done = dealt, 0
     while True:
         progress = False
         while produced < nblocks and (produced < W or consumed[produced - W] == g.n_tiles):
             produced += 1
             progress = True
-        for p in range(resident):
+        for p in list(running):
             while True:
-                if holding[p] is None:
-                    if ticket == g.tiles:
-                        break
-                    holding[p] = ticket
+                if nxt[p] < dealt:
+                    t = nxt[p]
+                elif p in holding:
+                    t = holding[p]
+                elif ticket < g.tiles:
+                    t = holding[p] = ticket
                     ticket += 1
                     progress = True
-                b = blocks[holding[p]]
+                else:
+                    running.remove(p)            # tickets exhausted: the pair exits
+                    if waiting:
+                        running.append(waiting.pop(0))
+                    progress = True
+                    break
+                b = blocks[t]
                 if b is not None and b >= produced:
                     break
                 if b is not None:
                     consumed[b] += 1
-                holding[p] = None
+                if nxt[p] < dealt:
+                    nxt[p] += pairs
+                else:
+                    del holding[p]
                 done += 1
                 progress = True
         if done == g.tiles:
@@ -176,12 +195,32 @@ def test_window_with_tickets_finishes_under_partial_residency(S, R, N):
                 assert _simulate_tickets(g, local, W, resident), (S, R, N, W, resident, local)
 
 
+@pytest.mark.parametrize("S,R,N", [(4, 4096, 4096), (8, 1024, 4096), (3, 600, 392),
+                                   (5, 2560, 1024)])
+def test_window_with_local_tiles_dealt_finishes_under_partial_residency(S, R, N):
+    # the kernel deals the local shard's tiles (position 0: the first MT x NT
+    # in schedule order, no rows to wait for, no credits) and draws the rest
+    g = B_.ag_gemm_geometry_of(S, S * R, 256, N, 0, 0)
+    for local in {0, S - 1}:
+        blocks = _block_of(g, local)
+        n_local = g.m_tiles * g.n_tiles
+        assert all(b is None for b in blocks[:n_local])
+        assert all(b is not None for b in blocks[n_local:])
+        for W in (8, 16):
+            for resident in (1, 7, 38, 76):
+                assert _simulate_tickets(g, local, W, resident, pairs=76, dealt=n_local), \
+                    (S, R, N, W, resident, local)
+
+
 def test_static_deal_can_stall_under_partial_residency():
     # workload 4's shape with a window of 16 slots: 76 pairs launched, 7 resident
     g = B_.ag_gemm_geometry_of(4, 4 * 4096, 256, 4096, 0, 0)
     assert _simulate_static(g, 0, 16, 76, 76)
     assert not _simulate_static(g, 0, 16, 76, 7)
     assert _simulate_tickets(g, 0, 16, 7)
+    assert _simulate_tickets(g, 0, 16, 7, pairs=76, dealt=g.m_tiles * g.n_tiles)
+    # dealing one remote tile more is enough to stall
+    assert not _simulate_tickets(g, 0, 16, 7, pairs=76, dealt=g.m_tiles * g.n_tiles + 76)
 
 
 def test_window_below_a_swizzle_group_can_stall():
