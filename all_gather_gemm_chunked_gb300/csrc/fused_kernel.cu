@@ -393,7 +393,9 @@ __device__ void tma_warp(const FusedParams& p, uint32_t rank, uint8_t* sA, uint8
       // (row0, pos - 1), or the window's [W][256][K] at (this CTA's half, slot)
       const bool win = pos > 0 && p.window > 0;
       const int32_t y = win ? static_cast<int32_t>(rank * kBlockM) : static_cast<int32_t>(row0);
-      const int32_t z = win ? static_cast<int32_t>(((pos - 1) * g.MT + mt) % p.window) : pos - 1;
+      const int32_t z = win ? static_cast<int32_t>(static_cast<uint32_t>((pos - 1) * g.MT + mt) %
+                                                   static_cast<uint32_t>(p.window))
+                            : pos - 1;
       const int32_t xb = static_cast<int32_t>(nt * g.BN + rank * half);
       for (int64_t kb = kbs; kb < kbe; ++kb) {
         if (!mbar_wait(&empty[stage], phase ^ 1u, p.pipe_timeout_ns, abort, gstatus)) {
@@ -493,13 +495,15 @@ __device__ void mma_warp(const FusedParams& p, const uint8_t* sA, const uint8_t*
     work_item(g, p.full_tiles, p.split, t, tile, part, parts, kbs, kbe);
     // fp32 accumulation spans the whole item (fp16), or segments of kSegBlocks (int8)
     const int64_t seg_len = kI8 ? kSegBlocks : kbe - kbs;
-    const int64_t nseg = ceil_div(kbe - kbs, seg_len);
+    // (no 64-bit division at the item boundary: kSegBlocks is a power of two)
+    const int64_t nseg = kI8 ? (kbe - kbs + kSegBlocks - 1) / kSegBlocks : 1;
     int64_t slot = -1;  // the window slot this remote tile reads (bounded staging)
     if (credit) {
       int pos;
       int64_t mt, nt;
       tile_coords(g, tile, pos, mt, nt);
-      if (pos > 0) slot = ((pos - 1) * g.MT + mt) % p.window;
+      if (pos > 0)
+        slot = static_cast<uint32_t>((pos - 1) * g.MT + mt) % static_cast<uint32_t>(p.window);
     }
     for (int64_t seg = 0; seg < nseg && ok; ++seg) {
       const uint32_t buf = unit & 1u, use = unit >> 1;
@@ -645,7 +649,8 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
     int part, parts;
     work_item(g, p.full_tiles, p.split, t, tile, part, parts, kbs, kbe);
     const int64_t seg_len = kI8 ? kSegBlocks : kbe - kbs;
-    const int64_t nseg = ceil_div(kbe - kbs, seg_len);
+    // (no 64-bit division at the item boundary: kSegBlocks is a power of two)
+    const int64_t nseg = kI8 ? (kbe - kbs + kSegBlocks - 1) / kSegBlocks : 1;
     // a split tile: earlier parts store partial sums, the last part adds them
     // (compiled only into the kernel a splitting plan launches: the split
     // paths would raise the register count of every tile's epilogue)

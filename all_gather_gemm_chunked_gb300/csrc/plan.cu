@@ -178,6 +178,11 @@ int check_problem(int S, int64_t M, int64_t K, int64_t N, int dtype, int64_t chu
   // TMA coordinates are 32-bit.
   if (K > (1LL << 31) || N > (1LL << 31) || R > (1LL << 31))
     return fail(AG_GEMM_ERR_UNSUPPORTED, "dimension too large for 32-bit TMA coordinates");
+  // The kernels decode tiles and work items in 32-bit arithmetic.
+  const int64_t tiles = static_cast<int64_t>(S) * ((R + agg::kPairM - 1) / agg::kPairM) *
+                        ((N + 127) / 128);  // an upper bound of the pair tiles
+  if (tiles >= (1LL << 30))
+    return fail(AG_GEMM_ERR_UNSUPPORTED, "more than 2^30 pair tiles");
   return AG_GEMM_OK;
 }
 

@@ -92,17 +92,25 @@ AGG_HD void make_geometry(Geometry& g, int S, int64_t M, int64_t K, int64_t N,
 
 // Tile t -> (consumption position, m-tile, n-tile).  Position 0 is the local
 // shard; within a position, groups of kGroupM m-tiles are walked m-fastest.
+// (32-bit arithmetic: a plan has fewer than 2^31 tiles, checked at validation.
+// The kernels decode a tile at every tile boundary, where 64-bit divisions
+// would delay the first loads of the next tile.)
 AGG_HD void tile_coords(const Geometry& g, int64_t t, int& pos, int64_t& mt,
                         int64_t& nt) {
-  int64_t per = g.MT * g.NT;
-  pos = (int)(t / per);
-  int64_t u = t - (int64_t)pos * per;
-  int64_t group = (int64_t)kGroupM * g.NT;
-  int64_t first_m = (u / group) * kGroupM;
-  int64_t gm = g.MT - first_m < kGroupM ? g.MT - first_m : kGroupM;
-  int64_t w = u % group;
-  mt = first_m + w % gm;
-  nt = w / gm;
+  const uint32_t MT = static_cast<uint32_t>(g.MT), NT = static_cast<uint32_t>(g.NT);
+  const uint32_t per = MT * NT, t32 = static_cast<uint32_t>(t);
+  const uint32_t p32 = t32 / per;
+  const uint32_t u = t32 - p32 * per;
+  const uint32_t group = static_cast<uint32_t>(kGroupM) * NT;
+  const uint32_t gi = u / group;
+  const uint32_t first_m = gi * static_cast<uint32_t>(kGroupM);
+  const uint32_t gm = MT - first_m < static_cast<uint32_t>(kGroupM) ? MT - first_m
+                                                                    : static_cast<uint32_t>(kGroupM);
+  const uint32_t w = u - gi * group;
+  const uint32_t n32 = w / gm;
+  pos = static_cast<int>(p32);
+  mt = first_m + (w - n32 * gm);
+  nt = n32;
 }
 
 // Work items of the fused kernel: the first `full` tiles whole, then the
@@ -117,14 +125,20 @@ AGG_HD void work_item(const Geometry& g, int64_t full, int split, int64_t i, int
     t = i;
     part = 0;
     parts = 1;
-  } else {
-    const int64_t tail = g.tiles - full, r = i - full;
-    part = static_cast<int>(r / tail);
-    t = full + (r - static_cast<int64_t>(part) * tail);
-    parts = split;
+    kb0 = 0;
+    kb1 = g.KB;
+    return;
   }
-  kb0 = g.KB * part / parts;
-  kb1 = g.KB * (part + 1) / parts;
+  // (32-bit: fewer than 2^31 tiles, K < 2^31 so KB * split < 2^32)
+  const uint32_t tail = static_cast<uint32_t>(g.tiles - full);
+  const uint32_t r = static_cast<uint32_t>(i - full);
+  const uint32_t pj = r / tail;
+  const uint32_t kb = static_cast<uint32_t>(g.KB), s = static_cast<uint32_t>(split);
+  part = static_cast<int>(pj);
+  t = full + (r - pj * tail);
+  parts = split;
+  kb0 = kb * pj / s;
+  kb1 = kb * (pj + 1) / s;
 }
 
 // Parts per tail tile for `pairs` CTA pairs: tiles % pairs tiles are left for
@@ -177,8 +191,9 @@ AGG_HD uint32_t window_target(const Geometry& g, int64_t W, int64_t b, uint32_t 
 AGG_HD bool rows_chunks(const Geometry& g, int64_t row0, int64_t& q0, int64_t& q1) {
   if (row0 >= g.R) return false;
   int64_t r1 = row0 + kBlockM < g.R ? row0 + kBlockM : g.R;
-  q0 = row0 / g.c;
-  q1 = (r1 - 1) / g.c;
+  const uint32_t c = static_cast<uint32_t>(g.c);  // (R <= 2^31)
+  q0 = static_cast<uint32_t>(row0) / c;
+  q1 = static_cast<uint32_t>(r1 - 1) / c;
   return true;
 }
 
