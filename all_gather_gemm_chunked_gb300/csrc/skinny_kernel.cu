@@ -142,18 +142,20 @@ __device__ __forceinline__ void widen16x(const uint4 v, uint4& a, uint4& b) {
 }
 
 // k-blocks [kb0, kb1) of unit u.
+// (32-bit: a skinny plan has fewer than 2^31 units)
 __device__ __forceinline__ void unit_blocks(const Geometry& g, int64_t KQ, int64_t u, int64_t& kb0,
                                             int64_t& kb1) {
-  kb0 = (u % KQ) * kSkUnitBlocks;
+  kb0 = static_cast<int64_t>(static_cast<uint32_t>(u) % static_cast<uint32_t>(KQ)) * kSkUnitBlocks;
   kb1 = kb0 + kSkUnitBlocks < g.KB ? kb0 + kSkUnitBlocks : g.KB;
 }
 
 // The piece that starts at unit u: n-tile nt, units [u, ue), k-blocks [kb0, kb1).
 __device__ __forceinline__ void piece_at(const Geometry& g, int64_t KQ, int64_t u, int64_t u1,
                                          int64_t& nt, int64_t& ue, int64_t& kb0, int64_t& kb1) {
-  nt = u / KQ;
+  const uint32_t u32 = static_cast<uint32_t>(u), kq = static_cast<uint32_t>(KQ);
+  nt = u32 / kq;
   ue = (nt + 1) * KQ < u1 ? (nt + 1) * KQ : u1;
-  kb0 = (u % KQ) * kSkUnitBlocks;
+  kb0 = static_cast<int64_t>(u32 - static_cast<uint32_t>(nt) * kq) * kSkUnitBlocks;
   const int64_t end = (ue - nt * KQ) * kSkUnitBlocks;
   kb1 = end < g.KB ? end : g.KB;
 }
@@ -242,7 +244,8 @@ __device__ uint32_t sk_parts_landed(const SkinnyParams& p, int lane) {
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int64_t i = i0 + u * 32;
-      if (v[u] < p.epoch) missing |= 1u << static_cast<uint32_t>(i / per_part);
+      if (v[u] < p.epoch)
+        missing |= 1u << (static_cast<uint32_t>(i) / static_cast<uint32_t>(per_part));
     }
   }
   fence_acq_rel_gpu();
@@ -327,7 +330,7 @@ __device__ void sk_tma_warp(const SkinnyParams& p, uint8_t* sRaw, const SkLayout
   Ring r(L.n_raw);
   int64_t i = 0;
   for (int64_t u = u0; u < u1; ++u, ++i, r.next()) {
-    const int64_t nt = u / KQ, q = u - nt * KQ;
+    const int64_t nt = static_cast<uint32_t>(u) / static_cast<uint32_t>(KQ), q = u - nt * KQ;
     uint8_t* st = sRaw + r.s * L.raw_stage;
     const int32_t x = static_cast<int32_t>(q * kSkARow);
     if (lane == 0) {
