@@ -128,7 +128,7 @@ __device__ bool wait_slot(const FusedParams& p, int64_t slot, uint32_t target, i
 }
 
 template <bool kI8, bool kTrace>
-__device__ void copy_warp(const FusedParams& p, int lane) {
+__device__ void copy_warp(const FusedParams& p, int lane, unsigned long long first_ticket) {
   const Geometry& g = p.g;
   [[maybe_unused]] uint32_t tn = 0;  // trace events of this warp
   // With bounded staging and the GEMM in the same launch, a block may only
@@ -136,9 +136,10 @@ __device__ void copy_warp(const FusedParams& p, int lane) {
   // copy-only launch has no readers and writes freely.)
   const bool credit = p.window > 0 && (p.flags & kFlagGemm) != 0;
   int64_t ready_block = -1;  // the last block whose slot this warp saw released
-  for (;;) {
-    unsigned long long ticket = 0;
-    if (lane == 0) ticket = atomicAdd(p.item_counter, 1ull);
+  for (bool first = true;; first = false) {
+    // (the first ticket was drawn by lane 0 while the CTA was being set up)
+    unsigned long long ticket = first_ticket;
+    if (lane == 0 && !first) ticket = atomicAdd(p.item_counter, 1ull);
     ticket = __shfl_sync(0xffffffffu, ticket, 0);
     const int64_t i = static_cast<int64_t>(ticket - p.item_base);
     if (i >= g.items) break;  // exactly one failing ticket per copy warp and run
@@ -910,6 +911,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
   const bool gemm = (p.flags & kFlagGemm) != 0;
+  // A copy warp draws its first ticket before the set-up below, so the
+  // atomic's latency overlaps it (tickets keep the copies live whichever CTAs
+  // are resident).
+  const bool copier = warp >= 2 && warp < 2 + kCopyWarpsPerCta && (p.flags & kFlagCopy) != 0;
+  unsigned long long first_ticket = 0;
+  if (copier && lane == 0) first_ticket = atomicAdd(p.item_counter, 1ull);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -948,7 +955,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (gemm && rank == 0 && lane == 0)
       mma_warp<kI8>(p, sA, sB, full, empty, tfull, tempty, ring, tmem, abort);
   } else if (warp < 2 + kCopyWarpsPerCta) {
-    if (p.flags & kFlagCopy) copy_warp<kI8, kTrace>(p, lane);
+    if (copier) copy_warp<kI8, kTrace>(p, lane, first_ticket);
   } else {
     if (gemm)
       epilogue_warp<kI8, kTrace, kSplit>(p, rank, warp & 3, (warp - 4) >> 2, lane, tfull, tempty,

@@ -331,12 +331,11 @@ int launch_skinny(ag_gemm_plan* p, agg::SkinnyParams& sp, int flags, cudaStream_
   sp.item_base = p->item_base;
   cudaError_t e = agg::launch_skinny(sp, p->sk_grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "skinny kernel launch");
-  // The W copy warps take the first W tasks without a ticket; the rest are
-  // drawn, and every copy warp draws one failing ticket.
+  // Every task is drawn by a ticket, and every copy warp draws one failing ticket.
   if (flags & agg::kFlagCopy) {
     const int64_t tasks = (p->g.S - 1) * p->g.Q * p->sk_np;
     const int64_t W = static_cast<int64_t>(p->sk_grid) * agg::kSkCopyWarpsPerCta;
-    p->item_base += static_cast<unsigned long long>((tasks > W ? tasks - W : 0) + W);
+    p->item_base += static_cast<unsigned long long>(tasks + W);
   }
   return AG_GEMM_OK;
 }

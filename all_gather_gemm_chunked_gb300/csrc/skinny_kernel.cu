@@ -163,29 +163,23 @@ __device__ __forceinline__ void piece_at(const Geometry& g, int64_t KQ, int64_t 
 // ------------------------------------------------------------------ copy warps
 // Copy task t = (k-part j, position pos, chunk q): the chunk's c rows over the
 // part's k-range, from the source shard into the int8 staging, then one
-// release of the task's own counter.  Tasks are numbered in part-major order;
-// copy warp w of the grid (W warps) takes task w first, without a ticket, so
-// the first parts are in flight at once, and every later task comes from a
-// grid-wide ticket counter: ticket i is task W + i.
+// release of the task's own counter.  Tasks are numbered in part-major order
+// and handed out by a grid-wide ticket counter (ticket i is task i), so the
+// resident warps always take the lowest tasks left; each warp draws its first
+// ticket before the CTA's set-up, so the first parts are in flight at once.
 template <bool kTrace>
-__device__ void sk_copy_warp(const SkinnyParams& p, int cw, int lane) {
+__device__ void sk_copy_warp(const SkinnyParams& p, int lane, unsigned long long first_ticket) {
   const Geometry& g = p.g;
   [[maybe_unused]] uint32_t tn = 0;  // trace events of this warp
   const int64_t tasks = (int64_t)(g.S - 1) * g.Q * p.np;
-  const int64_t W = static_cast<int64_t>(gridDim.x) * kSkCopyWarpsPerCta;
   for (bool first = true;; first = false) {
-    int64_t t;
-    if (first) {
-      t = static_cast<int64_t>(blockIdx.x) * kSkCopyWarpsPerCta + cw;
-      if (t >= tasks) continue;  // no task of its own: go to the tickets
-    } else {
-      unsigned long long ticket = 0;
-      if (lane == 0) ticket = atomicAdd(p.item_counter, 1ull);
-      ticket = __shfl_sync(0xffffffffu, ticket, 0);
-      t = W + static_cast<int64_t>(ticket - p.item_base);
-    }
+    // (the first ticket was drawn by lane 0 while the CTA was being set up)
+    unsigned long long ticket = first_ticket;
+    if (lane == 0 && !first) ticket = atomicAdd(p.item_counter, 1ull);
+    ticket = __shfl_sync(0xffffffffu, ticket, 0);
+    const int64_t t = static_cast<int64_t>(ticket - p.item_base);
     if (t >= tasks) break;  // exactly one failing ticket per copy warp and run
-    if (t < W && !first) {
+    if (t < 0) {
       // tickets behind this run's base: the counters were not reset after a
       // failed run; copy nothing (the readers time out and report it)
       if (lane == 0) sk_set_status(p.status, kStatusChunkTimeout, 0xFFFFFFu);
@@ -787,6 +781,14 @@ __global__ void __launch_bounds__(kSkThreads, 1) ag_skinny_kernel(const __grid_c
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool gemm = (p.flags & kFlagGemm) != 0;
+  int role, rank;
+  sk_role(warp, role, rank);
+  // A copy warp draws its first ticket before the set-up below, so the
+  // atomic's latency overlaps it (tickets keep the copies live whichever CTAs
+  // are resident).
+  const bool copier = role == kRoleCopy && (p.flags & kFlagCopy) != 0;
+  unsigned long long first_ticket = 0;
+  if (copier && lane == 0) first_ticket = atomicAdd(p.item_counter, 1ull);
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSkRawMax; ++s) {
       mbar_init(&raw_full[s], 1);
@@ -814,10 +816,8 @@ __global__ void __launch_bounds__(kSkThreads, 1) ag_skinny_kernel(const __grid_c
 
   if constexpr (kTrace)
     if (threadIdx.x == 0) trace_emit(p.trace, tc, kTrCtaSlot, kTrCtaStart, 0, 0);
-  int role, rank;
-  sk_role(warp, role, rank);
   if (role == kRoleCopy) {
-    if (p.flags & kFlagCopy) sk_copy_warp<kTrace>(p, rank, lane);
+    if (copier) sk_copy_warp<kTrace>(p, lane, first_ticket);
   } else if (gemm) {
     switch (role) {
       case kRoleMma:
@@ -892,19 +892,22 @@ __global__ void __launch_bounds__(256) ag_skinny_finish_kernel(
     skinny_cta_range(U, b, grid, lo, hi);
     return lo < hi;
   };
+  const bool narrow_mn = static_cast<uint64_t>(M) * static_cast<uint64_t>(N) < (1ull << 32);
   for (int64_t gi = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; gi < groups;
        gi += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t off = gi * 8, m = off / N, n = off - m * N;
+    const int64_t off = gi * 8;
+    const int64_t m = narrow_mn ? static_cast<uint32_t>(off) / static_cast<uint32_t>(N) : off / N;
+    const int64_t n = off - m * N;
     const int64_t nt = n / kSkN, nl = n - nt * kSkN;
     const int64_t b_lo = owner(nt * KQ);
     const int64_t b_hi = owner((nt + 1) * KQ - 1);
     int32_t c[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    // four slots per step: their eight 16-byte loads are issued before any is
-    // used (a CTA without units wrote no slot: its loads are skipped)
-    for (int64_t b0 = b_lo; b0 <= b_hi; b0 += 4) {
-      int4 x[8];
+    // eight slots per step: their sixteen 16-byte loads are issued before any
+    // is used (a CTA without units wrote no slot: its loads are skipped)
+    for (int64_t b0 = b_lo; b0 <= b_hi; b0 += 8) {
+      int4 x[16];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < 8; ++i) {
         const int64_t b = b0 + i;
         x[2 * i] = x[2 * i + 1] = make_int4(0, 0, 0, 0);
         if (b <= b_hi && has_units(b)) {
@@ -915,7 +918,7 @@ __global__ void __launch_bounds__(256) ag_skinny_finish_kernel(
         }
       }
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < 8; ++i) {
         const int4 x0 = x[2 * i], x1 = x[2 * i + 1];
         c[0] += x0.x; c[1] += x0.y; c[2] += x0.z; c[3] += x0.w;
         c[4] += x1.x; c[5] += x1.y; c[6] += x1.z; c[7] += x1.w;
