@@ -7,6 +7,7 @@
 #include <algorithm>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -18,10 +19,31 @@
 
 using agg::Geometry;
 
-// ------------------------------------------------------------------ errors
+// ------------------------------------------------------------------ errors, log
 namespace {
 thread_local int g_last_error = AG_GEMM_OK;
 thread_local char g_last_msg[512] = "";
+
+// AG_GEMM_LOG=0..3 in the environment (read once): 1 errors, 2 plans, 3 runs.
+int log_level() {
+  static const int level = [] {
+    const char* v = std::getenv("AG_GEMM_LOG");
+    if (!v || !*v) return 0;
+    const int l = std::atoi(v);
+    return l < 0 ? 0 : (l > 3 ? 3 : l);
+  }();
+  return level;
+}
+
+void log_msg(int level, const char* fmt, ...) {
+  if (log_level() < level) return;
+  char buf[640];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  std::fprintf(stderr, "[ag_gemm] %s\n", buf);
+}
 
 int fail(int code, const char* fmt, ...) {
   g_last_error = code;
@@ -29,6 +51,7 @@ int fail(int code, const char* fmt, ...) {
   va_start(ap, fmt);
   vsnprintf(g_last_msg, sizeof(g_last_msg), fmt, ap);
   va_end(ap);
+  log_msg(1, "error %d: %s", code, g_last_msg);
   return code;
 }
 
@@ -584,6 +607,8 @@ int run_impl(ag_gemm_plan* p, const void* const* shard_ptrs, const void* B, int6
     if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
     p->last_stream = stream;
     p->has_run = true;
+    log_msg(3, "plan %p: skinny run enqueued, mode %d, epoch %u", static_cast<void*>(p), mode,
+            p->epoch);
     return AG_GEMM_OK;
   }
   if (int8 && runs_gemm) {
@@ -617,6 +642,8 @@ int run_impl(ag_gemm_plan* p, const void* const* shard_ptrs, const void* B, int6
   if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
   p->last_stream = stream;
   p->has_run = true;
+  log_msg(3, "plan %p: fused run enqueued, mode %d, epoch %u, grid %d", static_cast<void*>(p),
+          mode, p->epoch, p->grid_override > 0 ? p->grid_override : p->grid);
   return AG_GEMM_OK;
 }
 
@@ -815,6 +842,14 @@ ag_gemm_plan* create_plan(int n_shards, int64_t M, int64_t K, int64_t N, int dty
     free_plan(p);
     return nullptr;
   }
+  log_msg(2,
+          "plan %p: %s path, S=%d M=%lld K=%lld N=%lld dtype=%d, chunk_rows=%lld (%lld chunks per "
+          "source), %lld pair tiles, grid %d, split %d (%lld tail tiles), staging %lld B%s",
+          static_cast<void*>(p), p->skinny ? "skinny" : "fused", g.S, (long long)g.M,
+          (long long)g.K, (long long)g.N, g.dtype, (long long)g.c, (long long)g.Q,
+          (long long)g.tiles, p->skinny ? p->sk_grid : p->grid, p->split,
+          (long long)(g.tiles - p->full_tiles), (long long)p->staging_bytes,
+          p->window > 0 ? " (staging window)" : "");
   return p;
 }
 
@@ -843,6 +878,7 @@ int64_t ag_gemm_choose_chunk_rows_bounded(int64_t R) {
 
 void ag_gemm_plan_destroy(ag_gemm_plan* plan) {
   if (!plan) return;
+  log_msg(2, "plan %p destroyed", static_cast<void*>(plan));
   DeviceGuard dg(plan->device);
   free_plan(plan);
 }

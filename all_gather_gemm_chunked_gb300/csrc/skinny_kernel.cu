@@ -892,22 +892,19 @@ __global__ void __launch_bounds__(256) ag_skinny_finish_kernel(
     skinny_cta_range(U, b, grid, lo, hi);
     return lo < hi;
   };
-  const bool narrow_mn = static_cast<uint64_t>(M) * static_cast<uint64_t>(N) < (1ull << 32);
   for (int64_t gi = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; gi < groups;
        gi += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t off = gi * 8;
-    const int64_t m = narrow_mn ? static_cast<uint32_t>(off) / static_cast<uint32_t>(N) : off / N;
-    const int64_t n = off - m * N;
+    const int64_t off = gi * 8, m = off / N, n = off - m * N;
     const int64_t nt = n / kSkN, nl = n - nt * kSkN;
     const int64_t b_lo = owner(nt * KQ);
     const int64_t b_hi = owner((nt + 1) * KQ - 1);
     int32_t c[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    // eight slots per step: their sixteen 16-byte loads are issued before any
-    // is used (a CTA without units wrote no slot: its loads are skipped)
-    for (int64_t b0 = b_lo; b0 <= b_hi; b0 += 8) {
-      int4 x[16];
+    // four slots per step: their eight 16-byte loads are issued before any is
+    // used (a CTA without units wrote no slot: its loads are skipped)
+    for (int64_t b0 = b_lo; b0 <= b_hi; b0 += 4) {
+      int4 x[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < 4; ++i) {
         const int64_t b = b0 + i;
         x[2 * i] = x[2 * i + 1] = make_int4(0, 0, 0, 0);
         if (b <= b_hi && has_units(b)) {
@@ -918,7 +915,7 @@ __global__ void __launch_bounds__(256) ag_skinny_finish_kernel(
         }
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < 4; ++i) {
         const int4 x0 = x[2 * i], x1 = x[2 * i + 1];
         c[0] += x0.x; c[1] += x0.y; c[2] += x0.z; c[3] += x0.w;
         c[4] += x1.x; c[5] += x1.y; c[6] += x1.z; c[7] += x1.w;

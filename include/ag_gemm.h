@@ -37,6 +37,11 @@
  *     ag_gemm_plan_create); the thread-local ag_gemm_last_error() and
  *     ag_gemm_last_error_message() describe the last failure.  Nothing aborts
  *     and no C++ exception crosses this boundary.
+ *   - Logging: the environment variable AG_GEMM_LOG (read once per process)
+ *     makes the library write lines starting "[ag_gemm] " to stderr: 1 every
+ *     error as it is raised, 2 also each plan's geometry, path, grid and split
+ *     at creation and its destruction, 3 also every run enqueued.  Unset or 0:
+ *     silent.
  */
 #ifndef AG_GEMM_H
 #define AG_GEMM_H
