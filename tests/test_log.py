@@ -43,3 +43,32 @@ def test_log_reports_errors(level):
     lines = [l for l in err.splitlines() if l.startswith("[ag_gemm]")]
     assert len(lines) == 1, err
     assert "error -1" in lines[0] and "K % 16 == 0" in lines[0]
+
+
+GPU_SCRIPT = r"""
+import sys
+sys.path.insert(0, {root!r})
+import torch
+from all_gather_gemm_chunked_gb300.plan import Plan
+dev = torch.device("cuda:0")
+shards = [torch.randn(128, 256, device=dev).half() for _ in range(2)]
+B = torch.randn(256, 128, device=dev).half()
+with Plan(2, 256, 256, 128, "f16") as plan:
+    plan.run(shards, B)
+    assert plan.status() == 0
+torch.cuda.synchronize()
+print("ok")
+"""
+
+
+@pytest.mark.gpu
+def test_log_plans_and_runs_gpu():
+    env = dict(os.environ, AG_GEMM_LOG="3")
+    r = subprocess.run([sys.executable, "-c", GPU_SCRIPT.format(root=ROOT)], env=env,
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stderr
+    lines = [l for l in r.stderr.splitlines() if l.startswith("[ag_gemm]")]
+    assert any("fused path" in l and "S=2 M=256 K=256 N=128" in l for l in lines), r.stderr
+    assert any("fused run enqueued" in l for l in lines), r.stderr
+    assert any("destroyed" in l for l in lines), r.stderr
+    assert not any("error" in l for l in lines), r.stderr
