@@ -62,6 +62,7 @@ def test_chunk_rule_keeps_64_to_128_chunks_when_possible(B):
     ((2, 256, 256, 128, 0, -1), -1),
     ((2, 0, 256, 128, 0, 0), -1),
     ((2, 256, 133008, 128, 1, 0), -2),      # int8 K too large for exact int32
+    ((2, 1 << 31, 256, 1 << 26, 0, 0), -2),  # 2^31 x 2^26 output: more than 2^30 pair tiles
 ])
 def test_validate_rejects(B, args, code):
     with pytest.raises(B.AgGemmError) as e:
