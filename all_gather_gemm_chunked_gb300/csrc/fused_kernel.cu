@@ -210,9 +210,15 @@ __device__ void copy_warp(const FusedParams& p, int lane, unsigned long long fir
 // and are the ones that free a slot: by then both TMA warps and the MMA
 // thread have read the item (their reads precede the loads and MMAs the
 // epilogue waited for).
+//
+// An entry is one 64-bit word, ((n + 1) << 32) | item for entry n, stored
+// with a relaxed store (into the peer's ring with st.shared::cluster) and
+// polled until its tag reads n + 1: the word is its own payload, so no
+// acquire is needed.  (Publishing with an mbarrier arrival at cluster scope
+// instead slowed the odd CTA's next gpu-scope acquire loads -- its chunk-
+// counter probes -- from ~0.55 us to ~2 us.)
 struct TileRing {
-  int32_t* tq;         // this CTA's ring of items
-  uint64_t* full;      // this CTA's "published" barriers (one arrival: the producer)
+  uint64_t* tag;       // this CTA's ring of tagged items
   uint64_t* empty;     // the even CTA's "read" barriers (kTqReaders arrivals)
   uint32_t empty0;     // shared::cluster address of the even CTA's empty[0]
 };
@@ -240,9 +246,22 @@ struct PairItems {
 __device__ __forceinline__ bool ring_read(const TileRing& r, uint32_t n, int64_t& t,
                                           uint64_t timeout_ns, volatile int* abort,
                                           const volatile uint32_t* gstatus, bool release) {
-  const uint32_t slot = n % kTq, ph = (n / kTq) & 1u;
-  if (!mbar_wait_cluster(&r.full[slot], ph, timeout_ns, abort, gstatus)) return false;
-  t = *reinterpret_cast<volatile int32_t*>(&r.tq[slot]);
+  const uint32_t slot = n % kTq;
+  const volatile uint64_t* w = r.tag + slot;
+  uint64_t v = *w;
+  if ((v >> 32) != n + 1u) {
+    const uint64_t start = globaltimer_ns();
+    for (;;) {
+      __nanosleep(32);
+      v = *w;
+      if ((v >> 32) == n + 1u) break;
+      if (*abort) return false;
+      const uint64_t waited = globaltimer_ns() - start;
+      if (waited > timeout_ns) return false;
+      if (waited > kSlowWaitNs && gstatus && *gstatus) return false;
+    }
+  }
+  t = static_cast<int32_t>(static_cast<uint32_t>(v));
   if (release) mbar_arrive_cluster(r.empty0 + slot * 8);
   return true;
 }
@@ -262,10 +281,10 @@ __device__ __forceinline__ bool ring_put(const FusedParams& p, const TileRing& r
   const uint32_t slot = n % kTq, ph = (n / kTq) & 1u;
   if (!mbar_wait_cluster(&r.empty[slot], ph ^ 1u, p.pipe_timeout_ns, abort, gstatus))
     return false;
-  r.tq[slot] = static_cast<int32_t>(t);
-  st_shared_cluster_u32(mapa_shared(smem_u32(&r.tq[slot]), 1), static_cast<uint32_t>(t));
-  mbar_arrive(&r.full[slot]);
-  mbar_arrive_cluster(mapa_shared(smem_u32(&r.full[slot]), 1));
+  const uint64_t v = (static_cast<uint64_t>(n + 1u) << 32) |
+                     static_cast<uint32_t>(static_cast<int32_t>(t));
+  *reinterpret_cast<volatile uint64_t*>(r.tag + slot) = v;
+  st_relaxed_cluster_u64(mapa_shared(smem_u32(r.tag + slot), 1), v);
   return true;
 }
 
@@ -902,10 +921,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t* tfull = bars + 2 * kStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint64_t* tq_full = drain + 1;
-  uint64_t* tq_empty = tq_full + kTq;
-  int32_t* tq = reinterpret_cast<int32_t*>(tq_empty + kTq);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tq + kTq);
+  uint64_t* tq_tag = drain + 1;
+  uint64_t* tq_empty = tq_tag + kTq;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tq_empty + kTq);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -929,9 +947,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     mbar_init(drain, 1);
     for (int i = 0; i < kTq; ++i) {
-      mbar_init(&tq_full[i], 1);
+      tq_tag[i] = 0;  // no entry yet (entry n carries the tag n + 1)
       mbar_init(&tq_empty[i], kTqReaders);
-      tq[i] = -1;
     }
     *tmem_slot = 0;
     *abort = 0;
@@ -945,7 +962,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();  // barriers initialised and TMEM allocated in both CTAs
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const TileRing ring{tq, tq_full, tq_empty, mapa_shared(smem_u32(tq_empty), 0)};
+  const TileRing ring{tq_tag, tq_empty, mapa_shared(smem_u32(tq_empty), 0)};
 
   if constexpr (kTrace)
     if (threadIdx.x == 0) trace_emit(p.trace, tc, kTrCtaSlot, kTrCtaStart, 0, 0);

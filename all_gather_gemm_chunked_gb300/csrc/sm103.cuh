@@ -106,9 +106,10 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
 }
-// 32-bit store to a shared::cluster address (possibly in the peer CTA).
-__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
-  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+// Relaxed 64-bit store at cluster scope to a shared::cluster address.
+__device__ __forceinline__ void st_relaxed_cluster_u64(uint32_t cluster_addr, uint64_t v) {
+  asm volatile("st.relaxed.cluster.shared::cluster.u64 [%0], %1;" ::"r"(cluster_addr), "l"(v)
+               : "memory");
 }
 // try_wait whose acquire covers the cluster: it orders this thread's later
 // reads after writes that the peer CTA released with its arrive.
