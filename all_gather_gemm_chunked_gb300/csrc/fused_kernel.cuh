@@ -96,9 +96,10 @@ constexpr int kTqReaders = 2 * kEpiWarps;
 constexpr int kSkMaxRows = 128;   // the gathered rows are the MMA's N operand (N <= 128 here)
 
 struct SkinnyParams {
-  CUtensorMap tm_b8;        // int8 B (2D: N, K), box 128 x 128, 128-byte swizzle
-  CUtensorMap tm_a8_local;  // int8 local shard (2D: K, R), box 128 x R, unswizzled
-  CUtensorMap tm_a8_stage;  // int8 staging (3D: K, R, S - 1), box 128 x R x (S - 1)
+  CUtensorMap tm_b8;        // int8 B, 128-byte swizzle: 3D (128, K, N / 128), box 128 x 64 x 2
+                            // when b3d, else 2D (N, K), box 128 x 64
+  CUtensorMap tm_a8_local;  // int8 local shard (2D: K, R), box 64 x R, unswizzled
+  CUtensorMap tm_a8_stage;  // int8 staging (3D: K, R, S - 1), box 64 x R x (S - 1)
   Geometry g;
   const void* src[kMaxShards];  // shard pointers by consumption position
   int8_t* staging;              // int8 [S-1][R][K]
@@ -122,6 +123,7 @@ struct SkinnyParams {
   int64_t kq;                   // 2-k-block units per n-tile: ceil(KB / 2)
   int64_t cmax;                 // workspace slots per n-tile
   int np;                       // k-parts of the remote rows (copy tasks and counters per chunk)
+  int b3d;                      // tm_b8 is the 3D view (N % 128 == 0)
   TraceBuf trace;               // event trace (count == nullptr: off)
 };
 constexpr int kSkCopyWarpsPerCta = 2;

@@ -104,27 +104,39 @@ int encode_f16(CUtensorMap* map, const void* base, int rank, const cuuint64_t* d
   return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, base, rank, dims, strides_bytes, box);
 }
 
-// int8 B (N, K) of the skinny path in 128 x 128 boxes (two k-blocks, 16 KB) with
-// 128-byte swizzle; rows past K and columns past N read as zero.
+// int8 B (K x N row-major) of the skinny path, one k-block (64 k-rows) of a
+// 256-column n-tile per load, 128-byte swizzle.  With N % 128 == 0 a 3D view
+// (128 columns, K, N / 128 column blocks) takes both 128-column halves in one
+// box of 128 x 64 x 2 (one TMA instruction); otherwise 2D (N, K) boxes of
+// 128 x 64, two per k-block.  Rows past K, columns past N and blocks past
+// N / 128 read as zero.
+bool b8_is_3d(int64_t N) { return N % 128 == 0; }
 int encode_b8(CUtensorMap* map, const void* base, int64_t K, int64_t N) {
+  if (b8_is_3d(N)) {
+    cuuint64_t dims[3] = {128, (cuuint64_t)K, (cuuint64_t)(N / 128)};
+    cuuint64_t strides[2] = {(cuuint64_t)N, 128};
+    cuuint32_t box[3] = {128, agg::kBlockK, 2};
+    return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, 3, dims, strides, box);
+  }
   cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)K};
   cuuint64_t strides[1] = {(cuuint64_t)N};
-  cuuint32_t box[2] = {128, 2 * agg::kBlockK};
+  cuuint32_t box[2] = {128, agg::kBlockK};
   return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, 2, dims, strides, box);
 }
-// int8 gathered rows of the skinny path, 128 k at a time, unswizzled: a shard
-// (K, R) in 128 x R boxes, the staging (K, R, S - 1) in 128 x R x (S - 1) boxes.
+// int8 gathered rows of the skinny path, one k-block (64 k) at a time,
+// unswizzled: a shard (K, R) in 64 x R boxes, the staging (K, R, S - 1) in
+// 64 x R x (S - 1) boxes.
 int encode_a8(CUtensorMap* map, const void* base, int64_t R, int64_t K) {
   cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)R};
   cuuint64_t strides[1] = {(cuuint64_t)K};
-  cuuint32_t box[2] = {2 * agg::kBlockK, (cuuint32_t)R};
+  cuuint32_t box[2] = {agg::kBlockK, (cuuint32_t)R};
   return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, 2, dims, strides, box,
                       CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 int encode_stage8(CUtensorMap* map, const void* base, int64_t slots, int64_t R, int64_t K) {
   cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)R, (cuuint64_t)slots};
   cuuint64_t strides[2] = {(cuuint64_t)K, (cuuint64_t)R * K};
-  cuuint32_t box[3] = {2 * agg::kBlockK, (cuuint32_t)R, (cuuint32_t)slots};
+  cuuint32_t box[3] = {agg::kBlockK, (cuuint32_t)R, (cuuint32_t)slots};
   return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, 3, dims, strides, box,
                       CU_TENSOR_MAP_SWIZZLE_NONE);
 }
@@ -561,6 +573,7 @@ int run_impl(ag_gemm_plan* p, const void* const* shard_ptrs, const void* B, int6
       p->cached_a8 = local_ptr;
     }
     sp.tm_b8 = p->tm_b8_cached;
+    sp.b3d = b8_is_3d(g.N) ? 1 : 0;
     sp.tm_a8_local = p->tm_a8_cached;
     sp.tm_a8_stage = p->tm_stage8;
     sp.staging = static_cast<int8_t*>(p->staging);

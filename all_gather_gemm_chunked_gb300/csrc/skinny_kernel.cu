@@ -20,13 +20,15 @@
 // TMEM, so the accumulator is single-buffered: at the end of each segment the
 // MMA waits until the epilogue has folded it into the sums.
 //
-// B moves in 16 KB TMA boxes (128 columns x 128 k-rows, 128-byte swizzled),
-// two per unit (2 k-blocks of one 256-column n-tile); a TMA box carries a
-// fixed cost of several hundred cycles, which is why the boxes are not
-// smaller.  The same raw stage takes the unit's gathered rows (M x 128 int8,
-// two more boxes: the local shard and all staged shards), so A arrives with
-// B.  The rows land in consumption order (local shard first), which the
-// epilogue maps back to global rows.
+// A raw stage holds one k-block of one 256-column n-tile: 16 KB of B (two
+// 128-column x 64-k-row halves, 128-byte swizzled), loaded with ONE TMA
+// instruction through a 3D view of B (128 columns, K, N / 128) when N is a
+// multiple of 128 -- a TMA instruction carries a fixed cost of several
+// hundred cycles -- else as two 2D boxes; then the k-block's gathered rows
+// (M x 64 int8, two more boxes: the local shard and all staged shards), so A
+// arrives with B.  Five such stages let a stage be refilled as soon as its one
+// k-block is widened.  The rows land in consumption order (local shard
+// first), which the epilogue maps back to global rows.
 //
 // Work: the (256-column n-tile, 2-k-block unit) pairs, n-tile major, are cut
 // into one contiguous range per CTA (stream-K), so a CTA holds at most a few
@@ -71,18 +73,20 @@ constexpr int kSkThreads = kSkWarps * 32;
 constexpr int kSkN = 256;              // n-tile (the MMA's N)
 constexpr int kSkHalf = 128;           // columns of one B box
 constexpr int kSkUnitBlocks = 2;       // k-blocks per unit (128 k-rows)
-constexpr int kSkRawMax = 3;           // raw stages (B boxes + rows), at most
+constexpr int kSkRawMax = 5;           // raw stages (one k-block of B + rows each), at most
 constexpr int kSkFpMax = 3;            // fp16 stages (B + A, one k-block each), at most
 constexpr int kSkBwThreads = 256;      // 8 B-widening warps
 constexpr int kSkAwThreads = 128;      // 4 A-widening warps
-constexpr int kSkBoxB = kSkHalf * kBlockK * kSkUnitBlocks;   // 16 KB: one int8 B box
-constexpr int kSkRawB = 2 * kSkBoxB;                         // 32 KB int8 B per raw stage
-constexpr int kSkARow = kBlockK * kSkUnitBlocks;             // 128 bytes of a row per unit
+constexpr int kSkBoxB = kSkHalf * kBlockK;     // 8 KB: 128 columns x 64 k-rows of int8 B
+constexpr int kSkRawB = 2 * kSkBoxB;           // 16 KB int8 B per raw stage (one k-block)
+constexpr int kSkARow = kBlockK;               // 64 bytes of a row per raw stage
 constexpr int kSkFpB = kSkN * kBlockK * 2;                   // 32 KB: one fp16 k-block of B
-// M <= 64: raw 2 x (32 + 8) KB, fp16 3 x (32 + 8) KB = 200 KB;
-// M <= 128: raw 2 x (32 + 16) KB, fp16 2 x (32 + 16) KB = 192 KB.
-constexpr int kSkDataBytes = 200 * 1024;
-constexpr int kSkSmem = kSkDataBytes + 1024 + 1024;
+// M <= 64: raw 5 x 21 KB, fp16 3 x (32 + 8) KB = 225 KB;
+// M <= 128: raw 5 x 25 KB, fp16 2 x (32 + 16) KB = 221 KB.  (A raw stage is
+// 16 KB of B, the rows and up to 128 bytes of padding, rounded up to 1 KB so
+// that every stage's swizzled B boxes start 1024-byte aligned.)
+constexpr int kSkDataBytes = 225 * 1024;
+constexpr int kSkSmem = kSkDataBytes + 1024 /*alignment*/ + 256 /*barriers*/;
 constexpr uint32_t kSkDcol = 0;        // TMEM columns [0, 256): the fp32 accumulator
 constexpr uint32_t kSkScol = 256;      // [256, 512): int32 running sums
 
@@ -120,15 +124,23 @@ struct SkLayout {
   int mm;         // rows of the MMA (64 or 128)
   int a_stage;    // bytes of one fp16 A stage (mm rows x 128 bytes)
   int n_raw, n_fp;
-  int raw_stage;  // two B boxes, then mm rows x 128 bytes
+  int raw_stage;  // one k-block: two 8 KB B boxes, then the rows (sk_row_offset)
   __device__ __forceinline__ explicit SkLayout(int64_t M) {
     mm = M <= 64 ? 64 : 128;
     a_stage = mm * 128;
-    n_raw = 2;
+    n_raw = kSkRawMax;
     n_fp = mm == 64 ? 3 : 2;
-    raw_stage = kSkRawB + mm * kSkARow;
+    raw_stage = (kSkRawB + mm * kSkARow + 128 + 1023) & ~1023;
   }
 };
+
+// Byte offset of gathered row j (consumption order) in a raw stage's rows:
+// the local shard's R rows of 64 bytes, then the staged rows, which start at
+// the next 128-byte boundary (a TMA destination must be 128-byte aligned).
+__device__ __forceinline__ int sk_staged_offset(int R) { return (R * kSkARow + 127) & ~127; }
+__device__ __forceinline__ int sk_row_offset(int j, int R) {
+  return j < R ? j * kSkARow : sk_staged_offset(R) + (j - R) * kSkARow;
+}
 
 __device__ __forceinline__ void sk_set_status(uint32_t* status, uint32_t kind, uint32_t detail) {
   if (atomicCAS(status, 0u, kind) == 0u) atomicExch(status + 1, detail);
@@ -284,18 +296,22 @@ __device__ bool sk_wait_part(const SkinnyParams& p, int j, int lane, volatile in
 }
 
 // ------------------------------------------------------------------ TMA warp
-// Unit u (n-tile nt, unit q within it) into the raw stage at `st`: the two
-// B boxes, then the rows (the local shard, then every staged shard:
-// consumption order).
+// k-block kb of n-tile nt into the raw stage at `st`: B (both halves), then
+// the rows (the local shard, then every staged shard: consumption order).
 __device__ __forceinline__ void sk_issue_b(const SkinnyParams& p, uint8_t* st, uint64_t* bar,
-                                           int64_t nt, int64_t q) {
-  const int32_t y = static_cast<int32_t>(q * kSkARow);
-  tma_load_2d(st, &p.tm_b8, bar, static_cast<int32_t>(nt * kSkN), y);
-  tma_load_2d(st + kSkBoxB, &p.tm_b8, bar, static_cast<int32_t>(nt * kSkN + kSkHalf), y);
+                                           int64_t nt, int64_t kb) {
+  const int32_t y = static_cast<int32_t>(kb * kBlockK);
+  if (p.b3d) {
+    // both 128-column halves of the n-tile: blocks 2 nt and 2 nt + 1 of the 3D view
+    tma_load_3d(st, &p.tm_b8, bar, 0, y, static_cast<int32_t>(2 * nt));
+  } else {
+    tma_load_2d(st, &p.tm_b8, bar, static_cast<int32_t>(nt * kSkN), y);
+    tma_load_2d(st + kSkBoxB, &p.tm_b8, bar, static_cast<int32_t>(nt * kSkN + kSkHalf), y);
+  }
 }
 
-// The streamed gather: for each unit, B and the local shard's rows go out at
-// once (no wait: the local row group comes first, "AllGather + GEMM 通算融合
+// The streamed gather: for each k-block of a unit, B and the local shard's
+// rows go out at once (no wait: the local row group comes first, "AllGather + GEMM 通算融合
 // 算子示例", 流式流水线); the staged rows of the other shards go out as soon as
 // the k-part the unit reads has landed for every remote chunk, which the
 // warp's 32 lanes check together on the part's ready counters.  A part that
@@ -322,51 +338,56 @@ __device__ void sk_tma_warp(const SkinnyParams& p, uint8_t* sRaw, const SkLayout
   uint32_t issued = 0, issued_phase = 0;    // bit s: stage s used / parity of its last use
   bool ok = true, wait_failed = false;
   Ring r(L.n_raw);
-  int64_t i = 0;
-  for (int64_t u = u0; u < u1; ++u, ++i, r.next()) {
+  int64_t i = 0;  // raw stages issued
+  for (int64_t u = u0; u < u1 && ok; ++u) {
     const int64_t nt = static_cast<uint32_t>(u) / static_cast<uint32_t>(KQ), q = u - nt * KQ;
-    uint8_t* st = sRaw + r.s * L.raw_stage;
-    const int32_t x = static_cast<int32_t>(q * kSkARow);
-    if (lane == 0) {
-      if (i >= L.n_raw &&
-          !mbar_wait(&raw_empty[r.s], r.ph ^ 1u, p.pipe_timeout_ns, abort, gstatus))
-        ok = false;
-      if (ok) {
-        mbar_arrive_expect_tx(&raw_full[r.s], tx);
-        sk_issue_b(p, st, &raw_full[r.s], nt, q);
-        tma_load_2d(st + kSkRawB, &p.tm_a8_local, &raw_full[r.s], x, 0);
-        issued |= 1u << r.s;
-        issued_phase = (issued_phase & ~(1u << r.s)) | (r.ph << r.s);
-      }
-    }
-    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    if (!ok) break;
-    if (remote) {
-      const int j = skinny_part_of(q, KQ, p.np);
-      if (wait && !((ready >> j) & 1u)) {
-        if constexpr (kTrace)
-          if (lane == 0) trace_emit(p.trace, tn, threadIdx.x >> 5, kTrWaitStart, static_cast<uint32_t>(u), j);
-        if (!sk_wait_part(p, j, lane, abort)) {
+    int64_t kb0, kb1;
+    unit_blocks(g, KQ, u, kb0, kb1);
+    for (int64_t kb = kb0; kb < kb1; ++kb, ++i, r.next()) {
+      uint8_t* st = sRaw + r.s * L.raw_stage;
+      const int32_t x = static_cast<int32_t>(kb * kBlockK);
+      if (lane == 0) {
+        if (i >= L.n_raw &&
+            !mbar_wait(&raw_empty[r.s], r.ph ^ 1u, p.pipe_timeout_ns, abort, gstatus))
           ok = false;
-          wait_failed = true;
-          break;
-        }
-        if constexpr (kTrace)
-          if (lane == 0) trace_emit(p.trace, tn, threadIdx.x >> 5, kTrWaitEnd, static_cast<uint32_t>(u), j);
-        // the other parts have usually landed by now as well: one sweep over
-        // their counters spares the later units the wait
-        ready |= (1u << j) | sk_parts_landed(p, lane);
-        if (lane == 0) {
-          // the staged rows were written by other SMs' generic stores; TMA reads them
-          fence_acq_rel_gpu();
-          fence_proxy_async_global();
+        if (ok) {
+          mbar_arrive_expect_tx(&raw_full[r.s], tx);
+          sk_issue_b(p, st, &raw_full[r.s], nt, kb);
+          tma_load_2d(st + kSkRawB, &p.tm_a8_local, &raw_full[r.s], x, 0);
+          issued |= 1u << r.s;
+          issued_phase = (issued_phase & ~(1u << r.s)) | (r.ph << r.s);
         }
       }
-      if (lane == 0)
-        tma_load_3d(st + kSkRawB + g.R * kSkARow, &p.tm_a8_stage, &raw_full[r.s], x, 0, 0);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      if (remote) {
+        const int j = skinny_part_of(q, KQ, p.np);
+        if (wait && !((ready >> j) & 1u)) {
+          if constexpr (kTrace)
+            if (lane == 0) trace_emit(p.trace, tn, threadIdx.x >> 5, kTrWaitStart, static_cast<uint32_t>(u), j);
+          if (!sk_wait_part(p, j, lane, abort)) {
+            ok = false;
+            wait_failed = true;
+            break;
+          }
+          if constexpr (kTrace)
+            if (lane == 0) trace_emit(p.trace, tn, threadIdx.x >> 5, kTrWaitEnd, static_cast<uint32_t>(u), j);
+          // the other parts have usually landed by now as well: one sweep over
+          // their counters spares the later units the wait
+          ready |= (1u << j) | sk_parts_landed(p, lane);
+          if (lane == 0) {
+            // the staged rows were written by other SMs' generic stores; TMA reads them
+            fence_acq_rel_gpu();
+            fence_proxy_async_global();
+          }
+        }
+        if (lane == 0)
+          tma_load_3d(st + kSkRawB + sk_staged_offset(static_cast<int>(g.R)), &p.tm_a8_stage,
+                      &raw_full[r.s], x, 0, 0);
+      }
     }
     if constexpr (kTrace)
-      if (lane == 0) trace_emit(p.trace, tn, threadIdx.x >> 5, kTrUnitIssued, static_cast<uint32_t>(u), 0);
+      if (ok && lane == 0) trace_emit(p.trace, tn, threadIdx.x >> 5, kTrUnitIssued, static_cast<uint32_t>(u), 0);
   }
   if (!ok && lane == 0) {
     if (!wait_failed) sk_set_status(p.status, kStatusPipelineTimeout, 0x1100u);
@@ -402,20 +423,21 @@ __device__ void sk_bwiden(const SkinnyParams& p, const uint8_t* sRaw, const SkLa
   int64_t u0, u1;
   skinny_cta_range(p.n_tiles * KQ, blockIdx.x, gridDim.x, u0, u1);
   Ring rr(L.n_raw), fr(L.n_fp);
-  for (int64_t u = u0; u < u1; ++u, rr.next()) {
-    if (!mbar_wait(&raw_full[rr.s], rr.ph, p.pipe_timeout_ns, abort, gstatus)) {
-      if (lane == 0) {
-        sk_set_status(p.status, kStatusPipelineTimeout, 0x1200u);
-        *abort = 1;
-      }
-      return;
-    }
-    if constexpr (kTrace)
-      if (t == 0) trace_emit(p.trace, tn, threadIdx.x >> 5, kTrUnitLanded, static_cast<uint32_t>(u), 0);
+  for (int64_t u = u0; u < u1; ++u) {
     int64_t kb0, kb1;
     unit_blocks(g, KQ, u, kb0, kb1);
-    const uint8_t* raw = sRaw + rr.s * L.raw_stage;
-    for (int b = 0; b < static_cast<int>(kb1 - kb0); ++b, fr.next()) {
+    for (int b = 0; b < static_cast<int>(kb1 - kb0); ++b, fr.next(), rr.next()) {
+      if (!mbar_wait(&raw_full[rr.s], rr.ph, p.pipe_timeout_ns, abort, gstatus)) {
+        if (lane == 0) {
+          sk_set_status(p.status, kStatusPipelineTimeout, 0x1200u);
+          *abort = 1;
+        }
+        return;
+      }
+      if constexpr (kTrace)
+        if (t == 0 && b == 0)
+          trace_emit(p.trace, tn, threadIdx.x >> 5, kTrUnitLanded, static_cast<uint32_t>(u), 0);
+      const uint8_t* raw = sRaw + rr.s * L.raw_stage;
       if (!mbar_wait(&fp_empty[fr.s], fr.ph ^ 1u, p.pipe_timeout_ns, abort, gstatus)) {
         if (lane == 0) {
           sk_set_status(p.status, kStatusPipelineTimeout, 0x1201u);
@@ -424,7 +446,7 @@ __device__ void sk_bwiden(const SkinnyParams& p, const uint8_t* sRaw, const SkLa
         return;
       }
       // raw B arrives 128-byte swizzled: 16-byte chunk c of box row r sits at c ^ (r % 8)
-      const int r = b * kBlockK + krow;
+      const int r = krow;
       uint4 v[4];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -446,19 +468,20 @@ __device__ void sk_bwiden(const SkinnyParams& p, const uint8_t* sRaw, const SkLa
       }
       fence_proxy_async_shared();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&fp_full[fr.s]);
+      if (lane == 0) {
+        mbar_arrive(&fp_full[fr.s]);
+        mbar_arrive(&raw_empty[rr.s]);  // this k-block's raw stage is read
+      }
       if constexpr (kTrace)
         if (t == 0) trace_emit(p.trace, tn, threadIdx.x >> 5, kTrKbWidened, static_cast<uint32_t>(kb0 + b), u);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&raw_empty[rr.s]);
   }
 }
 
 // ------------------------------------------------------------------ A widening (4 warps)
 // Thread t widens the 16 k at k-offset (t % 4) * 16 of rows t / 4 + 32 e,
 // e < NE (NE = 2 for M <= 64, 4 for M <= 128), from the raw stage's rows
-// (128 bytes each, consumption order) into fp16 A stages: K-major, 128-byte
+// (64 bytes each, consumption order) into fp16 A stages: K-major, 128-byte
 // rows, 16-byte chunk c of row j at c ^ (j % 8).  Rows M .. mm - 1 are left
 // as they are: they only reach rows of the accumulator nobody reads.
 template <int NE>
@@ -468,22 +491,23 @@ __device__ void sk_awiden(const SkinnyParams& p, const uint8_t* sRaw, const SkLa
   const Geometry& g = p.g;
   const volatile uint32_t* gstatus = p.status;
   const int lane = t & 31, j0 = t >> 2, h = t & 3;
+  const int R = static_cast<int>(g.R);
   const int64_t KQ = p.kq;
   int64_t u0, u1;
   skinny_cta_range(p.n_tiles * KQ, blockIdx.x, gridDim.x, u0, u1);
   Ring rr(L.n_raw), ar(L.n_fp);
-  for (int64_t u = u0; u < u1; ++u, rr.next()) {
-    if (!mbar_wait(&raw_full[rr.s], rr.ph, p.pipe_timeout_ns, abort, gstatus)) {
-      if (lane == 0) {
-        sk_set_status(p.status, kStatusPipelineTimeout, 0x1300u);
-        *abort = 1;
-      }
-      return;
-    }
+  for (int64_t u = u0; u < u1; ++u) {
     int64_t kb0, kb1;
     unit_blocks(g, KQ, u, kb0, kb1);
-    const uint8_t* raw = sRaw + rr.s * L.raw_stage + kSkRawB;
-    for (int b = 0; b < static_cast<int>(kb1 - kb0); ++b, ar.next()) {
+    for (int b = 0; b < static_cast<int>(kb1 - kb0); ++b, ar.next(), rr.next()) {
+      if (!mbar_wait(&raw_full[rr.s], rr.ph, p.pipe_timeout_ns, abort, gstatus)) {
+        if (lane == 0) {
+          sk_set_status(p.status, kStatusPipelineTimeout, 0x1300u);
+          *abort = 1;
+        }
+        return;
+      }
+      const uint8_t* raw = sRaw + rr.s * L.raw_stage + kSkRawB;
       if (!mbar_wait(&a_empty[ar.s], ar.ph ^ 1u, p.pipe_timeout_ns, abort, gstatus)) {
         if (lane == 0) {
           sk_set_status(p.status, kStatusPipelineTimeout, 0x1301u);
@@ -496,7 +520,7 @@ __device__ void sk_awiden(const SkinnyParams& p, const uint8_t* sRaw, const SkLa
         const int j = j0 + 32 * e;
         if (j < g.M) {
           const uint4 v =
-              *reinterpret_cast<const uint4*>(raw + j * kSkARow + b * kBlockK + h * 16);
+              *reinterpret_cast<const uint4*>(raw + sk_row_offset(j, R) + h * 16);
           uint4 lo, hi;
           widen16x(v, lo, hi);
           uint8_t* dst = sA + ar.s * L.a_stage + j * 128;
@@ -506,10 +530,11 @@ __device__ void sk_awiden(const SkinnyParams& p, const uint8_t* sRaw, const SkLa
       }
       fence_proxy_async_shared();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&a_full[ar.s]);
+      if (lane == 0) {
+        mbar_arrive(&a_full[ar.s]);
+        mbar_arrive(&raw_empty[rr.s]);  // this k-block's raw stage is read
+      }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&raw_empty[rr.s]);
   }
 }
 
