@@ -427,6 +427,7 @@ class Runner:
         B_full = torch.empty((w.K, w.N * w.n_blocks), dtype=h_B.dtype, device=dev)
         self.Bd = B_full[:, cols]
         self.Bd.copy_(h_B)
+        self.cols = cols
         self.int8 = w.dtype == "i8"
         if self.int8:
             h_bias, h_scale = pin(x["bias"]), pin(x["scale"])
@@ -471,6 +472,100 @@ class Runner:
             self.h_D.copy_(self.D, non_blocking=True)
         else:
             self.h_C.copy_(self.C, non_blocking=True)
+
+    # -- end to end, pipelined over steps ------------------------------------
+    def _outputs(self):
+        return [self.Ci, self.D] if self.int8 else [self.C]
+
+    def _set_of(self, shards, Bd, outputs, extra=()):
+        # extra: the int8 path's bias and scale (copied in every step as well)
+        return {"shards": shards, "Bd": Bd, "out": outputs, "extra": list(extra)}
+
+    def _second_set(self):
+        """Device buffers for a second step in flight: the layout of the first
+        (B and C as column blocks of full-width matrices for the N-sharded layout)."""
+        torch, w, dev = self.torch, self.w, self.dev
+        shards = [torch.empty_like(t) for t in self.shards]
+        Bd = torch.empty((w.K, w.N * w.n_blocks), dtype=self.Bd.dtype, device=dev)[:, self.cols]
+        extra = ()
+        if self.int8:
+            out = [torch.empty_like(self.Ci), torch.empty_like(self.D)]
+            extra = (torch.empty_like(self.bias), torch.empty_like(self.scale))
+        else:
+            out = [torch.empty((w.M, w.N * w.n_blocks), dtype=torch.float32,
+                               device=dev)[:, self.cols]]
+        return self._set_of(shards, Bd, out, extra)
+
+    def _run_set(self, st):
+        if self.int8:
+            self.plan.dequant_run(st["shards"], st["Bd"], *st["extra"], *st["out"])
+        else:
+            self.plan.run(st["shards"], st["Bd"], st["out"][0])
+
+    def e2e_pipelined(self, n, gate_ms=20.0):
+        """Milliseconds per step of n end-to-end steps with two steps' buffers:
+        step i's host->device copies (on one stream) and step i-1's
+        device->host copies (on another) run beside step i-1's or step i's
+        run.  Every step still copies all of its inputs in and its outputs
+        out inside the timed region; only the order of the engines overlaps.
+        The runs stay on one stream, one at a time, as the plan requires."""
+        torch, dev, main = self.torch, self.dev, self.stream
+        if not hasattr(self, "_e2e"):
+            extra = (self.bias, self.scale) if self.int8 else ()
+            sets = [self._set_of(self.shards, self.Bd, self._outputs(), extra), self._second_set()]
+            hosts = [[self.h_Ci, self.h_D] if self.int8 else [self.h_C],
+                     [torch.empty_like(t).pin_memory() for t in
+                      ([self.h_Ci, self.h_D] if self.int8 else [self.h_C])]]
+            self._e2e = (sets, hosts, torch.cuda.Stream(dev), torch.cuda.Stream(dev))
+        sets, hosts, s_in, s_out = self._e2e
+        ev = lambda: torch.cuda.Event()  # noqa: E731
+        ev_in, ev_run, ev_out = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for attempt in range(4):
+            torch.cuda._sleep(int(gate_ms * 2.1e6))
+            gate = torch.cuda.Event()
+            gate.record(main)
+            start.record(main)
+            s_in.wait_event(start)
+            s_out.wait_event(start)
+            t0 = time.perf_counter()
+            for i in range(n):
+                b, st = i % 2, sets[i % 2]
+                with torch.cuda.stream(s_in):
+                    if i >= 2:
+                        s_in.wait_event(ev_run[b])  # step i - 2 has read these inputs
+                    for hs, ds in zip(self.h_shards, st["shards"]):
+                        ds.copy_(hs, non_blocking=True)
+                    st["Bd"].copy_(self.h_B, non_blocking=True)
+                    if self.int8:
+                        st["extra"][0].copy_(self.h_bias, non_blocking=True)
+                        st["extra"][1].copy_(self.h_scale, non_blocking=True)
+                    ev_in[b].record(s_in)
+                main.wait_event(ev_in[b])
+                if i >= 2:
+                    main.wait_event(ev_out[b])  # step i - 2's outputs have been read back
+                self._run_set(st)
+                ev_run[b].record(main)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(ev_run[b])
+                    for ht, dt in zip(hosts[b], st["out"]):
+                        ht.copy_(dt, non_blocking=True)
+                    ev_out[b].record(s_out)
+            for b in range(min(n, 2)):
+                main.wait_event(ev_out[b])
+            end.record(main)
+            host_ms = (time.perf_counter() - t0) * 1e3
+            late = gate.query()
+            torch.cuda.synchronize(dev)
+            if not late:
+                break
+            gate_ms = max(2.0 * gate_ms, 2.0 * host_ms)
+        # every step computed the same inputs: the last step's host copy must
+        # equal the other buffer set's device outputs bit for bit
+        last = hosts[(n - 1) % 2]
+        other = sets[n % 2]["out"]
+        self.e2e_outputs_match = all(torch.equal(h, d.cpu()) for h, d in zip(last, other))
+        return start.elapsed_time(end) / n
 
     def e2e_bytes(self):
         h2d = (sum(t.numel() * t.element_size() for t in self.h_shards)
@@ -629,11 +724,21 @@ def run_ours(args, w, rank, world, local_rank):
     ne = max(3, min(args.steps, 10))
     e2e_ms, _ = r.timed(ne, B_.MODE_PIPELINED, None, fn=r.e2e_step)
     r.check_status("end-to-end runs")
-    e2e_t = reduce_max(float(np.sum(e2e_ms)) / 1e3, dev)
+    e2e_serial_t = reduce_max(float(np.sum(e2e_ms)) / 1e3, dev)
+    r.e2e_pipelined(2)  # warm-up: the second buffer set and the copy streams
+    e2e_t = reduce_max(r.e2e_pipelined(ne) * ne / 1e3, dev)
+    r.check_status("pipelined end-to-end runs")
     h2d, d2h = r.e2e_bytes()
     unit = "TOP/s" if r.int8 else "TFLOP/s"
     e2e = {"value": whole_job_value(w.flops * ne, world, e2e_t), "unit": unit,
-           "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+           "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+           "steps": ne,
+           "overlap": "two steps' buffers: step i's host->device copies and step i-1's "
+                      "device->host copies run on their own streams beside the runs",
+           "serial": {"value": whole_job_value(w.flops * ne, world, e2e_serial_t),
+                      "unit": unit, "ms_per_step": e2e_serial_t * 1e3 / ne},
+           "ms_per_step": e2e_t * 1e3 / ne,
+           "outputs_match": bool(r.e2e_outputs_match)}
 
     peaks, peak_src = load_peaks()
     path_id = r.path
