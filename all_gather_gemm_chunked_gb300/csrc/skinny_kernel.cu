@@ -44,10 +44,10 @@
 // warps w with w % 4 == q, hence the epilogue warps 16, 1, 2, 3.
 //   warp 0                 MMA: one thread issues tcgen05.mma (M = 64 or 128,
 //                          N = 256, K = 16).
-//   warp 4                 TMA: streams the CTA's units (two B boxes + row
-//                          boxes) into a raw ring; B and the local rows go out
-//                          at once, the staged rows once the unit's k-part of
-//                          every remote chunk has landed.
+//   warp 4                 TMA: streams the CTA's units into a raw ring, one
+//                          k-block (B, then the row boxes) per stage; B and
+//                          the local rows go out at once, the staged rows once
+//                          the unit's k-part of every remote chunk has landed.
 //   warps 8, 12            copy: remote chunks, one k-part at a time, into the
 //                          int8 staging workspace; one ready counter per
 //                          (k-part, chunk).
@@ -790,7 +790,7 @@ __global__ void __launch_bounds__(kSkThreads, 1) ag_skinny_kernel(const __grid_c
   const SkLayout L(p.g.M);
   uint8_t* sFp = smem;                          // 1024-aligned swizzled fp16 B stages
   uint8_t* sA = sFp + L.n_fp * kSkFpB;          // swizzled fp16 A stages
-  uint8_t* sRaw = sA + L.n_fp * L.a_stage;      // raw ring: two B boxes, then the rows
+  uint8_t* sRaw = sA + L.n_fp * L.a_stage;      // raw ring: per k-block, B, then the rows
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kSkDataBytes);
   uint64_t* raw_full = bars;
   uint64_t* raw_empty = raw_full + kSkRawMax;
