@@ -472,6 +472,121 @@ __device__ void tma_warp(const FusedParams& p, uint32_t rank, uint8_t* sA, uint8
   __syncwarp();
 }
 
+// Two producers for a plan whose tiles are all dealt (fp16 / bf16 kernel):
+// producer 0 (warp 0) streams the pair's items 0, 2, 4, ..., producer 1 (the
+// extra warp) items 1, 3, 5, ...  Each decodes its next item and waits for
+// its chunks while the other streams, so a tile boundary no longer stalls the
+// ring for the decode, the chunk wait and the fences.  A producer issues an
+// item's first k-block only after the other has issued all of the previous
+// item (a hand-off barrier per producer), so every stage's uses stay in
+// order and each empty-barrier parity wait sees at most one pending use.
+// Item seq's k-blocks occupy the ring from global block seq * KB on (every
+// item is a whole tile).
+template <bool kI8, bool kTrace>
+__device__ void tma_warp_dealt(const FusedParams& p, uint32_t rank, uint8_t* sA, uint8_t* sB,
+                               uint64_t* full, uint64_t* empty, uint64_t* hand, int producer,
+                               int lane, volatile int* abort) {
+  const Geometry& g = p.g;
+  [[maybe_unused]] uint32_t tn = 0;  // trace events of this warp
+  const volatile uint32_t* gstatus = p.status;
+  const bool wait = (p.flags & kFlagWait) != 0;
+  const int half = g.BN / 2;
+  const uint32_t pair_tx = static_cast<uint32_t>(2 * (kABytes + half * kBlockK * 2));
+  const uint32_t full0 = mapa_shared(smem_u32(full), 0);
+  uint32_t issued = 0, issued_phase = 0;
+  if (lane == 0) {
+    tma_prefetch_desc(&p.tm_a_local);
+    tma_prefetch_desc(&p.tm_a_stage);
+    tma_prefetch_desc(&p.tm_b);
+  }
+  const PairItems items(p);
+  const uint64_t KB = static_cast<uint64_t>(g.KB);
+  bool ok = true;
+  uint32_t handoffs = 0;  // items of the other producer waited for
+  for (uint32_t seq = static_cast<uint32_t>(producer); ok && items.dealt(seq); seq += 2) {
+    const int64_t t = items.dealt_item(seq);
+    int64_t tile, kbs, kbe;
+    int part, parts;
+    work_item(g, p.full_tiles, p.split, t, tile, part, parts, kbs, kbe);
+    int pos;
+    int64_t mt, nt;
+    tile_coords(g, tile, pos, mt, nt);
+    const int64_t row0 = mt * kPairM + rank * kBlockM;
+    if constexpr (kTrace) {
+      int64_t q0 = 0, q1 = -1;
+      const bool rows = pos > 0 && wait && rows_chunks(g, row0, q0, q1);
+      const uint64_t aux = (static_cast<uint64_t>(pos) << 48) |
+                           (static_cast<uint64_t>(q0 & 0xFFFFFF) << 24) |
+                           static_cast<uint64_t>(q1 & 0xFFFFFF);
+      if (rows && lane == 0) trace_emit(p.trace, tn, threadIdx.x >> 5, kTrWaitStart, static_cast<uint32_t>(tile), aux);
+      if (pos > 0 && wait && !wait_chunks(p, pos, row0, lane, abort)) break;
+      if (rows && lane == 0) trace_emit(p.trace, tn, threadIdx.x >> 5, kTrWaitEnd, static_cast<uint32_t>(tile), aux);
+    } else {
+      if (pos > 0 && wait && !wait_chunks(p, pos, row0, lane, abort)) break;
+    }
+    if (lane == 0) {
+      if (pos > 0) {
+        fence_acq_rel_gpu();
+        fence_proxy_async_global();
+      }
+      // the other producer has issued every k-block of item seq - 1
+      if (seq > 0) {
+        ok = mbar_wait(&hand[producer ^ 1], handoffs & 1u, p.pipe_timeout_ns, abort, gstatus);
+        ++handoffs;
+      }
+      const bool win = pos > 0 && p.window > 0;
+      const int32_t y = win ? static_cast<int32_t>(rank * kBlockM) : static_cast<int32_t>(row0);
+      const int32_t z = win ? static_cast<int32_t>(static_cast<uint32_t>((pos - 1) * g.MT + mt) %
+                                                   static_cast<uint32_t>(p.window))
+                            : pos - 1;
+      const int32_t xb = static_cast<int32_t>(nt * g.BN + rank * half);
+      const uint64_t g0 = static_cast<uint64_t>(seq) * KB;
+      int stage = static_cast<int>(g0 % kStages);
+      uint32_t phase = static_cast<uint32_t>((g0 / kStages) & 1u);
+      for (int64_t kb = kbs; kb < kbe && ok; ++kb) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u, p.pipe_timeout_ns, abort, gstatus)) {
+          ok = false;
+          break;
+        }
+        const uint32_t bar = full0 + stage * 8;
+        if (rank == 0) mbar_arrive_expect_tx(&full[stage], pair_tx);
+        const int32_t x = static_cast<int32_t>(kb * kBlockK);
+        uint8_t* a_dst = sA + stage * kABytes;
+        if (pos == 0)
+          tma_load_2d_pair(a_dst, &p.tm_a_local, bar, x, y);
+        else
+          tma_load_3d_pair(a_dst, &p.tm_a_stage, bar, x, y, z);
+        uint8_t* b_dst = sB + stage * kBBytes;
+        if (p.b3d)
+          tma_load_3d_pair(b_dst, &p.tm_b, bar, 0, x, xb / 64);
+        else
+          for (int i = 0; i < half / 64; ++i)
+            tma_load_2d_pair(b_dst + i * (64 * kBlockK * 2), &p.tm_b, bar, xb + i * 64, x);
+        issued |= 1u << stage;
+        issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (ok) mbar_arrive(&hand[producer]);  // item seq is issued
+    }
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  }
+  if (lane == 0 && !ok) {
+    set_status(p.status, kStatusPipelineTimeout, 0x600u | (static_cast<uint32_t>(producer) << 4) | rank);
+    *abort = 1;
+    if (rank == 0) {
+      // Loads counted on this CTA's barriers must land before the pair
+      // exits (bounded: a stage reused by the other producer may be a phase on).
+      volatile int never = 0;
+      for (int s = 0; s < kStages; ++s)
+        if (issued & (1u << s)) mbar_wait(&full[s], (issued_phase >> s) & 1u, 20000000ull, &never);
+    }
+  }
+  __syncwarp();
+}
+
 // ------------------------------------------------------------------ MMA warp (even CTA)
 template <bool kI8>
 __device__ void mma_warp(const FusedParams& p, const uint8_t* sA, const uint8_t* sB,
@@ -906,7 +1021,7 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
 
 // ------------------------------------------------------------------ kernel
 template <bool kI8, bool kTrace, bool kSplit>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(fused_threads(kI8), 1)
     ag_fused_kernel(const __grid_constant__ FusedParams p) {
   [[maybe_unused]] uint32_t tc = 0;  // trace events of the CTA slot
   extern __shared__ uint8_t smem_raw[];
@@ -923,7 +1038,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t* drain = tempty + 2;
   uint64_t* tq_tag = drain + 1;
   uint64_t* tq_empty = tq_tag + kTq;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tq_empty + kTq);
+  uint64_t* hand = tq_empty + kTq;  // the two TMA producers' "item issued" barriers
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(hand + 2);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -946,6 +1062,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&tempty[b], 2 * kEpiWarps);  // the epilogue warps of both CTAs of the pair
     }
     mbar_init(drain, 1);
+    mbar_init(&hand[0], 1);
+    mbar_init(&hand[1], 1);
     for (int i = 0; i < kTq; ++i) {
       tq_tag[i] = 0;  // no entry yet (entry n carries the tag n + 1)
       mbar_init(&tq_empty[i], kTqReaders);
@@ -966,8 +1084,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if constexpr (kTrace)
     if (threadIdx.x == 0) trace_emit(p.trace, tc, kTrCtaSlot, kTrCtaStart, 0, 0);
+  // two TMA producers when every tile of the plan is dealt (fp16 / bf16 kernel)
+  const bool two_producers = !kI8 && p.work_items == p.static_items;
   if (warp == 0) {
-    if (gemm) tma_warp<kI8, kTrace>(p, rank, sA, sB, full, empty, ring, lane, abort);
+    if (gemm) {
+      if (two_producers)
+        tma_warp_dealt<kI8, kTrace>(p, rank, sA, sB, full, empty, hand, 0, lane, abort);
+      else
+        tma_warp<kI8, kTrace>(p, rank, sA, sB, full, empty, ring, lane, abort);
+    }
+  } else if (!kI8 && warp == kExtraTmaWarp) {
+    if (gemm && two_producers)
+      tma_warp_dealt<kI8, kTrace>(p, rank, sA, sB, full, empty, hand, 1, lane, abort);
   } else if (warp == 1) {
     if (gemm && rank == 0 && lane == 0)
       mma_warp<kI8>(p, sA, sB, full, empty, tfull, tempty, ring, tmem, abort);
@@ -1061,7 +1189,7 @@ cudaError_t fused_max_clusters(int dtype, int grid, int* clusters) {
   const void* fn = fused_fn(dtype, false, false);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(fused_threads(dtype == 1));
   cfg.dynamicSmemBytes = kSmemBytes;
   return cudaOccupancyMaxActiveClusters(clusters, fn, &cfg);
 }
@@ -1069,7 +1197,7 @@ cudaError_t fused_max_clusters(int dtype, int grid, int* clusters) {
 cudaError_t launch_fused(const FusedParams& p, int grid, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(fused_threads(p.g.dtype == 1));
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
   const void* fn = fused_fn(p.g.dtype, p.trace.ev != nullptr, p.split > 1);

@@ -75,7 +75,13 @@ struct FusedParams {
   TraceBuf trace;               // event trace (count == nullptr: off)
 };
 
-constexpr int kThreads = 384;                         // 12 warps
+constexpr int kThreads = 384;                         // 12 warps (int8 kernel)
+// The fp16 / bf16 kernel adds a second TMA producer warp (warp 12), used when
+// every tile of the plan is dealt; the int8 kernel's 168 registers per thread
+// leave no room for a thirteenth warp.
+constexpr int kExtraTmaWarp = 12;
+constexpr int kThreadsF16 = 416;
+__host__ __device__ constexpr int fused_threads(bool i8) { return i8 ? kThreads : kThreadsF16; }
 constexpr int kEpiWarps = 8;                          // 4 lane quadrants x 2 column halves
 constexpr int kABytes = kBlockM * kBlockK * 2;        // 16 KB: this CTA's 128 rows of A
 constexpr int kBBytes = kMaxBlockN / 2 * kBlockK * 2; // 16 KB: this CTA's half of B's columns
