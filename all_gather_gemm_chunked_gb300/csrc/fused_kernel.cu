@@ -325,6 +325,91 @@ __device__ bool wait_chunks(const FusedParams& p, int pos, int64_t row0, int lan
   return ok;
 }
 
+// A work item's operand sources: A rows from the local shard at row0, or the
+// staging: [S-1][R][K] at (row0, pos - 1), or the window's [W][256][K] at
+// (this CTA's half, slot); B's columns from xb.
+struct ItemSource {
+  int pos;
+  int32_t y, z, xb;
+};
+__device__ __forceinline__ ItemSource item_source(const FusedParams& p, uint32_t rank, int pos,
+                                                  int64_t mt, int64_t nt, int64_t row0,
+                                                  int half) {
+  const Geometry& g = p.g;
+  const bool win = pos > 0 && p.window > 0;
+  ItemSource s;
+  s.pos = pos;
+  s.y = win ? static_cast<int32_t>(rank * kBlockM) : static_cast<int32_t>(row0);
+  s.z = win ? static_cast<int32_t>(static_cast<uint32_t>((pos - 1) * g.MT + mt) %
+                                   static_cast<uint32_t>(p.window))
+            : pos - 1;
+  s.xb = static_cast<int32_t>(nt * g.BN + rank * half);
+  return s;
+}
+
+// A remote item's wait for the chunks its 128 rows read (all lanes), with the
+// trace's wait events; true when the rows may be loaded.
+template <bool kTrace>
+__device__ __forceinline__ bool wait_item_rows(const FusedParams& p, int pos, int64_t row0,
+                                               int64_t tile, bool wait, int lane,
+                                               volatile int* abort, uint32_t& tn) {
+  if constexpr (kTrace) {
+    int64_t q0 = 0, q1 = -1;
+    const bool rows = pos > 0 && wait && rows_chunks(p.g, row0, q0, q1);
+    const uint64_t aux = (static_cast<uint64_t>(pos) << 48) |
+                         (static_cast<uint64_t>(q0 & 0xFFFFFF) << 24) |
+                         static_cast<uint64_t>(q1 & 0xFFFFFF);
+    if (rows && lane == 0) trace_emit(p.trace, tn, threadIdx.x >> 5, kTrWaitStart, static_cast<uint32_t>(tile), aux);
+    if (pos > 0 && wait && !wait_chunks(p, pos, row0, lane, abort)) return false;
+    if (rows && lane == 0) trace_emit(p.trace, tn, threadIdx.x >> 5, kTrWaitEnd, static_cast<uint32_t>(tile), aux);
+    return true;
+  } else {
+    return !(pos > 0 && wait && !wait_chunks(p, pos, row0, lane, abort));
+  }
+}
+
+// Lane 0: stream k-blocks [kbs, kbe) of an item into the ring from (stage,
+// phase) on; the pair's bytes are counted on the even CTA's full barrier.
+// false on timeout / abort.
+struct RingPos {
+  int stage;
+  uint32_t phase, issued, issued_phase;  // issued bit s: stage s used; its last parity
+};
+__device__ __forceinline__ bool issue_kblocks(const FusedParams& p, uint32_t rank, uint8_t* sA,
+                                              uint8_t* sB, uint64_t* full, uint64_t* empty,
+                                              const ItemSource& src, int64_t kbs, int64_t kbe,
+                                              RingPos& r, volatile int* abort) {
+  const int half = p.g.BN / 2;
+  const uint32_t pair_tx = static_cast<uint32_t>(2 * (kABytes + half * kBlockK * 2));
+  const uint32_t full0 = mapa_shared(smem_u32(full), 0);  // the even CTA's barriers
+  for (int64_t kb = kbs; kb < kbe; ++kb) {
+    if (!mbar_wait(&empty[r.stage], r.phase ^ 1u, p.pipe_timeout_ns, abort, p.status)) return false;
+    const uint32_t bar = full0 + r.stage * 8;
+    if (rank == 0) mbar_arrive_expect_tx(&full[r.stage], pair_tx);
+    const int32_t x = static_cast<int32_t>(kb * kBlockK);
+    uint8_t* a_dst = sA + r.stage * kABytes;
+    if (src.pos == 0)
+      tma_load_2d_pair(a_dst, &p.tm_a_local, bar, x, src.y);
+    else
+      tma_load_3d_pair(a_dst, &p.tm_a_stage, bar, x, src.y, src.z);
+    uint8_t* b_dst = sB + r.stage * kBBytes;
+    // One TMA instruction per operand and k-block where possible: the TMA
+    // unit's per-instruction cost, not bandwidth, limits the ring on GB300.
+    if (p.b3d)
+      tma_load_3d_pair(b_dst, &p.tm_b, bar, 0, x, src.xb / 64);
+    else
+      for (int i = 0; i < half / 64; ++i)
+        tma_load_2d_pair(b_dst + i * (64 * kBlockK * 2), &p.tm_b, bar, src.xb + i * 64, x);
+    r.issued |= 1u << r.stage;
+    r.issued_phase = (r.issued_phase & ~(1u << r.stage)) | (r.phase << r.stage);
+    if (++r.stage == kStages) {
+      r.stage = 0;
+      r.phase ^= 1u;
+    }
+  }
+  return true;
+}
+
 template <bool kI8, bool kTrace>
 __device__ void tma_warp(const FusedParams& p, uint32_t rank, uint8_t* sA, uint8_t* sB,
                          uint64_t* full, uint64_t* empty, const TileRing& ring, int lane,
@@ -334,10 +419,7 @@ __device__ void tma_warp(const FusedParams& p, uint32_t rank, uint8_t* sA, uint8
   const volatile uint32_t* gstatus = p.status;
   const bool wait = (p.flags & kFlagWait) != 0;
   const int half = g.BN / 2;                                   // B columns this CTA stages
-  const uint32_t pair_tx = static_cast<uint32_t>(2 * (kABytes + half * kBlockK * 2));
-  const uint32_t full0 = mapa_shared(smem_u32(full), 0);       // the even CTA's barriers
-  int stage = 0;
-  uint32_t phase = 0, issued = 0, issued_phase = 0;  // bit s: stage s used / parity of last use
+  RingPos r{0, 0u, 0u, 0u};
   if (lane == 0) {
     tma_prefetch_desc(&p.tm_a_local);
     tma_prefetch_desc(&p.tm_a_stage);
@@ -390,18 +472,7 @@ __device__ void tma_warp(const FusedParams& p, uint32_t rank, uint8_t* sA, uint8
     int64_t mt, nt;
     tile_coords(g, tile, pos, mt, nt);
     const int64_t row0 = mt * kPairM + rank * kBlockM;
-    if constexpr (kTrace) {
-      int64_t q0 = 0, q1 = -1;
-      const bool rows = pos > 0 && wait && rows_chunks(g, row0, q0, q1);
-      const uint64_t aux = (static_cast<uint64_t>(pos) << 48) |
-                           (static_cast<uint64_t>(q0 & 0xFFFFFF) << 24) |
-                           static_cast<uint64_t>(q1 & 0xFFFFFF);
-      if (rows && lane == 0) trace_emit(p.trace, tn, threadIdx.x >> 5, kTrWaitStart, static_cast<uint32_t>(tile), aux);
-      if (pos > 0 && wait && !wait_chunks(p, pos, row0, lane, abort)) break;
-      if (rows && lane == 0) trace_emit(p.trace, tn, threadIdx.x >> 5, kTrWaitEnd, static_cast<uint32_t>(tile), aux);
-    } else {
-      if (pos > 0 && wait && !wait_chunks(p, pos, row0, lane, abort)) break;
-    }
+    if (!wait_item_rows<kTrace>(p, pos, row0, tile, wait, lane, abort, tn)) break;
     unsigned long long ticket = 0;
     if (lane == 1 && draw) ticket = atomicAdd(p.tile_counter, 1ull);
     if (lane == 0) {
@@ -409,42 +480,8 @@ __device__ void tma_warp(const FusedParams& p, uint32_t rank, uint8_t* sA, uint8
         fence_acq_rel_gpu();
         fence_proxy_async_global();
       }
-      // A rows: the local shard at row0, or the staging: [S-1][R][K] at
-      // (row0, pos - 1), or the window's [W][256][K] at (this CTA's half, slot)
-      const bool win = pos > 0 && p.window > 0;
-      const int32_t y = win ? static_cast<int32_t>(rank * kBlockM) : static_cast<int32_t>(row0);
-      const int32_t z = win ? static_cast<int32_t>(static_cast<uint32_t>((pos - 1) * g.MT + mt) %
-                                                   static_cast<uint32_t>(p.window))
-                            : pos - 1;
-      const int32_t xb = static_cast<int32_t>(nt * g.BN + rank * half);
-      for (int64_t kb = kbs; kb < kbe; ++kb) {
-        if (!mbar_wait(&empty[stage], phase ^ 1u, p.pipe_timeout_ns, abort, gstatus)) {
-          ok = false;
-          break;
-        }
-        const uint32_t bar = full0 + stage * 8;
-        if (rank == 0) mbar_arrive_expect_tx(&full[stage], pair_tx);
-        const int32_t x = static_cast<int32_t>(kb * kBlockK);
-        uint8_t* a_dst = sA + stage * kABytes;
-        if (pos == 0)
-          tma_load_2d_pair(a_dst, &p.tm_a_local, bar, x, y);
-        else
-          tma_load_3d_pair(a_dst, &p.tm_a_stage, bar, x, y, z);
-        uint8_t* b_dst = sB + stage * kBBytes;
-        // One TMA instruction per operand and k-block where possible: the TMA
-        // unit's per-instruction cost, not bandwidth, limits the ring on GB300.
-        if (p.b3d)
-          tma_load_3d_pair(b_dst, &p.tm_b, bar, 0, x, xb / 64);
-        else
-          for (int i = 0; i < half / 64; ++i)
-            tma_load_2d_pair(b_dst + i * (64 * kBlockK * 2), &p.tm_b, bar, xb + i * 64, x);
-        issued |= 1u << stage;
-        issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
+      ok = issue_kblocks(p, rank, sA, sB, full, empty, item_source(p, rank, pos, mt, nt, row0, half),
+                         kbs, kbe, r, abort);
     }
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     if (lane == 1 && ok && draw) {
@@ -466,7 +503,7 @@ __device__ void tma_warp(const FusedParams& p, uint32_t rank, uint8_t* sA, uint8
       volatile int never = 0;
       const uint64_t limit = ok ? p.pipe_timeout_ns : 20000000ull;
       for (int s = 0; s < kStages; ++s)
-        if (issued & (1u << s)) mbar_wait(&full[s], (issued_phase >> s) & 1u, limit, &never);
+        if (r.issued & (1u << s)) mbar_wait(&full[s], (r.issued_phase >> s) & 1u, limit, &never);
     }
   }
   __syncwarp();
@@ -491,9 +528,6 @@ __device__ void tma_warp_dealt(const FusedParams& p, uint32_t rank, uint8_t* sA,
   const volatile uint32_t* gstatus = p.status;
   const bool wait = (p.flags & kFlagWait) != 0;
   const int half = g.BN / 2;
-  const uint32_t pair_tx = static_cast<uint32_t>(2 * (kABytes + half * kBlockK * 2));
-  const uint32_t full0 = mapa_shared(smem_u32(full), 0);
-  uint32_t issued = 0, issued_phase = 0;
   if (lane == 0) {
     tma_prefetch_desc(&p.tm_a_local);
     tma_prefetch_desc(&p.tm_a_stage);
@@ -503,6 +537,7 @@ __device__ void tma_warp_dealt(const FusedParams& p, uint32_t rank, uint8_t* sA,
   const uint64_t KB = static_cast<uint64_t>(g.KB);
   bool ok = true;
   uint32_t handoffs = 0;  // items of the other producer waited for
+  RingPos r{0, 0u, 0u, 0u};
   for (uint32_t seq = static_cast<uint32_t>(producer); ok && items.dealt(seq); seq += 2) {
     const int64_t t = items.dealt_item(seq);
     int64_t tile, kbs, kbe;
@@ -512,17 +547,9 @@ __device__ void tma_warp_dealt(const FusedParams& p, uint32_t rank, uint8_t* sA,
     int64_t mt, nt;
     tile_coords(g, tile, pos, mt, nt);
     const int64_t row0 = mt * kPairM + rank * kBlockM;
-    if constexpr (kTrace) {
-      int64_t q0 = 0, q1 = -1;
-      const bool rows = pos > 0 && wait && rows_chunks(g, row0, q0, q1);
-      const uint64_t aux = (static_cast<uint64_t>(pos) << 48) |
-                           (static_cast<uint64_t>(q0 & 0xFFFFFF) << 24) |
-                           static_cast<uint64_t>(q1 & 0xFFFFFF);
-      if (rows && lane == 0) trace_emit(p.trace, tn, threadIdx.x >> 5, kTrWaitStart, static_cast<uint32_t>(tile), aux);
-      if (pos > 0 && wait && !wait_chunks(p, pos, row0, lane, abort)) break;
-      if (rows && lane == 0) trace_emit(p.trace, tn, threadIdx.x >> 5, kTrWaitEnd, static_cast<uint32_t>(tile), aux);
-    } else {
-      if (pos > 0 && wait && !wait_chunks(p, pos, row0, lane, abort)) break;
+    if (!wait_item_rows<kTrace>(p, pos, row0, tile, wait, lane, abort, tn)) {
+      ok = false;
+      break;
     }
     if (lane == 0) {
       if (pos > 0) {
@@ -534,41 +561,13 @@ __device__ void tma_warp_dealt(const FusedParams& p, uint32_t rank, uint8_t* sA,
         ok = mbar_wait(&hand[producer ^ 1], handoffs & 1u, p.pipe_timeout_ns, abort, gstatus);
         ++handoffs;
       }
-      const bool win = pos > 0 && p.window > 0;
-      const int32_t y = win ? static_cast<int32_t>(rank * kBlockM) : static_cast<int32_t>(row0);
-      const int32_t z = win ? static_cast<int32_t>(static_cast<uint32_t>((pos - 1) * g.MT + mt) %
-                                                   static_cast<uint32_t>(p.window))
-                            : pos - 1;
-      const int32_t xb = static_cast<int32_t>(nt * g.BN + rank * half);
+      // item seq's k-blocks start at global ring block seq * KB
       const uint64_t g0 = static_cast<uint64_t>(seq) * KB;
-      int stage = static_cast<int>(g0 % kStages);
-      uint32_t phase = static_cast<uint32_t>((g0 / kStages) & 1u);
-      for (int64_t kb = kbs; kb < kbe && ok; ++kb) {
-        if (!mbar_wait(&empty[stage], phase ^ 1u, p.pipe_timeout_ns, abort, gstatus)) {
-          ok = false;
-          break;
-        }
-        const uint32_t bar = full0 + stage * 8;
-        if (rank == 0) mbar_arrive_expect_tx(&full[stage], pair_tx);
-        const int32_t x = static_cast<int32_t>(kb * kBlockK);
-        uint8_t* a_dst = sA + stage * kABytes;
-        if (pos == 0)
-          tma_load_2d_pair(a_dst, &p.tm_a_local, bar, x, y);
-        else
-          tma_load_3d_pair(a_dst, &p.tm_a_stage, bar, x, y, z);
-        uint8_t* b_dst = sB + stage * kBBytes;
-        if (p.b3d)
-          tma_load_3d_pair(b_dst, &p.tm_b, bar, 0, x, xb / 64);
-        else
-          for (int i = 0; i < half / 64; ++i)
-            tma_load_2d_pair(b_dst + i * (64 * kBlockK * 2), &p.tm_b, bar, xb + i * 64, x);
-        issued |= 1u << stage;
-        issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
+      r.stage = static_cast<int>(g0 % kStages);
+      r.phase = static_cast<uint32_t>((g0 / kStages) & 1u);
+      if (ok)
+        ok = issue_kblocks(p, rank, sA, sB, full, empty,
+                           item_source(p, rank, pos, mt, nt, row0, half), kbs, kbe, r, abort);
       if (ok) mbar_arrive(&hand[producer]);  // item seq is issued
     }
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -581,7 +580,7 @@ __device__ void tma_warp_dealt(const FusedParams& p, uint32_t rank, uint8_t* sA,
       // exits (bounded: a stage reused by the other producer may be a phase on).
       volatile int never = 0;
       for (int s = 0; s < kStages; ++s)
-        if (issued & (1u << s)) mbar_wait(&full[s], (issued_phase >> s) & 1u, 20000000ull, &never);
+        if (r.issued & (1u << s)) mbar_wait(&full[s], (r.issued_phase >> s) & 1u, 20000000ull, &never);
     }
   }
   __syncwarp();
