@@ -591,6 +591,26 @@ class Runner:
             raise RuntimeError(f"{self.w.name}: warm-up run failed: status "
                                f"{self.plan.status_word():#x}")
 
+    def read_floor(self, n, flush):
+        """Median device time (ms) of one library kernel that only reads B once
+        (a PyTorch int64 sum over its bytes), each after the same L2 flush: what
+        a single launch needs just to stream B from HBM, start-up included.  For
+        the skinny int8 path, which is bound by reading B, it is the practical
+        floor beside the copy-bandwidth roofline.  None if B is not contiguous."""
+        torch = self.torch
+        if not self.Bd.is_contiguous():
+            return None
+        flat = self.Bd.reshape(-1)
+        src = flat.view(torch.int64) if flat.numel() % 8 == 0 else flat
+        out = torch.empty((), dtype=torch.int64, device=self.dev)
+
+        def body():
+            torch.sum(src, dim=0, dtype=torch.int64, out=out)
+
+        body()
+        torch.cuda.synchronize(self.dev)
+        return float(np.median(timed_events(torch, self.stream, self.dev, n, body, flush)[0]))
+
     def check_status(self, what):
         if self.plan.status() != 0:
             raise RuntimeError(f"{self.w.name}: {what} failed: status {self.plan.status_word():#x}")
@@ -650,6 +670,16 @@ def roofline_of(w, path_id, kernel_ms, clk, peaks, peak_src):
     return r
 
 
+def add_read_floor(roof, w, floor_ms, run_ms):
+    """Record beside an HBM roofline the measured time of a bare read of B."""
+    if floor_ms is None:
+        return
+    roof["read_floor_ms"] = floor_ms
+    roof["read_floor_gbs"] = w.K * w.N / (floor_ms * 1e-3) * 1e-9
+    roof["frac_of_read_floor"] = floor_ms / run_ms
+    roof["read_floor_kernel"] = "torch.sum over B's bytes (one launch reading B once)"
+
+
 def measure_extra(torch, w, dev, args, flush_fn, peaks, peak_src):
     """A compact record of one more workload, timed like the headline one."""
     r = Runner(torch, w, dev, args)
@@ -661,9 +691,12 @@ def measure_extra(torch, w, dev, args, flush_fn, peaks, peak_src):
         r.check_status("timed runs")
         mean_ms, med_ms = float(np.mean(times)), float(np.median(times))
         unit = "TOP/s" if w.dtype == "i8" else "TFLOP/s"
+        roof = roofline_of(w, r.path, mean_ms, None, peaks, peak_src)
+        if r.path == B_.PATH_SKINNY_I8:
+            add_read_floor(roof, w, r.read_floor(steps, flush_fn), mean_ms)
         rec = {"workload": w.name, "value": w.flops / (mean_ms * 1e-3) * 1e-12, "unit": unit,
                "steps": steps, "ms_per_step": mean_ms, "ms_per_step_median": med_ms,
-               "roofline": roofline_of(w, r.path, mean_ms, None, peaks, peak_src),
+               "roofline": roof,
                "config": workload_config(w, flush_fn is not None), "enqueue": gate}
         if not args.no_modes:
             rec["modes"] = r.modes(max(3, min(steps, 10)), flush_fn, med_ms)
@@ -747,6 +780,8 @@ def run_ours(args, w, rank, world, local_rank):
     # kernel and the fused kernel (int8); the skinny and the finish kernel (skinny)
     launches_per_run = 1 if path_id == B_.PATH_FUSED_F16 else 2
     roofline = roofline_of(w, path_id, float(np.mean(times_ms)), clk, peaks, peak_src)
+    if path_id == B_.PATH_SKINNY_I8:
+        add_read_floor(roofline, w, r.read_floor(args.steps, flush_fn), float(np.mean(times_ms)))
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
