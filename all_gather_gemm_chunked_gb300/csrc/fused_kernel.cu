@@ -517,8 +517,9 @@ __device__ void tma_warp(const FusedParams& p, uint32_t rank, uint8_t* sA, uint8
 // item's first k-block only after the other has issued all of the previous
 // item (a hand-off barrier per producer), so every stage's uses stay in
 // order and each empty-barrier parity wait sees at most one pending use.
-// Item seq's k-blocks occupy the ring from global block seq * KB on (every
-// item is a whole tile).
+// Item seq's k-blocks occupy the ring from the global block that follows
+// every earlier item's: KB per whole tile, a tail part's K share after them
+// (the pair's whole tiles come first among its dealt items).
 template <bool kI8, bool kTrace>
 __device__ void tma_warp_dealt(const FusedParams& p, uint32_t rank, uint8_t* sA, uint8_t* sB,
                                uint64_t* full, uint64_t* empty, uint64_t* hand, int producer,
@@ -535,6 +536,12 @@ __device__ void tma_warp_dealt(const FusedParams& p, uint32_t rank, uint8_t* sA,
   }
   const PairItems items(p);
   const uint64_t KB = static_cast<uint64_t>(g.KB);
+  // this pair's whole tiles: items pair, pair + pairs, ... below full_tiles
+  // (32-bit: a plan has fewer than 2^30 tiles)
+  const uint32_t pairs32 = static_cast<uint32_t>(items.pairs);
+  const uint32_t pair32 = static_cast<uint32_t>(items.pair);
+  const uint32_t full32 = static_cast<uint32_t>(p.full_tiles);
+  const uint32_t n_whole = pair32 < full32 ? (full32 - pair32 + pairs32 - 1) / pairs32 : 0u;
   bool ok = true;
   uint32_t handoffs = 0;  // items of the other producer waited for
   RingPos r{0, 0u, 0u, 0u};
@@ -561,8 +568,14 @@ __device__ void tma_warp_dealt(const FusedParams& p, uint32_t rank, uint8_t* sA,
         ok = mbar_wait(&hand[producer ^ 1], handoffs & 1u, p.pipe_timeout_ns, abort, gstatus);
         ++handoffs;
       }
-      // item seq's k-blocks start at global ring block seq * KB
-      const uint64_t g0 = static_cast<uint64_t>(seq) * KB;
+      // item seq's k-blocks start at global ring block g0
+      uint64_t g0 = static_cast<uint64_t>(seq < n_whole ? seq : n_whole) * KB;
+      for (uint32_t j = n_whole; j < seq; ++j) {
+        int64_t tj, kj0, kj1;
+        int pj, nj;
+        work_item(g, p.full_tiles, p.split, items.dealt_item(j), tj, pj, nj, kj0, kj1);
+        g0 += static_cast<uint64_t>(kj1 - kj0);
+      }
       r.stage = static_cast<int>(g0 % kStages);
       r.phase = static_cast<uint32_t>((g0 / kStages) & 1u);
       if (ok)
@@ -738,6 +751,87 @@ __device__ __forceinline__ void signal_part(const FusedParams& p, int64_t tail, 
   if (lane == 0) red_release_gpu_add(p.part_flags + tail, 1u);
 }
 
+// fp16 split plan: zero the C blocks of the tail tiles, into which both
+// K-parts of each tile add with TMA reductions (two fp32 additions onto +0
+// give the same sum in either order).  A task is 32 rows of a tail tile over
+// all its columns, stored from this warp's staging box filled with zeros.
+// Tasks are drawn by ticket; this run's tickets start at zero_base (the
+// counter is first raised to it).  A warp draws one ticket, or -- before it
+// waits for the zeros itself -- every ticket left, so the resident CTAs zero
+// them all whichever CTAs run.  The warp counts the tasks it did once their
+// stores are performed.
+__device__ void zero_tail_tiles(const FusedParams& p, uint8_t* box, int lane, bool all) {
+  const Geometry& g = p.g;
+  uint4* row = reinterpret_cast<uint4*>(box + lane * 128);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) row[c] = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_shared();
+  __syncwarp();
+  constexpr uint32_t kGroups = kPairM / 32;  // 32-row groups of a pair tile
+  uint32_t done = 0;
+  if (lane == 0) atomicMax(p.zero_ticket, p.zero_base);
+  for (;;) {
+    unsigned long long ticket = 0;
+    if (lane == 0) ticket = atomicAdd(p.zero_ticket, 1ull) - p.zero_base;
+    ticket = __shfl_sync(0xffffffffu, ticket, 0);
+    if (ticket >= static_cast<unsigned long long>(p.zero_tasks)) break;
+    if (lane == 0) {
+      const uint32_t tk = static_cast<uint32_t>(ticket);
+      const int64_t tile = p.full_tiles + tk / kGroups;
+      int pos;
+      int64_t mt, nt;
+      tile_coords(g, tile, pos, mt, nt);
+      const int src = source_of(g, p.local, pos);
+      const int64_t r0 = mt * kPairM + (tk % kGroups) * 32;
+      if (r0 < g.R)
+        for (int b = 0; b < g.BN / 32; ++b) {
+          const int64_t n0 = nt * g.BN + b * 32;
+          if (n0 >= g.N) break;
+          tma_store_3d(&p.tm_c, box, static_cast<int32_t>(n0), static_cast<int32_t>(r0), src);
+        }
+      bulk_commit_group();
+    }
+    ++done;
+    if (!all) break;
+  }
+  if (lane == 0 && done > 0) {
+    bulk_wait_group_all();       // the zeros are written
+    fence_proxy_async_global();  // (async-proxy writes, ordered before the release)
+    red_release_gpu_add(p.zero_done, done);
+  }
+  __syncwarp();
+}
+
+// A split tile's first reduction waits (bounded) until this run's zero tasks
+// are all done; lane 0 then orders its TMA reductions after the zeros.
+__device__ bool wait_zeroed(const FusedParams& p, uint32_t rank, int lane, volatile int* abort) {
+  bool ok = true;
+  if (lane == 0) {
+    if (ld_acquire_gpu(p.zero_done) < p.zero_target) {
+      const uint64_t deadline = globaltimer_ns() + p.pipe_timeout_ns;
+      uint32_t spins = 0;
+      while (ld_acquire_gpu(p.zero_done) < p.zero_target) {
+        __nanosleep(128);
+        if (++spins == 16) {
+          spins = 0;
+          if (*abort || *reinterpret_cast<volatile uint32_t*>(p.status) != 0u ||
+              globaltimer_ns() > deadline) {
+            ok = false;
+            break;
+          }
+        }
+      }
+    }
+    if (ok) {
+      fence_proxy_async_global();
+    } else {
+      set_status(p.status, kStatusPipelineTimeout, 0x700u | rank);
+      *abort = 1;
+    }
+  }
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
 template <bool kI8, bool kTrace, bool kSplit>
 __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int half, int lane,
                               uint64_t* tfull, uint64_t* tempty, const TileRing& ring,
@@ -754,6 +848,19 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
   // (at most 4 chunks of 32), kept in registers across the tile's segments
   uint32_t sums[kI8 ? 128 : 1];
   uint32_t unit = 0;
+  // fp16 split plan: the warp draws zero tasks once -- one task after its
+  // last whole tile (while its pair computes a tail part, or as the pair
+  // finishes), or every task left before a first reduction that comes
+  // earlier -- so all pairs zero the tail tiles, about one task per warp,
+  // while the parts are computed, and no zeroing competes with the full
+  // rounds' loads (measured: zeroing after the first item slowed the next two
+  // rounds by ~2 us; only the pairs without a part, zeroing after their last
+  // item, took ~7 us); `zeroed`: this run's zero tasks seen done
+  bool drew = true, zeroed = true;
+  if constexpr (kSplit && !kI8) {
+    drew = p.zero_tasks <= 0;
+    zeroed = drew;
+  }
   const PairItems items(p);
   for (uint32_t seq = 0; !items.done(seq); ++seq) {
     int64_t t = -1;
@@ -782,14 +889,15 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
     int64_t tile, kbs, kbe;
     int part, parts;
     work_item(g, p.full_tiles, p.split, t, tile, part, parts, kbs, kbe);
-    const int64_t seg_len = kI8 ? kSegBlocks : kbe - kbs;
     // (no 64-bit division at the item boundary: kSegBlocks is a power of two)
     const int64_t nseg = kI8 ? (kbe - kbs + kSegBlocks - 1) / kSegBlocks : 1;
-    // a split tile: earlier parts store partial sums, the last part adds them
-    // (compiled only into the kernel a splitting plan launches: the split
-    // paths would raise the register count of every tile's epilogue)
-    const bool store_part = kSplit && parts > 1 && part < parts - 1;
-    const bool add_parts = kSplit && parts > 1 && part == parts - 1;
+    // a split tile (compiled only into the kernel a splitting plan launches:
+    // the split paths would raise the register count of every tile's
+    // epilogue): int8 -- earlier parts store partial sums, the last part adds
+    // them; fp16 -- every part adds its sums into the zeroed C block
+    const bool store_part = kI8 && kSplit && parts > 1 && part < parts - 1;
+    const bool add_parts = kI8 && kSplit && parts > 1 && part == parts - 1;
+    const bool reduce = !kI8 && kSplit && parts > 1;
     const int64_t tail = tile - p.full_tiles;
     // Partial sums of part j of this tail tile, laid out for this warp: 16-byte
     // vector c of every lane of the warp is contiguous (512 bytes), so each
@@ -846,55 +954,28 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
         // shared box -> one TMA store of 32 full 128-byte row segments.  Rows
         // past the shard and columns past N are clipped by the descriptor.
         const int64_t r0 = mt * kPairM + rank * kBlockM + quad * 32;
-        if (add_parts && !wait_parts(p, tail, rank, lane, abort)) {
-          if (lane == 0) bulk_wait_group_all();
-          return;
+        if (reduce && !drew) {
+          if (lane == 0) bulk_wait_group_read<0>();  // the box is no longer read
+          __syncwarp();
+          zero_tail_tiles(p, box, lane, true);
+          drew = true;
         }
-        if constexpr (kTrace)
-          if (add_parts && quad == 0 && half == 0 && lane == 0)
-            trace_emit(p.trace, tn, threadIdx.x >> 5, kTrPartsReady, static_cast<uint32_t>(tile), 0);
+        if (reduce && !zeroed) {
+          if (!wait_zeroed(p, rank, lane, abort)) {
+            if (lane == 0) bulk_wait_group_all();
+            return;
+          }
+          zeroed = true;
+          if constexpr (kTrace)
+            if (quad == 0 && half == 0 && lane == 0)
+              trace_emit(p.trace, tn, threadIdx.x >> 5, kTrPartsReady, static_cast<uint32_t>(tile), 0);
+        }
         for (int jj = 0; jj < nchunks; ++jj) {
           const int j = chunk0 + jj;
           uint32_t v[32];
           tmem_ld32(lane_base + buf * 256u + j * 32, v);
           tmem_ld_wait();
           if (jj == nchunks - 1) release();
-          if (store_part) {
-            // this part's fp32 sums of the thread's row, 32 columns
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-              *part_vec(part, jj * 8 + c) =
-                  make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-            continue;
-          }
-          if (add_parts) {
-            // (part 0 + part 1 + ...) + this part, in that order; 4 vectors
-            // of the partials in flight at a time
-#pragma unroll
-            for (int c0 = 0; c0 < 8; c0 += 4) {
-              uint4 x[4];
-#pragma unroll
-              for (int c = 0; c < 4; ++c) x[c] = __ldcg(part_vec(0, jj * 8 + c0 + c));
-              for (int pj = 1; pj < parts - 1; ++pj) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                  const uint4 y = __ldcg(part_vec(pj, jj * 8 + c0 + c));
-                  x[c].x = __float_as_uint(__fadd_rn(__uint_as_float(x[c].x), __uint_as_float(y.x)));
-                  x[c].y = __float_as_uint(__fadd_rn(__uint_as_float(x[c].y), __uint_as_float(y.y)));
-                  x[c].z = __float_as_uint(__fadd_rn(__uint_as_float(x[c].z), __uint_as_float(y.z)));
-                  x[c].w = __float_as_uint(__fadd_rn(__uint_as_float(x[c].w), __uint_as_float(y.w)));
-                }
-              }
-#pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                uint32_t* vv = v + 4 * (c0 + c);
-                vv[0] = __float_as_uint(__fadd_rn(__uint_as_float(x[c].x), __uint_as_float(vv[0])));
-                vv[1] = __float_as_uint(__fadd_rn(__uint_as_float(x[c].y), __uint_as_float(vv[1])));
-                vv[2] = __float_as_uint(__fadd_rn(__uint_as_float(x[c].z), __uint_as_float(vv[2])));
-                vv[3] = __float_as_uint(__fadd_rn(__uint_as_float(x[c].w), __uint_as_float(vv[3])));
-              }
-            }
-          }
           const int64_t n0 = nt * g.BN + j * 32;
           if (r0 >= g.R || n0 >= g.N) continue;  // warp-uniform: nothing of this box exists
           if (lane == 0) bulk_wait_group_read<0>();  // the previous store has read the box
@@ -910,11 +991,13 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
           fence_proxy_async_shared();
           __syncwarp();
           if (lane == 0) {
-            tma_store_3d(&p.tm_c, box, static_cast<int32_t>(n0), static_cast<int32_t>(r0), src);
+            if (reduce)
+              tma_reduce_add_3d(&p.tm_c, box, static_cast<int32_t>(n0), static_cast<int32_t>(r0), src);
+            else
+              tma_store_3d(&p.tm_c, box, static_cast<int32_t>(n0), static_cast<int32_t>(r0), src);
             bulk_commit_group();
           }
         }
-        if (store_part) signal_part(p, tail, lane);
       } else {
         const bool first = seg == 0, last = seg == nseg - 1;
         // fp32 partials (exact integers) -> int32, added to the running sums;
@@ -1013,6 +1096,19 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
       if (quad == 0 && half == 0 && lane == 0)
         trace_emit(p.trace, tn, threadIdx.x >> 5, kTrTileDone, static_cast<uint32_t>(tile),
                    static_cast<uint64_t>(part) | (static_cast<uint64_t>(parts) << 8));
+    // (every item of an fp16 split plan is dealt: the next is a tail part, or
+    // there is none, once its index reaches full_tiles)
+    if (!drew && items.dealt_item(seq + 1) >= p.full_tiles) {
+      if (lane == 0) bulk_wait_group_read<0>();  // the box is no longer read
+      __syncwarp();
+      zero_tail_tiles(p, box, lane, false);
+      drew = true;
+    }
+  }
+  if (!drew) {
+    if (lane == 0) bulk_wait_group_read<0>();  // the box is no longer read
+    __syncwarp();
+    zero_tail_tiles(p, box, lane, false);
   }
   if (lane == 0) bulk_wait_group_all();  // every C store performed before the CTA exits
   __syncwarp();

@@ -39,10 +39,12 @@ struct FusedParams {
   unsigned long long* tile_counter;  // work items handed out so far (monotonic)
   unsigned long long tile_base;      // tile_counter value at the start of this run
   // Work items: tiles [0, full_tiles) whole, the others in `split` K-parts.
-  // Every part but the last stores its partial sums (fp32, or int32 on the
-  // int8 path) to `partials` and counts its 16 epilogue warps on the tile's
-  // flag; the last part waits for the flag to reach part_target, adds the
-  // partials in part order and writes the outputs.
+  // int8: every part but the last stores its partial sums (int32) to
+  // `partials` and counts its 16 epilogue warps on the tile's flag; the last
+  // part waits for the flag to reach part_target, adds the partials in part
+  // order and writes the outputs.  fp16 / bf16 (two parts): both parts add
+  // their fp32 sums into C with TMA reductions, into tiles that the epilogue
+  // warps zeroed at the start of the run (zero tasks, drawn by ticket).
   int64_t full_tiles;
   int64_t work_items;
   int64_t static_items;      // items below this are dealt round-robin: pair k takes k, k + pairs, ...
@@ -50,6 +52,11 @@ struct FusedParams {
   void* partials;            // [tail tiles][split - 1][2 CTAs][128 rows][BN] 4-byte sums
   uint32_t* part_flags;      // [tail tiles], monotonic
   uint32_t part_target;      // flag value once every earlier part of this run has stored
+  int64_t zero_tasks;        // fp16 split: 32-row groups of the tail tiles to zero (0: none)
+  unsigned long long* zero_ticket;  // zero tasks handed out so far (monotonic)
+  unsigned long long zero_base;     // this run's first ticket (the counter is raised to it)
+  uint32_t* zero_done;       // zero tasks completed, monotonic
+  uint32_t zero_target;      // zero_done once this run's tasks are all done
   uint32_t* status;             // [2]: status word, detail
   float* C;                     // f16 path output, M x N fp32
   int32_t* C_i32;               // i8 path outputs

@@ -330,6 +330,12 @@ struct ag_gemm_plan {
   int64_t partials_bytes = 0;
   uint32_t* part_flags = nullptr;
   uint32_t part_epoch = 0;       // runs of the GEMM since the last reset
+  // fp16 / bf16 split: both parts add into C blocks zeroed at the start of a run
+  int64_t zero_tasks = 0;        // 32-row groups of the tail tiles
+  unsigned long long* zero_ticket = nullptr;  // zero tasks handed out (monotonic)
+  unsigned long long zero_base = 0;
+  uint32_t* zero_done = nullptr;  // zero tasks done (monotonic)
+  uint32_t zero_epoch = 0;       // runs of the GEMM since the last reset
   // event trace (ag_gemm_plan_set_trace): [0] count, then the events
   unsigned long long* trace_buf = nullptr;
   int64_t trace_cap = 0;
@@ -357,6 +363,8 @@ void free_plan(ag_gemm_plan* p) {
   cudaFree(p->trace_buf);
   cudaFree(p->partials);
   cudaFree(p->part_flags);
+  cudaFree(p->zero_ticket);
+  cudaFree(p->zero_done);
   if (p->done) cudaEventDestroy(p->done);
   delete p;
 }
@@ -385,7 +393,7 @@ int launch_fused(ag_gemm_plan* p, agg::FusedParams& fp, int flags, cudaStream_t 
   fp.split = p->split;
   fp.partials = p->partials;
   fp.part_flags = p->part_flags;
-  if ((flags & agg::kFlagGemm) && p->split > 1) {
+  if ((flags & agg::kFlagGemm) && p->split > 1 && p->part_flags) {
     // every earlier part's 16 epilogue warps count once on the tile's flag per
     // run: restart the flags before they would overflow
     const uint64_t per_run = static_cast<uint64_t>(p->split - 1) * 2 * agg::kEpiWarps;
@@ -398,13 +406,32 @@ int launch_fused(ag_gemm_plan* p, agg::FusedParams& fp, int flags, cudaStream_t 
     ++p->part_epoch;
     fp.part_target = static_cast<uint32_t>(p->part_epoch * per_run);
   }
+  fp.zero_tasks = (flags & agg::kFlagGemm) ? p->zero_tasks : 0;
+  fp.zero_ticket = p->zero_ticket;
+  fp.zero_base = p->zero_base;
+  fp.zero_done = p->zero_done;
+  fp.zero_target = 0;
+  if (fp.zero_tasks > 0) {
+    // restart the count of zero tasks done before it would overflow
+    if ((static_cast<uint64_t>(p->zero_epoch) + 1) * static_cast<uint64_t>(p->zero_tasks) >=
+        (1ull << 31)) {
+      cudaError_t e = cudaMemsetAsync(p->zero_done, 0, sizeof(uint32_t), stream);
+      if (e != cudaSuccess) return cuda_fail(e, "zero-task count reset");
+      p->zero_epoch = 0;
+    }
+    ++p->zero_epoch;
+    fp.zero_target = static_cast<uint32_t>(p->zero_epoch * p->zero_tasks);
+  }
   const int grid = p->grid_override > 0 ? p->grid_override : p->grid;
-  // Whole tiles are dealt round-robin (they wait on no other pair).  With a
-  // staging window the remote tiles' credits tie them together, so only the
-  // local shard's tiles (consumption position 0: the first MT x NT in schedule
-  // order, which neither wait for rows nor add credits) are dealt and every
-  // remote tile is drawn.
-  const int64_t stat = p->window > 0 ? p->g.MT * p->g.NT : p->full_tiles;
+  // Whole tiles are dealt round-robin (they wait on no other pair), and so
+  // are the fp16 / bf16 split parts, which add into zeroed C blocks and wait
+  // on no other part.  With a staging window the remote tiles' credits tie
+  // them together, so only the local shard's tiles (consumption position 0:
+  // the first MT x NT in schedule order, which neither wait for rows nor add
+  // credits) are dealt and every remote tile is drawn; int8 split parts are
+  // drawn, the last part of a tile after all the others it adds.
+  const int64_t stat = p->window > 0 ? p->g.MT * p->g.NT
+                                     : (p->zero_tasks > 0 ? p->work_items : p->full_tiles);
   fp.static_items = stat;
   cudaError_t e = agg::launch_fused(fp, grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "fused kernel launch");
@@ -417,6 +444,11 @@ int launch_fused(ag_gemm_plan* p, agg::FusedParams& fp, int flags, cudaStream_t 
   if ((flags & agg::kFlagGemm) && p->work_items > stat)
     p->tile_base += static_cast<unsigned long long>(p->work_items - stat) +
                     static_cast<unsigned long long>(grid / 2);
+  // A run draws each zero task's ticket once, plus at most one failing ticket
+  // per epilogue warp; the next run's tickets start past all of them.
+  if (fp.zero_tasks > 0)
+    p->zero_base += static_cast<unsigned long long>(p->zero_tasks) +
+                    static_cast<unsigned long long>(grid) * agg::kEpiWarps;
   return AG_GEMM_OK;
 }
 
@@ -790,7 +822,11 @@ ag_gemm_plan* create_plan(int n_shards, int64_t M, int64_t K, int64_t N, int dty
   const int64_t tail = p->split > 1 ? g.tiles % (p->grid / 2) : 0;
   p->full_tiles = g.tiles - tail;
   p->work_items = p->full_tiles + tail * p->split;
-  p->partials_bytes = tail * (p->split - 1) * 2 * agg::kBlockM * g.BN * 4;
+  const bool i8 = g.dtype == AG_GEMM_I8;
+  // int8 parts hand partial sums to the last part; fp16 / bf16 parts add
+  // into C blocks zeroed by 32-row tasks
+  p->partials_bytes = i8 ? tail * (p->split - 1) * 2 * agg::kBlockM * g.BN * 4 : 0;
+  p->zero_tasks = i8 ? 0 : tail * (agg::kPairM / 32);
   p->staging_bytes = p->window > 0 ? static_cast<int64_t>(p->window) * agg::kPairM * g.K * 2
                                    : slots * g.R * g.K * 2;
   p->skinny = skinny;
@@ -814,10 +850,15 @@ ag_gemm_plan* create_plan(int n_shards, int64_t M, int64_t K, int64_t N, int dty
       (p->window > 0 &&
        ((e = cudaMalloc(&p->credits, sizeof(uint32_t) * p->window)) != cudaSuccess ||
         (e = cudaMemset(p->credits, 0, sizeof(uint32_t) * p->window)) != cudaSuccess)) ||
-      (tail > 0 &&
+      (p->partials_bytes > 0 &&
        ((e = cudaMalloc(&p->partials, static_cast<size_t>(p->partials_bytes))) != cudaSuccess ||
         (e = cudaMalloc(&p->part_flags, sizeof(uint32_t) * tail)) != cudaSuccess ||
-        (e = cudaMemset(p->part_flags, 0, sizeof(uint32_t) * tail)) != cudaSuccess))) {
+        (e = cudaMemset(p->part_flags, 0, sizeof(uint32_t) * tail)) != cudaSuccess)) ||
+      (p->zero_tasks > 0 &&
+       ((e = cudaMalloc(&p->zero_ticket, sizeof(unsigned long long))) != cudaSuccess ||
+        (e = cudaMemset(p->zero_ticket, 0, sizeof(unsigned long long))) != cudaSuccess ||
+        (e = cudaMalloc(&p->zero_done, sizeof(uint32_t))) != cudaSuccess ||
+        (e = cudaMemset(p->zero_done, 0, sizeof(uint32_t))) != cudaSuccess))) {
     cuda_fail(e, "plan allocation");
     free_plan(p);
     return nullptr;
@@ -1005,10 +1046,15 @@ int ag_gemm_plan_reset(ag_gemm_plan* plan, void* stream_v) {
       (plan->part_flags &&
        (e = cudaMemsetAsync(plan->part_flags, 0,
                             sizeof(uint32_t) * (plan->g.tiles - plan->full_tiles), stream)) != cudaSuccess) ||
+      (plan->zero_ticket &&
+       ((e = cudaMemsetAsync(plan->zero_ticket, 0, sizeof(unsigned long long), stream)) != cudaSuccess ||
+        (e = cudaMemsetAsync(plan->zero_done, 0, sizeof(uint32_t), stream)) != cudaSuccess)) ||
       (e = cudaEventRecord(plan->done, stream)) != cudaSuccess)
     return cuda_fail(e, "plan reset");
   plan->credit_epoch = 0;
   plan->part_epoch = 0;
+  plan->zero_epoch = 0;
+  plan->zero_base = 0;
   plan->epoch = 0;
   plan->item_base = 0;
   plan->tile_base = 0;
@@ -1246,6 +1292,11 @@ extern "C" int ag_gemm_run_noalloc(int n_shards, int64_t M, int64_t K, int64_t N
   fp.work_items = g.tiles;
   fp.split = 1;
   fp.static_items = g.tiles;  // every tile dealt round-robin
+  fp.zero_tasks = 0;
+  fp.zero_ticket = nullptr;
+  fp.zero_base = 0;
+  fp.zero_done = nullptr;
+  fp.zero_target = 0;
   fp.status = status;
   fp.C = C;
   fp.local = 0;

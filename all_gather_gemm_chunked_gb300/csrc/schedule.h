@@ -143,14 +143,18 @@ AGG_HD void work_item(const Geometry& g, int64_t full, int split, int64_t i, int
 
 // Parts per tail tile for `pairs` CTA pairs: tiles % pairs tiles are left for
 // the last round.  When they fill at most half of the pairs, each is split in
-// two along K, which halves that round -- worth it when a tile is long: the
-// partial sums' store and addition cost a few microseconds whatever K, a half
-// tile of 64 k-blocks only ~10 us (measured on 4096^3 fp16: no gain), so
-// only tiles of at least 128 k-blocks (K >= 8192) are split.
+// two along K, which halves that round -- worth it when a tile is long enough
+// for the parts' extra work.  int8 parts hand partial sums to the last part
+// (a store, a wait and an addition: a few microseconds whatever K; a half
+// tile of 64 k-blocks saves only ~10 us), so only tiles of at least 128
+// k-blocks (K >= 8192) are split.  fp16 / bf16 parts add into C blocks
+// zeroed at the start of the run, with TMA reductions that cost what the
+// plain store costs, so tiles of at least 32 k-blocks (K >= 2048) are.
 inline int choose_split(const Geometry& g, int64_t pairs) {
   if (pairs < 2) return 1;
   const int64_t tail = g.tiles % pairs;
-  if (tail == 0 || 2 * tail > pairs || g.KB < 128) return 1;
+  const int64_t min_kb = g.dtype == 1 ? 128 : 32;  // int8 : fp16 / bf16
+  if (tail == 0 || 2 * tail > pairs || g.KB < min_kb) return 1;
   return 2;
 }
 

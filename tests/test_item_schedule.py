@@ -1,26 +1,33 @@
 """Work items of the fused kernel, host side, without a GPU.
 
 A pair's items are the whole tiles dealt to it round-robin (items k, k + P,
-... below the dealt count), then items drawn from a grid-wide ticket counter
-in schedule order -- the split parts of the last round's tiles, whose last
-part waits for the earlier parts' partial sums.  The even CTA keeps up to two
-drawn items reserved ahead of the one it works on.  This simulation checks
-that every item completes when only some of the launched pairs are resident
-(the others start as resident pairs exit), for the split counts the plan
-chooses, and that the item decode visits every (tile, part) exactly once.
+... below the dealt count), then, on the int8 path, items drawn from a
+grid-wide ticket counter in schedule order -- the split parts of the last
+round's tiles, whose last part waits for the earlier parts' partial sums.
+The even CTA keeps up to two drawn items reserved ahead of the one it works
+on.  This simulation checks that every item completes when only some of the
+launched pairs are resident (the others start as resident pairs exit), for
+the split counts the plan chooses, and that the item decode visits every
+(tile, part) exactly once.  On the fp16 / bf16 path every item, split parts
+included, is dealt (the parts add into zeroed C blocks and wait on no other
+part): the two TMA producers of a pair then place item seq's k-blocks in the
+shared ring after all earlier items' k-blocks, which is checked against a
+plain running sum, and the zero tasks cover every tail tile's rows once.
 """
 import pytest
 
 
-def split_of(tiles, pairs, kb):
+def split_of(tiles, pairs, kb, i8=True):
     """The plan's rule: split the last round's tiles in two when they fill at
-    most half of the pairs and a tile has at least 128 k-blocks."""
+    most half of the pairs and a tile has at least 128 k-blocks (int8) or 32
+    (fp16 / bf16)."""
     tail = tiles % pairs
-    return 2 if pairs >= 2 and tail and 2 * tail <= pairs and kb >= 128 else 1
+    min_kb = 128 if i8 else 32
+    return 2 if pairs >= 2 and tail and 2 * tail <= pairs and kb >= min_kb else 1
 
 
-def items_of(tiles, pairs, kb):
-    s = split_of(tiles, pairs, kb)
+def items_of(tiles, pairs, kb, i8=True):
+    s = split_of(tiles, pairs, kb, i8)
     tail = tiles % pairs if s > 1 else 0
     full = tiles - tail
     work = full + tail * s
@@ -32,6 +39,11 @@ def items_of(tiles, pairs, kb):
         part = r // tail
         return full + r - part * tail, part, s
     return full, work, decode
+
+
+def part_blocks(kb, part, parts):
+    """k-blocks [kb0, kb1) of part `part` of `parts` (the kernel's split)."""
+    return kb * part // parts, kb * (part + 1) // parts
 
 
 def simulate(tiles, pairs, kb, resident, ahead=2):
@@ -119,5 +131,54 @@ def test_split_rule():
     assert split_of(256, 76, 128) == 2       # 28 tiles left for 76 pairs
     assert split_of(1024, 76, 428) == 2      # 36 left (the int8 workload of 4 x 4096 rows)
     assert split_of(512, 76, 128) == 1       # 56 left: more than half of the pairs
-    assert split_of(256, 76, 64) == 1        # short tiles: the split would not pay
+    assert split_of(256, 76, 64) == 1        # int8, short tiles: the hand-off would not pay
     assert split_of(228, 76, 128) == 1       # no partial round
+    assert split_of(256, 76, 64, i8=False) == 2    # fp16 4096^3: parts add into C
+    assert split_of(256, 76, 32, i8=False) == 2
+    assert split_of(256, 76, 31, i8=False) == 1    # too short even so
+    assert split_of(512, 76, 64, i8=False) == 1
+
+
+def dealt_ring_block(seq, pair, pairs, full, split, kb, tiles):
+    """The kernel's placement of a pair's dealt item seq in the k-block ring:
+    KB per whole tile before it (the pair's whole tiles come first), then the
+    k-blocks of the tail parts between its whole tiles and it."""
+    n_whole = (full - pair + pairs - 1) // pairs if pair < full else 0
+    g0 = min(seq, n_whole) * kb
+    tail = tiles - full
+    for j in range(n_whole, seq):
+        i = pair + j * pairs
+        part = (i - full) // tail
+        b0, b1 = part_blocks(kb, part, split)
+        g0 += b1 - b0
+    return g0
+
+
+@pytest.mark.parametrize("tiles,pairs,kb", [(256, 76, 64), (24, 76, 33), (8, 4, 40), (300, 76, 37),
+                                            (7, 6, 64), (100, 76, 128)])
+def test_dealt_ring_positions_follow_every_earlier_item(tiles, pairs, kb):
+    full, work, decode = items_of(tiles, pairs, kb, i8=False)
+    split = split_of(tiles, pairs, kb, i8=False)
+    for pair in range(pairs):
+        items = list(range(pair, work, pairs))   # every item dealt round-robin
+        running = 0
+        for seq, i in enumerate(items):
+            assert dealt_ring_block(seq, pair, pairs, full, split, kb, tiles) == running
+            t, part, parts = decode(i)
+            b0, b1 = part_blocks(kb, part, parts)
+            assert 0 <= b0 < b1 <= kb
+            running += b1 - b0
+
+
+@pytest.mark.parametrize("tiles,pairs", [(256, 76), (24, 76), (7, 6)])
+def test_zero_tasks_cover_every_tail_tile_once(tiles, pairs):
+    kb = 64
+    full, work, decode = items_of(tiles, pairs, kb, i8=False)
+    tail = tiles - full
+    assert tail > 0
+    tasks = tail * (256 // 32)                   # 32-row groups of a pair tile
+    covered = [(full + tk // 8, (tk % 8) * 32) for tk in range(tasks)]
+    assert len(set(covered)) == tasks
+    assert {t for t, _ in covered} == set(range(full, tiles))
+    # the parts that add into them are exactly the tail tiles' parts
+    assert {decode(i)[0] for i in range(full, work)} == set(range(full, tiles))

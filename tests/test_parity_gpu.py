@@ -588,13 +588,17 @@ def test_nshard_pitch_checks():
 
 
 # ---------------------------------------------------------------------------
-# the last round's tiles split along K over otherwise idle CTA pairs: earlier
-# parts store partial sums, the last part adds them in part order
+# the last round's tiles split along K over otherwise idle CTA pairs: int8
+# parts store partial sums and the last part adds them in part order; fp16 /
+# bf16 parts both add into C blocks zeroed at the start of the run
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("dt,S,R,K,N", [
     ("f16", 2, 384, 8192, 512),    # 8 tiles, 2 parts of 64 k-blocks each
     ("bf16", 3, 300, 8192, 264),   # 12 tiles (ragged rows and columns), 2 parts each
+    ("f16", 2, 384, 2048, 512),    # 8 tiles, 2 parts of 16 k-blocks
+    ("f16", 3, 200, 2112, 264),    # 6 tiles of 200 rows, 2 parts of 16 and 17 k-blocks
+    ("bf16", 2, 640, 4096, 520),   # 18 tiles (ragged last m-tile and n-tile), 2 parts of 32
     ("i8", 2, 384, 8256, 512),     # 4 tiles, 2 parts of 64 and 65 k-blocks (int32 partials)
 ])
 def test_split_tail_parity_modes_and_repeats(oracle, dt, S, R, K, N):
@@ -610,7 +614,8 @@ def test_split_tail_parity_modes_and_repeats(oracle, dt, S, R, K, N):
         else:
             ref = (oracle.ag_gemm_f16 if dt == "f16" else oracle.ag_gemm_bf16)(x["shards"], x["B"])
             check_f16(first, ref, K, f"split tail {dt}")
-        # the part flags are monotonic across runs and modes; a reset restarts them
+        # the part flags and zero-task counters are monotonic across runs and
+        # modes; a reset restarts them
         for mode in (B_.MODE_PIPELINED, B_.MODE_COMPUTE_ONLY, B_.MODE_SEQUENTIAL,
                      B_.MODE_PIPELINED):
             again = run(x, S, R, K, N, plan=plan, mode=mode)
@@ -624,14 +629,19 @@ def test_split_tail_parity_modes_and_repeats(oracle, dt, S, R, K, N):
 
 def test_split_tail_plan_geometry():
     """The split is chosen for the device's full grid: when the last round's
-    tiles fill at most half of the CTA pairs and a tile has at least 128
-    k-blocks, each is split in two along K."""
+    tiles fill at most half of the CTA pairs and a tile has at least 32
+    k-blocks (fp16 / bf16) or 128 (int8), each is split in two along K."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     pairs = sms // 2
     with Plan(2, 4096, 8192, 4096, "f16") as p:      # 256 pair tiles, 128 k-blocks
         g = p.geometry
         assert g["split_tiles"] == 256 % pairs and g["split_parts"] == 2
-    with Plan(2, 4096, 4096, 4096, "f16") as p:      # 64 k-blocks: the split would not pay
+    with Plan(2, 4096, 4096, 4096, "f16") as p:      # 64 k-blocks: fp16 parts add into C
+        g = p.geometry
+        assert g["split_tiles"] == 256 % pairs and g["split_parts"] == 2
+    with Plan(2, 4096, 4096, 4096, "i8") as p:       # int8 at 64 k-blocks: the hand-off would not pay
+        assert p.geometry["split_parts"] == 1
+    with Plan(2, 4096, 1024, 4096, "f16") as p:      # 16 k-blocks: too short
         assert p.geometry["split_parts"] == 1
     with Plan(8, 8192, 4096, 4096, "f16") as p:      # 512 tiles: the last round is too full
         assert p.geometry["split_parts"] == 1

@@ -144,7 +144,8 @@ GRID_CASES = [
     ("f16", 4, 600, 256, 384, 8),
     ("i8", 5, 520, 1056, 208, 9),
     ("f16", 3, 1000, 512, 520, None),
-    ("f16", 2, 1536, 8192, 512, None),    # 24 tiles split in two along K (fp32 partial sums)
+    ("f16", 2, 1536, 8192, 512, None),    # 24 tiles split in two along K (both parts add into C)
+    ("bf16", 2, 1536, 2048, 520, None),   # 24 tiles of 32 k-blocks split in two
     ("i8", 3, 512, 8192, 768, None),      # 18 tiles split in two (int32 partial sums)
 ]
 
