@@ -954,7 +954,8 @@ int ag_gemm_plan_geometry(const ag_gemm_plan* plan, ag_gemm_geometry* out) {
   if (!plan->skinny) {
     out->split_tiles = plan->g.tiles - plan->full_tiles;
     out->split_parts = plan->split;
-    out->workspace_bytes += plan->partials_bytes + 4 * out->split_tiles;
+    out->workspace_bytes += plan->partials_bytes + (plan->part_flags ? 4 * out->split_tiles : 0) +
+                            (plan->zero_ticket ? 12 : 0);
   }
   if (plan->window > 0) {
     out->workspace_bytes += plan->staging_bytes - out->staging_bytes + 4 * plan->window;

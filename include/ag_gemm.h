@@ -338,8 +338,10 @@ int ag_gemm_plan_set_debug(ag_gemm_plan *plan, int flags, int64_t arg);
  *                         (id = tile, aux = part | parts << 8; parts = 1 for a whole tile)
  *   ACC_READY             fused: the accumulator of a work item's last segment is ready
  *                         for the epilogue (id, aux as for TILE_DONE)
- *   PARTS_READY           fused: the last part of a split tile saw every earlier part's
- *                         partial sums stored (id = tile)
+ *   PARTS_READY           fused, split tile: int8 -- its last part saw every earlier
+ *                         part's partial sums stored; fp16 / bf16 -- a part saw the run's
+ *                         zeroing of the tail tiles done, before its first reduction into
+ *                         C (id = tile)
  *   UNIT_ISSUED           skinny: a unit's loads issued (id = unit)
  *   UNIT_LANDED           skinny: a unit's operands in shared memory (id = unit)
  *   KB_WIDENED            skinny: a k-block of B widened to fp16 (id = k-block of the n-tile, aux = unit)
