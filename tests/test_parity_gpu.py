@@ -525,6 +525,8 @@ def _nshard_inputs(dt, D, R, K, ns, seed):
     ("f16", 2, 256, 512, 256),
     ("f16", 4, 96, 320, 72),     # n_shard not a multiple of 64: the 2-D B map
     ("bf16", 3, 130, 256, 136),  # ragged rows per shard
+    ("f16", 2, 256, 2048, 256),  # 2 tiles per rank, split in two along K: zeroed and reduced
+                                 # C blocks inside a wider C (row pitch 2 x 256)
 ])
 def test_nshard_ranks_assemble_the_product(oracle, dt, D, R, K, ns):
     x, shards, Bfull = _nshard_inputs(dt, D, R, K, ns, 5000 + D * 7 + K)
