@@ -191,17 +191,18 @@ __device__ void copy_warp(const FusedParams& p, int lane, unsigned long long fir
 }
 
 // ------------------------------------------------------------------ work items
-// A pair's items: first the whole tiles dealt round-robin -- pair k takes
-// items k, k + pairs, ... below static_items -- then items handed out at run
-// time.  The dealt items wait on no other pair (plain staging, or the local
-// shard's tiles of a plan with a staging window), so they need no
-// coordination; the rest -- the split parts of the last round's tiles, and
-// the remote tiles when a staging window's credits tie tiles to one another
-// -- are drawn from a grid-wide ticket counter in schedule order.  Whichever pairs
-// are resident therefore always take the lowest items left: no item waits on
-// a pair that has not started (the window's credits and a split tile's
-// partial sums come only from items drawn earlier), even when fewer pairs are
-// resident than were launched.
+// A pair's items: first the items dealt round-robin -- pair k takes items
+// k, k + pairs, ... below static_items -- then items handed out at run time.
+// The dealt items wait on no other pair (whole tiles of plain staging, the
+// local shard's tiles of a plan with a staging window, and the fp16 / bf16
+// split parts, which add into C blocks that ticketed tasks zero), so they
+// need no coordination; the rest -- the int8 split parts of the last round's
+// tiles, and the remote tiles when a staging window's credits tie tiles to
+// one another -- are drawn from a grid-wide ticket counter in schedule
+// order.  Whichever pairs are resident therefore always take the lowest items
+// left: no item waits on a pair that has not started (the window's credits
+// and an int8 split tile's partial sums come only from items drawn earlier),
+// even when fewer pairs are resident than were launched.
 //
 // The even CTA's TMA warp (lane 1) draws the tickets and publishes the drawn
 // items, two ahead of use, in a kTq-deep ring in the shared memory of both
@@ -713,9 +714,9 @@ __device__ __forceinline__ void st_v4(void* ptr, uint32_t a, uint32_t b, uint32_
                : "memory");
 }
 
-// A split tile's last part: lane 0 waits (bounded) until every warp of the
-// earlier parts has stored its partial sums; then every lane acquires the flag,
-// which orders its reads of the partials after those stores.
+// An int8 split tile's last part: lane 0 waits (bounded) until every warp of
+// the earlier parts has stored its partial sums; then every lane acquires the
+// flag, which orders its reads of the partials after those stores.
 __device__ bool wait_parts(const FusedParams& p, int64_t tail, uint32_t rank, int lane,
                            volatile int* abort) {
   const uint32_t* flag = p.part_flags + tail;

@@ -116,8 +116,9 @@ AGG_HD void tile_coords(const Geometry& g, int64_t t, int& pos, int64_t& mt,
 // Work items of the fused kernel: the first `full` tiles whole, then the
 // remaining (tail) tiles in `split` parts along K -- the tiles that would
 // leave most CTA pairs idle in the last round.  Tail items go part-major (the
-// first part of every tail tile, then the second ...), so the last part of a
-// tile, which adds the others' partial sums, is handed out after all of them.
+// first part of every tail tile, then the second ...), so on the int8 path,
+// where they are drawn, the last part of a tile, which adds the others'
+// partial sums, is handed out after all of them.
 // Item i -> tile t, part j of `parts`, and the part's k-blocks [kb0, kb1).
 AGG_HD void work_item(const Geometry& g, int64_t full, int split, int64_t i, int64_t& t,
                       int& part, int& parts, int64_t& kb0, int64_t& kb1) {

@@ -41,7 +41,8 @@ enum : uint32_t {
   kTrPieceDone = 11, // skinny: a piece's int32 sums stored to its workspace slot
   kTrCopyStart = 12, // a copy warp starts a copy item / task (before its loads)
   kTrAccReady = 13,  // fused: the accumulator of a work item's last segment is ready
-  kTrPartsReady = 14,// fused: a split tile's last part saw every earlier part stored
+  kTrPartsReady = 14,// fused split tile: int8, its last part saw every earlier part stored;
+                     // fp16 / bf16, a part saw the run's zeroing done
 };
 
 // The buffer is cut into one region per (CTA, warp slot): 32 slots per CTA,
