@@ -758,8 +758,9 @@ __device__ __forceinline__ void signal_part(const FusedParams& p, int64_t tail, 
 // all its columns, stored from this warp's staging box filled with zeros.
 // Tasks are drawn by ticket; this run's tickets start at zero_base (the
 // counter is first raised to it).  A warp draws one ticket, or -- before it
-// waits for the zeros itself -- every ticket left, so the resident CTAs zero
-// them all whichever CTAs run.  The warp counts the tasks it did once their
+// waits for the zeros itself -- every ticket left (it draws at most twice a
+// run, so at most two of its tickets fail), so the resident CTAs zero them
+// all whichever CTAs run.  The warp counts the tasks it did once their
 // stores are performed.
 __device__ void zero_tail_tiles(const FusedParams& p, uint8_t* box, int lane, bool all) {
   const Geometry& g = p.g;
@@ -849,14 +850,16 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
   // (at most 4 chunks of 32), kept in registers across the tile's segments
   uint32_t sums[kI8 ? 128 : 1];
   uint32_t unit = 0;
-  // fp16 split plan: the warp draws zero tasks once -- one task after its
-  // last whole tile (while its pair computes a tail part, or as the pair
-  // finishes), or every task left before a first reduction that comes
-  // earlier -- so all pairs zero the tail tiles, about one task per warp,
-  // while the parts are computed, and no zeroing competes with the full
-  // rounds' loads (measured: zeroing after the first item slowed the next two
-  // rounds by ~2 us; only the pairs without a part, zeroing after their last
-  // item, took ~7 us); `zeroed`: this run's zero tasks seen done
+  // fp16 split plan: the warp draws one zero task after its last whole tile
+  // (while its pair computes a tail part, or as the pair finishes; at the end
+  // if it had no item), and every task left before its first reduction, so
+  // that it never waits for a task no running warp holds (fewer pairs may be
+  // resident than were launched).  All pairs thus zero the tail tiles, about
+  // one task per warp, while the parts are computed, and no zeroing competes
+  // with the full rounds' loads (measured: zeroing after the first item
+  // slowed the next two rounds by ~2 us; only the pairs without a part,
+  // zeroing after their last item, took ~7 us); `zeroed`: this run's zero
+  // tasks seen done
   bool drew = true, zeroed = true;
   if constexpr (kSplit && !kI8) {
     drew = p.zero_tasks <= 0;
@@ -900,7 +903,7 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
     const bool add_parts = kI8 && kSplit && parts > 1 && part == parts - 1;
     const bool reduce = !kI8 && kSplit && parts > 1;
     const int64_t tail = tile - p.full_tiles;
-    // Partial sums of part j of this tail tile, laid out for this warp: 16-byte
+    // int8: partial sums of part j of this tail tile, laid out for this warp: 16-byte
     // vector c of every lane of the warp is contiguous (512 bytes), so each
     // store and load of the warp moves whole lines.  Vector c (c < BN / 8) of
     // a lane holds its row's columns 4c .. 4c + 3 of the warp's half of the
@@ -910,7 +913,7 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
     const int64_t vecs = g.BN / 8;
     const int64_t part_stride = 2 * kEpiWarps * vecs * 32;
     uint4* const part_base =
-        parts > 1 ? static_cast<uint4*>(p.partials) +
+        kI8 && parts > 1 ? static_cast<uint4*>(p.partials) +
                         ((((tail * (p.split - 1)) * 2 + rank) * kEpiWarps + half * 4 + quad) * vecs *
                              32 + lane)
                   : nullptr;
@@ -955,13 +958,11 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
         // shared box -> one TMA store of 32 full 128-byte row segments.  Rows
         // past the shard and columns past N are clipped by the descriptor.
         const int64_t r0 = mt * kPairM + rank * kBlockM + quad * 32;
-        if (reduce && !drew) {
+        if (reduce && !zeroed) {
           if (lane == 0) bulk_wait_group_read<0>();  // the box is no longer read
           __syncwarp();
           zero_tail_tiles(p, box, lane, true);
           drew = true;
-        }
-        if (reduce && !zeroed) {
           if (!wait_zeroed(p, rank, lane, abort)) {
             if (lane == 0) bulk_wait_group_all();
             return;

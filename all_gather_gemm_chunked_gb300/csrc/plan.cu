@@ -444,11 +444,11 @@ int launch_fused(ag_gemm_plan* p, agg::FusedParams& fp, int flags, cudaStream_t 
   if ((flags & agg::kFlagGemm) && p->work_items > stat)
     p->tile_base += static_cast<unsigned long long>(p->work_items - stat) +
                     static_cast<unsigned long long>(grid / 2);
-  // A run draws each zero task's ticket once, plus at most one failing ticket
-  // per epilogue warp; the next run's tickets start past all of them.
+  // A run draws each zero task's ticket once, plus at most two failing
+  // tickets per epilogue warp; the next run's tickets start past all of them.
   if (fp.zero_tasks > 0)
     p->zero_base += static_cast<unsigned long long>(p->zero_tasks) +
-                    static_cast<unsigned long long>(grid) * agg::kEpiWarps;
+                    2ull * static_cast<unsigned long long>(grid) * agg::kEpiWarps;
   return AG_GEMM_OK;
 }
 

@@ -182,3 +182,60 @@ def test_zero_tasks_cover_every_tail_tile_once(tiles, pairs):
     assert {t for t, _ in covered} == set(range(full, tiles))
     # the parts that add into them are exactly the tail tiles' parts
     assert {decode(i)[0] for i in range(full, work)} == set(range(full, tiles))
+
+
+def simulate_zeroing(tiles, pairs, kb, resident, warps=16):
+    """The fp16 split tail's zero tasks under partial residency: each pair
+    runs its dealt items in order; after its last whole tile each of its
+    warps draws one zero task, before its first part each warp draws every
+    task left and then waits until all tasks are done, and a pair with no
+    part draws one per warp at its end.  A drawn task is done by its warp
+    at once.  A resident pair that waits for tasks which no resident pair
+    holds would never finish; a waiting pair leaves room for no other."""
+    full, work, decode = items_of(tiles, pairs, kb, i8=False)
+    tasks = (tiles - full) * 8
+    state = {"next": 0, "done": 0}
+
+    def draw(n):
+        take = min(n, tasks - state["next"])
+        state["next"] += take
+        state["done"] += take               # done at once by the warp that drew it
+
+    waiting, running = list(range(pairs)), []
+    pos = {}
+    while waiting and len(running) < resident:
+        p = waiting.pop(0); running.append(p); pos[p] = 0
+    finished = 0
+    for _ in range(10 * work + 10 * pairs + 100):
+        if not running:
+            return finished == pairs
+        p = running[0]
+        items = list(range(p, work, pairs))
+        i = pos[p]
+        if i < len(items):
+            _, part, parts = decode(items[i])
+            if parts > 1:
+                if i == 0 or decode(items[i - 1])[2] == 1:
+                    draw(tasks)             # every task left, before the first wait
+                if state["done"] < tasks:
+                    return False            # would wait for tasks nobody running holds
+            pos[p] = i + 1
+            if parts == 1 and (i + 1 == len(items) or decode(items[i + 1])[2] > 1):
+                draw(warps)                 # one task per warp after the last whole tile
+            running.append(running.pop(0))
+            continue
+        if not items or decode(items[-1])[2] > 1:
+            draw(0)                         # (its single draw came earlier, or none needed)
+        running.pop(0)
+        finished += 1
+        if waiting:
+            q = waiting.pop(0); running.append(q); pos[q] = 0
+    return False
+
+
+@pytest.mark.parametrize("tiles,kb", [(256, 64), (80, 32), (24, 64), (100, 37)])
+def test_zero_tasks_never_wait_on_a_pair_that_has_not_started(tiles, kb):
+    pairs = 76
+    assert split_of(tiles, pairs, kb, i8=False) == 2
+    for resident in (1, 2, 7, 38, 76):
+        assert simulate_zeroing(tiles, pairs, kb, resident), (tiles, kb, resident)

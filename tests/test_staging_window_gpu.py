@@ -146,6 +146,9 @@ GRID_CASES = [
     ("f16", 3, 1000, 512, 520, None),
     ("f16", 2, 1536, 8192, 512, None),    # 24 tiles split in two along K (both parts add into C)
     ("bf16", 2, 1536, 2048, 520, None),   # 24 tiles of 32 k-blocks split in two
+    ("f16", 2, 2560, 2048, 1024, None),   # 76 whole tiles, then 4 split ones: on a small grid
+                                          # a pair reaches its parts long before the others'
+                                          # pairs start, and zeroes the tail blocks itself
     ("i8", 3, 512, 8192, 768, None),      # 18 tiles split in two (int32 partial sums)
 ]
 
