@@ -959,9 +959,15 @@ __device__ void epilogue_warp(const FusedParams& p, uint32_t rank, int quad, int
         // past the shard and columns past N are clipped by the descriptor.
         const int64_t r0 = mt * kPairM + rank * kBlockM + quad * 32;
         if (reduce && !zeroed) {
-          if (lane == 0) bulk_wait_group_read<0>();  // the box is no longer read
-          __syncwarp();
-          zero_tail_tiles(p, box, lane, true);
+          // every task left, unless they are all done already (as they are
+          // when every pair runs: 1000 warps drawing at once cost ~2 us)
+          uint32_t all_done = 0;
+          if (lane == 0) all_done = ld_acquire_gpu(p.zero_done) >= p.zero_target ? 1u : 0u;
+          if (__shfl_sync(0xffffffffu, all_done, 0) == 0u) {
+            if (lane == 0) bulk_wait_group_read<0>();  // the box is no longer read
+            __syncwarp();
+            zero_tail_tiles(p, box, lane, true);
+          }
           drew = true;
           if (!wait_zeroed(p, rank, lane, abort)) {
             if (lane == 0) bulk_wait_group_all();
